@@ -27,10 +27,11 @@ order of the additions, so only the tolerance bounds those.
 from __future__ import annotations
 
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
-ROW_CHUNK = 16          # rows per vectorised chunk (bounds memory at V = 262,144)
 VOCAB_CHUNK = 16384     # vocabulary rows of W per matmul step
 
 
@@ -60,30 +61,33 @@ def row_stats(logits: np.ndarray) -> dict:
     R, V = x.shape
     out = {k: np.empty(R, np.float64) for k in ("m", "lse", "H", "kappa", "conf")}
     out["argmax"] = np.empty(R, np.int64)
-    for r0 in range(0, R, ROW_CHUNK):
-        blk = x[r0:r0 + ROW_CHUNK].astype(np.float64)
-        for j, l in enumerate(blk):
-            i = r0 + j
-            m = l.max()
-            a = int(np.argmax(l))
-            out["m"][i] = m
-            out["argmax"][i] = a
-            if m == -np.inf:
-                for k in ("lse", "H", "kappa", "conf"):
-                    out[k][i] = np.nan
-                out["argmax"][i] = 0
-                continue
-            e = np.exp(l - m)
-            Z = e.sum()
-            lse = m + math.log(Z)
-            p = np.exp(l - lse)
-            pos = p > 0
-            H = -np.sum(p[pos] * np.log(p[pos]))
-            rest = np.delete(e, a).sum()
-            out["lse"][i] = lse
-            out["H"][i] = H
-            out["kappa"][i] = math.log1p(rest)
-            out["conf"][i] = 1.0 / Z
+
+    def one_row(i: int) -> None:
+        l = x[i].astype(np.float64)
+        m = l.max()
+        a = int(np.argmax(l))
+        out["m"][i] = m
+        out["argmax"][i] = a
+        if m == -np.inf:
+            for k in ("lse", "H", "kappa", "conf"):
+                out[k][i] = np.nan
+            out["argmax"][i] = 0
+            return
+        e = np.exp(l - m)
+        Z = e.sum()
+        lse = m + math.log(Z)
+        p = np.exp(l - lse)
+        pos = p > 0
+        H = -np.sum(p[pos] * np.log(p[pos]))
+        rest = np.delete(e, a).sum()
+        out["lse"][i] = lse
+        out["H"][i] = H
+        out["kappa"][i] = math.log1p(rest)
+        out["conf"][i] = 1.0 / Z
+
+    # rows are independent; the pool only spreads them over the host's cores
+    with ThreadPoolExecutor(max(1, min(32, os.cpu_count() or 1))) as ex:
+        list(ex.map(one_row, range(R)))
     return out
 
 
@@ -93,7 +97,9 @@ def entropy_accept(H: np.ndarray, kappa: np.ndarray, n_req: int, L_c: int,
 
     For request q with positions 0..L_c-1 (rows q*L_c + j) and budget B_q:
       order  = positions from most to least confident: kappa ascending (= confidence
-               descending), equal confidence broken by the lower position first;
+               descending), equal confidence broken by the lower position first; a
+               position without a distribution (NaN statistics: all logits -inf) has no
+               confidence and goes after every other;
       C_k    = H[order_1] + ... + H[order_k];
       n      = the largest k in 0..L_c with C_k <= B_q - positions are taken in order
                and taking stops at the first one that would carry the running
@@ -111,12 +117,12 @@ def entropy_accept(H: np.ndarray, kappa: np.ndarray, n_req: int, L_c: int,
     n_acc = np.empty(n_req, np.int64)
     for q in range(n_req):
         base = q * L_c
-        pos = sorted(range(L_c), key=lambda j: (kappa[base + j], j))
+        pos = sorted(range(L_c), key=lambda j: (bool(np.isnan(kappa[base + j])), kappa[base + j], j))
         B = float(budgets[q])
         running, n = 0.0, 0
         for k, j in enumerate(pos):
             running += H[base + j]
-            if running <= B:
+            if running <= B:         # False once the sum is NaN: a NaN position stops it
                 n = k + 1
             else:
                 break

@@ -320,3 +320,11 @@ def test_row_subset_matches_full():
     full = soft_embed(x, st["lse"], 0, V, Wb, 2.0)
     sub = soft_embed(x, st["lse"], 0, V, Wb, 2.0, rows=np.array([4, 1]))
     assert np.array_equal(sub, full[[4, 1]])
+
+
+def test_position_without_distribution_goes_last_and_stops_the_sum():
+    H = np.array([0.5, np.nan, 0.2, 0.1])
+    kappa = np.array([1.0, np.nan, 0.5, 2.0])
+    out = entropy_accept(H, kappa, 1, 4, np.array([100.0]))
+    assert list(out["order"]) == [2, 0, 3, 1]
+    assert out["n_accepted"][0] == 3 and list(out["mask"]) == [1, 0, 1, 1]
