@@ -1,0 +1,316 @@
+"""Benchmark of the fused denoising-sampler step on GB300.
+
+Workload: one 256-position canvas over V = 262,144 vocabulary entries with hidden
+size d = 2,816 (synthetic, seeded; the shapes of the DiffusionGemma sampler).  A step
+is one dg_sampler_step call: row statistics, entropy-bound acceptance and the
+self-conditioning soft embedding.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the CPU oracle as it stands on the host cores, on a bounded
+sample of canvas positions per step (the pages ship no runnable reference).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "canvas positions/sec per fused sampler step (V=262144,d=2816); % of roofline"
+UNIT = "positions/s"
+WORKLOAD = "canvas256"
+KERNELS_PER_STEP = 4   # row stats, acceptance, soft-embed product, split-K reduce
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def config_of(wl, extra=None) -> dict:
+    c = {"workload": f"{wl.name}: {wl.n_req} request x {wl.L_c} positions, V={wl.V}, d={wl.d}, "
+                     f"fp32 logits, bf16 W, gamma={wl.gamma}",
+         "rows": wl.R, "V": wl.V, "d": wl.d,
+         "budget_nats": list(wl.budget) if isinstance(wl.budget, tuple) else wl.budget,
+         "l2": "no flush: each step reads 1.62 GiB of logits and W, 13x the 129 MB L2"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def source_sha(files=("soft_embed.cu", "dg_common.cuh")) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "denoising_sampler_step_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "window": "from warm-up start to the end of the end-to-end loop"}
+
+
+# --------------------------------------------------------------------------- CPU oracle legs
+
+def oracle_seconds(x, Wb, wl, rows, budget):
+    """Times the oracle on `rows` canvas positions: their statistics, their acceptance
+    as one request, and their soft embeddings over the full vocabulary."""
+    import numpy as np
+    from oracle import entropy_accept, row_stats, soft_embed
+    t0 = time.perf_counter()
+    st = row_stats(x[rows])
+    entropy_accept(st["H"], st["kappa"], 1, len(rows), np.array([budget], np.float32))
+    soft_embed(x[rows], st["lse"], 0, wl.V, Wb, wl.gamma)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(x, Wb, wl, min_seconds: float = 10.0) -> dict:
+    """Whole-canvas passes of the oracle, repeated until about min_seconds have passed."""
+    import numpy as np
+    rows = np.arange(wl.R)
+    total, passes = 0.0, 0
+    while passes == 0 or (total < min_seconds and passes < 8):
+        total += oracle_seconds(x, Wb, wl, rows, float(wl.budget))
+        passes += 1
+    return {"value": passes * wl.R / total, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{passes} whole-canvas pass(es) of {wl.name} ({wl.R} positions, full V and d): fp64 "
+                      f"statistics, acceptance and soft embedding, {total:.1f} s; numpy BLAS and the "
+                      f"oracle's row pool on all host cores"}
+
+
+def run_reference(args) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+    from denoising_sampler_step_gb300 import inputs
+    wl = inputs.WORKLOADS[WORKLOAD]
+    x = inputs.logits(wl)
+    Wb = inputs.embedding_bf16(wl)
+    rows_per_step = 1
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        oracle_seconds(x, Wb, wl, rng.choice(wl.R, rows_per_step, replace=False), float(wl.budget))
+    times = [oracle_seconds(x, Wb, wl, rng.choice(wl.R, rows_per_step, replace=False), float(wl.budget))
+             for _ in range(args.steps)]
+    total = sum(times)
+    value = rows_per_step * args.steps / total
+    sample = (f"{rows_per_step} random canvas position(s) of {wl.name} per step (full V and d per row), "
+              f"fp64 oracle; {total:.1f} s over {args.steps} steps")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(wl),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from denoising_sampler_step_gb300 import binding as B
+    from denoising_sampler_step_gb300 import cost, inputs
+    from denoising_sampler_step_gb300.step import SamplerStep
+
+    # each rank serves its own canvases (independent requests: weak scaling)
+    base = inputs.WORKLOADS[WORKLOAD]
+    wl = base.with_(seed=base.seed + 1000 * rank)
+    x = inputs.logits(wl)
+    Wb = inputs.embedding_bf16(wl)
+    budgets = inputs.budgets(wl)
+    dev = torch.device("cuda", local)
+    xd = torch.from_numpy(x).to(dev)
+    Wd = torch.from_numpy(Wb.view(np.int16)).to(dev).view(torch.bfloat16)
+    bd = torch.from_numpy(budgets).to(dev)
+    step = SamplerStep(Wd, wl.n_req, wl.L_c, wl.V, wl.gamma, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        step(xd, bd)
+    B.dg_get_device_status()
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(xd, bd)
+    ev1.record(stream)
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    B.dg_get_device_status()
+
+    # per-kernel durations on the launching stream (same inputs, same shapes)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    comp = {"row_stats": 0.0, "accept": 0.0, "soft_embed": 0.0}
+    out = step.out
+    nrep = max(args.steps, 10)
+    for _ in range(nrep):
+        evs[0].record(stream)
+        B.dg_row_stats(xd, stream=stream, out=out)
+        evs[1].record(stream)
+        B.dg_entropy_accept(out["H"], out["kappa"], wl.n_req, wl.L_c, bd, stream=stream, out=out)
+        evs[2].record(stream)
+        B.dg_soft_embed(xd, out["lse"], 0, wl.V, Wd, wl.gamma, out=out["E"], ws=step.ws, stream=stream)
+        evs[3].record(stream)
+        torch.cuda.synchronize(dev)
+        comp["row_stats"] += evs[0].elapsed_time(evs[1])
+        comp["accept"] += evs[1].elapsed_time(evs[2])
+        comp["soft_embed"] += evs[2].elapsed_time(evs[3])
+    comp = {k: v / nrep for k, v in comp.items()}
+
+    # end to end through the public API: pinned host inputs in, results out, every step
+    h = step.host_buffers()
+    h["logits"].copy_(torch.from_numpy(x))
+    h["budgets"].copy_(torch.from_numpy(budgets))
+    for _ in range(3):
+        step.run_from_host(h)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step.run_from_host(h)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = t.tolist()
+
+    pk = peaks()
+    sc = cost.StepCost(rows=wl.R, V=wl.V, d=wl.d, vocab=wl.V)
+    t_roof = sc.roofline_seconds(pk["hbm_gbs"], pk["bf16_tflops"])
+    achieved = sc.gemm_bytes / (comp["soft_embed"] * 1e-3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "soft_embed_traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            tj = json.load(f)
+        if tj.get("kernel_source_sha") == source_sha():
+            traffic = tj.get("traffic_bytes_per_launch")
+    ms_step = ms / args.steps
+    line = {
+        "metric": METRIC,
+        "value": world * wl.R * args.steps / (ms * 1e-3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32 statistics, bf16 x bf16 -> f32 tensor-core product",
+        "data": "synthetic",
+        "config": config_of(wl, {"parallelism": f"replicas x{world} (independent canvases per GPU)"}),
+        "step_roofline": {"t_roof_us": t_roof * 1e6, "t_step_us": ms_step * 1e3,
+                          "frac": t_roof / (ms_step * 1e-3), "peaks": pk["source"]},
+        "roofline": {"kernel": "soft_embed (tcgen05 product + split-K reduce)", "bound": "hbm",
+                     "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+                     "algorithmic_bytes_per_launch": sc.gemm_bytes, "launch_us": comp["soft_embed"] * 1e3,
+                     "peak_source": pk["source"]},
+        "kernel_us": {k: v * 1e3 for k, v in comp.items()},
+        "e2e": {"value": world * wl.R * args.steps / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": step.h2d_bytes(h), "d2h_bytes_per_step": step.d2h_bytes(),
+                "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(x, Wb, wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

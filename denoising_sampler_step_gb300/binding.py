@@ -1,0 +1,172 @@
+"""Python binding of libdgsamp: argument marshalling only.
+
+Every function here has the name of the C entry point it calls (include/dgsamp.h)
+and does nothing but turn torch CUDA tensors into pointers, sizes and the current
+stream, allocate outputs with torch when the caller gives none, and raise on a
+non-zero status.  All arithmetic runs in the library's CUDA kernels; there is no
+other path.  Importing this module fails if the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdgsamp.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m denoising_sampler_step_gb300.build` "
+        "(or __graft_entry__.build()); there is no fallback path")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_i64, _i32, _f32, _p, _sz = ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+
+lib.dg_version.restype = ctypes.c_int
+lib.dg_last_error.restype = ctypes.c_char_p
+lib.dg_row_stats.argtypes = [_p, _i64, _i64, _i64, _p, _p, _p, _p, _p, _p]
+lib.dg_row_stats.restype = ctypes.c_int
+lib.dg_soft_embed_workspace_size.argtypes = [_i64, _i64, _i64]
+lib.dg_soft_embed_workspace_size.restype = _sz
+lib.dg_soft_embed.argtypes = [_p, _i64, _p, _i64, _i64, _i64, _p, _i64, _i64, _i64, _f32, _p, _i64, _p, _sz, _p]
+lib.dg_soft_embed.restype = ctypes.c_int
+lib.dg_entropy_accept.argtypes = [_p, _p, _i32, _i32, _p, _i32, _p, _p, _p, _p]
+lib.dg_entropy_accept.restype = ctypes.c_int
+lib.dg_sum_partials.argtypes = [ctypes.POINTER(_p), _i32, _i64, _i64, _i64, _f32, _p, _i64, _p]
+lib.dg_sum_partials.restype = ctypes.c_int
+lib.dg_sampler_step.argtypes = [_p, _i32, _i32, _i64, _i64, _p, _i64, _i64, _i64, _i64, _i64, _f32, _p, _i32,
+                                _p, _p, _p, _p, _p, _p, _p, _p, _p, _i64, _p, _sz, _p]
+lib.dg_sampler_step.restype = ctypes.c_int
+lib.dg_get_device_status.argtypes = [_p]
+lib.dg_get_device_status.restype = ctypes.c_int
+
+STATUS = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED", 3: "DG_ERR_CUDA", 4: "DG_ERR_TIMEOUT"}
+
+
+class DgError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = lib.dg_last_error().decode(errors="replace")
+        super().__init__(f"{where}: {STATUS.get(status, status)}: {msg}")
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise DgError(status, where)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ld(t: torch.Tensor) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("expected a 2-D tensor with unit column stride")
+    return t.stride(0)
+
+
+def _new(shape, dtype, device):
+    return torch.empty(shape, dtype=dtype, device=device)
+
+
+def dg_row_stats(logits: torch.Tensor, V: int | None = None, stream=None, out: dict | None = None) -> dict:
+    """Row statistics of fp32 logits [R, >=V] -> dict m, lse, H, kappa (fp32), argmax (int32)."""
+    R = logits.shape[0]
+    V = logits.shape[1] if V is None else V
+    dev = logits.device
+    o = out
+    if o is None:
+        o = {k: _new(R, torch.float32, dev) for k in ("m", "lse", "H", "kappa")}
+        o["argmax"] = _new(R, torch.int32, dev)
+    _check(lib.dg_row_stats(_ptr(logits), R, V, _ld(logits), _ptr(o["m"]), _ptr(o["lse"]), _ptr(o["H"]),
+                            _ptr(o["kappa"]), _ptr(o["argmax"]), _stream(stream)), "dg_row_stats")
+    return o
+
+
+def dg_soft_embed_workspace_size(R: int, vocab_len: int, d: int) -> int:
+    return int(lib.dg_soft_embed_workspace_size(R, vocab_len, d))
+
+
+def workspace(R: int, vocab_len: int, d: int, device) -> torch.Tensor:
+    """A workspace tensor large enough for dg_soft_embed / dg_sampler_step."""
+    n = max(16, dg_soft_embed_workspace_size(R, vocab_len, d))
+    return torch.empty((n + 15) // 16 * 16, dtype=torch.uint8, device=device)
+
+
+def dg_soft_embed(logits: torch.Tensor, lse: torch.Tensor, vocab_start: int, vocab_end: int,
+                  W_shard: torch.Tensor, gamma: float, out: torch.Tensor | None = None,
+                  ws: torch.Tensor | None = None, stream=None, R: int | None = None) -> torch.Tensor:
+    """E = gamma * softmax(logits)[:, s:e] @ W_shard[0:e-s] (W_shard: bf16 [rows_pad, >=d])."""
+    R = logits.shape[0] if R is None else R
+    d = W_shard.shape[1]
+    if W_shard.dtype not in (torch.bfloat16, torch.int16):
+        raise TypeError("W_shard must hold bfloat16 values")
+    if out is None:
+        out = _new((R, d), torch.float32, logits.device)
+    if ws is None:
+        ws = workspace(R, max(1, vocab_end - vocab_start), d, logits.device)
+    _check(lib.dg_soft_embed(_ptr(logits), _ld(logits), _ptr(lse), R, vocab_start, vocab_end, _ptr(W_shard),
+                             W_shard.shape[0], _ld(W_shard), d, gamma, _ptr(out), _ld(out), _ptr(ws), ws.numel(),
+                             _stream(stream)), "dg_soft_embed")
+    return out
+
+
+def dg_entropy_accept(H: torch.Tensor, kappa: torch.Tensor, n_req: int, L_c: int, budgets: torch.Tensor,
+                      min_accept: int = 0, stream=None, out: dict | None = None) -> dict:
+    dev = H.device
+    R = n_req * L_c
+    o = out if out is not None else {"order": _new(R, torch.int32, dev), "mask": _new(R, torch.uint8, dev),
+                                     "n_accepted": _new(n_req, torch.int32, dev)}
+    _check(lib.dg_entropy_accept(_ptr(H), _ptr(kappa), n_req, L_c, _ptr(budgets), min_accept, _ptr(o["order"]),
+                                 _ptr(o["mask"]), _ptr(o["n_accepted"]), _stream(stream)), "dg_entropy_accept")
+    return o
+
+
+def dg_sum_partials(partials: list, gamma: float, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    R, d = partials[0].shape
+    ldp = _ld(partials[0])
+    if any(tuple(p.shape) != (R, d) or _ld(p) != ldp for p in partials):
+        raise ValueError("partials must share shape and leading dimension")
+    if out is None:
+        out = _new((R, d), torch.float32, partials[0].device)
+    arr = (_p * len(partials))(*[p.data_ptr() for p in partials])
+    _check(lib.dg_sum_partials(arr, len(partials), R, d, ldp, gamma, _ptr(out), _ld(out), _stream(stream)),
+           "dg_sum_partials")
+    return out
+
+
+def dg_sampler_step(logits: torch.Tensor, n_req: int, L_c: int, W: torch.Tensor, gamma: float,
+                    budgets: torch.Tensor, min_accept: int = 0, vocab_start: int = 0, vocab_end: int | None = None,
+                    V: int | None = None, out: dict | None = None, ws: torch.Tensor | None = None,
+                    stream=None) -> dict:
+    """One fused sampler step; returns dict m, lse, H, kappa, argmax, order, mask, n_accepted, E."""
+    R = n_req * L_c
+    V = logits.shape[1] if V is None else V
+    vocab_end = V if vocab_end is None else vocab_end
+    d = W.shape[1]
+    dev = logits.device
+    o = out
+    if o is None:
+        o = {k: _new(R, torch.float32, dev) for k in ("m", "lse", "H", "kappa")}
+        o.update(argmax=_new(R, torch.int32, dev), order=_new(R, torch.int32, dev), mask=_new(R, torch.uint8, dev),
+                 n_accepted=_new(n_req, torch.int32, dev), E=_new((R, d), torch.float32, dev))
+    if ws is None:
+        ws = workspace(R, max(1, vocab_end - vocab_start), d, dev)
+    _check(lib.dg_sampler_step(_ptr(logits), n_req, L_c, V, _ld(logits), _ptr(W), vocab_start, vocab_end,
+                               W.shape[0], _ld(W), d, gamma, _ptr(budgets), min_accept, _ptr(o["m"]), _ptr(o["lse"]),
+                               _ptr(o["H"]), _ptr(o["kappa"]), _ptr(o["argmax"]), _ptr(o["order"]), _ptr(o["mask"]),
+                               _ptr(o["n_accepted"]), _ptr(o["E"]), _ld(o["E"]), _ptr(ws), ws.numel(),
+                               _stream(stream)), "dg_sampler_step")
+    return o
+
+
+def dg_get_device_status(stream=None) -> None:
+    _check(lib.dg_get_device_status(_stream(stream)), "dg_get_device_status")

@@ -1,0 +1,110 @@
+// Entropy-bound acceptance: per request, order the canvas positions from most to
+// least confident and accept them until the running entropy would pass the budget
+// (agentlenshq.com, "サンプリングループとエントロピー境界デノイジング").
+//
+// One CTA per request, one thread per (padded) position:
+//   1. key = (order-preserving bits of kappa) << 32 | position, so that a single
+//      64-bit ascending sort gives confidence descending with ties broken by the
+//      lower position; NaN kappa (no distribution) maps above every number;
+//   2. bitonic sort of the keys in shared memory;
+//   3. inclusive prefix sum of H in sorted order, in fp64 (warp shuffles, then the
+//      per-warp totals);
+//   4. n = the first k whose running sum is not <= B (NaN counts as passing it),
+//      raised to min(min_accept, L_c); mask[order_j] = j < n.
+#include "dg_common.cuh"
+#include "dg_internal.h"
+
+namespace dg {
+
+namespace {
+
+// Monotone map from float to uint32: a < b  <=>  key(a) < key(b) for numbers
+// (-0 and +0 equal); any NaN maps to the largest key.
+__device__ __forceinline__ uint32_t order_bits(float x) {
+    if (x != x) return 0xffffffffu;
+    const uint32_t u = __float_as_uint(x == 0.0f ? 0.0f : x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(1024)
+    accept_kernel(const float *__restrict__ H, const float *__restrict__ kappa, int L_c,
+                  const float *__restrict__ budgets, int min_accept, int32_t *__restrict__ order,
+                  uint8_t *__restrict__ mask, int32_t *__restrict__ n_accepted) {
+    extern __shared__ unsigned long long keys[];  // blockDim.x entries
+    __shared__ double warp_tot[32];
+    __shared__ int first_fail;
+
+    const int q = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int NT = blockDim.x;
+    const int64_t base = (int64_t)q * L_c;
+
+    keys[tid] = (tid < L_c) ? (((unsigned long long)order_bits(kappa[base + tid]) << 32) | (unsigned)tid)
+                            : ~0ull;
+    if (tid == 0) first_fail = L_c;
+    __syncthreads();
+
+    for (int k = 2; k <= NT; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const int p = tid ^ j;
+            if (p > tid) {
+                const unsigned long long a = keys[tid], b = keys[p];
+                const bool ascending = (tid & k) == 0;
+                if ((a > b) == ascending) {
+                    keys[tid] = b;
+                    keys[p] = a;
+                }
+            }
+            __syncthreads();
+        }
+    }
+
+    const int pos = (int)(keys[tid] & 0xffffffffu);
+    double h = (tid < L_c) ? (double)H[base + pos] : 0.0;
+    // inclusive scan in fp64
+    const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const double o = __shfl_up_sync(0xffffffffu, h, off);
+        if (lane >= off) h += o;
+    }
+    if (lane == 31) warp_tot[warp] = h;
+    __syncthreads();
+    if (warp == 0) {
+        double w = (lane < NT / 32) ? warp_tot[lane] : 0.0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const double o = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += o;
+        }
+        if (lane < NT / 32) warp_tot[lane] = w;
+    }
+    __syncthreads();
+    if (warp > 0) h += warp_tot[warp - 1];
+
+    const double B = (double)budgets[q];
+    if (tid < L_c && !(h <= B)) atomicMin(&first_fail, tid);
+    __syncthreads();
+    int n = first_fail;
+    const int floor_n = min(min_accept, L_c);
+    if (n < floor_n) n = floor_n;
+    if (tid < L_c) {
+        order[base + tid] = pos;
+        mask[base + pos] = (uint8_t)(tid < n ? 1 : 0);
+    }
+    if (tid == 0) n_accepted[q] = n;
+}
+
+}  // namespace
+
+cudaError_t launch_entropy_accept(const float *H, const float *kappa, int32_t n_req, int32_t L_c,
+                                  const float *budgets, int32_t min_accept, int32_t *order,
+                                  uint8_t *mask, int32_t *n_accepted, cudaStream_t stream) {
+    int nt = 32;
+    while (nt < L_c) nt <<= 1;
+    accept_kernel<<<n_req, nt, nt * sizeof(unsigned long long), stream>>>(H, kappa, L_c, budgets, min_accept,
+                                                                        order, mask, n_accepted);
+    return cudaGetLastError();
+}
+
+}  // namespace dg

@@ -1,0 +1,230 @@
+// The C ABI of libdgsamp: argument checks, status codes and launches.
+// Declarations and the contract of every entry point are in include/dgsamp.h.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "dg_common.cuh"
+#include "dg_internal.h"
+
+namespace dg {
+
+__device__ unsigned int g_device_error = 0;
+
+namespace {
+
+thread_local char t_last_error[512] = "";
+
+dg_status fail(dg_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+dg_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(DG_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+dg_status check_stats_args(const float *logits, int64_t R, int64_t V, int64_t ldl) {
+    if (R < 0 || V < 1 || ldl < V) return fail(DG_ERR_INVALID_ARG, "row stats: need R >= 0, V >= 1, ldl >= V");
+    if (R > 0 && !logits) return fail(DG_ERR_INVALID_ARG, "row stats: logits is NULL");
+    if (V > 0x7ffffff0LL || R > (1LL << 28)) return fail(DG_ERR_UNSUPPORTED, "row stats: V or R too large");
+    if (R > 0 && (!aligned16(logits) || (ldl & 3)))
+        return fail(DG_ERR_UNSUPPORTED, "row stats: logits must be 16-byte aligned with ldl %% 4 == 0");
+    return DG_OK;
+}
+
+dg_status check_accept_args(const float *H, const float *kappa, int32_t n_req, int32_t L_c, const float *budgets,
+                            int32_t min_accept, const int32_t *order, const uint8_t *mask,
+                            const int32_t *n_accepted) {
+    if (n_req < 0 || L_c < 1 || min_accept < 0)
+        return fail(DG_ERR_INVALID_ARG, "accept: need n_req >= 0, L_c >= 1, min_accept >= 0");
+    if (L_c > 1024) return fail(DG_ERR_UNSUPPORTED, "accept: L_c = %d is above 1024", L_c);
+    if (n_req > 0 && (!H || !kappa || !budgets || !order || !mask || !n_accepted))
+        return fail(DG_ERR_INVALID_ARG, "accept: a pointer is NULL");
+    return DG_OK;
+}
+
+dg_status check_embed_args(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t s, int64_t e,
+                           const uint16_t *W, int64_t rows_pad, int64_t ldw, int64_t d, const float *out,
+                           int64_t ldo) {
+    if (R < 0 || d < 1) return fail(DG_ERR_INVALID_ARG, "soft embed: need R >= 0 and d >= 1");
+    if (s < 0 || e < s)
+        return fail(DG_ERR_INVALID_ARG, "soft embed: slice [%lld, %lld) is reversed or negative", (long long)s,
+                    (long long)e);
+    if (e > ldl)
+        return fail(DG_ERR_INVALID_ARG, "soft embed: slice end %lld is past ldl %lld", (long long)e, (long long)ldl);
+    if (e - s > rows_pad)
+        return fail(DG_ERR_INVALID_ARG,
+                    "soft embed: the slice has %lld vocabulary entries but the shard only %lld rows",
+                    (long long)(e - s), (long long)rows_pad);
+    if (ldw < d || ldo < d) return fail(DG_ERR_INVALID_ARG, "soft embed: need ldw >= d and ldo >= d");
+    if (R > 0 && (!logits || !lse || !out || (e > s && !W)))
+        return fail(DG_ERR_INVALID_ARG, "soft embed: a pointer is NULL");
+    if (R > (1LL << 30) || d > (1LL << 30) || e > 0x7fffff00LL)
+        return fail(DG_ERR_UNSUPPORTED, "soft embed: a size is too large");
+    if (R > 0 && e > s) {
+        if (!aligned16(logits) || (ldl & 3))
+            return fail(DG_ERR_UNSUPPORTED, "soft embed: logits must be 16-byte aligned with ldl %% 4 == 0");
+        if (!aligned16(W) || (ldw & 7))
+            return fail(DG_ERR_UNSUPPORTED, "soft embed: W must be 16-byte aligned with ldw %% 8 == 0");
+    }
+    return DG_OK;
+}
+
+dg_status run_soft_embed(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t s, int64_t e,
+                         const uint16_t *W, int64_t ldw, int64_t d, float gamma, float *out, int64_t ldo,
+                         void *ws, size_t ws_bytes, cudaStream_t stream) {
+    if (R == 0) return DG_OK;
+    if (e == s) {
+        cudaError_t err = launch_fill_zero(out, R, d, ldo, stream);
+        return err == cudaSuccess ? DG_OK : cuda_fail(err, "soft embed (empty slice)");
+    }
+    const int sms = device_sm_count();
+    if (sms <= 0) return fail(DG_ERR_CUDA, "soft embed: no CUDA device");
+    SoftEmbedPlan plan;
+    if (!plan_soft_embed(R, s, e, d, sms, &plan)) return fail(DG_ERR_INVALID_ARG, "soft embed: no plan for shape");
+    if (!ws || ws_bytes < plan.workspace_bytes)
+        return fail(DG_ERR_INVALID_ARG, "soft embed: workspace of %zu bytes is below the %zu needed", ws_bytes,
+                    plan.workspace_bytes);
+    if (!aligned16(ws)) return fail(DG_ERR_UNSUPPORTED, "soft embed: workspace must be 16-byte aligned");
+    const char *msg = "soft embed";
+    cudaError_t err = launch_soft_embed(logits, ldl, lse, R, s, e, W, ldw, d, gamma, out, ldo, ws, plan, stream, &msg);
+    return err == cudaSuccess ? DG_OK : cuda_fail(err, msg);
+}
+
+}  // namespace
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < kMaxDevices) {
+        const int c = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < kMaxDevices) g_sm_count[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+}  // namespace dg
+
+using namespace dg;
+
+extern "C" {
+
+int dg_version(void) { return 100; }
+
+const char *dg_last_error(void) { return t_last_error; }
+
+dg_status dg_row_stats(const float *logits, int64_t R, int64_t V, int64_t ldl, float *m, float *lse, float *H,
+                       float *kappa, int32_t *argmax, dg_stream_t stream) {
+    t_last_error[0] = 0;
+    dg_status st = check_stats_args(logits, R, V, ldl);
+    if (st != DG_OK || R == 0) return st;
+    cudaError_t e = launch_row_stats(logits, R, V, ldl, m, lse, H, kappa, argmax, (cudaStream_t)stream);
+    return e == cudaSuccess ? DG_OK : cuda_fail(e, "row stats launch");
+}
+
+size_t dg_soft_embed_workspace_size(int64_t R, int64_t vocab_len, int64_t d) {
+    if (R <= 0 || vocab_len <= 0 || d <= 0) return 0;
+    const int sms = device_sm_count();
+    SoftEmbedPlan plan;
+    if (!plan_soft_embed(R, 0, vocab_len, d, sms, &plan)) return 0;
+    // a slice that starts off a multiple of 4 reads up to one more block
+    SoftEmbedPlan plan2;
+    if (plan_soft_embed(R, 3, vocab_len + 3, d, sms, &plan2) && plan2.workspace_bytes > plan.workspace_bytes)
+        return plan2.workspace_bytes;
+    return plan.workspace_bytes;
+}
+
+dg_status dg_soft_embed(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t vocab_start,
+                        int64_t vocab_end, const uint16_t *W_shard, int64_t rows_pad, int64_t ldw, int64_t d,
+                        float gamma, float *out, int64_t ldo, void *workspace, size_t workspace_bytes,
+                        dg_stream_t stream) {
+    t_last_error[0] = 0;
+    dg_status st = check_embed_args(logits, ldl, lse, R, vocab_start, vocab_end, W_shard, rows_pad, ldw, d, out, ldo);
+    if (st != DG_OK) return st;
+    return run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W_shard, ldw, d, gamma, out, ldo, workspace,
+                          workspace_bytes, (cudaStream_t)stream);
+}
+
+dg_status dg_entropy_accept(const float *H, const float *kappa, int32_t n_req, int32_t L_c, const float *budgets,
+                            int32_t min_accept, int32_t *order, uint8_t *mask, int32_t *n_accepted,
+                            dg_stream_t stream) {
+    t_last_error[0] = 0;
+    dg_status st = check_accept_args(H, kappa, n_req, L_c, budgets, min_accept, order, mask, n_accepted);
+    if (st != DG_OK || n_req == 0) return st;
+    cudaError_t e = launch_entropy_accept(H, kappa, n_req, L_c, budgets, min_accept, order, mask, n_accepted,
+                                          (cudaStream_t)stream);
+    return e == cudaSuccess ? DG_OK : cuda_fail(e, "accept launch");
+}
+
+dg_status dg_sum_partials(const float *const *partials, int32_t T, int64_t R, int64_t d, int64_t ldp, float gamma,
+                          float *out, int64_t ldo, dg_stream_t stream) {
+    t_last_error[0] = 0;
+    if (T < 1 || T > kMaxPartials) return fail(DG_ERR_INVALID_ARG, "sum partials: need 1 <= T <= %d", kMaxPartials);
+    if (R < 0 || d < 1 || ldp < d || ldo < d) return fail(DG_ERR_INVALID_ARG, "sum partials: bad sizes");
+    if (R == 0) return DG_OK;
+    if (!partials || !out) return fail(DG_ERR_INVALID_ARG, "sum partials: a pointer is NULL");
+    for (int t = 0; t < T; ++t)
+        if (!partials[t]) return fail(DG_ERR_INVALID_ARG, "sum partials: partials[%d] is NULL", t);
+    cudaError_t e = launch_sum_partials(partials, T, R, d, ldp, gamma, out, ldo, (cudaStream_t)stream);
+    return e == cudaSuccess ? DG_OK : cuda_fail(e, "sum partials launch");
+}
+
+dg_status dg_sampler_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, int64_t ldl, const uint16_t *W,
+                          int64_t vocab_start, int64_t vocab_end, int64_t rows_pad, int64_t ldw, int64_t d,
+                          float gamma, const float *budgets, int32_t min_accept, float *m, float *lse, float *H,
+                          float *kappa, int32_t *argmax, int32_t *order, uint8_t *mask, int32_t *n_accepted, float *E,
+                          int64_t ldo, void *workspace, size_t workspace_bytes, dg_stream_t stream) {
+    t_last_error[0] = 0;
+    if (n_req < 0 || L_c < 1) return fail(DG_ERR_INVALID_ARG, "step: need n_req >= 0 and L_c >= 1");
+    const int64_t R = (int64_t)n_req * L_c;
+    dg_status st = check_stats_args(logits, R, V, ldl);
+    if (st != DG_OK) return st;
+    st = check_accept_args(H, kappa, n_req, L_c, budgets, min_accept, order, mask, n_accepted);
+    if (st != DG_OK) return st;
+    if (vocab_end > V)
+        return fail(DG_ERR_INVALID_ARG, "step: slice end %lld is past V %lld", (long long)vocab_end, (long long)V);
+    st = check_embed_args(logits, ldl, lse, R, vocab_start, vocab_end, W, rows_pad, ldw, d, E, ldo);
+    if (st != DG_OK) return st;
+    if (R > 0 && (!m || !lse || !H || !kappa || !argmax)) return fail(DG_ERR_INVALID_ARG, "step: a pointer is NULL");
+    if (R == 0) return DG_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = launch_row_stats(logits, R, V, ldl, m, lse, H, kappa, argmax, s);
+    if (e != cudaSuccess) return cuda_fail(e, "step: row stats launch");
+    e = launch_entropy_accept(H, kappa, n_req, L_c, budgets, min_accept, order, mask, n_accepted, s);
+    if (e != cudaSuccess) return cuda_fail(e, "step: accept launch");
+    return run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, ldw, d, gamma, E, ldo, workspace,
+                          workspace_bytes, s);
+}
+
+dg_status dg_get_device_status(dg_stream_t stream) {
+    t_last_error[0] = 0;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "device status: stream");
+    unsigned int word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_device_error, sizeof(word));
+    if (e != cudaSuccess) return cuda_fail(e, "device status: read");
+    if (word) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
+        if (e != cudaSuccess) return cuda_fail(e, "device status: clear");
+        return fail(DG_ERR_TIMEOUT, "a kernel gave up waiting on a device barrier");
+    }
+    return DG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,255 @@
+// Row statistics of the sampler step: max, argmax, log-sum-exp, entropy and
+// -ln(confidence) of the softmax over the full vocabulary, one pass over the logits.
+//
+// What it computes: calvarado04.com, eq. e^sc (p_i is a softmax over all V tokens);
+// agentlenshq.com, "サンプリングループとエントロピー境界デノイジング" (a candidate and an
+// entropy at every canvas position).
+//
+// Design (HBM-bound: every logit is read once, 4 bytes per vocabulary entry):
+//   - one thread-block cluster per row; the row is cut into CLUSTER contiguous
+//     pieces, one per CTA;
+//   - 128-bit read-only loads, coalesced, several in flight per thread per batch;
+//   - each thread keeps an online state (m, a, rest, t) over the entries it saw:
+//       m    = running max, a = index of its first occurrence,
+//       rest = sum over the entries other than a of exp(l - m),
+//       t    = sum over all entries of exp(l - m) * (l - m)   (<= 0);
+//     keeping the argmax's own 1 out of `rest` preserves kappa = log1p(rest) for
+//     rows that are nearly one-hot;
+//   - warp-shuffle, then CTA, then cluster (distributed shared memory) merges, in a
+//     fixed order so the result is bitwise reproducible.
+//   Final: lnZ = log1p(rest), lse = m + lnZ, H = lnZ - t / (1 + rest), kappa = lnZ.
+#include <cooperative_groups.h>
+#include <float.h>
+
+#include "dg_common.cuh"
+#include "dg_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace dg {
+
+namespace {
+
+constexpr int kStatsThreads = 256;
+constexpr int kStatsVec = 4;  // float4 loads per thread per batch
+
+struct RowState {
+    float m;
+    int a;
+    float rest;
+    float t;
+};
+
+__device__ __forceinline__ float4 ld_stream(const float4 *p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// A := A merged with B.  The larger max wins; equal maxima keep the lower index.
+__device__ __forceinline__ void merge(RowState &A, const RowState &B) {
+    const bool b_wins = (B.m > A.m) || (B.m == A.m && B.a < A.a);
+    RowState hi = b_wins ? B : A;
+    const RowState lo = b_wins ? A : B;
+    if (lo.m != -INFINITY) {
+        const float dm = lo.m - hi.m;              // <= 0
+        const float s = ex2_approx(dm * kLog2e);   // rescale lo to hi's max
+        const float S_lo = lo.rest + 1.0f;         // lo's full sum, its argmax included
+        hi.rest = fmaf(s, S_lo, hi.rest);
+        hi.t = fmaf(s, fmaf(dm, S_lo, lo.t), hi.t);
+    }
+    A = hi;
+}
+
+__device__ __forceinline__ RowState shfl_down(const RowState &s, int off) {
+    RowState o;
+    o.m = __shfl_down_sync(0xffffffffu, s.m, off);
+    o.a = __shfl_down_sync(0xffffffffu, s.a, off);
+    o.rest = __shfl_down_sync(0xffffffffu, s.rest, off);
+    o.t = __shfl_down_sync(0xffffffffu, s.t, off);
+    return o;
+}
+
+// Folds N values x[j] (vocabulary index 4*base[j/4] + j%4, increasing in j) into st.
+template <int N>
+__device__ __forceinline__ void absorb(RowState &st, float (&x)[N], const int (&base)[N / 4]) {
+    float bm = x[0];
+#pragma unroll
+    for (int j = 1; j < N; ++j) bm = fmaxf(bm, x[j]);
+    if (bm > st.m) {
+        // a new maximum: rebase the state, then take its first occurrence out of the sums
+        if (st.m == -INFINITY) {
+            st.rest = 0.0f;
+            st.t = 0.0f;
+        } else {
+            const float dm = st.m - bm;
+            const float s = ex2_approx(dm * kLog2e);
+            const float S = st.rest + 1.0f;
+            st.t = s * fmaf(dm, S, st.t);
+            st.rest = s * S;
+        }
+        st.m = bm;
+        int ja = N;
+#pragma unroll
+        for (int j = N - 1; j >= 0; --j)
+            if (x[j] == bm) ja = j;
+#pragma unroll
+        for (int j = 0; j < N; ++j)
+            if (j == ja) {
+                st.a = 4 * base[j / 4] + (j % 4);
+                x[j] = -INFINITY;
+            }
+    }
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        const float d = fmaxf(x[j] - st.m, -FLT_MAX);  // -inf entries: exp gives 0 and 0*d = 0
+        const float e = ex2_approx(d * kLog2e);
+        st.rest += e;
+        st.t = fmaf(e, d, st.t);
+    }
+}
+
+template <int CLUSTER>
+__global__ void __launch_bounds__(kStatsThreads, 4)
+    row_stats_kernel(const float *__restrict__ logits, int64_t V, int64_t ldl, float *__restrict__ out_m,
+                     float *__restrict__ out_lse, float *__restrict__ out_H,
+                     float *__restrict__ out_kappa, int32_t *__restrict__ out_argmax) {
+    __shared__ RowState warp_state[kStatsThreads / 32];
+    __shared__ RowState cta_state[CLUSTER];
+
+    const int rank = (int)(blockIdx.x % CLUSTER);
+    const int64_t row = blockIdx.x / CLUSTER;
+    const float *rowp = logits + row * ldl;
+    const float4 *rowv = reinterpret_cast<const float4 *>(rowp);
+    const int64_t nv = V >> 2;  // whole float4s in the row
+    const int64_t per = (nv + CLUSTER - 1) / CLUSTER;
+    const int64_t v_begin = min(nv, (int64_t)rank * per);
+    const int64_t v_end = min(nv, v_begin + per);
+
+    if constexpr (CLUSTER > 1) {
+        // every CTA of the cluster must be running before the distributed-shared-memory stores below
+        asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    }
+
+    RowState st{-INFINITY, 0x7fffffff, 0.0f, 0.0f};
+    for (int64_t b = v_begin + threadIdx.x; b < v_end; b += (int64_t)kStatsThreads * kStatsVec) {
+        float x[4 * kStatsVec];
+        int base[kStatsVec];
+#pragma unroll
+        for (int k = 0; k < kStatsVec; ++k) {
+            const int64_t vi = b + (int64_t)k * kStatsThreads;
+            base[k] = (int)vi;
+            float4 v = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            if (vi < v_end) v = ld_stream(rowv + vi);
+            x[4 * k + 0] = v.x;
+            x[4 * k + 1] = v.y;
+            x[4 * k + 2] = v.z;
+            x[4 * k + 3] = v.w;
+        }
+        absorb<4 * kStatsVec>(st, x, base);
+    }
+    // ragged tail (V % 4 entries), taken by the last piece's first thread
+    if (rank == CLUSTER - 1 && threadIdx.x == 0 && (V & 3)) {
+        float x[4];
+        int base[1] = {(int)nv};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) x[c] = (4 * nv + c < V) ? rowp[4 * nv + c] : -INFINITY;
+        absorb<4>(st, x, base);
+    }
+
+    // warp, then CTA
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        RowState o = shfl_down(st, off);
+        merge(st, o);
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) warp_state[warp] = st;
+    __syncthreads();
+    if (warp == 0) {
+        st = (lane < kStatsThreads / 32) ? warp_state[lane]
+                                         : RowState{-INFINITY, 0x7fffffff, 0.0f, 0.0f};
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            RowState o = shfl_down(st, off);
+            merge(st, o);
+        }
+    }
+
+    // cluster: every CTA posts its state into the leader's shared memory
+    if constexpr (CLUSTER > 1) {
+        cg::cluster_group cluster = cg::this_cluster();
+        asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+        if (threadIdx.x == 0) {
+            RowState *dst = cluster.map_shared_rank(cta_state, 0);
+            dst[rank] = st;
+        }
+        cluster.sync();
+        if (rank != 0) return;
+        if (threadIdx.x == 0) {
+            st = cta_state[0];
+#pragma unroll
+            for (int r = 1; r < CLUSTER; ++r) merge(st, cta_state[r]);
+        }
+    }
+
+    if (threadIdx.x == 0) {
+        float lse, H, kappa;
+        int a = st.a;
+        if (st.m == -INFINITY) {
+            lse = H = kappa = __int_as_float(0x7fc00000);
+            a = 0;
+        } else {
+            const float lnZ = log1pf(st.rest);
+            lse = st.m + lnZ;
+            H = lnZ - st.t / (1.0f + st.rest);
+            kappa = lnZ;
+        }
+        if (out_m) out_m[row] = st.m;
+        if (out_lse) out_lse[row] = lse;
+        if (out_H) out_H[row] = H;
+        if (out_kappa) out_kappa[row] = kappa;
+        if (out_argmax) out_argmax[row] = a;
+    }
+}
+
+template <int CLUSTER>
+cudaError_t launch_stats(const float *logits, int64_t R, int64_t V, int64_t ldl, float *m, float *lse,
+                         float *H, float *kappa, int32_t *argmax, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(R * CLUSTER), 1, 1);
+    cfg.blockDim = dim3(kStatsThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, row_stats_kernel<CLUSTER>, logits, V, ldl, m, lse, H, kappa, argmax);
+}
+
+}  // namespace
+
+int stats_cluster_size(int64_t V) {
+    // about 16K entries (64 KiB) or more per CTA; at most 8 CTAs (the portable cluster limit)
+    int c = 1;
+    while (c < 8 && V / (c * 2) >= 16384) c *= 2;
+    return c;
+}
+
+cudaError_t launch_row_stats(const float *logits, int64_t R, int64_t V, int64_t ldl, float *m, float *lse,
+                             float *H, float *kappa, int32_t *argmax, cudaStream_t stream) {
+    switch (stats_cluster_size(V)) {
+        case 1: return launch_stats<1>(logits, R, V, ldl, m, lse, H, kappa, argmax, stream);
+        case 2: return launch_stats<2>(logits, R, V, ldl, m, lse, H, kappa, argmax, stream);
+        case 4: return launch_stats<4>(logits, R, V, ldl, m, lse, H, kappa, argmax, stream);
+        default: return launch_stats<8>(logits, R, V, ldl, m, lse, H, kappa, argmax, stream);
+    }
+}
+
+}  // namespace dg

@@ -1,0 +1,75 @@
+"""A resident sampler step: device buffers for one workload shape, and the two ways to
+run it (inputs already on the device, or inputs copied from pinned host memory and
+results copied back, all on one stream).
+
+PyTorch only provides the memory and the stream; each step is one call of
+dg_sampler_step in libdgsamp.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+
+class SamplerStep:
+    """Owns the embedding table W (bf16, resident), the workspace and the outputs."""
+
+    def __init__(self, W: torch.Tensor, n_req: int, L_c: int, V: int, gamma: float,
+                 vocab_start: int = 0, vocab_end: int | None = None, min_accept: int = 0,
+                 device: str | torch.device = "cuda"):
+        self.device = torch.device(device)
+        self.W = W
+        self.n_req, self.L_c, self.V = n_req, L_c, V
+        self.R = n_req * L_c
+        self.d = W.shape[1]
+        self.gamma = float(gamma)
+        self.vocab_start = vocab_start
+        self.vocab_end = V if vocab_end is None else vocab_end
+        self.min_accept = min_accept
+        R, d, dev = self.R, self.d, self.device
+        self.out = {k: torch.empty(R, dtype=torch.float32, device=dev) for k in ("m", "lse", "H", "kappa")}
+        self.out.update(argmax=torch.empty(R, dtype=torch.int32, device=dev),
+                        order=torch.empty(R, dtype=torch.int32, device=dev),
+                        mask=torch.empty(R, dtype=torch.uint8, device=dev),
+                        n_accepted=torch.empty(n_req, dtype=torch.int32, device=dev),
+                        E=torch.empty((R, d), dtype=torch.float32, device=dev))
+        self.ws = B.workspace(R, max(1, self.vocab_end - self.vocab_start), d, dev)
+        self.logits_dev = None
+        self.budgets_dev = torch.empty(n_req, dtype=torch.float32, device=dev)
+
+    # -- device-resident inputs
+    def __call__(self, logits: torch.Tensor, budgets: torch.Tensor, stream=None) -> dict:
+        return B.dg_sampler_step(logits, self.n_req, self.L_c, self.W, self.gamma, budgets,
+                                 min_accept=self.min_accept, vocab_start=self.vocab_start,
+                                 vocab_end=self.vocab_end, V=self.V, out=self.out, ws=self.ws,
+                                 stream=stream)
+
+    # -- host inputs and results
+    def host_buffers(self, ldl: int | None = None) -> dict:
+        """Pinned host tensors for the inputs and results of run_from_host()."""
+        ldl = self.V if ldl is None else ldl
+        h = {"logits": torch.empty((self.R, ldl), dtype=torch.float32, pin_memory=True),
+             "budgets": torch.empty(self.n_req, dtype=torch.float32, pin_memory=True)}
+        for k, v in self.out.items():
+            h["out_" + k] = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+        if self.logits_dev is None or self.logits_dev.shape != h["logits"].shape:
+            self.logits_dev = torch.empty(h["logits"].shape, dtype=torch.float32, device=self.device)
+        return h
+
+    def run_from_host(self, h: dict, stream=None) -> None:
+        """H2D of logits and budgets, one step, D2H of every result; asynchronous on `stream`."""
+        s = torch.cuda.current_stream(self.device) if stream is None else stream
+        with torch.cuda.stream(s):
+            self.logits_dev.copy_(h["logits"], non_blocking=True)
+            self.budgets_dev.copy_(h["budgets"], non_blocking=True)
+            self(self.logits_dev, self.budgets_dev, stream=s)
+            for k, v in self.out.items():
+                h["out_" + k].copy_(v, non_blocking=True)
+
+    @staticmethod
+    def h2d_bytes(h: dict) -> int:
+        return h["logits"].numel() * 4 + h["budgets"].numel() * 4
+
+    def d2h_bytes(self) -> int:
+        return sum(v.numel() * v.element_size() for v in self.out.values())

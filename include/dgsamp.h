@@ -1,0 +1,189 @@
+/*
+ * dgsamp: the DiffusionGemma denoising-sampler step on one NVIDIA GB300 (sm_103a).
+ *
+ * One sampler step, per canvas position (row) of logits over the full vocabulary:
+ *   - softmax statistics: max, log-sum-exp, entropy, argmax candidate, confidence;
+ *   - entropy-bound acceptance per request: positions ordered from most to least
+ *     confident, accepted until the running entropy would pass the budget;
+ *   - the self-conditioning soft embedding E = gamma * softmax(logits)[:, s:e] @ W_shard,
+ *     the probability-weighted mean of the token-embedding rows over a vocabulary slice.
+ *
+ * Sources (the pages this library restates):
+ *   [P1] calvarado04.com, post on the vLLM change that makes DiffusionGemma
+ *        self-conditioning work under tensor parallelism: eq. e^sc (the expected
+ *        embedding p_i W), "The fix" (the vocabulary-partition identity, the sliced
+ *        product, the sum over ranks, gamma applied after it, org_vocab_start/end
+ *        bounds that keep padded shard rows out), "Why not just all-gather the weights".
+ *   [P2] agentlenshq.com, "DiffusionGemma: vLLMでネイティブにサポートされた初のDiffusion LLM",
+ *        section "サンプリングループとエントロピー境界デノイジング" (candidates at every
+ *        position, the entropy-bound acceptance rule) and "安定性のための自己条件付け"
+ *        (the full softmax distribution feeds the probability-weighted mean embedding).
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers owned by the caller unless stated otherwise.  The
+ *     library never allocates device memory, never frees, and never synchronises
+ *     inside a call (dg_get_device_status is the one exception and says so).
+ *   - Work is queued asynchronously on `stream` (NULL = the legacy default stream);
+ *     outputs are valid once the stream has reached the call.
+ *   - Matrices are row-major with a leading dimension (elements between rows).
+ *   - Logits are fp32; the embedding table is bfloat16, passed as its 16-bit patterns.
+ *   - Arguments are checked on the host before any launch: a bad argument returns
+ *     DG_ERR_INVALID_ARG or DG_ERR_UNSUPPORTED and queues nothing.  A CUDA launch
+ *     error returns DG_ERR_CUDA.  dg_last_error() describes the last failure of the
+ *     calling thread.
+ *   - A kernel that waits on an in-kernel barrier gives up after about a second,
+ *     records DG_ERR_TIMEOUT in a device word and returns; dg_get_device_status()
+ *     reports and clears it.
+ */
+#ifndef DGSAMP_H
+#define DGSAMP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t. */
+typedef struct CUstream_st *dg_stream_t;
+
+typedef enum dg_status {
+    DG_OK = 0,
+    DG_ERR_INVALID_ARG = 1,  /* null pointer, negative size, inconsistent bounds */
+    DG_ERR_UNSUPPORTED = 2,  /* well-formed but outside what the kernels handle (alignment, L_c > 1024) */
+    DG_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    DG_ERR_TIMEOUT = 4       /* a device-side wait gave up (reported by dg_get_device_status) */
+} dg_status;
+
+/* Library version, major*10000 + minor*100 + patch. */
+int dg_version(void);
+
+/* Text of the last failure on the calling thread ("" if none).  Owned by the library. */
+const char *dg_last_error(void);
+
+/*
+ * Row statistics ([P1] eq. e^sc: p_i is a softmax over all V entries; [P2] sampling loop:
+ * a candidate and an entropy at every position).
+ *
+ *   logits  [R, ldl] fp32, ldl >= V.  Row i holds l_{i,0..V-1}.
+ *   m       [R] fp32   m_i = max_v l_{i,v}
+ *   lse     [R] fp32   lse_i = m_i + ln Z_i,  Z_i = sum_v exp(l_{i,v} - m_i)
+ *   H       [R] fp32   entropy -sum_v p ln p in nats, p_{i,v} = exp(l_{i,v} - lse_i)
+ *   kappa   [R] fp32   -ln(confidence) = ln Z_i, where confidence = p_{i,argmax};
+ *                      computed as log1p of the sum over the non-argmax entries, so
+ *                      rows near one-hot keep distinct values (small kappa = confident)
+ *   argmax  [R] int32  the smallest index attaining m_i (the candidate token)
+ * Any output pointer may be NULL to skip it.
+ * -inf logits are allowed (masked vocabulary: probability 0).  A row that is all
+ * -inf gives NaN statistics and argmax 0.  NaN logits are undefined.
+ * Requires: logits 16-byte aligned, ldl % 4 == 0 (else DG_ERR_UNSUPPORTED); V >= 1.
+ * R == 0 queues nothing.
+ */
+dg_status dg_row_stats(const float *logits, int64_t R, int64_t V, int64_t ldl,
+                       float *m, float *lse, float *H, float *kappa, int32_t *argmax,
+                       dg_stream_t stream);
+
+/*
+ * Bytes of device workspace dg_soft_embed (and dg_sampler_step) needs for R rows, a
+ * vocabulary slice of vocab_len entries and hidden size d on the current device.
+ * Returns 0 for an invalid shape or when no device is present.
+ */
+size_t dg_soft_embed_workspace_size(int64_t R, int64_t vocab_len, int64_t d);
+
+/*
+ * Self-conditioning soft embedding over the vocabulary slice [vocab_start, vocab_end)
+ * ([P1] eq. e^sc and "The fix": S = P[:, s:e] W_shard[0:e-s], E = gamma * S).
+ *
+ *   logits     [R, ldl] fp32, the FULL-width logits (columns [vocab_start, vocab_end) are read)
+ *   lse        [R] fp32, the full-vocabulary log-sum-exp from dg_row_stats.  The
+ *              probabilities are exp(l - lse): never renormalised inside the slice.
+ *   W_shard    [rows_pad, ldw] bf16 bit patterns; row j is vocabulary entry vocab_start + j.
+ *              Only rows [0, vocab_end - vocab_start) are read: padding rows after
+ *              them are never touched (they may hold anything, NaN included).
+ *   gamma      the normaliser, applied once after the sum (pass 1 for a partial that
+ *              will be summed with other slices first)
+ *   out        [R, ldo] fp32 result E
+ *   workspace  device scratch of at least dg_soft_embed_workspace_size(R, e - s, d)
+ *              bytes, 16-byte aligned, owned by the caller; its contents on entry do
+ *              not matter.
+ * The probabilities are rounded to bfloat16 before the product (the pages cast them
+ * to the embedding dtype); the product accumulates in fp32 and the split-K partial
+ * sums are added in a fixed order, so the result is bitwise reproducible.
+ * Errors: vocab_end - vocab_start > rows_pad, a negative or reversed slice, or a
+ * slice past ldl are DG_ERR_INVALID_ARG (the contraction-length mismatch the pages
+ * report becomes an error instead of a crash).  logits/W_shard not 16-byte aligned,
+ * ldl % 4 != 0 or ldw % 8 != 0 are DG_ERR_UNSUPPORTED.  An empty slice writes zeros.
+ */
+dg_status dg_soft_embed(const float *logits, int64_t ldl, const float *lse, int64_t R,
+                        int64_t vocab_start, int64_t vocab_end,
+                        const uint16_t *W_shard, int64_t rows_pad, int64_t ldw, int64_t d,
+                        float gamma, float *out, int64_t ldo,
+                        void *workspace, size_t workspace_bytes, dg_stream_t stream);
+
+/*
+ * Entropy-bound acceptance ([P2] sampling loop: tokens are kept from most to least
+ * confident until the cumulative entropy would exceed a fixed budget).
+ *
+ *   H, kappa    [n_req * L_c] fp32 from dg_row_stats; rows q*L_c .. q*L_c+L_c-1 are request q
+ *   budgets     [n_req] fp32, nats
+ *   min_accept  accept at least min(min_accept, L_c) positions per request (0 = the literal rule)
+ *   order       [n_req * L_c] int32: order[q*L_c + j] = the position (0..L_c-1) that is
+ *               j-th most confident (kappa ascending; equal kappa: lower position first)
+ *   mask        [n_req * L_c] uint8: 1 where the position is accepted
+ *   n_accepted  [n_req] int32: n = max{k : H[order_1] + ... + H[order_k] <= B_q}, taken
+ *               as a prefix (the first position that would pass the budget stops it),
+ *               then raised to min_accept.  The running sum is kept in fp64.
+ * Requires 1 <= L_c <= 1024 (else DG_ERR_UNSUPPORTED), n_req >= 0, min_accept >= 0.
+ * A position with NaN statistics (an all -inf row) sorts last and stops the running sum.
+ */
+dg_status dg_entropy_accept(const float *H, const float *kappa, int32_t n_req, int32_t L_c,
+                            const float *budgets, int32_t min_accept,
+                            int32_t *order, uint8_t *mask, int32_t *n_accepted,
+                            dg_stream_t stream);
+
+/*
+ * Sum of per-slice partial products on one device: out = gamma * (S_0 + ... + S_{T-1}),
+ * added in index order in fp32 ([P1] "The fix": E = gamma * sum_r S^(r); here the T
+ * partials sit on one GPU, so the sum is a kernel, not a collective).
+ *
+ *   partials  HOST array of T device pointers, each [R, ldp] fp32
+ *   out       [R, ldo] fp32 (may alias partials[0] only if ldo == ldp)
+ * Requires 1 <= T <= 16.
+ */
+dg_status dg_sum_partials(const float *const *partials, int32_t T, int64_t R, int64_t d,
+                          int64_t ldp, float gamma, float *out, int64_t ldo,
+                          dg_stream_t stream);
+
+/*
+ * One fused sampler step on one stream: row statistics, then acceptance and the soft
+ * embedding over the slice [vocab_start, vocab_end) (pass 0 and V for the whole
+ * vocabulary, W then being the full table with rows_pad >= V).
+ *
+ *   logits [n_req*L_c, ldl] fp32; W [rows_pad, ldw] bf16 bits; budgets [n_req] fp32
+ *   outputs: m, lse, H, kappa [R] fp32; argmax [R] int32; order [R] int32; mask [R] uint8;
+ *            n_accepted [n_req] int32; E [R, ldo] fp32
+ *   workspace  >= dg_soft_embed_workspace_size(R, vocab_end - vocab_start, d) bytes
+ * All output pointers are required.  The argument rules of the three calls above apply.
+ */
+dg_status dg_sampler_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, int64_t ldl,
+                          const uint16_t *W, int64_t vocab_start, int64_t vocab_end,
+                          int64_t rows_pad, int64_t ldw, int64_t d, float gamma,
+                          const float *budgets, int32_t min_accept,
+                          float *m, float *lse, float *H, float *kappa, int32_t *argmax,
+                          int32_t *order, uint8_t *mask, int32_t *n_accepted,
+                          float *E, int64_t ldo,
+                          void *workspace, size_t workspace_bytes, dg_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reports (and clears) the device-side error word:
+ * DG_ERR_TIMEOUT if a kernel gave up waiting since the last call, DG_ERR_CUDA if
+ * the stream reports a CUDA error, else DG_OK.  This call blocks the host.
+ */
+dg_status dg_get_device_status(dg_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DGSAMP_H */

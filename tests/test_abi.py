@@ -1,0 +1,105 @@
+"""The C-ABI library: it builds, loads, exports every declared entry point, and rejects
+bad arguments on the host before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dgsamp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from denoising_sampler_step_gb300 import build
+    build.build()
+    from denoising_sampler_step_gb300 import binding
+    return binding
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dg_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for n in ["dg_row_stats", "dg_soft_embed", "dg_entropy_accept", "dg_sum_partials", "dg_sampler_step",
+              "dg_soft_embed_workspace_size", "dg_get_device_status", "dg_last_error", "dg_version"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    so = ctypes.CDLL(lib.LIB_PATH)
+    for n in declared_symbols():
+        assert hasattr(so, n), n
+
+
+def test_python_binding_names_match_c(lib):
+    for n in declared_symbols():
+        if n in ("dg_last_error", "dg_version"):
+            continue
+        assert callable(getattr(lib, n)), n
+
+
+def test_version(lib):
+    assert lib.lib.dg_version() == 100
+
+
+def test_row_stats_rejects_bad_arguments(lib):
+    L = lib.lib
+    assert L.dg_row_stats(None, 4, 16, 16, None, None, None, None, None, None) == 1
+    assert L.dg_row_stats(ctypes.c_void_p(16), 4, 0, 16, None, None, None, None, None, None) == 1
+    assert L.dg_row_stats(ctypes.c_void_p(16), 4, 32, 16, None, None, None, None, None, None) == 1
+    # misaligned base or leading dimension
+    assert L.dg_row_stats(ctypes.c_void_p(20), 4, 16, 16, None, None, None, None, None, None) == 2
+    assert L.dg_row_stats(ctypes.c_void_p(16), 4, 15, 15, None, None, None, None, None, None) == 2
+    assert b"16-byte" in L.dg_last_error()
+    # nothing to do: no launch, no error
+    assert L.dg_row_stats(None, 0, 16, 16, None, None, None, None, None, None) == 0
+
+
+def test_accept_rejects_bad_arguments(lib):
+    L = lib.lib
+    p = ctypes.c_void_p(256)
+    assert L.dg_entropy_accept(p, p, 1, 1025, p, 0, p, p, p, None) == 2
+    assert L.dg_entropy_accept(p, p, 1, 0, p, 0, p, p, p, None) == 1
+    assert L.dg_entropy_accept(p, p, -1, 16, p, 0, p, p, p, None) == 1
+    assert L.dg_entropy_accept(p, p, 1, 16, p, -1, p, p, p, None) == 1
+    assert L.dg_entropy_accept(None, p, 1, 16, p, 0, p, p, p, None) == 1
+    assert L.dg_entropy_accept(None, None, 0, 16, None, 0, None, None, None, None) == 0
+
+
+def test_soft_embed_rejects_the_contraction_mismatch(lib):
+    """The pages' crash: a slice of e-s vocabulary entries against a shard with fewer
+    rows.  The library answers with an error instead of reading out of range."""
+    L = lib.lib
+    p = ctypes.c_void_p(256)
+    # 262144 probabilities against a 65536-row shard
+    st = L.dg_soft_embed(p, 262144, p, 256, 0, 262144, p, 65536, 2816, 2816, 53.0, p, 2816, p, 1 << 30, None)
+    assert st == 1 and b"shard" in L.dg_last_error()
+    assert L.dg_soft_embed(p, 4096, p, 16, 100, 50, p, 4096, 256, 256, 1.0, p, 256, p, 1 << 20, None) == 1
+    assert L.dg_soft_embed(p, 4096, p, 16, 0, 5000, p, 8192, 256, 256, 1.0, p, 256, p, 1 << 20, None) == 1
+    assert L.dg_soft_embed(p, 4096, p, 16, 0, 4096, p, 4096, 100, 256, 1.0, p, 256, p, 1 << 20, None) == 1
+    # unaligned W leading dimension / logits leading dimension
+    assert L.dg_soft_embed(p, 4096, p, 16, 0, 4096, p, 4096, 260, 258, 1.0, p, 258, p, 1 << 20, None) == 2
+    assert L.dg_soft_embed(p, 4097, p, 16, 0, 4096, p, 4096, 256, 256, 1.0, p, 256, p, 1 << 20, None) == 2
+
+
+def test_sum_partials_rejects_bad_arguments(lib):
+    L = lib.lib
+    arr = (ctypes.c_void_p * 17)(*([256] * 17))
+    assert L.dg_sum_partials(arr, 0, 4, 4, 4, 1.0, ctypes.c_void_p(256), 4, None) == 1
+    assert L.dg_sum_partials(arr, 17, 4, 4, 4, 1.0, ctypes.c_void_p(256), 4, None) == 1
+    arr2 = (ctypes.c_void_p * 2)(256, None)
+    assert L.dg_sum_partials(arr2, 2, 4, 4, 4, 1.0, ctypes.c_void_p(256), 4, None) == 1
+
+
+def test_step_checks_slice_against_vocabulary(lib):
+    L = lib.lib
+    p = ctypes.c_void_p(256)
+    st = L.dg_sampler_step(p, 1, 16, 4096, 4096, p, 0, 8192, 8192, 256, 256, 16.0, p, 0,
+                           p, p, p, p, p, p, p, p, p, 256, p, 1 << 20, None)
+    assert st == 1
