@@ -33,6 +33,8 @@ lib.dg_soft_embed_workspace_size.argtypes = [_i64, _i64, _i64]
 lib.dg_soft_embed_workspace_size.restype = _sz
 lib.dg_soft_embed.argtypes = [_p, _i64, _p, _i64, _i64, _i64, _p, _i64, _i64, _i64, _f32, _p, _i64, _p, _sz, _p]
 lib.dg_soft_embed.restype = ctypes.c_int
+lib.dg_soft_embed_no_alloc.argtypes = [_p, _i64, _p, _i64, _i64, _i64, _p, _i64, _i64, _i64, _f32, _p, _i64, _p]
+lib.dg_soft_embed_no_alloc.restype = ctypes.c_int
 lib.dg_entropy_accept.argtypes = [_p, _p, _i32, _i32, _p, _i32, _p, _p, _p, _p]
 lib.dg_entropy_accept.restype = ctypes.c_int
 lib.dg_sum_partials.argtypes = [ctypes.POINTER(_p), _i32, _i64, _i64, _i64, _f32, _p, _i64, _p]
@@ -116,6 +118,19 @@ def dg_soft_embed(logits: torch.Tensor, lse: torch.Tensor, vocab_start: int, voc
     _check(lib.dg_soft_embed(_ptr(logits), _ld(logits), _ptr(lse), R, vocab_start, vocab_end, _ptr(W_shard),
                              W_shard.shape[0], _ld(W_shard), d, gamma, _ptr(out), _ld(out), _ptr(ws), ws.numel(),
                              _stream(stream)), "dg_soft_embed")
+    return out
+
+
+def dg_soft_embed_no_alloc(logits: torch.Tensor, lse: torch.Tensor, vocab_start: int, vocab_end: int,
+                           W_shard: torch.Tensor, gamma: float, out: torch.Tensor, stream=None,
+                           R: int | None = None) -> torch.Tensor:
+    """dg_soft_embed without a workspace: the library's fixed scratch array holds the
+    partial tiles.  `out` [R, >=d] fp32 must be given; nothing is allocated."""
+    R = logits.shape[0] if R is None else R
+    d = W_shard.shape[1]
+    _check(lib.dg_soft_embed_no_alloc(_ptr(logits), _ld(logits), _ptr(lse), R, vocab_start, vocab_end,
+                                      _ptr(W_shard), W_shard.shape[0], _ld(W_shard), d, gamma, _ptr(out), _ld(out),
+                                      _stream(stream)), "dg_soft_embed_no_alloc")
     return out
 
 

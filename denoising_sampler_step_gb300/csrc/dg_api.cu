@@ -14,8 +14,6 @@ namespace dg {
 
 __device__ unsigned int g_device_error = 0;
 
-namespace {
-
 thread_local char t_last_error[512] = "";
 
 dg_status fail(dg_status st, const char *fmt, ...) {
@@ -31,6 +29,8 @@ dg_status cuda_fail(cudaError_t e, const char *what) {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+namespace {
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
@@ -54,6 +54,8 @@ dg_status check_accept_args(const float *H, const float *kappa, int32_t n_req, i
         return fail(DG_ERR_INVALID_ARG, "accept: a pointer is NULL");
     return DG_OK;
 }
+
+}  // namespace
 
 dg_status check_embed_args(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t s, int64_t e,
                            const uint16_t *W, int64_t rows_pad, int64_t ldw, int64_t d, const float *out,
@@ -81,6 +83,8 @@ dg_status check_embed_args(const float *logits, int64_t ldl, const float *lse, i
     }
     return DG_OK;
 }
+
+namespace {
 
 dg_status run_soft_embed(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t s, int64_t e,
                          const uint16_t *W, int64_t ldw, int64_t d, float gamma, float *out, int64_t ldo,

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/dgsamp.h"
+
 namespace dg {
 
 int stats_cluster_size(int64_t V);
@@ -38,5 +40,15 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
                               const SoftEmbedPlan &plan, cudaStream_t stream, const char **msg);
 
 int device_sm_count();
+
+// Shared by the C entry points: the calling thread's error text, fail() sets it and
+// returns st; check_embed_args() holds the argument rules of dg_soft_embed.
+extern thread_local char t_last_error[512];
+dg_status fail(dg_status st, const char *fmt, ...);
+dg_status cuda_fail(cudaError_t e, const char *what);
+bool aligned16(const void *p);
+dg_status check_embed_args(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t s, int64_t e,
+                           const uint16_t *W, int64_t rows_pad, int64_t ldw, int64_t d, const float *out,
+                           int64_t ldo);
 
 }  // namespace dg

@@ -122,6 +122,31 @@ dg_status dg_soft_embed(const float *logits, int64_t ldl, const float *lse, int6
                         void *workspace, size_t workspace_bytes, dg_stream_t stream);
 
 /*
+ * dg_soft_embed for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this call: it exists for code that is handed only its input and
+ * output buffers (a plugin inside another framework's memory pool, a server under
+ * a fixed memory budget that must not allocate once it is running) and so cannot
+ * supply the workspace dg_soft_embed asks for.
+ *
+ * Same arguments, results and errors as dg_soft_embed, without the workspace: the
+ * split-K partial tiles go to a 16 MiB array compiled into the library, which every
+ * GPU that loads the library holds until the process exits.  The call allocates
+ * and frees nothing.  A shape whose output, padded to whole tiles and held in fp32,
+ * needs more than 16 MiB even with one vocabulary split (about 4 Mi entries: R = 1024
+ * at d = 2816 fits, R = 8192 does not) returns
+ * DG_ERR_UNSUPPORTED.  Results match dg_soft_embed within the soft-embedding
+ * tolerance; the number of splits (hence the order of the additions) may differ.
+ * The array is shared by every call on a device and keeps the last call's data;
+ * calls whose kernels may overlap on the GPU race on it, so order them on one
+ * stream.  The first call on each device looks up the array's device address with
+ * that device current: make it before any stream capture.
+ */
+dg_status dg_soft_embed_no_alloc(const float *logits, int64_t ldl, const float *lse, int64_t R,
+                                 int64_t vocab_start, int64_t vocab_end,
+                                 const uint16_t *W_shard, int64_t rows_pad, int64_t ldw, int64_t d,
+                                 float gamma, float *out, int64_t ldo, dg_stream_t stream);
+
+/*
  * Entropy-bound acceptance ([P2] sampling loop: tokens are kept from most to least
  * confident until the cumulative entropy would exceed a fixed budget).
  *
