@@ -8,7 +8,8 @@
 // Design (HBM-bound: every logit is read once, 4 bytes per vocabulary entry):
 //   - one thread-block cluster per row; the row is cut into CLUSTER contiguous
 //     pieces, one per CTA;
-//   - 128-bit read-only loads, coalesced, several in flight per thread per batch;
+//   - 128-bit read-only loads, coalesced; each thread keeps two batches of four in
+//     flight (the next batch loads while the current one is folded in);
 //   - each thread keeps an online state (m, a, rest, t) over the entries it saw:
 //       m    = running max, a = index of its first occurrence,
 //       rest = sum over the entries other than a of exp(l - m),
@@ -134,21 +135,36 @@ __global__ void __launch_bounds__(kStatsThreads, 4)
     }
 
     RowState st{-INFINITY, 0x7fffffff, 0.0f, 0.0f};
-    for (int64_t b = v_begin + threadIdx.x; b < v_end; b += (int64_t)kStatsThreads * kStatsVec) {
+    // software pipeline: the next batch's loads are in flight while this batch is folded in
+    constexpr int64_t kStep = (int64_t)kStatsThreads * kStatsVec;
+    float4 cur[kStatsVec], nxt[kStatsVec];
+    auto load_batch = [&](int64_t b, float4 (&v)[kStatsVec]) {
+#pragma unroll
+        for (int k = 0; k < kStatsVec; ++k) {
+            const int64_t vi = b + (int64_t)k * kStatsThreads;
+            v[k] = (vi < v_end) ? ld_stream(rowv + vi) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+    };
+    int64_t b = v_begin + threadIdx.x;
+    if (b < v_end) load_batch(b, cur);
+    for (; b < v_end; b += kStep) {
+        const bool more = b + kStep < v_end;
+        if (more) load_batch(b + kStep, nxt);
         float x[4 * kStatsVec];
         int base[kStatsVec];
 #pragma unroll
         for (int k = 0; k < kStatsVec; ++k) {
-            const int64_t vi = b + (int64_t)k * kStatsThreads;
-            base[k] = (int)vi;
-            float4 v = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            if (vi < v_end) v = ld_stream(rowv + vi);
-            x[4 * k + 0] = v.x;
-            x[4 * k + 1] = v.y;
-            x[4 * k + 2] = v.z;
-            x[4 * k + 3] = v.w;
+            base[k] = (int)(b + (int64_t)k * kStatsThreads);
+            x[4 * k + 0] = cur[k].x;
+            x[4 * k + 1] = cur[k].y;
+            x[4 * k + 2] = cur[k].z;
+            x[4 * k + 3] = cur[k].w;
         }
         absorb<4 * kStatsVec>(st, x, base);
+        if (more) {
+#pragma unroll
+            for (int k = 0; k < kStatsVec; ++k) cur[k] = nxt[k];
+        }
     }
     // ragged tail (V % 4 entries), taken by the last piece's first thread
     if (rank == CLUSTER - 1 && threadIdx.x == 0 && (V & 3)) {

@@ -6,25 +6,33 @@
 // rows, the probabilities cast to the embedding dtype, gamma applied after the sum;
 // padded shard rows are never part of the product).
 //
-// Kernel design (one dense contraction on the 5th-generation tensor cores):
-//   - a CTA owns an output tile of 128 rows x 256 columns and one contiguous range of
-//     vocabulary blocks (split-K); the fp32 accumulator lives in tensor memory (256
-//     TMEM columns);
-//   - warp 0 streams, per 32-entry vocabulary block, the logits tile [128 x 32] fp32
-//     and the W tile [32 x 256] bf16 into shared memory with TMA (128-byte swizzle);
-//   - warps 2..5 turn the logits tile into the bf16 A operand, exp2(l*log2e - lse*log2e)
-//     rounded to nearest even, written in the K-major 64-byte-swizzled layout the
-//     tensor core reads; probabilities never go to global memory;
-//   - warp 1 issues tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32), W being the
-//     N-major B operand straight from the TMA tile; tcgen05.commit frees the stage;
-//   - after the last block the same four warps read the accumulator back with
-//     tcgen05.ld and store the partial tile; a second kernel adds the split partials
-//     in split order, multiplies by gamma and writes E (deterministic).
+// Kernel design (the one dense contraction of the step, on the tcgen05 tensor cores):
+//   - a cluster of two CTAs owns 256 output rows (128 each) x up to 512 output
+//     columns and one contiguous range of 32-entry vocabulary blocks (split-K over
+//     the vocabulary); each CTA's fp32 accumulator fills its 512 TMEM columns;
+//   - per block, each CTA's warp 0 loads its logits tile [128 x 32] fp32 by TMA and
+//     half of the W tile [32 x 512] bf16 by TMA multicast into both CTAs, so every W
+//     byte leaves L2 once per cluster;
+//   - warps 2..5 turn the logits tile into the bf16 A operand,
+//     exp2(l*log2e - lse*log2e) rounded to nearest even, in the K-major 64-byte-swizzled
+//     layout; the probabilities never go to global memory;
+//   - warp 1 issues tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32) for the two
+//     256-column halves; tcgen05.commit, multicast to both CTAs, frees the stage once
+//     both have consumed it;
+//   - the same four warps then read the accumulator with tcgen05.ld and store the
+//     partial tile; splitk_reduce_kernel adds the split partials in split order,
+//     multiplies by gamma and writes E (bitwise reproducible).
+//   A column tail of 256 or fewer (d = 2816 = 5 x 512 + 256) is a half-width tile with
+//   4/3 of the vocabulary range per split, so all clusters carry similar work.
+//   The TMA thread also pulls the tiles PREFETCH blocks ahead into L2 (no shared memory
+//   used), and W loads mark their lines evict-first, which keeps the logits (read by
+//   every column tile of a row block) in L2.
 //   Every barrier wait is bounded (about a second); a wait that gives up records
 //   DG_ERR_TIMEOUT, drains what is in flight and leaves the kernel.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "dg_common.cuh"
@@ -34,31 +42,38 @@ namespace dg {
 
 namespace {
 
-constexpr int BM = 128;          // rows per tile (TMEM lanes)
-constexpr int BN = 256;          // output columns per tile (one MMA N)
+constexpr int BM = 128;          // rows per CTA (TMEM lanes)
+constexpr int BN = 512;          // output columns per cluster tile (two MMAs of N = 256)
 constexpr int BK = 32;           // vocabulary entries per stage
-constexpr int STAGES = 5;
+constexpr int STAGES = 4;
 constexpr int THREADS = 192;     // warp 0: TMA, warp 1: MMA, warps 2..5: A producers + epilogue
-constexpr int TMEM_COLS = 256;
+constexpr int TMEM_COLS = 512;
+constexpr uint16_t kPairMask = 0x3;
+constexpr int PREFETCH = 8;      // vocabulary blocks pulled into L2 ahead of their TMA loads
 
-constexpr int L_BYTES = BM * BK * 4;   // logits tile, rows of 128 B (128-byte swizzle)
-constexpr int W_BOX_BYTES = BK * 64 * 2;
-constexpr int W_BYTES = BK * BN * 2;   // 4 TMA boxes of [32 rows x 64 columns]
-constexpr int A_BYTES = BM * BK * 2;   // bf16 probabilities, rows of 64 B (64-byte swizzle)
+constexpr int L_BYTES = BM * BK * 4;      // logits tile, rows of 128 B (128-byte swizzle)
+constexpr int W_BOX_BYTES = BK * 64 * 2;  // one TMA box: 32 rows x 64 columns
+constexpr int W_HALF_BYTES = 4 * W_BOX_BYTES;
+constexpr int W_BYTES = BK * BN * 2;      // up to 8 boxes
+constexpr int A_BYTES = BM * BK * 2;      // bf16 probabilities, rows of 64 B (64-byte swizzle)
 constexpr int STAGE_BYTES = L_BYTES + W_BYTES + A_BYTES;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
 static_assert(L_BYTES % 1024 == 0 && W_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "1 KiB alignment");
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 
 struct Params {
     const float *lse;
-    float *ws;           // partial tiles
+    float *ws;           // partial tiles [split][m_tile][n_tile][BN/4][BM][4]
     int64_t k_begin;     // first vocabulary column of block 0 (multiple of 4)
     int64_t vocab_start;
     int64_t vocab_end;
     int64_t nkb;
     int R;
-    int m_tiles, n_tiles, splits;
+    int m_tiles, n_tiles;
+    int n_full;          // n-tiles of full width (two halves)
+    int tail_halves;     // 1 if the last n-tile is 256 wide or less, else 0
+    int splits, tail_splits;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -73,30 +88,50 @@ __global__ void __launch_bounds__(THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
-    uint64_t *full_tma = bars;               // TMA bytes landed (logits + W)
-    uint64_t *full_a = bars + STAGES;        // A operand written by the 128 producer threads
-    uint64_t *empty = bars + 2 * STAGES;     // MMA done with the stage
-    uint64_t *acc_full = bars + 3 * STAGES;  // accumulator complete
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * STAGES + 1);
+    uint64_t *full_l = bars;                 // logits tile landed
+    uint64_t *full_w = bars + STAGES;        // W tile landed (both halves)
+    uint64_t *full_a = bars + 2 * STAGES;    // A operand written by the 128 producer threads
+    uint64_t *empty = bars + 3 * STAGES;     // both CTAs' MMAs done with the stage
+    uint64_t *acc_full = bars + 4 * STAGES;  // accumulator complete
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 4 * STAGES + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
 
-    const int bid = blockIdx.x;
-    const int nt = bid % p.n_tiles;
-    const int mt = (bid / p.n_tiles) % p.m_tiles;
-    const int split = bid / (p.n_tiles * p.m_tiles);
-    const int64_t kb0 = (int64_t)split * p.nkb / p.splits;
-    const int64_t kb1 = (int64_t)(split + 1) * p.nkb / p.splits;
+    // work of this cluster: (n-tile, m-pair, split)
+    const int pair = blockIdx.x >> 1;
+    const int m_pairs = p.m_tiles >> 1;
+    const int full_pairs = p.splits * m_pairs * p.n_full;
+    int nt, mp, j, S, halves;
+    if (pair < full_pairs) {
+        nt = pair % p.n_full;
+        mp = (pair / p.n_full) % m_pairs;
+        j = pair / (p.n_full * m_pairs);
+        S = p.splits;
+        halves = 2;
+    } else {
+        const int q = pair - full_pairs;
+        nt = p.n_full;
+        mp = q % m_pairs;
+        j = q / m_pairs;
+        S = p.tail_splits;
+        halves = 1;
+    }
+    const int mt = 2 * mp + (int)rank;
+    const int64_t kb0 = (int64_t)j * p.nkb / S;
+    const int64_t kb1 = (int64_t)(j + 1) * p.nkb / S;
     const int nkb = (int)(kb1 - kb0);
     const int row0 = mt * BM;
     const int col0 = nt * BN;
+    const uint32_t w_bytes = (uint32_t)halves * W_HALF_BYTES;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&full_tma[s]), 1);
+            mbar_init(smem_u32(&full_l[s]), 1);
+            mbar_init(smem_u32(&full_w[s]), 1);
             mbar_init(smem_u32(&full_a[s]), 128);
-            mbar_init(smem_u32(&empty[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 2);
         }
         mbar_init(smem_u32(acc_full), 1);
         *abort_flag = 0;
@@ -109,6 +144,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the peer's barriers exist before any multicast or commit reaches them
+    cluster_sync_all();
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
@@ -117,6 +154,16 @@ __global__ void __launch_bounds__(THREADS, 1)
             int issued[STAGES];
 #pragma unroll
             for (int s = 0; s < STAGES; ++s) issued[s] = 0;
+            const int nbox = 2 * halves;  // this CTA's share of the 4 * halves W boxes
+            const uint64_t w_policy = l2_policy_evict_first();
+            // L2 prefetch of the first blocks: logits tile and this CTA's W boxes
+            auto prefetch_block = [&](int i) {
+                const int64_t k = p.k_begin + (kb0 + i) * BK;
+                tma_prefetch_l2_2d(&tm_logits, (int)k, row0);
+                for (int b = 0; b < nbox; ++b)
+                    tma_prefetch_l2_2d(&tm_w, col0 + 64 * ((int)rank * nbox + b), (int)(k - p.vocab_start));
+            };
+            for (int i = 0; i < PREFETCH && i < nkb; ++i) prefetch_block(i);
             bool ok = true;
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % STAGES;
@@ -125,33 +172,40 @@ __global__ void __launch_bounds__(THREADS, 1)
                     ok = false;
                     break;
                 }
+                if (i + PREFETCH < nkb) prefetch_block(i + PREFETCH);
                 uint8_t *st = smem + s * STAGE_BYTES;
-                const uint32_t bar = smem_u32(&full_tma[s]);
-                mbar_arrive_expect_tx(bar, L_BYTES + W_BYTES);
                 const int64_t k = p.k_begin + (kb0 + i) * BK;
-                tma_load_2d(smem_u32(st), &tm_logits, bar, (int)k, row0);
+                const uint32_t bl = smem_u32(&full_l[s]);
+                mbar_arrive_expect_tx(bl, L_BYTES);
+                tma_load_2d(smem_u32(st), &tm_logits, bl, (int)k, row0);
+                const uint32_t bw = smem_u32(&full_w[s]);
+                mbar_arrive_expect_tx(bw, w_bytes);
                 const int wy = (int)(k - p.vocab_start);
-#pragma unroll
-                for (int j = 0; j < BN / 64; ++j)
-                    tma_load_2d(smem_u32(st + L_BYTES + j * W_BOX_BYTES), &tm_w, bar, col0 + 64 * j, wy);
+                for (int b = 0; b < nbox; ++b) {
+                    const int box = (int)rank * nbox + b;
+                    tma_load_2d_multicast_hint(smem_u32(st + L_BYTES + box * W_BOX_BYTES), &tm_w, bw, col0 + 64 * box,
+                                               wy, kPairMask, w_policy);
+                }
                 issued[s] = (int)u + 1;
             }
             if (!ok) {
-                // let every copy already issued land before the CTA leaves
                 for (int s = 0; s < STAGES; ++s)
-                    if (issued[s] > 0) drain_wait(smem_u32(&full_tma[s]), (issued[s] - 1) & 1);
+                    if (issued[s] > 0) {
+                        drain_wait(smem_u32(&full_l[s]), (issued[s] - 1) & 1);
+                        drain_wait(smem_u32(&full_w[s]), (issued[s] - 1) & 1);
+                    }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, /*A K-major*/ 0, /*B N-major*/ 1);
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, 256, /*A K-major*/ 0, /*B N-major*/ 1);
             bool issued_any = false;
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % STAGES;
                 const uint32_t ph = (uint32_t)(i / STAGES) & 1;
                 if (!mbar_wait(smem_u32(&full_a[s]), ph, abort_flag)) break;
-                if (!mbar_wait(smem_u32(&full_tma[s]), ph, abort_flag)) break;
+                if (!mbar_wait(smem_u32(&full_w[s]), ph, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t a_addr = smem_u32(smem + s * STAGE_BYTES + L_BYTES + W_BYTES);
                 const uint32_t b_addr = smem_u32(smem + s * STAGE_BYTES + L_BYTES);
@@ -159,11 +213,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     // A: K-major, 64-byte rows, 8-row groups 512 B apart; +32 B per K=16 step
                     const uint64_t a_desc = smem_desc(a_addr + kk * 32, 16, 512, 4);
-                    // B: N-major, 64-column atoms 4 KiB apart (LBO), 8-row groups 1 KiB apart (SBO)
-                    const uint64_t b_desc = smem_desc(b_addr + kk * 2048, W_BOX_BYTES, 1024, 2);
-                    umma_bf16(tmem_base, a_desc, b_desc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                    for (int h = 0; h < halves; ++h) {
+                        // B: N-major, 64-column atoms 4 KiB apart (LBO), 8-row groups 1 KiB apart (SBO)
+                        const uint64_t b_desc = smem_desc(b_addr + h * W_HALF_BYTES + kk * 2048, W_BOX_BYTES, 1024, 2);
+                        umma_bf16(tmem_base + h * 256, a_desc, b_desc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
-                umma_commit(smem_u32(&empty[s]));
+                umma_commit_multicast(smem_u32(&empty[s]), kPairMask);
                 issued_any = true;
             }
             umma_commit(smem_u32(acc_full));
@@ -180,7 +236,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int i = 0; i < nkb; ++i) {
             const int s = i % STAGES;
             const uint32_t ph = (uint32_t)(i / STAGES) & 1;
-            if (!mbar_wait(smem_u32(&full_tma[s]), ph, abort_flag)) {
+            if (!mbar_wait(smem_u32(&full_l[s]), ph, abort_flag)) {
                 ok = false;
                 break;
             }
@@ -217,7 +273,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         // epilogue: accumulator -> partial tile, layout [BN/4 column groups][128 rows][4]
         float4 *dst = reinterpret_cast<float4 *>(p.ws) +
-                      ((int64_t)(split * p.m_tiles + mt) * p.n_tiles + nt) * (BN / 4) * BM;
+                      ((int64_t)(j * p.m_tiles + mt) * p.n_tiles + nt) * (BN / 4) * BM;
         // tcgen05.ld is warp-collective: the warp goes on only if every lane got here cleanly
         bool have_acc = false;
         if (nkb > 0 && __all_sync(0xffffffffu, ok)) {
@@ -228,24 +284,26 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_after();
             const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll 1
-            for (int j = 0; j < BN / 32; ++j) {
+            for (int jc = 0; jc < halves * 8; ++jc) {
                 uint32_t v[32];
-                tmem_ld_32x32b_x32(trow + j * 32, v);
+                tmem_ld_32x32b_x32(trow + jc * 32, v);
                 tmem_ld_wait();
 #pragma unroll
                 for (int c4 = 0; c4 < 8; ++c4) {
                     const float4 o = make_float4(__uint_as_float(v[4 * c4]), __uint_as_float(v[4 * c4 + 1]),
                                                  __uint_as_float(v[4 * c4 + 2]), __uint_as_float(v[4 * c4 + 3]));
-                    dst[(j * 8 + c4) * BM + r] = o;
+                    dst[(jc * 8 + c4) * BM + r] = o;
                 }
             }
         } else if (nkb == 0) {
-            for (int cg4 = 0; cg4 < BN / 4; ++cg4) dst[cg4 * BM + r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int cg4 = 0; cg4 < halves * 64; ++cg4) dst[cg4 * BM + r] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    // neither CTA leaves while the other may still multicast into it or commit to it
+    cluster_sync_all();
     if (warp == 0) {
         __syncwarp();
         tc_fence_after();
@@ -253,25 +311,26 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
-// E[i, c] = gamma * sum over splits of the partial tiles, in split order.
-__global__ void splitk_reduce_kernel(const float4 *__restrict__ ws, int splits, int m_tiles, int n_tiles, int R,
-                                     int d, float gamma, float *__restrict__ out, int64_t ldo, int vec_out) {
-    const int64_t groups = (int64_t)n_tiles * (BN / 4);  // column groups of 4
-    const int64_t total = (int64_t)R * groups;
-    const int64_t tile_stride = (int64_t)m_tiles * n_tiles * (BN / 4) * BM;
+// E[i, c] = gamma * sum over the splits of column c's tile, in split order.
+__global__ void splitk_reduce_kernel(const float4 *__restrict__ ws, const Params p, int d, float gamma,
+                                     float *__restrict__ out, int64_t ldo, int vec_out) {
+    const int64_t groups = ((int64_t)d + 3) / 4;  // column groups of 4
+    const int64_t total = (int64_t)p.R * groups;
+    const int64_t tile_elems = (int64_t)(BN / 4) * BM;  // float4 per partial tile
     for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
          t += (int64_t)gridDim.x * blockDim.x) {
         // consecutive threads take consecutive rows of one column group: coalesced reads
-        const int64_t g = t / R;
-        const int i = (int)(t - g * R);
+        const int64_t g = t / p.R;
+        const int i = (int)(t - g * p.R);
         const int c = (int)(g * 4);
-        if (c >= d) continue;
         const int mt = i / BM, r = i % BM;
-        const int nt = (int)(g / (BN / 4)), cg = (int)(g % (BN / 4));
-        const float4 *src = ws + ((int64_t)mt * n_tiles + nt) * (BN / 4) * BM + (int64_t)cg * BM + r;
+        const int nt = c / BN, cg = (c % BN) / 4;
+        const int S = nt < p.n_full ? p.splits : p.tail_splits;
+        const int64_t split_stride = (int64_t)p.m_tiles * p.n_tiles * tile_elems;
+        const float4 *src = ws + ((int64_t)mt * p.n_tiles + nt) * tile_elems + (int64_t)cg * BM + r;
         float4 acc = src[0];
-        for (int s = 1; s < splits; ++s) {
-            const float4 v = src[s * tile_stride];
+        for (int s = 1; s < S; ++s) {
+            const float4 v = src[s * split_stride];
             acc.x += v.x;
             acc.y += v.y;
             acc.z += v.z;
@@ -301,6 +360,19 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
+// Column tiling of d: n_full tiles of 512 columns, then (if tail) one of <= 256.
+void column_tiles(int64_t d, int *n_tiles, int *n_full, int *tail) {
+    const int nt = (int)((d + BN - 1) / BN);
+    const int64_t last = d - (int64_t)(nt - 1) * BN;
+    *n_tiles = nt;
+    *tail = last <= BN / 2 ? 1 : 0;
+    *n_full = nt - *tail;
+}
+
+// A half-width block moves its logits tile (16 KiB) and half the W bytes of a full
+// block: about 3/4 of a full block's cost, so the tail gets 3/4 of the splits.
+int tail_splits_of(int splits, int tail) { return tail ? (3 * splits + 3) / 4 : 0; }
+
 }  // namespace
 
 size_t soft_embed_workspace_bytes(const SoftEmbedPlan &plan, int splits) {
@@ -309,17 +381,42 @@ size_t soft_embed_workspace_bytes(const SoftEmbedPlan &plan, int splits) {
 
 bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t d, int num_sms,
                      SoftEmbedPlan *plan) {
-    if (R <= 0 || d <= 0 || vocab_end <= vocab_start || vocab_start < 0 || num_sms <= 0) return false;
+    if (R <= 0 || d <= 0 || vocab_end <= vocab_start || vocab_start < 0 || num_sms < 2) return false;
     SoftEmbedPlan pl;
     pl.k_begin = vocab_start & ~int64_t(3);
     pl.nkb = (vocab_end - pl.k_begin + BK - 1) / BK;
-    pl.m_tiles = (int)((R + BM - 1) / BM);
-    pl.n_tiles = (int)((d + BN - 1) / BN);
-    const int64_t tiles = (int64_t)pl.m_tiles * pl.n_tiles;
-    int64_t splits = tiles >= num_sms ? 1 : num_sms / tiles;
-    if (splits > pl.nkb) splits = pl.nkb;
-    if (splits < 1) splits = 1;
-    pl.splits = (int)splits;
+    const int64_t m_pairs = (R + 2 * BM - 1) / (2 * BM);
+    pl.m_tiles = (int)(2 * m_pairs);
+    int n_full, tail;
+    column_tiles(d, &pl.n_tiles, &n_full, &tail);
+    // choose the vocabulary splits that finish soonest: whole waves of clusters times
+    // the largest per-cluster work (vocabulary blocks x 256-column halves)
+    const int64_t clusters = num_sms / 2;
+    int best = 1;
+    double best_t = 1e300;
+    // at least 16 blocks (four rounds of the stage ring) per split, at most 64 splits
+    int64_t max_s = pl.nkb / 16;
+    if (max_s > 64) max_s = 64;
+    if (max_s < 1) max_s = 1;
+    for (int64_t S = 1; S <= max_s; ++S) {
+        const int64_t St = tail_splits_of((int)S, tail);
+        const int64_t pairs = m_pairs * (n_full * S + St);
+        const double waves = (double)((pairs + clusters - 1) / clusters);
+        // cost units per vocabulary block: 4 for a full-width cluster, 3 for the half-width tail
+        double work = n_full ? 4.0 * (double)((pl.nkb + S - 1) / S) : 0.0;
+        if (St) work = fmax(work, 3.0 * (double)((pl.nkb + St - 1) / St));
+        const double t = waves * work;
+        if (t < best_t * 0.98) {
+            best_t = t;
+            best = (int)S;
+        }
+    }
+    // tuning override: DGSAMP_SOFT_EMBED_SPLITS=<n> forces the split count (clamped)
+    if (const char *env = getenv("DGSAMP_SOFT_EMBED_SPLITS")) {
+        const long v = strtol(env, nullptr, 10);
+        if (v >= 1) best = (int)(v < pl.nkb ? v : pl.nkb);
+    }
+    pl.splits = best;
     pl.workspace_bytes = soft_embed_workspace_bytes(pl, pl.splits);
     *plan = pl;
     return true;
@@ -368,6 +465,8 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
         *msg = "could not raise the shared-memory limit of the soft-embed kernel";
         return attr_err;
     }
+    int n_tiles, n_full, tail;
+    column_tiles(d, &n_tiles, &n_full, &tail);
     Params p;
     p.lse = lse;
     p.ws = static_cast<float *>(workspace);
@@ -377,24 +476,38 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     p.nkb = plan.nkb;
     p.R = (int)R;
     p.m_tiles = plan.m_tiles;
-    p.n_tiles = plan.n_tiles;
+    p.n_tiles = n_tiles;
+    p.n_full = n_full;
+    p.tail_halves = tail;
     p.splits = plan.splits;
-    const unsigned grid = (unsigned)(plan.splits * plan.m_tiles * plan.n_tiles);
-    soft_embed_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(tm_l, tm_w, p);
-    cudaError_t e = cudaGetLastError();
+    p.tail_splits = tail_splits_of(plan.splits, tail);
+    const int64_t pairs = (int64_t)(plan.m_tiles / 2) * (n_full * (int64_t)p.splits + p.tail_splits);
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, soft_embed_kernel, tm_l, tm_w, p);
     if (e != cudaSuccess) {
         *msg = "soft-embed kernel launch failed";
         return e;
     }
     const int vec_out = (ldo % 4 == 0) && (((uintptr_t)out & 15) == 0);
-    const int64_t total = R * (int64_t)plan.n_tiles * (BN / 4);
+    const int64_t total = R * ((d + 3) / 4);
     int64_t blocks = (total + 255) / 256;
     const int64_t cap = (int64_t)device_sm_count() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const float4 *>(workspace), plan.splits,
-                                                               plan.m_tiles, plan.n_tiles, (int)R, (int)d, gamma, out,
-                                                               ldo, vec_out);
+    splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const float4 *>(workspace), p, (int)d,
+                                                               gamma, out, ldo, vec_out);
     e = cudaGetLastError();
     if (e != cudaSuccess) *msg = "split-K reduce launch failed";
     return e;
