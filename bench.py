@@ -188,12 +188,11 @@ def main() -> None:
     import __graft_entry__
     __graft_entry__.build()
     from denoising_sampler_step_gb300 import binding as B
-    from denoising_sampler_step_gb300 import cost, inputs
+    from denoising_sampler_step_gb300 import cost, inputs, replicas
     from denoising_sampler_step_gb300.step import SamplerStep
 
     # each rank serves its own canvases (independent requests: weak scaling)
-    base = inputs.WORKLOADS[WORKLOAD]
-    wl = base.with_(seed=base.seed + 1000 * rank)
+    wl = replicas.rank_workload(inputs.WORKLOADS[WORKLOAD], rank)
     x = inputs.logits(wl)
     Wb = inputs.embedding_bf16(wl)
     budgets = inputs.budgets(wl)
@@ -259,10 +258,7 @@ def main() -> None:
     e2e_ms = e0.elapsed_time(e1)
     clk = clocks.stop()
 
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = t.tolist()
+    ms, e2e_ms = replicas.max_over_ranks([ms, e2e_ms], device=dev)
 
     pk = peaks()
     sc = cost.StepCost(rows=wl.R, V=wl.V, d=wl.d, vocab=wl.V)
@@ -278,7 +274,7 @@ def main() -> None:
     ms_step = ms / args.steps
     line = {
         "metric": METRIC,
-        "value": world * wl.R * args.steps / (ms * 1e-3),
+        "value": replicas.whole_job_rate(wl.R, args.steps, world, ms),
         "unit": UNIT,
         "n_gpus": world,
         "steps": args.steps,
@@ -298,7 +294,7 @@ def main() -> None:
                      "algorithmic_bytes_per_launch": sc.gemm_bytes, "launch_us": comp["soft_embed"] * 1e3,
                      "peak_source": pk["source"]},
         "kernel_us": {k: v * 1e3 for k, v in comp.items()},
-        "e2e": {"value": world * wl.R * args.steps / (e2e_ms * 1e-3), "unit": UNIT,
+        "e2e": {"value": replicas.whole_job_rate(wl.R, args.steps, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": step.h2d_bytes(h), "d2h_bytes_per_step": step.d2h_bytes(),
                 "ms_per_step": e2e_ms / args.steps},
         "gpu_launches": KERNELS_PER_STEP * args.steps,

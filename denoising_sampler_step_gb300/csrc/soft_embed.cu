@@ -49,7 +49,10 @@ constexpr int STAGES = 4;
 constexpr int THREADS = 192;     // warp 0: TMA, warp 1: MMA, warps 2..5: A producers + epilogue
 constexpr int TMEM_COLS = 512;
 constexpr uint16_t kPairMask = 0x3;
-constexpr int PREFETCH = 8;      // vocabulary blocks pulled into L2 ahead of their TMA loads
+#ifndef DG_SE_PREFETCH
+#define DG_SE_PREFETCH 8
+#endif
+constexpr int PREFETCH = DG_SE_PREFETCH;  // vocabulary blocks pulled into L2 ahead of their TMA loads
 
 constexpr int L_BYTES = BM * BK * 4;      // logits tile, rows of 128 B (128-byte swizzle)
 constexpr int W_BOX_BYTES = BK * 64 * 2;  // one TMA box: 32 rows x 64 columns
