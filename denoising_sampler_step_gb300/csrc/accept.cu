@@ -6,7 +6,8 @@
 //   1. key = (order-preserving bits of kappa) << 32 | position, so that a single
 //      64-bit ascending sort gives confidence descending with ties broken by the
 //      lower position; NaN kappa (no distribution) maps above every number;
-//   2. bitonic sort of the keys in shared memory;
+//   2. bitonic sort of the keys: warp shuffles for partners within a warp, shared memory
+//      for the others;
 //   3. inclusive prefix sum of H in sorted order, in fp64 (warp shuffles, then the
 //      per-warp totals);
 //   4. n = the first k whose running sum is not <= B (NaN counts as passing it),
@@ -31,6 +32,7 @@ __global__ void __launch_bounds__(1024)
                   const float *__restrict__ budgets, int min_accept, int32_t *__restrict__ order,
                   uint8_t *__restrict__ mask, int32_t *__restrict__ n_accepted) {
     extern __shared__ unsigned long long keys[];  // blockDim.x entries
+    __shared__ float H_s[1024];
     __shared__ double warp_tot[32];
     __shared__ int first_fail;
 
@@ -39,28 +41,34 @@ __global__ void __launch_bounds__(1024)
     const int NT = blockDim.x;
     const int64_t base = (int64_t)q * L_c;
 
-    keys[tid] = (tid < L_c) ? (((unsigned long long)order_bits(kappa[base + tid]) << 32) | (unsigned)tid)
-                            : ~0ull;
+    unsigned long long key =
+        (tid < L_c) ? (((unsigned long long)order_bits(kappa[base + tid]) << 32) | (unsigned)tid) : ~0ull;
+    if (tid < L_c) H_s[tid] = H[base + tid];  // gathered in sorted order below
     if (tid == 0) first_fail = L_c;
-    __syncthreads();
 
+    // bitonic sort: partners within a warp exchange by shuffle, farther ones through shared memory
     for (int k = 2; k <= NT; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
-            const int p = tid ^ j;
-            if (p > tid) {
-                const unsigned long long a = keys[tid], b = keys[p];
-                const bool ascending = (tid & k) == 0;
-                if ((a > b) == ascending) {
-                    keys[tid] = b;
-                    keys[p] = a;
-                }
+            unsigned long long other;
+            if (j >= 32) {
+                keys[tid] = key;
+                __syncthreads();
+                other = keys[tid ^ j];
+                __syncthreads();
+            } else {
+                other = __shfl_xor_sync(0xffffffffu, key, j);
             }
-            __syncthreads();
+            const bool ascending = (tid & k) == 0;
+            const bool lower = (tid & j) == 0;
+            const unsigned long long lo = key < other ? key : other;
+            const unsigned long long hi = key < other ? other : key;
+            key = (lower == ascending) ? lo : hi;
         }
     }
+    __syncthreads();  // H_s and first_fail visible
 
-    const int pos = (int)(keys[tid] & 0xffffffffu);
-    double h = (tid < L_c) ? (double)H[base + pos] : 0.0;
+    const int pos = (int)(key & 0xffffffffu);
+    double h = (tid < L_c) ? (double)H_s[pos] : 0.0;
     // inclusive scan in fp64
     const int lane = tid & 31, warp = tid >> 5;
 #pragma unroll
@@ -99,12 +107,23 @@ __global__ void __launch_bounds__(1024)
 
 cudaError_t launch_entropy_accept(const float *H, const float *kappa, int32_t n_req, int32_t L_c,
                                   const float *budgets, int32_t min_accept, int32_t *order,
-                                  uint8_t *mask, int32_t *n_accepted, cudaStream_t stream) {
+                                  uint8_t *mask, int32_t *n_accepted, cudaStream_t stream, bool overlap_previous) {
     int nt = 32;
     while (nt < L_c) nt <<= 1;
-    accept_kernel<<<n_req, nt, nt * sizeof(unsigned long long), stream>>>(H, kappa, L_c, budgets, min_accept,
-                                                                        order, mask, n_accepted);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)n_req, 1, 1);
+    cfg.blockDim = dim3((unsigned)nt, 1, 1);
+    cfg.dynamicSmemBytes = nt * sizeof(unsigned long long);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    // the previous kernel on the stream signals early that this one may start (it reads
+    // only data that kernels before it wrote)
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = overlap_previous ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, accept_kernel, H, kappa, (int)L_c, budgets, (int)min_accept, order, mask,
+                              n_accepted);
 }
 
 }  // namespace dg

@@ -88,7 +88,8 @@ namespace {
 
 dg_status run_soft_embed(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t s, int64_t e,
                          const uint16_t *W, int64_t ldw, int64_t d, float gamma, float *out, int64_t ldo,
-                         void *ws, size_t ws_bytes, cudaStream_t stream) {
+                         void *ws, size_t ws_bytes, cudaStream_t stream, StreamHook between = nullptr,
+                         void *ctx = nullptr) {
     if (R == 0) return DG_OK;
     if (e == s) {
         cudaError_t err = launch_fill_zero(out, R, d, ldo, stream);
@@ -103,8 +104,25 @@ dg_status run_soft_embed(const float *logits, int64_t ldl, const float *lse, int
                     plan.workspace_bytes);
     if (!aligned16(ws)) return fail(DG_ERR_UNSUPPORTED, "soft embed: workspace must be 16-byte aligned");
     const char *msg = "soft embed";
-    cudaError_t err = launch_soft_embed(logits, ldl, lse, R, s, e, W, ldw, d, gamma, out, ldo, ws, plan, stream, &msg);
+    cudaError_t err =
+        launch_soft_embed(logits, ldl, lse, R, s, e, W, ldw, d, gamma, out, ldo, ws, plan, stream, &msg, between, ctx);
     return err == cudaSuccess ? DG_OK : cuda_fail(err, msg);
+}
+
+// The acceptance launch of a step, queued between the soft-embed product and its reduce
+// so that it runs on a spare SM while the product streams (it reads only row statistics).
+struct AcceptArgs {
+    const float *H, *kappa, *budgets;
+    int32_t n_req, L_c, min_accept;
+    int32_t *order;
+    uint8_t *mask;
+    int32_t *n_accepted;
+};
+
+cudaError_t accept_hook(void *ctx, cudaStream_t stream) {
+    const AcceptArgs *a = static_cast<const AcceptArgs *>(ctx);
+    return launch_entropy_accept(a->H, a->kappa, a->n_req, a->L_c, a->budgets, a->min_accept, a->order, a->mask,
+                                 a->n_accepted, stream, /*overlap_previous=*/true);
 }
 
 }  // namespace
@@ -209,10 +227,15 @@ dg_status dg_sampler_step(const float *logits, int32_t n_req, int32_t L_c, int64
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = launch_row_stats(logits, R, V, ldl, m, lse, H, kappa, argmax, s);
     if (e != cudaSuccess) return cuda_fail(e, "step: row stats launch");
-    e = launch_entropy_accept(H, kappa, n_req, L_c, budgets, min_accept, order, mask, n_accepted, s);
-    if (e != cudaSuccess) return cuda_fail(e, "step: accept launch");
+    if (vocab_end == vocab_start) {
+        e = launch_entropy_accept(H, kappa, n_req, L_c, budgets, min_accept, order, mask, n_accepted, s);
+        if (e != cudaSuccess) return cuda_fail(e, "step: accept launch");
+        return run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, ldw, d, gamma, E, ldo, workspace,
+                              workspace_bytes, s);
+    }
+    AcceptArgs acc{H, kappa, budgets, n_req, L_c, min_accept, order, mask, n_accepted};
     return run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, ldw, d, gamma, E, ldo, workspace,
-                          workspace_bytes, s);
+                          workspace_bytes, s, accept_hook, &acc);
 }
 
 dg_status dg_get_device_status(dg_stream_t stream) {

@@ -9,13 +9,14 @@
 
 namespace dg {
 
-int stats_cluster_size(int64_t V);
+int stats_cluster_size(int64_t R, int64_t V);
 cudaError_t launch_row_stats(const float *logits, int64_t R, int64_t V, int64_t ldl, float *m, float *lse,
                              float *H, float *kappa, int32_t *argmax, cudaStream_t stream);
 
 cudaError_t launch_entropy_accept(const float *H, const float *kappa, int32_t n_req, int32_t L_c,
                                   const float *budgets, int32_t min_accept, int32_t *order,
-                                  uint8_t *mask, int32_t *n_accepted, cudaStream_t stream);
+                                  uint8_t *mask, int32_t *n_accepted, cudaStream_t stream,
+                                  bool overlap_previous = false);
 
 constexpr int kMaxPartials = 16;
 cudaError_t launch_sum_partials(const float *const *partials, int32_t T, int64_t R, int64_t d, int64_t ldp,
@@ -33,11 +34,15 @@ bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t 
                      SoftEmbedPlan *plan);
 // Workspace bytes a plan needs with a given number of splits.
 size_t soft_embed_workspace_bytes(const SoftEmbedPlan &plan, int splits);
-// Queues the product and the split-K reduce.  On failure *msg names the step.
+// Queues the product, then `between(ctx, stream)` if given (work that may overlap the
+// product: the product lets the next kernel on the stream start early), then the split-K
+// reduce.  On failure *msg names the step.
+typedef cudaError_t (*StreamHook)(void *ctx, cudaStream_t stream);
 cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse, int64_t R,
                               int64_t vocab_start, int64_t vocab_end, const uint16_t *W, int64_t ldw,
                               int64_t d, float gamma, float *out, int64_t ldo, void *workspace,
-                              const SoftEmbedPlan &plan, cudaStream_t stream, const char **msg);
+                              const SoftEmbedPlan &plan, cudaStream_t stream, const char **msg,
+                              StreamHook between = nullptr, void *ctx = nullptr);
 
 int device_sm_count();
 

@@ -21,6 +21,7 @@
 //   Final: lnZ = log1p(rest), lse = m + lnZ, H = lnZ - t / (1 + rest), kappa = lnZ.
 #include <cooperative_groups.h>
 #include <float.h>
+#include <stdlib.h>
 
 #include "dg_common.cuh"
 #include "dg_internal.h"
@@ -251,16 +252,23 @@ cudaError_t launch_stats(const float *logits, int64_t R, int64_t V, int64_t ldl,
 
 }  // namespace
 
-int stats_cluster_size(int64_t V) {
-    // about 16K entries (64 KiB) or more per CTA; at most 8 CTAs (the portable cluster limit)
+int stats_cluster_size(int64_t R, int64_t V) {
+    // at least 16K entries (64 KiB) per CTA, at most 8 CTAs (the portable cluster limit),
+    // and no more than about 1024 CTAs in all: few rows split finer, many rows not at all
     int c = 1;
-    while (c < 8 && V / (c * 2) >= 16384) c *= 2;
+    while (c < 8 && V / (c * 2) >= 16384 && R * c * 2 <= 1024) c *= 2;
     return c;
 }
 
 cudaError_t launch_row_stats(const float *logits, int64_t R, int64_t V, int64_t ldl, float *m, float *lse,
                              float *H, float *kappa, int32_t *argmax, cudaStream_t stream) {
-    switch (stats_cluster_size(V)) {
+    int c = stats_cluster_size(R, V);
+    // tuning override: DGSAMP_STATS_CLUSTER=1|2|4|8 forces the CTAs per row
+    if (const char *env = getenv("DGSAMP_STATS_CLUSTER")) {
+        const int v = atoi(env);
+        if (v == 1 || v == 2 || v == 4 || v == 8) c = v;
+    }
+    switch (c) {
         case 1: return launch_stats<1>(logits, R, V, ldl, m, lse, H, kappa, argmax, stream);
         case 2: return launch_stats<2>(logits, R, V, ldl, m, lse, H, kappa, argmax, stream);
         case 4: return launch_stats<4>(logits, R, V, ldl, m, lse, H, kappa, argmax, stream);

@@ -10,12 +10,13 @@
 //   - a cluster of two CTAs owns 256 output rows (128 each) x up to 512 output
 //     columns and one contiguous range of 32-entry vocabulary blocks (split-K over
 //     the vocabulary); each CTA's fp32 accumulator fills its 512 TMEM columns;
-//   - per block, each CTA's warp 0 loads its logits tile [128 x 32] fp32 by TMA and
-//     half of the W tile [32 x 512] bf16 by TMA multicast into both CTAs, so every W
-//     byte leaves L2 once per cluster;
-//   - warps 2..5 turn the logits tile into the bf16 A operand,
-//     exp2(l*log2e - lse*log2e) rounded to nearest even, in the K-major 64-byte-swizzled
-//     layout; the probabilities never go to global memory;
+//   - per block, each CTA loads its logits tile [128 x 32] fp32 by TMA into a logits ring
+//     (warp 2) and half of the W tile [32 x 512] bf16 by TMA multicast into both CTAs'
+//     W + A ring (warp 0), so every W byte leaves L2 once per cluster;
+//   - eight producer warps (two per TMEM lane quarter, each half of a row's block) turn
+//     the logits tile into the bf16 A operand, exp2(l*log2e - lse*log2e) rounded to
+//     nearest even, in the K-major 64-byte-swizzled layout, and hand the logits slot
+//     back at once; the probabilities never go to global memory;
 //   - warp 1 issues tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32) for the two
 //     256-column halves; tcgen05.commit, multicast to both CTAs, frees the stage once
 //     both have consumed it;
@@ -24,9 +25,8 @@
 //     multiplies by gamma and writes E (bitwise reproducible).
 //   A column tail of 256 or fewer (d = 2816 = 5 x 512 + 256) is a half-width tile with
 //   4/3 of the vocabulary range per split, so all clusters carry similar work.
-//   The TMA thread also pulls the tiles PREFETCH blocks ahead into L2 (no shared memory
-//   used), and W loads mark their lines evict-first, which keeps the logits (read by
-//   every column tile of a row block) in L2.
+//   W loads mark their lines evict-first, which keeps the logits (read by every column
+//   tile of a row block) in L2.
 //   Every barrier wait is bounded (about a second); a wait that gives up records
 //   DG_ERR_TIMEOUT, drains what is in flight and leaves the kernel.
 #include <cuda.h>
@@ -44,23 +44,29 @@ namespace {
 
 constexpr int BM = 128;          // rows per CTA (TMEM lanes)
 constexpr int BN = 512;          // output columns per cluster tile (two MMAs of N = 256)
-constexpr int BK = 32;           // vocabulary entries per stage
-constexpr int STAGES = 4;
-constexpr int THREADS = 192;     // warp 0: TMA, warp 1: MMA, warps 2..5: A producers + epilogue
+constexpr int BK = 32;           // vocabulary entries per block
+#ifndef DG_SE_LSTAGES
+#define DG_SE_LSTAGES 4
+#endif
+#ifndef DG_SE_WSTAGES
+#define DG_SE_WSTAGES 4
+#endif
+constexpr int LSTAGES = DG_SE_LSTAGES;  // logits ring, released by the producers once read
+constexpr int WSTAGES = DG_SE_WSTAGES;  // W + A ring, released once both CTAs' MMAs are done
+constexpr int PRODUCER_WARPS = 8;       // two per TMEM lane quarter, each half of a row's block
+constexpr int THREADS = 32 * (3 + PRODUCER_WARPS);  // warp 0: W TMA, 1: MMA, 2: logits TMA
 constexpr int TMEM_COLS = 512;
 constexpr uint16_t kPairMask = 0x3;
-#ifndef DG_SE_PREFETCH
-#define DG_SE_PREFETCH 8
-#endif
-constexpr int PREFETCH = DG_SE_PREFETCH;  // vocabulary blocks pulled into L2 ahead of their TMA loads
 
 constexpr int L_BYTES = BM * BK * 4;      // logits tile, rows of 128 B (128-byte swizzle)
 constexpr int W_BOX_BYTES = BK * 64 * 2;  // one TMA box: 32 rows x 64 columns
 constexpr int W_HALF_BYTES = 4 * W_BOX_BYTES;
 constexpr int W_BYTES = BK * BN * 2;      // up to 8 boxes
 constexpr int A_BYTES = BM * BK * 2;      // bf16 probabilities, rows of 64 B (64-byte swizzle)
-constexpr int STAGE_BYTES = L_BYTES + W_BYTES + A_BYTES;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int L_RING = LSTAGES * L_BYTES;
+constexpr int WA_BYTES = W_BYTES + A_BYTES;
+constexpr int WA_RING = WSTAGES * WA_BYTES;
+constexpr int SMEM_BYTES = L_RING + WA_RING + 1024 /*align*/ + 256 /*barriers*/;
 
 static_assert(L_BYTES % 1024 == 0 && W_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "1 KiB alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
@@ -90,15 +96,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                       const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
-    uint64_t *full_l = bars;                 // logits tile landed
-    uint64_t *full_w = bars + STAGES;        // W tile landed (both halves)
-    uint64_t *full_a = bars + 2 * STAGES;    // A operand written by the 128 producer threads
-    uint64_t *empty = bars + 3 * STAGES;     // both CTAs' MMAs done with the stage
-    uint64_t *acc_full = bars + 4 * STAGES;  // accumulator complete
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 4 * STAGES + 1);
+    uint8_t *l_ring = smem;
+    uint8_t *wa_ring = smem + L_RING;  // slot s: W tile, then the A tile
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L_RING + WA_RING);
+    uint64_t *full_l = bars;                   // logits tile landed
+    uint64_t *empty_l = full_l + LSTAGES;      // the producer warps have read it
+    uint64_t *full_w = empty_l + LSTAGES;      // W tile landed (both halves)
+    uint64_t *full_a = full_w + WSTAGES;       // A operand written by the producer warps
+    uint64_t *empty = full_a + WSTAGES;        // both CTAs' MMAs done with the W + A slot
+    uint64_t *acc_full = empty + WSTAGES;      // accumulator complete
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
+    // the kernel queued next may start now: it never reads what this kernel writes
+    // (the split-K reduce after it is an ordinary launch and waits for completion)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
 
@@ -127,13 +139,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int nkb = (int)(kb1 - kb0);
     const int row0 = mt * BM;
     const int col0 = nt * BN;
-    const uint32_t w_bytes = (uint32_t)halves * W_HALF_BYTES;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < LSTAGES; ++s) {
             mbar_init(smem_u32(&full_l[s]), 1);
+            mbar_init(smem_u32(&empty_l[s]), PRODUCER_WARPS);
+        }
+        for (int s = 0; s < WSTAGES; ++s) {
             mbar_init(smem_u32(&full_w[s]), 1);
-            mbar_init(smem_u32(&full_a[s]), 128);
+            mbar_init(smem_u32(&full_a[s]), PRODUCER_WARPS);
             mbar_init(smem_u32(&empty[s]), 2);
         }
         mbar_init(smem_u32(acc_full), 1);
@@ -152,52 +166,58 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ W TMA (this CTA's half, multicast)
         if (lane == 0) {
-            int issued[STAGES];
-#pragma unroll
-            for (int s = 0; s < STAGES; ++s) issued[s] = 0;
+            int issued[WSTAGES];
+            for (int s = 0; s < WSTAGES; ++s) issued[s] = 0;
             const int nbox = 2 * halves;  // this CTA's share of the 4 * halves W boxes
             const uint64_t w_policy = l2_policy_evict_first();
-            // L2 prefetch of the first blocks: logits tile and this CTA's W boxes
-            auto prefetch_block = [&](int i) {
-                const int64_t k = p.k_begin + (kb0 + i) * BK;
-                tma_prefetch_l2_2d(&tm_logits, (int)k, row0);
-                for (int b = 0; b < nbox; ++b)
-                    tma_prefetch_l2_2d(&tm_w, col0 + 64 * ((int)rank * nbox + b), (int)(k - p.vocab_start));
-            };
-            for (int i = 0; i < PREFETCH && i < nkb; ++i) prefetch_block(i);
+            const uint32_t w_bytes = (uint32_t)halves * W_HALF_BYTES;
             bool ok = true;
             for (int i = 0; i < nkb; ++i) {
-                const int s = i % STAGES;
-                const uint32_t u = (uint32_t)(i / STAGES);
+                const int s = i % WSTAGES;
+                const uint32_t u = (uint32_t)(i / WSTAGES);
                 if (u > 0 && !mbar_wait(smem_u32(&empty[s]), (u - 1) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
-                if (i + PREFETCH < nkb) prefetch_block(i + PREFETCH);
-                uint8_t *st = smem + s * STAGE_BYTES;
                 const int64_t k = p.k_begin + (kb0 + i) * BK;
-                const uint32_t bl = smem_u32(&full_l[s]);
-                mbar_arrive_expect_tx(bl, L_BYTES);
-                tma_load_2d(smem_u32(st), &tm_logits, bl, (int)k, row0);
                 const uint32_t bw = smem_u32(&full_w[s]);
                 mbar_arrive_expect_tx(bw, w_bytes);
                 const int wy = (int)(k - p.vocab_start);
                 for (int b = 0; b < nbox; ++b) {
                     const int box = (int)rank * nbox + b;
-                    tma_load_2d_multicast_hint(smem_u32(st + L_BYTES + box * W_BOX_BYTES), &tm_w, bw, col0 + 64 * box,
-                                               wy, kPairMask, w_policy);
+                    tma_load_2d_multicast_hint(smem_u32(wa_ring + s * WA_BYTES + box * W_BOX_BYTES), &tm_w, bw,
+                                               col0 + 64 * box, wy, kPairMask, w_policy);
                 }
                 issued[s] = (int)u + 1;
             }
-            if (!ok) {
-                for (int s = 0; s < STAGES; ++s)
-                    if (issued[s] > 0) {
-                        drain_wait(smem_u32(&full_l[s]), (issued[s] - 1) & 1);
-                        drain_wait(smem_u32(&full_w[s]), (issued[s] - 1) & 1);
-                    }
+            if (!ok)
+                for (int s = 0; s < WSTAGES; ++s)
+                    if (issued[s] > 0) drain_wait(smem_u32(&full_w[s]), (issued[s] - 1) & 1);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ logits TMA
+        if (lane == 0) {
+            int issued[LSTAGES];
+            for (int s = 0; s < LSTAGES; ++s) issued[s] = 0;
+            bool ok = true;
+            for (int i = 0; i < nkb; ++i) {
+                const int s = i % LSTAGES;
+                const uint32_t u = (uint32_t)(i / LSTAGES);
+                if (u > 0 && !mbar_wait(smem_u32(&empty_l[s]), (u - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int64_t k = p.k_begin + (kb0 + i) * BK;
+                const uint32_t bl = smem_u32(&full_l[s]);
+                mbar_arrive_expect_tx(bl, L_BYTES);
+                tma_load_2d(smem_u32(l_ring + s * L_BYTES), &tm_logits, bl, (int)k, row0);
+                issued[s] = (int)u + 1;
             }
+            if (!ok)
+                for (int s = 0; s < LSTAGES; ++s)
+                    if (issued[s] > 0) drain_wait(smem_u32(&full_l[s]), (issued[s] - 1) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -205,13 +225,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             constexpr uint32_t idesc = idesc_bf16_f32(BM, 256, /*A K-major*/ 0, /*B N-major*/ 1);
             bool issued_any = false;
             for (int i = 0; i < nkb; ++i) {
-                const int s = i % STAGES;
-                const uint32_t ph = (uint32_t)(i / STAGES) & 1;
+                const int s = i % WSTAGES;
+                const uint32_t ph = (uint32_t)(i / WSTAGES) & 1;
                 if (!mbar_wait(smem_u32(&full_a[s]), ph, abort_flag)) break;
                 if (!mbar_wait(smem_u32(&full_w[s]), ph, abort_flag)) break;
                 tc_fence_after();
-                const uint32_t a_addr = smem_u32(smem + s * STAGE_BYTES + L_BYTES + W_BYTES);
-                const uint32_t b_addr = smem_u32(smem + s * STAGE_BYTES + L_BYTES);
+                const uint32_t b_addr = smem_u32(wa_ring + s * WA_BYTES);
+                const uint32_t a_addr = b_addr + W_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     // A: K-major, 64-byte rows, 8-row groups 512 B apart; +32 B per K=16 step
@@ -230,51 +250,68 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else {
         // ------------------------------------------------------------ A producers, then epilogue
-        const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+        const int pw = warp - 3;          // producer warp 0..7
+        const int quarter = warp & 3;     // TMEM lane quarter this warp may access
+        const int half = pw >> 2;         // which 16 of the block's 32 entries (and, later, which columns)
         const int r = quarter * 32 + lane;
         const int row = row0 + r;
         const bool valid_row = row < p.R;
         const float neg_lse2 = valid_row ? -p.lse[row] * kLog2e : 0.0f;
         bool ok = true;
         for (int i = 0; i < nkb; ++i) {
-            const int s = i % STAGES;
-            const uint32_t ph = (uint32_t)(i / STAGES) & 1;
-            if (!mbar_wait(smem_u32(&full_l[s]), ph, abort_flag)) {
+            const int sl = i % LSTAGES;
+            const int s = i % WSTAGES;
+            const uint32_t ul = (uint32_t)(i / LSTAGES);
+            const uint32_t u = (uint32_t)(i / WSTAGES);
+            // every lane waits (acquire), the warp decides together
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_l[sl]), ul & 1, abort_flag))) {
                 ok = false;
                 break;
             }
-            const uint8_t *lt = smem + s * STAGE_BYTES;
-            uint8_t *at = smem + s * STAGE_BYTES + L_BYTES + W_BYTES;
-            const int64_t k = p.k_begin + (kb0 + i) * BK;
-            const bool edge = (k < p.vocab_start) || (k + BK > p.vocab_end);
-            uint32_t packed[BK / 2];
+            const uint8_t *lt = l_ring + sl * L_BYTES;
+            const int64_t k = p.k_begin + (kb0 + i) * BK + 16 * half;
+            const bool edge = (k < p.vocab_start) || (k + 16 > p.vocab_end);
+            uint32_t packed[8];
 #pragma unroll
-            for (int c = 0; c < BK / 4; ++c) {
+            for (int cc = 0; cc < 4; ++cc) {
+                const int c = 4 * half + cc;  // 16-byte chunk of the 128-byte row
                 const float4 v = *reinterpret_cast<const float4 *>(lt + r * 128 + ((c ^ (r & 7)) << 4));
                 float e0 = ex2_approx(fmaf(v.x, kLog2e, neg_lse2));
                 float e1 = ex2_approx(fmaf(v.y, kLog2e, neg_lse2));
                 float e2 = ex2_approx(fmaf(v.z, kLog2e, neg_lse2));
                 float e3 = ex2_approx(fmaf(v.w, kLog2e, neg_lse2));
                 if (edge) {
-                    const int64_t v0 = k + 4 * c;
+                    const int64_t v0 = k + 4 * cc;
                     if (v0 + 0 < p.vocab_start || v0 + 0 >= p.vocab_end) e0 = 0.f;
                     if (v0 + 1 < p.vocab_start || v0 + 1 >= p.vocab_end) e1 = 0.f;
                     if (v0 + 2 < p.vocab_start || v0 + 2 >= p.vocab_end) e2 = 0.f;
                     if (v0 + 3 < p.vocab_start || v0 + 3 >= p.vocab_end) e3 = 0.f;
                 }
                 if (!valid_row) e0 = e1 = e2 = e3 = 0.f;
-                packed[2 * c] = pack_bf16x2(e0, e1);
-                packed[2 * c + 1] = pack_bf16x2(e2, e3);
+                packed[2 * cc] = pack_bf16x2(e0, e1);
+                packed[2 * cc + 1] = pack_bf16x2(e2, e3);
             }
+            // the logits slot is free once all producer warps have read it
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&empty_l[sl]));
+            // the A slot is free once both CTAs' MMAs of its previous round are done
+            if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[s]), (u - 1) & 1, abort_flag))) {
+                ok = false;
+                break;
+            }
+            uint8_t *at = wa_ring + s * WA_BYTES + W_BYTES;
 #pragma unroll
-            for (int c8 = 0; c8 < BK / 8; ++c8) {
-                uint4 w = make_uint4(packed[4 * c8], packed[4 * c8 + 1], packed[4 * c8 + 2], packed[4 * c8 + 3]);
+            for (int h8 = 0; h8 < 2; ++h8) {
+                const int c8 = 2 * half + h8;  // 16-byte chunk of the 64-byte A row
+                const uint4 w = make_uint4(packed[4 * h8], packed[4 * h8 + 1], packed[4 * h8 + 2], packed[4 * h8 + 3]);
                 *reinterpret_cast<uint4 *>(at + r * 64 + ((c8 ^ ((r >> 1) & 3)) << 4)) = w;
             }
             fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&full_a[s]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&full_a[s]));
         }
-        // epilogue: accumulator -> partial tile, layout [BN/4 column groups][128 rows][4]
+        // epilogue: accumulator -> partial tile, layout [BN/4 column groups][128 rows][4];
+        // the two warps of a lane quarter take one half of the columns each
         float4 *dst = reinterpret_cast<float4 *>(p.ws) +
                       ((int64_t)(j * p.m_tiles + mt) * p.n_tiles + nt) * (BN / 4) * BM;
         // tcgen05.ld is warp-collective: the warp goes on only if every lane got here cleanly
@@ -283,11 +320,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             const bool got = mbar_wait(smem_u32(acc_full), 0, abort_flag);
             have_acc = __all_sync(0xffffffffu, got);
         }
+        const int chunks = halves * 4;  // 32-column chunks per warp
         if (have_acc) {
             tc_fence_after();
             const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll 1
-            for (int jc = 0; jc < halves * 8; ++jc) {
+            for (int jj = 0; jj < chunks; ++jj) {
+                const int jc = half * chunks + jj;
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(trow + jc * 32, v);
                 tmem_ld_wait();
@@ -299,7 +338,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
         } else if (nkb == 0) {
-            for (int cg4 = 0; cg4 < halves * 64; ++cg4) dst[cg4 * BM + r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int cg4 = half * chunks * 8; cg4 < (half + 1) * chunks * 8; ++cg4)
+                dst[cg4 * BM + r] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
 
@@ -428,7 +468,7 @@ bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t 
 cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t vocab_start,
                               int64_t vocab_end, const uint16_t *W, int64_t ldw, int64_t d, float gamma, float *out,
                               int64_t ldo, void *workspace, const SoftEmbedPlan &plan, cudaStream_t stream,
-                              const char **msg) {
+                              const char **msg, StreamHook between, void *ctx) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
     if (!encode) {
         *msg = "cuTensorMapEncodeTiled is not available from the driver";
@@ -502,6 +542,13 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     if (e != cudaSuccess) {
         *msg = "soft-embed kernel launch failed";
         return e;
+    }
+    if (between) {
+        e = between(ctx, stream);
+        if (e != cudaSuccess) {
+            *msg = "launch between the product and the reduce failed";
+            return e;
+        }
     }
     const int vec_out = (ldo % 4 == 0) && (((uintptr_t)out & 15) == 0);
     const int64_t total = R * ((d + 3) / 4);

@@ -67,6 +67,35 @@ class SamplerStep:
             for k, v in self.out.items():
                 h["out_" + k].copy_(v, non_blocking=True)
 
+    def run_pipelined(self, h: dict, steps: int, stream=None) -> None:
+        """`steps` steps from host buffers, the upload of each step's logits overlapping
+        the previous step's kernels: two device logits buffers, uploads on a copy stream,
+        kernels and the read-back of every step's results on `stream`, ordered by events."""
+        s = torch.cuda.current_stream(self.device) if stream is None else stream
+        if not hasattr(self, "_copy_stream"):
+            self._copy_stream = torch.cuda.Stream(device=self.device)
+            self._bufs = [self.logits_dev, torch.empty_like(self.logits_dev)]
+            self._budget_bufs = [self.budgets_dev, torch.empty_like(self.budgets_dev)]
+        cs = self._copy_stream
+        uploaded = [torch.cuda.Event() for _ in range(2)]
+        consumed = [torch.cuda.Event() for _ in range(2)]
+        cs.wait_stream(s)
+        for t in range(steps):
+            b = t & 1
+            with torch.cuda.stream(cs):
+                if t >= 2:
+                    cs.wait_event(consumed[b])
+                self._bufs[b].copy_(h["logits"], non_blocking=True)
+                self._budget_bufs[b].copy_(h["budgets"], non_blocking=True)
+                uploaded[b].record(cs)
+            with torch.cuda.stream(s):
+                s.wait_event(uploaded[b])
+                self(self._bufs[b], self._budget_bufs[b], stream=s)
+                consumed[b].record(s)
+                for k, v in self.out.items():
+                    h["out_" + k].copy_(v, non_blocking=True)
+        s.wait_stream(cs)
+
     @staticmethod
     def h2d_bytes(h: dict) -> int:
         return h["logits"].numel() * 4 + h["budgets"].numel() * 4
