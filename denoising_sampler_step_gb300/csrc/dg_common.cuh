@@ -178,12 +178,6 @@ __device__ __forceinline__ void tma_load_2d_multicast_hint(uint32_t dst, const v
         : "memory");
 }
 
-// Starts pulling a tile into L2 only (no shared memory, no completion to wait for).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const void *tmap, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
-                 : "memory");
-}
-
 // L2 policy that marks the lines it touches as first to evict (data read once).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t pol;

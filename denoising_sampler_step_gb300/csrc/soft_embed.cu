@@ -12,7 +12,8 @@
 //     the vocabulary); each CTA's fp32 accumulator fills its 512 TMEM columns;
 //   - per block, each CTA loads its logits tile [128 x 32] fp32 by TMA into a logits ring
 //     (warp 2) and half of the W tile [32 x 512] bf16 by TMA multicast into both CTAs'
-//     W + A ring (warp 0), so every W byte leaves L2 once per cluster;
+//     W ring (warp 0), so every W byte leaves L2 once per cluster; the W ring is the
+//     deepest (the W stream is the DRAM-latency-bound one), the A ring shallow;
 //   - eight producer warps (two per TMEM lane quarter, each half of a row's block) turn
 //     the logits tile into the bf16 A operand, exp2(l*log2e - lse*log2e) rounded to
 //     nearest even, in the K-major 64-byte-swizzled layout, and hand the logits slot
@@ -23,8 +24,8 @@
 //   - the same four warps then read the accumulator with tcgen05.ld and store the
 //     partial tile; splitk_reduce_kernel adds the split partials in split order,
 //     multiplies by gamma and writes E (bitwise reproducible).
-//   A column tail of 256 or fewer (d = 2816 = 5 x 512 + 256) is a half-width tile with
-//   4/3 of the vocabulary range per split, so all clusters carry similar work.
+//   A column tail of 256 or fewer (d = 2816 = 5 x 512 + 256) is a half-width tile; it gets
+//   as many splits as the full tiles, since a block's time is set by the stage round trip.
 //   W loads mark their lines evict-first, which keeps the logits (read by every column
 //   tile of a row block) in L2.
 //   Every barrier wait is bounded (about a second); a wait that gives up records
@@ -51,12 +52,23 @@ constexpr int BK = 32;           // vocabulary entries per block
 #ifndef DG_SE_WSTAGES
 #define DG_SE_WSTAGES 4
 #endif
+#ifndef DG_SE_ASTAGES
+#define DG_SE_ASTAGES 4
+#endif
 constexpr int LSTAGES = DG_SE_LSTAGES;  // logits ring, released by the producers once read
-constexpr int WSTAGES = DG_SE_WSTAGES;  // W + A ring, released once both CTAs' MMAs are done
+constexpr int WSTAGES = DG_SE_WSTAGES;  // W ring, released once both CTAs' MMAs are done
+constexpr int ASTAGES = DG_SE_ASTAGES;  // A ring, released once this CTA's MMAs are done
 constexpr int PRODUCER_WARPS = 8;       // two per TMEM lane quarter, each half of a row's block
 constexpr int THREADS = 32 * (3 + PRODUCER_WARPS);  // warp 0: W TMA, 1: MMA, 2: logits TMA
 constexpr int TMEM_COLS = 512;
 constexpr uint16_t kPairMask = 0x3;
+#ifndef DG_SE_MULTICAST
+#define DG_SE_MULTICAST 1
+#endif
+// 1: clusters of two CTAs (two 128-row halves) share each W tile by TMA multicast;
+// 0: independent CTAs, each loading its whole W tile (the row halves meet in L2)
+constexpr bool kMulticast = DG_SE_MULTICAST != 0;
+constexpr int kCtasPerUnit = kMulticast ? 2 : 1;
 
 constexpr int L_BYTES = BM * BK * 4;      // logits tile, rows of 128 B (128-byte swizzle)
 constexpr int W_BOX_BYTES = BK * 64 * 2;  // one TMA box: 32 rows x 64 columns
@@ -64,9 +76,9 @@ constexpr int W_HALF_BYTES = 4 * W_BOX_BYTES;
 constexpr int W_BYTES = BK * BN * 2;      // up to 8 boxes
 constexpr int A_BYTES = BM * BK * 2;      // bf16 probabilities, rows of 64 B (64-byte swizzle)
 constexpr int L_RING = LSTAGES * L_BYTES;
-constexpr int WA_BYTES = W_BYTES + A_BYTES;
-constexpr int WA_RING = WSTAGES * WA_BYTES;
-constexpr int SMEM_BYTES = L_RING + WA_RING + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int W_RING = WSTAGES * W_BYTES;
+constexpr int A_RING = ASTAGES * A_BYTES;
+constexpr int SMEM_BYTES = L_RING + W_RING + A_RING + 1024 /*align*/ + 256 /*barriers*/;
 
 static_assert(L_BYTES % 1024 == 0 && W_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "1 KiB alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
@@ -97,14 +109,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *l_ring = smem;
-    uint8_t *wa_ring = smem + L_RING;  // slot s: W tile, then the A tile
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L_RING + WA_RING);
+    uint8_t *w_ring = smem + L_RING;
+    uint8_t *a_ring = smem + L_RING + W_RING;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L_RING + W_RING + A_RING);
     uint64_t *full_l = bars;                   // logits tile landed
     uint64_t *empty_l = full_l + LSTAGES;      // the producer warps have read it
     uint64_t *full_w = empty_l + LSTAGES;      // W tile landed (both halves)
-    uint64_t *full_a = full_w + WSTAGES;       // A operand written by the producer warps
-    uint64_t *empty = full_a + WSTAGES;        // both CTAs' MMAs done with the W + A slot
-    uint64_t *acc_full = empty + WSTAGES;      // accumulator complete
+    uint64_t *empty = full_w + WSTAGES;        // both CTAs' MMAs done with the W slot
+    uint64_t *full_a = empty + WSTAGES;        // A operand written by the producer warps
+    uint64_t *empty_a = full_a + ASTAGES;      // this CTA's MMAs done with the A slot
+    uint64_t *acc_full = empty_a + ASTAGES;    // accumulator complete
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -112,11 +126,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     // (the split-K reduce after it is an ordinary launch and waits for completion)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
+    const uint32_t rank = kMulticast ? cluster_ctarank() : 0;
 
-    // work of this cluster: (n-tile, m-pair, split)
-    const int pair = blockIdx.x >> 1;
-    const int m_pairs = p.m_tiles >> 1;
+    // work of this cluster (or CTA): (n-tile, row block, split)
+    const int pair = blockIdx.x / kCtasPerUnit;
+    const int m_pairs = p.m_tiles / kCtasPerUnit;
     const int full_pairs = p.splits * m_pairs * p.n_full;
     int nt, mp, j, S, halves;
     if (pair < full_pairs) {
@@ -133,7 +147,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         S = p.tail_splits;
         halves = 1;
     }
-    const int mt = 2 * mp + (int)rank;
+    const int mt = kCtasPerUnit * mp + (int)rank;
     const int64_t kb0 = (int64_t)j * p.nkb / S;
     const int64_t kb1 = (int64_t)(j + 1) * p.nkb / S;
     const int nkb = (int)(kb1 - kb0);
@@ -147,8 +161,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int s = 0; s < WSTAGES; ++s) {
             mbar_init(smem_u32(&full_w[s]), 1);
+            mbar_init(smem_u32(&empty[s]), kCtasPerUnit);
+        }
+        for (int s = 0; s < ASTAGES; ++s) {
             mbar_init(smem_u32(&full_a[s]), PRODUCER_WARPS);
-            mbar_init(smem_u32(&empty[s]), 2);
+            mbar_init(smem_u32(&empty_a[s]), 1);
         }
         mbar_init(smem_u32(acc_full), 1);
         *abort_flag = 0;
@@ -170,7 +187,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             int issued[WSTAGES];
             for (int s = 0; s < WSTAGES; ++s) issued[s] = 0;
-            const int nbox = 2 * halves;  // this CTA's share of the 4 * halves W boxes
+            const int nbox = 4 * halves / kCtasPerUnit;  // this CTA's share of the 4 * halves W boxes
             const uint64_t w_policy = l2_policy_evict_first();
             const uint32_t w_bytes = (uint32_t)halves * W_HALF_BYTES;
             bool ok = true;
@@ -187,8 +204,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int wy = (int)(k - p.vocab_start);
                 for (int b = 0; b < nbox; ++b) {
                     const int box = (int)rank * nbox + b;
-                    tma_load_2d_multicast_hint(smem_u32(wa_ring + s * WA_BYTES + box * W_BOX_BYTES), &tm_w, bw,
-                                               col0 + 64 * box, wy, kPairMask, w_policy);
+                    if (kMulticast)
+                        tma_load_2d_multicast_hint(smem_u32(w_ring + s * W_BYTES + box * W_BOX_BYTES), &tm_w, bw,
+                                                   col0 + 64 * box, wy, kPairMask, w_policy);
+                    else
+                        tma_load_2d_hint(smem_u32(w_ring + s * W_BYTES + box * W_BOX_BYTES), &tm_w, bw,
+                                         col0 + 64 * box, wy, w_policy);
                 }
                 issued[s] = (int)u + 1;
             }
@@ -225,13 +246,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             constexpr uint32_t idesc = idesc_bf16_f32(BM, 256, /*A K-major*/ 0, /*B N-major*/ 1);
             bool issued_any = false;
             for (int i = 0; i < nkb; ++i) {
-                const int s = i % WSTAGES;
-                const uint32_t ph = (uint32_t)(i / WSTAGES) & 1;
-                if (!mbar_wait(smem_u32(&full_a[s]), ph, abort_flag)) break;
-                if (!mbar_wait(smem_u32(&full_w[s]), ph, abort_flag)) break;
+                const int s = i % WSTAGES, sa = i % ASTAGES;
+                if (!mbar_wait(smem_u32(&full_a[sa]), (uint32_t)(i / ASTAGES) & 1, abort_flag)) break;
+                if (!mbar_wait(smem_u32(&full_w[s]), (uint32_t)(i / WSTAGES) & 1, abort_flag)) break;
                 tc_fence_after();
-                const uint32_t b_addr = smem_u32(wa_ring + s * WA_BYTES);
-                const uint32_t a_addr = b_addr + W_BYTES;
+                const uint32_t b_addr = smem_u32(w_ring + s * W_BYTES);
+                const uint32_t a_addr = smem_u32(a_ring + sa * A_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     // A: K-major, 64-byte rows, 8-row groups 512 B apart; +32 B per K=16 step
@@ -242,7 +262,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                         umma_bf16(tmem_base + h * 256, a_desc, b_desc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
-                umma_commit_multicast(smem_u32(&empty[s]), kPairMask);
+                if (kMulticast)
+                    umma_commit_multicast(smem_u32(&empty[s]), kPairMask);
+                else
+                    umma_commit(smem_u32(&empty[s]));
+                umma_commit(smem_u32(&empty_a[sa]));
                 issued_any = true;
             }
             umma_commit(smem_u32(acc_full));
@@ -260,9 +284,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         bool ok = true;
         for (int i = 0; i < nkb; ++i) {
             const int sl = i % LSTAGES;
-            const int s = i % WSTAGES;
+            const int s = i % ASTAGES;
             const uint32_t ul = (uint32_t)(i / LSTAGES);
-            const uint32_t u = (uint32_t)(i / WSTAGES);
+            const uint32_t u = (uint32_t)(i / ASTAGES);
             // every lane waits (acquire), the warp decides together
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_l[sl]), ul & 1, abort_flag))) {
                 ok = false;
@@ -294,12 +318,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             // the logits slot is free once all producer warps have read it
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty_l[sl]));
-            // the A slot is free once both CTAs' MMAs of its previous round are done
-            if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[s]), (u - 1) & 1, abort_flag))) {
+            // the A slot is free once this CTA's MMAs of its previous round are done
+            if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty_a[s]), (u - 1) & 1, abort_flag))) {
                 ok = false;
                 break;
             }
-            uint8_t *at = wa_ring + s * WA_BYTES + W_BYTES;
+            uint8_t *at = a_ring + s * A_BYTES;
 #pragma unroll
             for (int h8 = 0; h8 < 2; ++h8) {
                 const int c8 = 2 * half + h8;  // 16-byte chunk of the 64-byte A row
@@ -412,9 +436,9 @@ void column_tiles(int64_t d, int *n_tiles, int *n_full, int *tail) {
     *n_full = nt - *tail;
 }
 
-// A half-width block moves its logits tile (16 KiB) and half the W bytes of a full
-// block: about 3/4 of a full block's cost, so the tail gets 3/4 of the splits.
-int tail_splits_of(int splits, int tail) { return tail ? (3 * splits + 3) / 4 : 0; }
+// A block costs about the same time whatever its width (the stage round trip, not the
+// bytes, sets the pace), so the half-width tail gets as many splits as the full tiles.
+int tail_splits_of(int splits, int tail) { return tail ? splits : 0; }
 
 }  // namespace
 
@@ -428,13 +452,13 @@ bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t 
     SoftEmbedPlan pl;
     pl.k_begin = vocab_start & ~int64_t(3);
     pl.nkb = (vocab_end - pl.k_begin + BK - 1) / BK;
-    const int64_t m_pairs = (R + 2 * BM - 1) / (2 * BM);
-    pl.m_tiles = (int)(2 * m_pairs);
+    const int64_t m_pairs = (R + kCtasPerUnit * BM - 1) / (kCtasPerUnit * BM);  // row blocks per unit
+    pl.m_tiles = (int)(kCtasPerUnit * m_pairs);
     int n_full, tail;
     column_tiles(d, &pl.n_tiles, &n_full, &tail);
     // choose the vocabulary splits that finish soonest: whole waves of clusters times
     // the largest per-cluster work (vocabulary blocks x 256-column halves)
-    const int64_t clusters = num_sms / 2;
+    const int64_t clusters = num_sms / kCtasPerUnit;
     int best = 1;
     double best_t = 1e300;
     // at least 16 blocks (four rounds of the stage ring) per split, at most 64 splits
@@ -445,10 +469,10 @@ bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t 
         const int64_t St = tail_splits_of((int)S, tail);
         const int64_t pairs = m_pairs * (n_full * S + St);
         const double waves = (double)((pairs + clusters - 1) / clusters);
-        // cost units per vocabulary block: 4 for a full-width cluster, 3 for the half-width tail
-        double work = n_full ? 4.0 * (double)((pl.nkb + S - 1) / S) : 0.0;
-        if (St) work = fmax(work, 3.0 * (double)((pl.nkb + St - 1) / St));
-        const double t = waves * work;
+        // every cluster costs its number of vocabulary blocks
+        double work = (double)((pl.nkb + S - 1) / S);
+        if (St) work = fmax(work, (double)((pl.nkb + St - 1) / St));
+        const double t = waves * (work + 32.0);  // a wave also pays its pipeline fill and epilogue
         if (t < best_t * 0.98) {
             best_t = t;
             best = (int)S;
@@ -524,16 +548,16 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     p.tail_halves = tail;
     p.splits = plan.splits;
     p.tail_splits = tail_splits_of(plan.splits, tail);
-    const int64_t pairs = (int64_t)(plan.m_tiles / 2) * (n_full * (int64_t)p.splits + p.tail_splits);
+    const int64_t pairs = (int64_t)(plan.m_tiles / kCtasPerUnit) * (n_full * (int64_t)p.splits + p.tail_splits);
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+    cfg.gridDim = dim3((unsigned)(kCtasPerUnit * pairs), 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = kCtasPerUnit;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
