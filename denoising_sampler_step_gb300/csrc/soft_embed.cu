@@ -12,16 +12,16 @@
 //     the vocabulary); each CTA's fp32 accumulator fills its 512 TMEM columns;
 //   - per block, each CTA loads its logits tile [128 x 32] fp32 by TMA into a logits ring
 //     (warp 2) and half of the W tile [32 x 512] bf16 by TMA multicast into both CTAs'
-//     W ring (warp 0), so every W byte leaves L2 once per cluster; the W ring is the
-//     deepest (the W stream is the DRAM-latency-bound one), the A ring shallow;
-//   - eight producer warps (two per TMEM lane quarter, each half of a row's block) turn
+//     W ring (warp 0), so every W byte leaves L2 once per cluster; a W slot is
+//     released when both CTAs' MMAs have read it, an A slot when this CTA's have;
+//   - eight producer warps (two groups of four taking alternate blocks, 32 rows each) turn
 //     the logits tile into the bf16 A operand, exp2(l*log2e - lse*log2e) rounded to
 //     nearest even, in the K-major 64-byte-swizzled layout, and hand the logits slot
 //     back at once; the probabilities never go to global memory;
 //   - warp 1 issues tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32) for the two
 //     256-column halves; tcgen05.commit, multicast to both CTAs, frees the stage once
 //     both have consumed it;
-//   - the same four warps then read the accumulator with tcgen05.ld and store the
+//   - the same eight warps then read the accumulator with tcgen05.ld and store the
 //     partial tile; splitk_reduce_kernel adds the split partials in split order,
 //     multiplies by gamma and writes E (bitwise reproducible).
 //   A column tail of 256 or fewer (d = 2816 = 5 x 512 + 256) is a half-width tile; it gets
@@ -58,8 +58,13 @@ constexpr int BK = 32;           // vocabulary entries per block
 constexpr int LSTAGES = DG_SE_LSTAGES;  // logits ring, released by the producers once read
 constexpr int WSTAGES = DG_SE_WSTAGES;  // W ring, released once both CTAs' MMAs are done
 constexpr int ASTAGES = DG_SE_ASTAGES;  // A ring, released once this CTA's MMAs are done
-constexpr int PRODUCER_WARPS = 8;       // two per TMEM lane quarter, each half of a row's block
-constexpr int THREADS = 32 * (3 + PRODUCER_WARPS);  // warp 0: W TMA, 1: MMA, 2: logits TMA
+constexpr int PRODUCER_WARPS = 8;       // two groups of four (alternate blocks), 32 rows each
+// Warp roles.  A thread blocked in a barrier wait or in a full MMA/TMA queue slows the
+// shared-memory work of the other warps on its scheduler (warp % 4), so: warp 4 issues the
+// MMAs and warp 8 the logits TMA (scheduler 0, no producers); warp 11 issues the W TMA
+// (scheduler 3, two producers); warps 1-3, 5-7, 9 and 10 produce A.  Every warp takes part
+// in the epilogue.
+constexpr int THREADS = 384;
 constexpr int TMEM_COLS = 512;
 constexpr uint16_t kPairMask = 0x3;
 #ifndef DG_SE_MULTICAST
@@ -82,6 +87,8 @@ constexpr int SMEM_BYTES = L_RING + W_RING + A_RING + 1024 /*align*/ + 256 /*bar
 
 static_assert(L_BYTES % 1024 == 0 && W_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "1 KiB alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+// each producer group keeps to every other slot of the logits and A rings
+static_assert(LSTAGES % 2 == 0 && ASTAGES % 2 == 0, "even ring depths");
 
 struct Params {
     const float *lse;
@@ -157,14 +164,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < LSTAGES; ++s) {
             mbar_init(smem_u32(&full_l[s]), 1);
-            mbar_init(smem_u32(&empty_l[s]), PRODUCER_WARPS);
+            mbar_init(smem_u32(&empty_l[s]), PRODUCER_WARPS / 2);
         }
         for (int s = 0; s < WSTAGES; ++s) {
             mbar_init(smem_u32(&full_w[s]), 1);
             mbar_init(smem_u32(&empty[s]), kCtasPerUnit);
         }
         for (int s = 0; s < ASTAGES; ++s) {
-            mbar_init(smem_u32(&full_a[s]), PRODUCER_WARPS);
+            mbar_init(smem_u32(&full_a[s]), PRODUCER_WARPS / 2);
             mbar_init(smem_u32(&empty_a[s]), 1);
         }
         mbar_init(smem_u32(acc_full), 1);
@@ -181,8 +188,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     // the peer's barriers exist before any multicast or commit reaches them
     cluster_sync_all();
     const uint32_t tmem_base = *tmem_slot;
+    bool ok = true;  // false once this thread gave up on a wait
 
-    if (warp == 0) {
+    if (warp == 11) {
         // ------------------------------------------------------------ W TMA (this CTA's half, multicast)
         if (lane == 0) {
             int issued[WSTAGES];
@@ -190,7 +198,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int nbox = 4 * halves / kCtasPerUnit;  // this CTA's share of the 4 * halves W boxes
             const uint64_t w_policy = l2_policy_evict_first();
             const uint32_t w_bytes = (uint32_t)halves * W_HALF_BYTES;
-            bool ok = true;
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % WSTAGES;
                 const uint32_t u = (uint32_t)(i / WSTAGES);
@@ -217,12 +224,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int s = 0; s < WSTAGES; ++s)
                     if (issued[s] > 0) drain_wait(smem_u32(&full_w[s]), (issued[s] - 1) & 1);
         }
-    } else if (warp == 2) {
+    } else if (warp == 8) {
         // ------------------------------------------------------------ logits TMA
         if (lane == 0) {
             int issued[LSTAGES];
             for (int s = 0; s < LSTAGES; ++s) issued[s] = 0;
-            bool ok = true;
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % LSTAGES;
                 const uint32_t u = (uint32_t)(i / LSTAGES);
@@ -240,15 +246,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int s = 0; s < LSTAGES; ++s)
                     if (issued[s] > 0) drain_wait(smem_u32(&full_l[s]), (issued[s] - 1) & 1);
         }
-    } else if (warp == 1) {
+    } else if (warp == 4) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(BM, 256, /*A K-major*/ 0, /*B N-major*/ 1);
             bool issued_any = false;
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % WSTAGES, sa = i % ASTAGES;
-                if (!mbar_wait(smem_u32(&full_a[sa]), (uint32_t)(i / ASTAGES) & 1, abort_flag)) break;
-                if (!mbar_wait(smem_u32(&full_w[s]), (uint32_t)(i / WSTAGES) & 1, abort_flag)) break;
+                if (!mbar_wait(smem_u32(&full_a[sa]), (uint32_t)(i / ASTAGES) & 1, abort_flag) ||
+                    !mbar_wait(smem_u32(&full_w[s]), (uint32_t)(i / WSTAGES) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
                 const uint32_t b_addr = smem_u32(w_ring + s * W_BYTES);
                 const uint32_t a_addr = smem_u32(a_ring + sa * A_BYTES);
@@ -272,17 +281,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             umma_commit(smem_u32(acc_full));
             if (*abort_flag && issued_any) drain_wait(smem_u32(acc_full), 0);
         }
-    } else {
-        // ------------------------------------------------------------ A producers, then epilogue
-        const int pw = warp - 3;          // producer warp 0..7
-        const int quarter = warp & 3;     // TMEM lane quarter this warp may access
-        const int half = pw >> 2;         // which 16 of the block's 32 entries (and, later, which columns)
-        const int r = quarter * 32 + lane;
+    } else if ((warp & 3) != 0 && warp < 11) {
+        // ------------------------------------------------------------ A producers
+        // two groups of four warps take alternate blocks, each warp 32 rows x all 32 entries:
+        // a warp has two block times for the dependent chain of one block
+        const int pw = 3 * (warp >> 2) + (warp & 3) - 1;  // producer 0..7 (warps 1-3, 5-7, 9, 10)
+        const int grp = pw >> 2;                           // blocks i with i % 2 == grp
+        const int r = (pw & 3) * 32 + lane;                // row of the tile
         const int row = row0 + r;
         const bool valid_row = row < p.R;
         const float neg_lse2 = valid_row ? -p.lse[row] * kLog2e : 0.0f;
-        bool ok = true;
-        for (int i = 0; i < nkb; ++i) {
+        for (int i = grp; i < nkb; i += 2) {
             const int sl = i % LSTAGES;
             const int s = i % ASTAGES;
             const uint32_t ul = (uint32_t)(i / LSTAGES);
@@ -293,29 +302,28 @@ __global__ void __launch_bounds__(THREADS, 1)
                 break;
             }
             const uint8_t *lt = l_ring + sl * L_BYTES;
-            const int64_t k = p.k_begin + (kb0 + i) * BK + 16 * half;
-            const bool edge = (k < p.vocab_start) || (k + 16 > p.vocab_end);
-            uint32_t packed[8];
+            const int64_t k = p.k_begin + (kb0 + i) * BK;
+            const bool edge = (k < p.vocab_start) || (k + BK > p.vocab_end);
+            uint32_t packed[16];
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int c = 4 * half + cc;  // 16-byte chunk of the 128-byte row
+            for (int c = 0; c < 8; ++c) {  // 16-byte chunk of the 128-byte row
                 const float4 v = *reinterpret_cast<const float4 *>(lt + r * 128 + ((c ^ (r & 7)) << 4));
                 float e0 = ex2_approx(fmaf(v.x, kLog2e, neg_lse2));
                 float e1 = ex2_approx(fmaf(v.y, kLog2e, neg_lse2));
                 float e2 = ex2_approx(fmaf(v.z, kLog2e, neg_lse2));
                 float e3 = ex2_approx(fmaf(v.w, kLog2e, neg_lse2));
                 if (edge) {
-                    const int64_t v0 = k + 4 * cc;
+                    const int64_t v0 = k + 4 * c;
                     if (v0 + 0 < p.vocab_start || v0 + 0 >= p.vocab_end) e0 = 0.f;
                     if (v0 + 1 < p.vocab_start || v0 + 1 >= p.vocab_end) e1 = 0.f;
                     if (v0 + 2 < p.vocab_start || v0 + 2 >= p.vocab_end) e2 = 0.f;
                     if (v0 + 3 < p.vocab_start || v0 + 3 >= p.vocab_end) e3 = 0.f;
                 }
                 if (!valid_row) e0 = e1 = e2 = e3 = 0.f;
-                packed[2 * cc] = pack_bf16x2(e0, e1);
-                packed[2 * cc + 1] = pack_bf16x2(e2, e3);
+                packed[2 * c] = pack_bf16x2(e0, e1);
+                packed[2 * c + 1] = pack_bf16x2(e2, e3);
             }
-            // the logits slot is free once all producer warps have read it
+            // the logits slot is free once the group's four warps have read it
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty_l[sl]));
             // the A slot is free once this CTA's MMAs of its previous round are done
@@ -325,32 +333,39 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             uint8_t *at = a_ring + s * A_BYTES;
 #pragma unroll
-            for (int h8 = 0; h8 < 2; ++h8) {
-                const int c8 = 2 * half + h8;  // 16-byte chunk of the 64-byte A row
-                const uint4 w = make_uint4(packed[4 * h8], packed[4 * h8 + 1], packed[4 * h8 + 2], packed[4 * h8 + 3]);
+            for (int c8 = 0; c8 < 4; ++c8) {  // 16-byte chunk of the 64-byte A row
+                const uint4 w = make_uint4(packed[4 * c8], packed[4 * c8 + 1], packed[4 * c8 + 2], packed[4 * c8 + 3]);
                 *reinterpret_cast<uint4 *>(at + r * 64 + ((c8 ^ ((r >> 1) & 3)) << 4)) = w;
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&full_a[s]));
         }
-        // epilogue: accumulator -> partial tile, layout [BN/4 column groups][128 rows][4];
-        // the two warps of a lane quarter take one half of the columns each
+    }
+
+    // ---------------------------------------------------------------- epilogue (all warps)
+    // accumulator -> partial tile, layout [BN/4 column groups][128 rows][4]; a warp reads the
+    // TMEM lane quarter of its scheduler, the three warps of a quarter one third of the columns each
+    __syncwarp();
+    {
+        const int quarter = warp & 3;
+        const int third = warp >> 2;
+        const int r = quarter * 32 + lane;
         float4 *dst = reinterpret_cast<float4 *>(p.ws) +
                       ((int64_t)(j * p.m_tiles + mt) * p.n_tiles + nt) * (BN / 4) * BM;
+        const int nch = halves * 8;  // 32-column chunks of this tile
+        const int c_lo = third * nch / 3, c_hi = (third + 1) * nch / 3;
         // tcgen05.ld is warp-collective: the warp goes on only if every lane got here cleanly
         bool have_acc = false;
         if (nkb > 0 && __all_sync(0xffffffffu, ok)) {
             const bool got = mbar_wait(smem_u32(acc_full), 0, abort_flag);
             have_acc = __all_sync(0xffffffffu, got);
         }
-        const int chunks = halves * 4;  // 32-column chunks per warp
         if (have_acc) {
             tc_fence_after();
             const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll 1
-            for (int jj = 0; jj < chunks; ++jj) {
-                const int jc = half * chunks + jj;
+            for (int jc = c_lo; jc < c_hi; ++jc) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(trow + jc * 32, v);
                 tmem_ld_wait();
@@ -362,8 +377,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
         } else if (nkb == 0) {
-            for (int cg4 = half * chunks * 8; cg4 < (half + 1) * chunks * 8; ++cg4)
-                dst[cg4 * BM + r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int cg4 = c_lo * 8; cg4 < c_hi * 8; ++cg4) dst[cg4 * BM + r] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
 
