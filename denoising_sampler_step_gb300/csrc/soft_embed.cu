@@ -49,16 +49,18 @@ constexpr int BK = 32;           // vocabulary entries per block
 #ifndef DG_SE_LSTAGES
 #define DG_SE_LSTAGES 4
 #endif
-#ifndef DG_SE_WSTAGES
-#define DG_SE_WSTAGES 4
-#endif
-#ifndef DG_SE_ASTAGES
-#define DG_SE_ASTAGES 4
+#ifndef DG_SE_STAGES
+#define DG_SE_STAGES 4
 #endif
 constexpr int LSTAGES = DG_SE_LSTAGES;  // logits ring, released by the producers once read
-constexpr int WSTAGES = DG_SE_WSTAGES;  // W ring, released once both CTAs' MMAs are done
-constexpr int ASTAGES = DG_SE_ASTAGES;  // A ring, released once this CTA's MMAs are done
-constexpr int PRODUCER_WARPS = 8;       // two groups of four (alternate blocks), 32 rows each
+constexpr int STAGES = DG_SE_STAGES;    // W and A rings (one index), released once both CTAs' MMAs are done
+constexpr int PRODUCER_WARPS = 8;
+#ifndef DG_SE_PGROUPS
+#define DG_SE_PGROUPS 2
+#endif
+constexpr int PGROUPS = DG_SE_PGROUPS;           // producer groups, taking the blocks in turn
+constexpr int GROUP_WARPS = PRODUCER_WARPS / PGROUPS;
+constexpr int ROWS_PER_LANE = 128 / (32 * GROUP_WARPS);
 // Warp roles.  A thread blocked in a barrier wait or in a full MMA/TMA queue slows the
 // shared-memory work of the other warps on its scheduler (warp % 4), so: warp 4 issues the
 // MMAs and warp 8 the logits TMA (scheduler 0, no producers); warp 11 issues the W TMA
@@ -81,14 +83,14 @@ constexpr int W_HALF_BYTES = 4 * W_BOX_BYTES;
 constexpr int W_BYTES = BK * BN * 2;      // up to 8 boxes
 constexpr int A_BYTES = BM * BK * 2;      // bf16 probabilities, rows of 64 B (64-byte swizzle)
 constexpr int L_RING = LSTAGES * L_BYTES;
-constexpr int W_RING = WSTAGES * W_BYTES;
-constexpr int A_RING = ASTAGES * A_BYTES;
+constexpr int W_RING = STAGES * W_BYTES;
+constexpr int A_RING = STAGES * A_BYTES;
 constexpr int SMEM_BYTES = L_RING + W_RING + A_RING + 1024 /*align*/ + 256 /*barriers*/;
 
 static_assert(L_BYTES % 1024 == 0 && W_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "1 KiB alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 // each producer group keeps to every other slot of the logits and A rings
-static_assert(LSTAGES % 2 == 0 && ASTAGES % 2 == 0, "even ring depths");
+static_assert(LSTAGES % PGROUPS == 0 && STAGES % PGROUPS == 0, "ring depths a multiple of the producer groups");
 
 struct Params {
     const float *lse;
@@ -122,10 +124,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t *full_l = bars;                   // logits tile landed
     uint64_t *empty_l = full_l + LSTAGES;      // the producer warps have read it
     uint64_t *full_w = empty_l + LSTAGES;      // W tile landed (both halves)
-    uint64_t *empty = full_w + WSTAGES;        // both CTAs' MMAs done with the W slot
-    uint64_t *full_a = empty + WSTAGES;        // A operand written by the producer warps
-    uint64_t *empty_a = full_a + ASTAGES;      // this CTA's MMAs done with the A slot
-    uint64_t *acc_full = empty_a + ASTAGES;    // accumulator complete
+    uint64_t *full_a = full_w + STAGES;        // A operand written by a producer group
+    uint64_t *empty = full_a + STAGES;         // both CTAs' MMAs done with the W + A slot
+    uint64_t *acc_full = empty + STAGES;       // accumulator complete
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -164,15 +165,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < LSTAGES; ++s) {
             mbar_init(smem_u32(&full_l[s]), 1);
-            mbar_init(smem_u32(&empty_l[s]), PRODUCER_WARPS / 2);
+            mbar_init(smem_u32(&empty_l[s]), GROUP_WARPS);
         }
-        for (int s = 0; s < WSTAGES; ++s) {
+        for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_u32(&full_w[s]), 1);
+            mbar_init(smem_u32(&full_a[s]), GROUP_WARPS);
             mbar_init(smem_u32(&empty[s]), kCtasPerUnit);
-        }
-        for (int s = 0; s < ASTAGES; ++s) {
-            mbar_init(smem_u32(&full_a[s]), PRODUCER_WARPS / 2);
-            mbar_init(smem_u32(&empty_a[s]), 1);
         }
         mbar_init(smem_u32(acc_full), 1);
         *abort_flag = 0;
@@ -193,14 +191,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 11) {
         // ------------------------------------------------------------ W TMA (this CTA's half, multicast)
         if (lane == 0) {
-            int issued[WSTAGES];
-            for (int s = 0; s < WSTAGES; ++s) issued[s] = 0;
+            int issued[STAGES];
+            for (int s = 0; s < STAGES; ++s) issued[s] = 0;
             const int nbox = 4 * halves / kCtasPerUnit;  // this CTA's share of the 4 * halves W boxes
             const uint64_t w_policy = l2_policy_evict_first();
             const uint32_t w_bytes = (uint32_t)halves * W_HALF_BYTES;
             for (int i = 0; i < nkb; ++i) {
-                const int s = i % WSTAGES;
-                const uint32_t u = (uint32_t)(i / WSTAGES);
+                const int s = i % STAGES;
+                const uint32_t u = (uint32_t)(i / STAGES);
                 if (u > 0 && !mbar_wait(smem_u32(&empty[s]), (u - 1) & 1, abort_flag)) {
                     ok = false;
                     break;
@@ -221,7 +219,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 issued[s] = (int)u + 1;
             }
             if (!ok)
-                for (int s = 0; s < WSTAGES; ++s)
+                for (int s = 0; s < STAGES; ++s)
                     if (issued[s] > 0) drain_wait(smem_u32(&full_w[s]), (issued[s] - 1) & 1);
         }
     } else if (warp == 8) {
@@ -250,32 +248,40 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(BM, 256, /*A K-major*/ 0, /*B N-major*/ 1);
+            // operand descriptors of slot 0; a slot, a K = 16 step or a 256-column half is a
+            // constant added to the start-address field (addresses stay below 2^18 bytes)
+            // A: K-major, 64-byte rows, 8-row groups 512 B apart; +32 B per K = 16 step
+            const uint64_t a_desc0 = smem_desc(smem_u32(a_ring), 16, 512, 4);
+            // B: N-major, 64-column atoms 4 KiB apart (LBO), 8-row groups 1 KiB apart (SBO);
+            // +2 KiB per K = 16 step
+            const uint64_t b_desc0 = smem_desc(smem_u32(w_ring), W_BOX_BYTES, 1024, 2);
+            constexpr uint64_t kA_K16 = 32 >> 4, kB_K16 = 2048 >> 4, kB_HALF = W_HALF_BYTES >> 4;
             bool issued_any = false;
             for (int i = 0; i < nkb; ++i) {
-                const int s = i % WSTAGES, sa = i % ASTAGES;
-                if (!mbar_wait(smem_u32(&full_a[sa]), (uint32_t)(i / ASTAGES) & 1, abort_flag) ||
-                    !mbar_wait(smem_u32(&full_w[s]), (uint32_t)(i / WSTAGES) & 1, abort_flag)) {
+                const int s = i % STAGES;
+                const uint32_t ph = (uint32_t)(i / STAGES) & 1;
+                // both tests issued before either result is used (their latencies overlap);
+                // the bounded waits only when a tile is not there yet
+                const bool a_in = mbar_try_wait(smem_u32(&full_a[s]), ph);
+                const bool w_in = mbar_try_wait(smem_u32(&full_w[s]), ph);
+                if (!(a_in && w_in) && (!mbar_wait(smem_u32(&full_a[s]), ph, abort_flag) ||
+                                        !mbar_wait(smem_u32(&full_w[s]), ph, abort_flag))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t b_addr = smem_u32(w_ring + s * W_BYTES);
-                const uint32_t a_addr = smem_u32(a_ring + sa * A_BYTES);
-#pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
-                    // A: K-major, 64-byte rows, 8-row groups 512 B apart; +32 B per K=16 step
-                    const uint64_t a_desc = smem_desc(a_addr + kk * 32, 16, 512, 4);
-                    for (int h = 0; h < halves; ++h) {
-                        // B: N-major, 64-column atoms 4 KiB apart (LBO), 8-row groups 1 KiB apart (SBO)
-                        const uint64_t b_desc = smem_desc(b_addr + h * W_HALF_BYTES + kk * 2048, W_BOX_BYTES, 1024, 2);
-                        umma_bf16(tmem_base + h * 256, a_desc, b_desc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
-                    }
-                }
+                const uint64_t ad = a_desc0 + (uint64_t)((s * A_BYTES) >> 4);
+                const uint64_t bd = b_desc0 + (uint64_t)((s * W_BYTES) >> 4);
+                const uint32_t acc = i > 0 ? 1u : 0u;
+                umma_bf16(tmem_base, ad, bd, idesc, acc);
+                if (halves == 2) umma_bf16(tmem_base + 256, ad, bd + kB_HALF, idesc, acc);
+                umma_bf16(tmem_base, ad + kA_K16, bd + kB_K16, idesc, 1u);
+                if (halves == 2) umma_bf16(tmem_base + 256, ad + kA_K16, bd + kB_HALF + kB_K16, idesc, 1u);
+                // one commit releases the W and A slots once both CTAs' MMAs have read them
                 if (kMulticast)
                     umma_commit_multicast(smem_u32(&empty[s]), kPairMask);
                 else
                     umma_commit(smem_u32(&empty[s]));
-                umma_commit(smem_u32(&empty_a[sa]));
                 issued_any = true;
             }
             umma_commit(smem_u32(acc_full));
@@ -283,19 +289,26 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if ((warp & 3) != 0 && warp < 11) {
         // ------------------------------------------------------------ A producers
-        // two groups of four warps take alternate blocks, each warp 32 rows x all 32 entries:
-        // a warp has two block times for the dependent chain of one block
+        // PGROUPS groups take the blocks in turn, so a warp has PGROUPS block times for the
+        // dependent chain of one block (barrier waits, stores, proxy fence, arrival); a
+        // warp converts ROWS_PER_LANE * 32 rows x all 32 entries of its group's block
         const int pw = 3 * (warp >> 2) + (warp & 3) - 1;  // producer 0..7 (warps 1-3, 5-7, 9, 10)
-        const int grp = pw >> 2;                           // blocks i with i % 2 == grp
-        const int r = (pw & 3) * 32 + lane;                // row of the tile
-        const int row = row0 + r;
-        const bool valid_row = row < p.R;
-        const float neg_lse2 = valid_row ? -p.lse[row] * kLog2e : 0.0f;
-        for (int i = grp; i < nkb; i += 2) {
+        const int grp = pw / GROUP_WARPS;
+        const int wig = pw % GROUP_WARPS;
+        int rr[ROWS_PER_LANE];
+        float neg_lse2[ROWS_PER_LANE];
+#pragma unroll
+        for (int q = 0; q < ROWS_PER_LANE; ++q) {
+            rr[q] = (wig * ROWS_PER_LANE + q) * 32 + lane;  // row of the tile
+            const int row = row0 + rr[q];
+            // rows past R are zero-filled by the TMA: an offset of -inf makes their entries 0
+            neg_lse2[q] = row < p.R ? -p.lse[row] * kLog2e : -INFINITY;
+        }
+        for (int i = grp; i < nkb; i += PGROUPS) {
             const int sl = i % LSTAGES;
-            const int s = i % ASTAGES;
+            const int s = i % STAGES;
             const uint32_t ul = (uint32_t)(i / LSTAGES);
-            const uint32_t u = (uint32_t)(i / ASTAGES);
+            const uint32_t u = (uint32_t)(i / STAGES);
             // every lane waits (acquire), the warp decides together
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_l[sl]), ul & 1, abort_flag))) {
                 ok = false;
@@ -304,41 +317,49 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint8_t *lt = l_ring + sl * L_BYTES;
             const int64_t k = p.k_begin + (kb0 + i) * BK;
             const bool edge = (k < p.vocab_start) || (k + BK > p.vocab_end);
-            uint32_t packed[16];
+            uint32_t packed[ROWS_PER_LANE][16];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {  // 16-byte chunk of the 128-byte row
-                const float4 v = *reinterpret_cast<const float4 *>(lt + r * 128 + ((c ^ (r & 7)) << 4));
-                float e0 = ex2_approx(fmaf(v.x, kLog2e, neg_lse2));
-                float e1 = ex2_approx(fmaf(v.y, kLog2e, neg_lse2));
-                float e2 = ex2_approx(fmaf(v.z, kLog2e, neg_lse2));
-                float e3 = ex2_approx(fmaf(v.w, kLog2e, neg_lse2));
-                if (edge) {
-                    const int64_t v0 = k + 4 * c;
-                    if (v0 + 0 < p.vocab_start || v0 + 0 >= p.vocab_end) e0 = 0.f;
-                    if (v0 + 1 < p.vocab_start || v0 + 1 >= p.vocab_end) e1 = 0.f;
-                    if (v0 + 2 < p.vocab_start || v0 + 2 >= p.vocab_end) e2 = 0.f;
-                    if (v0 + 3 < p.vocab_start || v0 + 3 >= p.vocab_end) e3 = 0.f;
+            for (int q = 0; q < ROWS_PER_LANE; ++q) {
+                const int r = rr[q];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {  // 16-byte chunk of the 128-byte row
+                    const float4 v = *reinterpret_cast<const float4 *>(lt + r * 128 + ((c ^ (r & 7)) << 4));
+                    float e0 = ex2_approx(fmaf(v.x, kLog2e, neg_lse2[q]));
+                    float e1 = ex2_approx(fmaf(v.y, kLog2e, neg_lse2[q]));
+                    float e2 = ex2_approx(fmaf(v.z, kLog2e, neg_lse2[q]));
+                    float e3 = ex2_approx(fmaf(v.w, kLog2e, neg_lse2[q]));
+                    if (edge) {
+                        const int64_t v0 = k + 4 * c;
+                        if (v0 + 0 < p.vocab_start || v0 + 0 >= p.vocab_end) e0 = 0.f;
+                        if (v0 + 1 < p.vocab_start || v0 + 1 >= p.vocab_end) e1 = 0.f;
+                        if (v0 + 2 < p.vocab_start || v0 + 2 >= p.vocab_end) e2 = 0.f;
+                        if (v0 + 3 < p.vocab_start || v0 + 3 >= p.vocab_end) e3 = 0.f;
+                    }
+                    packed[q][2 * c] = pack_bf16x2(e0, e1);
+                    packed[q][2 * c + 1] = pack_bf16x2(e2, e3);
                 }
-                if (!valid_row) e0 = e1 = e2 = e3 = 0.f;
-                packed[2 * c] = pack_bf16x2(e0, e1);
-                packed[2 * c + 1] = pack_bf16x2(e2, e3);
             }
-            // the logits slot is free once the group's four warps have read it
+            // the logits slot is free once the group's warps have read it
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty_l[sl]));
-            // the A slot is free once this CTA's MMAs of its previous round are done
-            if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty_a[s]), (u - 1) & 1, abort_flag))) {
+            // the A slot is free once both CTAs' MMAs of its previous round are done
+            if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[s]), (u - 1) & 1, abort_flag))) {
                 ok = false;
                 break;
             }
             uint8_t *at = a_ring + s * A_BYTES;
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {  // 16-byte chunk of the 64-byte A row
-                const uint4 w = make_uint4(packed[4 * c8], packed[4 * c8 + 1], packed[4 * c8 + 2], packed[4 * c8 + 3]);
-                *reinterpret_cast<uint4 *>(at + r * 64 + ((c8 ^ ((r >> 1) & 3)) << 4)) = w;
+            for (int q = 0; q < ROWS_PER_LANE; ++q) {
+                const int r = rr[q];
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {  // 16-byte chunk of the 64-byte A row
+                    const uint4 w = make_uint4(packed[q][4 * c8], packed[q][4 * c8 + 1], packed[q][4 * c8 + 2],
+                                               packed[q][4 * c8 + 3]);
+                    *reinterpret_cast<uint4 *>(at + r * 64 + ((c8 ^ ((r >> 1) & 3)) << 4)) = w;
+                }
             }
             fence_proxy_async_smem();
-            __syncwarp();
+            __syncwarp();  // every lane's A stores (and proxy fence) before the arrival
             if (lane == 0) mbar_arrive(smem_u32(&full_a[s]));
         }
     }
