@@ -89,7 +89,7 @@ namespace {
 dg_status run_soft_embed(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t s, int64_t e,
                          const uint16_t *W, int64_t ldw, int64_t d, float gamma, float *out, int64_t ldo,
                          void *ws, size_t ws_bytes, cudaStream_t stream, StreamHook between = nullptr,
-                         void *ctx = nullptr) {
+                         void *ctx = nullptr, bool overlap_previous = false) {
     if (R == 0) return DG_OK;
     if (e == s) {
         cudaError_t err = launch_fill_zero(out, R, d, ldo, stream);
@@ -105,7 +105,8 @@ dg_status run_soft_embed(const float *logits, int64_t ldl, const float *lse, int
     if (!aligned16(ws)) return fail(DG_ERR_UNSUPPORTED, "soft embed: workspace must be 16-byte aligned");
     const char *msg = "soft embed";
     cudaError_t err =
-        launch_soft_embed(logits, ldl, lse, R, s, e, W, ldw, d, gamma, out, ldo, ws, plan, stream, &msg, between, ctx);
+        launch_soft_embed(logits, ldl, lse, R, s, e, W, ldw, d, gamma, out, ldo, ws, plan, stream, &msg, between, ctx,
+                          overlap_previous);
     return err == cudaSuccess ? DG_OK : cuda_fail(err, msg);
 }
 
@@ -234,8 +235,10 @@ dg_status dg_sampler_step(const float *logits, int32_t n_req, int32_t L_c, int64
                               workspace_bytes, s);
     }
     AcceptArgs acc{H, kappa, budgets, n_req, L_c, min_accept, order, mask, n_accepted};
+    // the product overlaps the tail of the statistics kernel (its W and logits loads do not
+    // depend on it), the acceptance overlaps the product
     return run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, ldw, d, gamma, E, ldo, workspace,
-                          workspace_bytes, s, accept_hook, &acc);
+                          workspace_bytes, s, accept_hook, &acc, /*overlap_previous=*/true);
 }
 
 dg_status dg_get_device_status(dg_stream_t stream) {

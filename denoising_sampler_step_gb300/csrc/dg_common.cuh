@@ -28,6 +28,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// Programmatic dependent launch: wait until the grid this one was allowed to overlap has
+// completed (its writes visible); let the grid queued after this one start.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -175,6 +182,16 @@ __device__ __forceinline__ void tma_load_2d_multicast_hint(uint32_t dst, const v
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
         ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(dst),
         "l"(tmap), "r"(bar), "r"(x), "r"(y), "h"(cta_mask), "l"(policy)
+        : "memory");
+}
+
+// As tma_load_2d_multicast_hint for a 3-D tensor map (x innermost).
+__device__ __forceinline__ void tma_load_3d_multicast_hint(uint32_t dst, const void *tmap, uint32_t bar, int x,
+                                                           int y, int z, uint16_t cta_mask, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6, %7;" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(cta_mask), "l"(policy)
         : "memory");
 }
 

@@ -35,14 +35,16 @@ bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t 
 // Workspace bytes a plan needs with a given number of splits.
 size_t soft_embed_workspace_bytes(const SoftEmbedPlan &plan, int splits);
 // Queues the product, then `between(ctx, stream)` if given (work that may overlap the
-// product: the product lets the next kernel on the stream start early), then the split-K
-// reduce.  On failure *msg names the step.
+// product: the product lets the next kernel on the stream start early, once the kernel
+// before it has completed), then the split-K reduce.  overlap_previous: the product may
+// start while the kernel queued before it (the row statistics) still runs; it reads lse
+// only after that kernel has completed.  On failure *msg names the step.
 typedef cudaError_t (*StreamHook)(void *ctx, cudaStream_t stream);
 cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse, int64_t R,
                               int64_t vocab_start, int64_t vocab_end, const uint16_t *W, int64_t ldw,
                               int64_t d, float gamma, float *out, int64_t ldo, void *workspace,
                               const SoftEmbedPlan &plan, cudaStream_t stream, const char **msg,
-                              StreamHook between = nullptr, void *ctx = nullptr);
+                              StreamHook between = nullptr, void *ctx = nullptr, bool overlap_previous = false);
 
 int device_sm_count();
 

@@ -121,6 +121,9 @@ __global__ void __launch_bounds__(kStatsThreads, 4)
     __shared__ RowState warp_state[kStatsThreads / 32];
     __shared__ RowState cta_state[CLUSTER];
 
+    // the kernel queued next (the soft-embed product of a step) may start its CTAs now: it
+    // waits for this grid to complete before it reads anything this grid writes
+    grid_launch_dependents();
     const int rank = (int)(blockIdx.x % CLUSTER);
     const int64_t row = blockIdx.x / CLUSTER;
     const float *rowp = logits + row * ldl;

@@ -104,6 +104,7 @@ struct Params {
     int n_full;          // n-tiles of full width (two halves)
     int tail_halves;     // 1 if the last n-tile is 256 wide or less, else 0
     int splits, tail_splits;
+    int w3d;             // 1: the W map is 3-D (64 columns x rows x 64-column atoms), one load per CTA and block
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -130,9 +131,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
-    // the kernel queued next may start now: it never reads what this kernel writes
-    // (the split-K reduce after it is an ordinary launch and waits for completion)
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Overlap with the neighbours on the stream (programmatic dependent launch): this grid
+    // may start while the row-statistics grid before it runs, so every thread calls
+    // grid_dependency_wait() before it touches lse (or before it lets the next grid start);
+    // the W and logits loads of the first ring round do not depend on it and go first.
+    // The kernel queued next (the acceptance) reads only the row statistics, so each thread
+    // lets it start once its own wait has returned.
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = kMulticast ? cluster_ctarank() : 0;
 
@@ -195,10 +199,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int s = 0; s < STAGES; ++s) issued[s] = 0;
             const int nbox = 4 * halves / kCtasPerUnit;  // this CTA's share of the 4 * halves W boxes
             const uint64_t w_policy = l2_policy_evict_first();
-            const uint32_t w_bytes = (uint32_t)halves * W_HALF_BYTES;
+            // 3-D map: each CTA fetches four 64-column atoms in one load (the tail tile's
+            // second CTA reads atoms past d, which arrive zero-filled and are not used)
+            const bool w3d = kMulticast && p.w3d;
+            const uint32_t w_bytes = w3d ? (uint32_t)W_BYTES : (uint32_t)halves * W_HALF_BYTES;
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % STAGES;
                 const uint32_t u = (uint32_t)(i / STAGES);
+                if (i == STAGES) {  // the first round of W loads is out
+                    grid_dependency_wait();
+                    grid_launch_dependents();
+                }
                 if (u > 0 && !mbar_wait(smem_u32(&empty[s]), (u - 1) & 1, abort_flag)) {
                     ok = false;
                     break;
@@ -207,7 +218,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t bw = smem_u32(&full_w[s]);
                 mbar_arrive_expect_tx(bw, w_bytes);
                 const int wy = (int)(k - p.vocab_start);
-                for (int b = 0; b < nbox; ++b) {
+                if (w3d)
+                    tma_load_3d_multicast_hint(smem_u32(w_ring + s * W_BYTES + (int)rank * 4 * W_BOX_BYTES), &tm_w, bw,
+                                               0, wy, col0 / 64 + 4 * (int)rank, kPairMask, w_policy);
+                for (int b = 0; b < (w3d ? 0 : nbox); ++b) {
                     const int box = (int)rank * nbox + b;
                     if (kMulticast)
                         tma_load_2d_multicast_hint(smem_u32(w_ring + s * W_BYTES + box * W_BOX_BYTES), &tm_w, bw,
@@ -217,6 +231,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                                          col0 + 64 * box, wy, w_policy);
                 }
                 issued[s] = (int)u + 1;
+            }
+            if (nkb <= STAGES) {
+                grid_dependency_wait();
+                grid_launch_dependents();
             }
             if (!ok)
                 for (int s = 0; s < STAGES; ++s)
@@ -230,6 +248,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % LSTAGES;
                 const uint32_t u = (uint32_t)(i / LSTAGES);
+                if (i == LSTAGES) {  // the first round of logits loads is out
+                    grid_dependency_wait();
+                    grid_launch_dependents();
+                }
                 if (u > 0 && !mbar_wait(smem_u32(&empty_l[s]), (u - 1) & 1, abort_flag)) {
                     ok = false;
                     break;
@@ -240,6 +262,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tma_load_2d(smem_u32(l_ring + s * L_BYTES), &tm_logits, bl, (int)k, row0);
                 issued[s] = (int)u + 1;
             }
+            if (nkb <= LSTAGES) {
+                grid_dependency_wait();
+                grid_launch_dependents();
+            }
             if (!ok)
                 for (int s = 0; s < LSTAGES; ++s)
                     if (issued[s] > 0) drain_wait(smem_u32(&full_l[s]), (issued[s] - 1) & 1);
@@ -247,6 +273,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp == 4) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
+            grid_dependency_wait();  // nothing to issue before the producers' first tile anyway
+            grid_launch_dependents();
             constexpr uint32_t idesc = idesc_bf16_f32(BM, 256, /*A K-major*/ 0, /*B N-major*/ 1);
             // operand descriptors of slot 0; a slot, a K = 16 step or a 256-column half is a
             // constant added to the start-address field (addresses stay below 2^18 bytes)
@@ -295,6 +323,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int pw = 3 * (warp >> 2) + (warp & 3) - 1;  // producer 0..7 (warps 1-3, 5-7, 9, 10)
         const int grp = pw / GROUP_WARPS;
         const int wig = pw % GROUP_WARPS;
+        grid_dependency_wait();  // lse comes from the grid queued before this one
+        grid_launch_dependents();
         int rr[ROWS_PER_LANE];
         float neg_lse2[ROWS_PER_LANE];
 #pragma unroll
@@ -321,23 +351,26 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int q = 0; q < ROWS_PER_LANE; ++q) {
                 const int r = rr[q];
+                // all eight 16-byte loads first, then the exponentials, then the packing
+                float4 v[8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {  // 16-byte chunk of the 128-byte row
-                    const float4 v = *reinterpret_cast<const float4 *>(lt + r * 128 + ((c ^ (r & 7)) << 4));
-                    float e0 = ex2_approx(fmaf(v.x, kLog2e, neg_lse2[q]));
-                    float e1 = ex2_approx(fmaf(v.y, kLog2e, neg_lse2[q]));
-                    float e2 = ex2_approx(fmaf(v.z, kLog2e, neg_lse2[q]));
-                    float e3 = ex2_approx(fmaf(v.w, kLog2e, neg_lse2[q]));
-                    if (edge) {
-                        const int64_t v0 = k + 4 * c;
-                        if (v0 + 0 < p.vocab_start || v0 + 0 >= p.vocab_end) e0 = 0.f;
-                        if (v0 + 1 < p.vocab_start || v0 + 1 >= p.vocab_end) e1 = 0.f;
-                        if (v0 + 2 < p.vocab_start || v0 + 2 >= p.vocab_end) e2 = 0.f;
-                        if (v0 + 3 < p.vocab_start || v0 + 3 >= p.vocab_end) e3 = 0.f;
-                    }
-                    packed[q][2 * c] = pack_bf16x2(e0, e1);
-                    packed[q][2 * c + 1] = pack_bf16x2(e2, e3);
+                for (int c = 0; c < 8; ++c)  // 16-byte chunk of the 128-byte row
+                    v[c] = *reinterpret_cast<const float4 *>(lt + r * 128 + ((c ^ (r & 7)) << 4));
+                float e[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    e[4 * c + 0] = ex2_approx(fmaf(v[c].x, kLog2e, neg_lse2[q]));
+                    e[4 * c + 1] = ex2_approx(fmaf(v[c].y, kLog2e, neg_lse2[q]));
+                    e[4 * c + 2] = ex2_approx(fmaf(v[c].z, kLog2e, neg_lse2[q]));
+                    e[4 * c + 3] = ex2_approx(fmaf(v[c].w, kLog2e, neg_lse2[q]));
                 }
+                if (edge) {  // a block that straddles an end of the slice (warp-uniform, rare)
+#pragma unroll
+                    for (int t = 0; t < 32; ++t)
+                        if (k + t < p.vocab_start || k + t >= p.vocab_end) e[t] = 0.f;
+                }
+#pragma unroll
+                for (int t = 0; t < 16; ++t) packed[q][t] = pack_bf16x2(e[2 * t], e[2 * t + 1]);
             }
             // the logits slot is free once the group's warps have read it
             __syncwarp();
@@ -364,6 +397,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     }
 
+    // threads without a role in the main loop (warp 0, warp 11 and lanes 1-31 of the
+    // single-thread roles) and roles whose wait came last
+    grid_dependency_wait();
+    grid_launch_dependents();
     // ---------------------------------------------------------------- epilogue (all warps)
     // accumulator -> partial tile, layout [BN/4 column groups][128 rows][4]; a warp reads the
     // TMEM lane quarter of its scheduler, the three warps of a quarter one third of the columns each
@@ -430,8 +467,22 @@ __global__ void splitk_reduce_kernel(const float4 *__restrict__ ws, const Params
         const int S = nt < p.n_full ? p.splits : p.tail_splits;
         const int64_t split_stride = (int64_t)p.m_tiles * p.n_tiles * tile_elems;
         const float4 *src = ws + ((int64_t)mt * p.n_tiles + nt) * tile_elems + (int64_t)cg * BM + r;
+        // loads issued four at a time, added strictly in split order
         float4 acc = src[0];
-        for (int s = 1; s < S; ++s) {
+        int s = 1;
+        for (; s + 4 <= S; s += 4) {
+            float4 v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v[q] = src[(s + q) * split_stride];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                acc.x += v[q].x;
+                acc.y += v[q].y;
+                acc.z += v[q].z;
+                acc.w += v[q].w;
+            }
+        }
+        for (; s < S; ++s) {
             const float4 v = src[s * split_stride];
             acc.x += v.x;
             acc.y += v.y;
@@ -527,7 +578,7 @@ bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t 
 cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t vocab_start,
                               int64_t vocab_end, const uint16_t *W, int64_t ldw, int64_t d, float gamma, float *out,
                               int64_t ldo, void *workspace, const SoftEmbedPlan &plan, cudaStream_t stream,
-                              const char **msg, StreamHook between, void *ctx) {
+                              const char **msg, StreamHook between, void *ctx, bool overlap_previous) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
     if (!encode) {
         *msg = "cuTensorMapEncodeTiled is not available from the driver";
@@ -546,7 +597,20 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
             return cudaErrorInvalidValue;
         }
     }
-    {
+    // W: a 3-D view (64 columns of an atom, rows, atoms 128 bytes apart) when every atom's
+    // 64 columns lie inside the row pitch, else 2-D boxes of 64 columns
+    int w3d = 0;
+    const int64_t atoms = (d + 63) / 64;
+    if (kMulticast && atoms * 64 <= ldw) {
+        const cuuint64_t dims[3] = {64, (cuuint64_t)(vocab_end - vocab_start), (cuuint64_t)atoms};
+        const cuuint64_t strides[2] = {(cuuint64_t)ldw * 2, 128};
+        const cuuint32_t box[3] = {64, BK, 4};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        w3d = encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(W), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    if (!w3d) {
         const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)(vocab_end - vocab_start)};
         const cuuint64_t strides[1] = {(cuuint64_t)ldw * 2};
         const cuuint32_t box[2] = {64, BK};
@@ -583,6 +647,7 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     p.tail_halves = tail;
     p.splits = plan.splits;
     p.tail_splits = tail_splits_of(plan.splits, tail);
+    p.w3d = w3d;
     const int64_t pairs = (int64_t)(plan.m_tiles / kCtasPerUnit) * (n_full * (int64_t)p.splits + p.tail_splits);
 
     cudaLaunchConfig_t cfg = {};
@@ -590,13 +655,15 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kCtasPerUnit;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = overlap_previous ? 1 : 0;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, soft_embed_kernel, tm_l, tm_w, p);
     if (e != cudaSuccess) {
         *msg = "soft-embed kernel launch failed";
