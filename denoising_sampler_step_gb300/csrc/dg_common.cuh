@@ -154,6 +154,26 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+// Loads of a tcgen05 CTA pair: the tile lands in the executing CTA's shared memory and the
+// byte count completes on `bar`, which may be the barrier of the pair's other CTA (a
+// shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void *tmap, uint32_t bar, int x, int y,
+                                                      uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const void *tmap, uint32_t bar, int x, int y,
+                                                      int z, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
+        : "memory");
+}
+
 // The same load delivered to the same shared-memory offset of every CTA in cta_mask
 // (this GPU's own memory only); each destination's barrier at `bar` gets the bytes.
 __device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void *tmap, uint32_t bar, int x, int y,

@@ -49,8 +49,11 @@ constexpr int BK = 32;           // vocabulary entries per block
 #ifndef DG_SE_LSTAGES
 #define DG_SE_LSTAGES 4
 #endif
+#ifndef DG_SE_PAIR
+#define DG_SE_PAIR 0
+#endif
 #ifndef DG_SE_STAGES
-#define DG_SE_STAGES 4
+#define DG_SE_STAGES (DG_SE_PAIR ? 6 : 4)
 #endif
 constexpr int LSTAGES = DG_SE_LSTAGES;  // logits ring, released by the producers once read
 constexpr int STAGES = DG_SE_STAGES;    // W and A rings (one index), released once both CTAs' MMAs are done
@@ -69,25 +72,28 @@ constexpr int ROWS_PER_LANE = 128 / (32 * GROUP_WARPS);
 constexpr int THREADS = 384;
 constexpr int TMEM_COLS = 512;
 constexpr uint16_t kPairMask = 0x3;
-#ifndef DG_SE_MULTICAST
-#define DG_SE_MULTICAST 1
-#endif
-// 1: clusters of two CTAs (two 128-row halves) share each W tile by TMA multicast;
-// 0: independent CTAs, each loading its whole W tile (the row halves meet in L2)
-constexpr bool kMulticast = DG_SE_MULTICAST != 0;
-constexpr int kCtasPerUnit = kMulticast ? 2 : 1;
+// A cluster of two CTAs holds the two 128-row halves of a 256-row tile.
+// Default: each CTA issues M = 128 MMAs and the two share whole W tiles by TMA multicast.
+// DG_SE_PAIR=1: the two CTAs form a tcgen05 CTA pair; the even CTA issues M = 256 MMAs over
+//   both CTAs' rows and each CTA holds 128 of every 256 W columns (half-size W slots, a
+//   deeper ring).  Correct, but slower here: the odd CTA's producers must signal the even
+//   CTA's barrier with a cluster-scope release, which costs about a microsecond per block.
+constexpr bool kPair = DG_SE_PAIR != 0;
+constexpr int kCtasPerUnit = 2;
 
 constexpr int L_BYTES = BM * BK * 4;      // logits tile, rows of 128 B (128-byte swizzle)
 constexpr int W_BOX_BYTES = BK * 64 * 2;  // one TMA box: 32 rows x 64 columns
 constexpr int W_HALF_BYTES = 4 * W_BOX_BYTES;
-constexpr int W_BYTES = BK * BN * 2;      // up to 8 boxes
+constexpr int W_BYTES = BK * BN * 2;      // a block's whole W tile: 8 boxes
+constexpr int W_SLOT = kPair ? W_BYTES / 2 : W_BYTES;  // the part of it one CTA holds
+constexpr int W_ATOMS = W_SLOT / W_BOX_BYTES;          // 64-column atoms per CTA and block
 constexpr int A_BYTES = BM * BK * 2;      // bf16 probabilities, rows of 64 B (64-byte swizzle)
 constexpr int L_RING = LSTAGES * L_BYTES;
-constexpr int W_RING = STAGES * W_BYTES;
+constexpr int W_RING = STAGES * W_SLOT;
 constexpr int A_RING = STAGES * A_BYTES;
 constexpr int SMEM_BYTES = L_RING + W_RING + A_RING + 1024 /*align*/ + 256 /*barriers*/;
 
-static_assert(L_BYTES % 1024 == 0 && W_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "1 KiB alignment");
+static_assert(L_BYTES % 1024 == 0 && W_SLOT % 1024 == 0 && A_BYTES % 1024 == 0, "1 KiB alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 // each producer group keeps to every other slot of the logits and A rings
 static_assert(LSTAGES % PGROUPS == 0 && STAGES % PGROUPS == 0, "ring depths a multiple of the producer groups");
@@ -138,7 +144,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // The kernel queued next (the acceptance) reads only the row statistics, so each thread
     // lets it start once its own wait has returned.
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = kMulticast ? cluster_ctarank() : 0;
+    const uint32_t rank = cluster_ctarank();
 
     // work of this cluster (or CTA): (n-tile, row block, split)
     const int pair = blockIdx.x / kCtasPerUnit;
@@ -172,9 +178,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(smem_u32(&empty_l[s]), GROUP_WARPS);
         }
         for (int s = 0; s < STAGES; ++s) {
+            // pair: the even CTA's full_w counts both CTAs' W bytes, its full_a both CTAs'
+            // producer groups; one commit reaches each CTA's empty.  Multicast: each CTA's
+            // full_w counts the whole tile, and both CTAs' commits reach each empty.
             mbar_init(smem_u32(&full_w[s]), 1);
-            mbar_init(smem_u32(&full_a[s]), GROUP_WARPS);
-            mbar_init(smem_u32(&empty[s]), kCtasPerUnit);
+            mbar_init(smem_u32(&full_a[s]), kPair ? 2 * GROUP_WARPS : GROUP_WARPS);
+            mbar_init(smem_u32(&empty[s]), kPair ? 1 : kCtasPerUnit);
         }
         mbar_init(smem_u32(acc_full), 1);
         *abort_flag = 0;
@@ -183,7 +192,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         prefetch_tmap(&tm_w);
     }
     __syncwarp();
-    if (warp == 0) tmem_alloc<TMEM_COLS>(smem_u32(tmem_slot));
+    if (warp == 0) {
+        if (kPair)
+            tmem_alloc_pair<TMEM_COLS>(smem_u32(tmem_slot));  // a joint allocation in both CTAs
+        else
+            tmem_alloc<TMEM_COLS>(smem_u32(tmem_slot));
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -193,16 +207,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;  // false once this thread gave up on a wait
 
     if (warp == 11) {
-        // ------------------------------------------------------------ W TMA (this CTA's half, multicast)
+        // ------------------------------------------------------------ W TMA
+        // pair: this CTA's 128 columns of each 256-column half (atoms 4h + 2 rank, +1), the
+        //   bytes counted on the even CTA's full_w, which that CTA arms for both;
+        // multicast: this CTA's half of the boxes, delivered to both CTAs.
         if (lane == 0) {
             int issued[STAGES];
             for (int s = 0; s < STAGES; ++s) issued[s] = 0;
-            const int nbox = 4 * halves / kCtasPerUnit;  // this CTA's share of the 4 * halves W boxes
+            const int nbox = 4 * halves / kCtasPerUnit;  // multicast: this CTA's share of the 4 * halves boxes
             const uint64_t w_policy = l2_policy_evict_first();
-            // 3-D map: each CTA fetches four 64-column atoms in one load (the tail tile's
-            // second CTA reads atoms past d, which arrive zero-filled and are not used)
-            const bool w3d = kMulticast && p.w3d;
-            const uint32_t w_bytes = w3d ? (uint32_t)W_BYTES : (uint32_t)halves * W_HALF_BYTES;
+            // 3-D map: one load per CTA (pair: per 256-column half) fetches W_ATOMS or 2
+            // atoms; multicast tail tiles: the second CTA's atoms lie past d, arrive
+            // zero-filled and are not used
+            const bool w3d = p.w3d;
+            const uint32_t w_bytes = kPair ? (uint32_t)halves * 2 * 2 * W_BOX_BYTES
+                                           : (w3d ? (uint32_t)W_BYTES : (uint32_t)halves * W_HALF_BYTES);
+            const uint32_t lead = map_to_cta(smem_u32(&full_w[0]), 0);  // the even CTA's full_w[0]
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % STAGES;
                 const uint32_t u = (uint32_t)(i / STAGES);
@@ -216,19 +236,31 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 const int64_t k = p.k_begin + (kb0 + i) * BK;
                 const uint32_t bw = smem_u32(&full_w[s]);
-                mbar_arrive_expect_tx(bw, w_bytes);
                 const int wy = (int)(k - p.vocab_start);
+                if (kPair) {
+                    if (rank == 0) mbar_arrive_expect_tx(bw, w_bytes);
+                    const uint32_t bl = lead + 8u * (uint32_t)s;
+                    for (int h = 0; h < halves; ++h) {
+                        const uint32_t dst = smem_u32(w_ring + s * W_SLOT + h * 2 * W_BOX_BYTES);
+                        const int atom = col0 / 64 + 4 * h + 2 * (int)rank;
+                        if (w3d) {
+                            tma_load_3d_pair_hint(dst, &tm_w, bl, 0, wy, atom, w_policy);
+                        } else {
+                            tma_load_2d_pair_hint(dst, &tm_w, bl, 64 * atom, wy, w_policy);
+                            tma_load_2d_pair_hint(dst + W_BOX_BYTES, &tm_w, bl, 64 * (atom + 1), wy, w_policy);
+                        }
+                    }
+                    issued[s] = (int)u + 1;
+                    continue;
+                }
+                mbar_arrive_expect_tx(bw, w_bytes);
                 if (w3d)
-                    tma_load_3d_multicast_hint(smem_u32(w_ring + s * W_BYTES + (int)rank * 4 * W_BOX_BYTES), &tm_w, bw,
+                    tma_load_3d_multicast_hint(smem_u32(w_ring + s * W_SLOT + (int)rank * 4 * W_BOX_BYTES), &tm_w, bw,
                                                0, wy, col0 / 64 + 4 * (int)rank, kPairMask, w_policy);
                 for (int b = 0; b < (w3d ? 0 : nbox); ++b) {
                     const int box = (int)rank * nbox + b;
-                    if (kMulticast)
-                        tma_load_2d_multicast_hint(smem_u32(w_ring + s * W_BYTES + box * W_BOX_BYTES), &tm_w, bw,
-                                                   col0 + 64 * box, wy, kPairMask, w_policy);
-                    else
-                        tma_load_2d_hint(smem_u32(w_ring + s * W_BYTES + box * W_BOX_BYTES), &tm_w, bw,
-                                         col0 + 64 * box, wy, w_policy);
+                    tma_load_2d_multicast_hint(smem_u32(w_ring + s * W_SLOT + box * W_BOX_BYTES), &tm_w, bw,
+                                               col0 + 64 * box, wy, kPairMask, w_policy);
                 }
                 issued[s] = (int)u + 1;
             }
@@ -236,7 +268,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 grid_dependency_wait();
                 grid_launch_dependents();
             }
-            if (!ok)
+            // loads in flight finish before the CTA may leave (pair: the even CTA's full_w
+            // counts both CTAs' loads, and the odd CTA leaves only after the final cluster
+            // barrier, which the even CTA reaches after this drain)
+            if (!ok && (!kPair || rank == 0))
                 for (int s = 0; s < STAGES; ++s)
                     if (issued[s] > 0) drain_wait(smem_u32(&full_w[s]), (issued[s] - 1) & 1);
         }
@@ -272,10 +307,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp == 4) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // (pair: the even CTA's thread issues for both CTAs; the odd CTA's has no role)
+        if (lane == 0 && (!kPair || rank == 0)) {
             grid_dependency_wait();  // nothing to issue before the producers' first tile anyway
             grid_launch_dependents();
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, 256, /*A K-major*/ 0, /*B N-major*/ 1);
+            constexpr uint32_t idesc = idesc_bf16_f32(kPair ? 2 * BM : BM, 256, /*A K-major*/ 0, /*B N-major*/ 1);
             // operand descriptors of slot 0; a slot, a K = 16 step or a 256-column half is a
             // constant added to the start-address field (addresses stay below 2^18 bytes)
             // A: K-major, 64-byte rows, 8-row groups 512 B apart; +32 B per K = 16 step
@@ -283,36 +319,61 @@ __global__ void __launch_bounds__(THREADS, 1)
             // B: N-major, 64-column atoms 4 KiB apart (LBO), 8-row groups 1 KiB apart (SBO);
             // +2 KiB per K = 16 step
             const uint64_t b_desc0 = smem_desc(smem_u32(w_ring), W_BOX_BYTES, 1024, 2);
-            constexpr uint64_t kA_K16 = 32 >> 4, kB_K16 = 2048 >> 4, kB_HALF = W_HALF_BYTES >> 4;
+            // a CTA's part of one 256-column half: 4 atoms (multicast) or 2 (pair)
+            constexpr uint64_t kA_K16 = 32 >> 4, kB_K16 = 2048 >> 4, kB_HALF = (W_SLOT / 2) >> 4;
             bool issued_any = false;
+            // a block's two tiles are tested together (their latencies overlap), and right
+            // after the previous block's MMAs are issued, ahead of its commit; the bounded
+            // waits run only when a tile is not there yet
+            // pair: the odd CTA's producers and loads arrive from the other CTA, so the tests
+            // acquire at cluster scope
+            auto test = [&](uint32_t bar, uint32_t ph) {
+                return kPair ? mbar_try_wait_cluster(bar, ph) : mbar_try_wait(bar, ph);
+            };
+            auto wait = [&](uint32_t bar, uint32_t ph) {
+                return kPair ? mbar_wait_cluster(bar, ph, abort_flag) : mbar_wait(bar, ph, abort_flag);
+            };
+            bool a_in = nkb > 0 && test(smem_u32(&full_a[0]), 0);
+            bool w_in = nkb > 0 && test(smem_u32(&full_w[0]), 0);
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % STAGES;
                 const uint32_t ph = (uint32_t)(i / STAGES) & 1;
-                // both tests issued before either result is used (their latencies overlap);
-                // the bounded waits only when a tile is not there yet
-                const bool a_in = mbar_try_wait(smem_u32(&full_a[s]), ph);
-                const bool w_in = mbar_try_wait(smem_u32(&full_w[s]), ph);
-                if (!(a_in && w_in) && (!mbar_wait(smem_u32(&full_a[s]), ph, abort_flag) ||
-                                        !mbar_wait(smem_u32(&full_w[s]), ph, abort_flag))) {
+                if (!(a_in && w_in) && (!wait(smem_u32(&full_a[s]), ph) || !wait(smem_u32(&full_w[s]), ph))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint64_t ad = a_desc0 + (uint64_t)((s * A_BYTES) >> 4);
-                const uint64_t bd = b_desc0 + (uint64_t)((s * W_BYTES) >> 4);
+                const uint64_t bd = b_desc0 + (uint64_t)((s * W_SLOT) >> 4);
                 const uint32_t acc = i > 0 ? 1u : 0u;
-                umma_bf16(tmem_base, ad, bd, idesc, acc);
-                if (halves == 2) umma_bf16(tmem_base + 256, ad, bd + kB_HALF, idesc, acc);
-                umma_bf16(tmem_base, ad + kA_K16, bd + kB_K16, idesc, 1u);
-                if (halves == 2) umma_bf16(tmem_base + 256, ad + kA_K16, bd + kB_HALF + kB_K16, idesc, 1u);
+                if (kPair) {
+                    umma_bf16_pair(tmem_base, ad, bd, idesc, acc);
+                    if (halves == 2) umma_bf16_pair(tmem_base + 256, ad, bd + kB_HALF, idesc, acc);
+                    umma_bf16_pair(tmem_base, ad + kA_K16, bd + kB_K16, idesc, 1u);
+                    if (halves == 2) umma_bf16_pair(tmem_base + 256, ad + kA_K16, bd + kB_HALF + kB_K16, idesc, 1u);
+                } else {
+                    umma_bf16(tmem_base, ad, bd, idesc, acc);
+                    if (halves == 2) umma_bf16(tmem_base + 256, ad, bd + kB_HALF, idesc, acc);
+                    umma_bf16(tmem_base, ad + kA_K16, bd + kB_K16, idesc, 1u);
+                    if (halves == 2) umma_bf16(tmem_base + 256, ad + kA_K16, bd + kB_HALF + kB_K16, idesc, 1u);
+                }
+                if (i + 1 < nkb) {
+                    const int s1 = (i + 1) % STAGES;
+                    const uint32_t ph1 = (uint32_t)((i + 1) / STAGES) & 1;
+                    a_in = test(smem_u32(&full_a[s1]), ph1);
+                    w_in = test(smem_u32(&full_w[s1]), ph1);
+                }
                 // one commit releases the W and A slots once both CTAs' MMAs have read them
-                if (kMulticast)
-                    umma_commit_multicast(smem_u32(&empty[s]), kPairMask);
+                if (kPair)
+                    umma_commit_pair_multicast(smem_u32(&empty[s]), kPairMask);
                 else
-                    umma_commit(smem_u32(&empty[s]));
+                    umma_commit_multicast(smem_u32(&empty[s]), kPairMask);
                 issued_any = true;
             }
-            umma_commit(smem_u32(acc_full));
+            if (kPair)
+                umma_commit_pair_multicast(smem_u32(acc_full), kPairMask);
+            else
+                umma_commit(smem_u32(acc_full));
             if (*abort_flag && issued_any) drain_wait(smem_u32(acc_full), 0);
         }
     } else if ((warp & 3) != 0 && warp < 11) {
@@ -393,7 +454,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             fence_proxy_async_smem();
             __syncwarp();  // every lane's A stores (and proxy fence) before the arrival
-            if (lane == 0) mbar_arrive(smem_u32(&full_a[s]));
+            if (lane == 0) {
+                if (kPair && rank != 0)  // the even CTA's MMA thread reads this CTA's rows too
+                    mbar_arrive_remote(map_to_cta(smem_u32(&full_a[s]), 0));
+                else
+                    mbar_arrive(smem_u32(&full_a[s]));
+            }
         }
     }
 
@@ -446,7 +512,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc<TMEM_COLS>(tmem_base);
+        if (kPair)
+            tmem_dealloc_pair<TMEM_COLS>(tmem_base);
+        else
+            tmem_dealloc<TMEM_COLS>(tmem_base);
     }
 }
 
@@ -601,10 +670,10 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     // 64 columns lie inside the row pitch, else 2-D boxes of 64 columns
     int w3d = 0;
     const int64_t atoms = (d + 63) / 64;
-    if (kMulticast && atoms * 64 <= ldw) {
+    if (atoms * 64 <= ldw) {
         const cuuint64_t dims[3] = {64, (cuuint64_t)(vocab_end - vocab_start), (cuuint64_t)atoms};
         const cuuint64_t strides[2] = {(cuuint64_t)ldw * 2, 128};
-        const cuuint32_t box[3] = {64, BK, 4};
+        const cuuint32_t box[3] = {64, BK, kPair ? 2u : 4u};
         const cuuint32_t estr[3] = {1, 1, 1};
         w3d = encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(W), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
