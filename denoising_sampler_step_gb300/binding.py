@@ -44,6 +44,8 @@ lib.dg_sampler_step.argtypes = [_p, _i32, _i32, _i64, _i64, _p, _i64, _i64, _i64
 lib.dg_sampler_step.restype = ctypes.c_int
 lib.dg_get_device_status.argtypes = [_p]
 lib.dg_get_device_status.restype = ctypes.c_int
+lib.dg_check_wait_timeout.argtypes = [ctypes.c_uint32, _p]
+lib.dg_check_wait_timeout.restype = ctypes.c_int
 
 STATUS = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED", 3: "DG_ERR_CUDA", 4: "DG_ERR_TIMEOUT"}
 
@@ -185,3 +187,9 @@ def dg_sampler_step(logits: torch.Tensor, n_req: int, L_c: int, W: torch.Tensor,
 
 def dg_get_device_status(stream=None) -> None:
     _check(lib.dg_get_device_status(_stream(stream)), "dg_get_device_status")
+
+
+def dg_check_wait_timeout(limit_us: int, stream=None) -> None:
+    """Queues the diagnostic wait that gives up after limit_us; the next
+    dg_get_device_status() raises DgError with DG_ERR_TIMEOUT."""
+    _check(lib.dg_check_wait_timeout(int(limit_us), _stream(stream)), "dg_check_wait_timeout")

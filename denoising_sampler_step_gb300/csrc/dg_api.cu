@@ -241,6 +241,14 @@ dg_status dg_sampler_step(const float *logits, int32_t n_req, int32_t L_c, int64
                           workspace_bytes, s, accept_hook, &acc, /*overlap_previous=*/true);
 }
 
+dg_status dg_check_wait_timeout(uint32_t limit_us, dg_stream_t stream) {
+    t_last_error[0] = 0;
+    if (limit_us < 1 || limit_us > 1000000u)
+        return fail(DG_ERR_INVALID_ARG, "wait-timeout check: limit of %u us is outside 1 .. 1,000,000", limit_us);
+    cudaError_t e = launch_wait_timeout_check(limit_us, (cudaStream_t)stream);
+    return e == cudaSuccess ? DG_OK : cuda_fail(e, "wait-timeout check launch");
+}
+
 dg_status dg_get_device_status(dg_stream_t stream) {
     t_last_error[0] = 0;
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);

@@ -48,6 +48,9 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
 
 int device_sm_count();
 
+// One thread waits on a barrier nothing completes and records a timeout after limit_us.
+cudaError_t launch_wait_timeout_check(uint32_t limit_us, cudaStream_t stream);
+
 // Shared by the C entry points: the calling thread's error text, fail() sets it and
 // returns st; check_embed_args() holds the argument rules of dg_soft_embed.
 extern thread_local char t_last_error[512];

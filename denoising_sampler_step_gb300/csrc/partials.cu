@@ -68,6 +68,32 @@ cudaError_t launch_sum_partials(const float *const *partials, int32_t T, int64_t
     return cudaGetLastError();
 }
 
+namespace {
+
+// The timeout path of the bounded barrier waits, on a barrier whose phase never completes
+// (count 2, one arrival): the wait gives up after limit_ns and records the timeout.
+__global__ void wait_timeout_check_kernel(unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 2);
+    fence_mbar_init();
+    mbar_arrive(b);
+    const unsigned long long t0 = globaltimer_ns();
+    while (!mbar_try_wait(b, 0)) {
+        if (globaltimer_ns() - t0 > limit_ns) {
+            record_timeout();
+            return;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_wait_timeout_check(uint32_t limit_us, cudaStream_t stream) {
+    wait_timeout_check_kernel<<<1, 1, 0, stream>>>(1000ull * limit_us);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_fill_zero(float *out, int64_t R, int64_t d, int64_t ldo, cudaStream_t stream) {
     fill_zero_kernel<<<grid_for(R * d, 256), 256, 0, stream>>>(out, R, d, ldo);
     return cudaGetLastError();

@@ -207,6 +207,16 @@ dg_status dg_sampler_step(const float *logits, int32_t n_req, int32_t L_c, int64
  */
 dg_status dg_get_device_status(dg_stream_t stream);
 
+/*
+ * Diagnostic of the timeout path (no counterpart on the pages): queues on `stream` one
+ * thread that waits on a device barrier nothing ever completes, gives up after
+ * `limit_us` microseconds (1 .. 1,000,000) and records the timeout exactly as the
+ * product's bounded waits do.  The next dg_get_device_status() then returns
+ * DG_ERR_TIMEOUT, and the CUDA context stays usable.  DG_ERR_INVALID_ARG for a limit
+ * outside the range; DG_ERR_CUDA if the launch fails.  Asynchronous.
+ */
+dg_status dg_check_wait_timeout(uint32_t limit_us, dg_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -97,6 +97,13 @@ def test_sum_partials_rejects_bad_arguments(lib):
     assert L.dg_sum_partials(arr2, 2, 4, 4, 4, 1.0, ctypes.c_void_p(256), 4, None) == 1
 
 
+def test_wait_timeout_check_rejects_bad_limits(lib):
+    L = lib.lib
+    assert L.dg_check_wait_timeout(0, None) == 1
+    assert b"outside" in L.dg_last_error()
+    assert L.dg_check_wait_timeout(1000001, None) == 1
+
+
 def test_step_checks_slice_against_vocabulary(lib):
     L = lib.lib
     p = ctypes.c_void_p(256)

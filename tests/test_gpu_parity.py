@@ -302,3 +302,20 @@ def test_step_late_batch32_full_size(B, name):
     """8192 rows: statistics and acceptance on every row, the embedding on sampled rows."""
     wl = inputs.WORKLOADS[name]
     step_and_compare(B, wl, sample_rows=sampled_rows(wl.R, 30, 4))
+
+
+# --------------------------------------------------------------------------- failure detection
+
+def test_wait_timeout_is_reported_and_the_context_stays_usable(B):
+    """A device wait that can never complete gives up after its bound; the host reads
+    DG_ERR_TIMEOUT once, the word is cleared, and the next kernel runs correctly."""
+    B.dg_get_device_status()  # nothing pending
+    B.dg_check_wait_timeout(20000)  # 20 ms
+    with pytest.raises(B.DgError) as err:
+        B.dg_get_device_status()
+    assert err.value.status == 4
+    B.dg_get_device_status()  # cleared
+    wl = inputs.WORKLOADS["tiny"].with_(V=4096, L_c=9, seed=11)
+    x = inputs.logits(wl)
+    check_stats(B.dg_row_stats(dev(x)), row_stats(x))
+    B.dg_get_device_status()
