@@ -96,7 +96,9 @@ constexpr int SMEM_BYTES = L_RING + W_RING + A_RING + 1024 /*align*/ + 256 /*bar
 static_assert(L_BYTES % 1024 == 0 && W_SLOT % 1024 == 0 && A_BYTES % 1024 == 0, "1 KiB alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 // each producer group keeps to every other slot of the logits and A rings
-static_assert(LSTAGES % PGROUPS == 0 && STAGES % PGROUPS == 0, "ring depths a multiple of the producer groups");
+// a group waits only for phases its own blocks need, and no slot can run two phases ahead
+// of its waiter, so the depths need not be multiples of the group count
+static_assert(LSTAGES >= PGROUPS && STAGES >= PGROUPS, "a slot per producer group at least");
 
 struct Params {
     const float *lse;
