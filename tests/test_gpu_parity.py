@@ -304,6 +304,37 @@ def test_step_late_batch32_full_size(B, name):
     step_and_compare(B, wl, sample_rows=sampled_rows(wl.R, 30, 4))
 
 
+def test_step_captured_in_a_cuda_graph_matches_the_eager_step(B):
+    """Every call is capturable (no allocation, synchronisation or host copy inside); the
+    replayed graph, programmatic-launch edges included, gives bit-identical results."""
+    from denoising_sampler_step_gb300.step import SamplerStep
+    wl = inputs.WORKLOADS["tiny"].with_(V=40000, L_c=64, n_req=2, d=256, seed=21)
+    x = dev(inputs.logits(wl))
+    Wd = w_dev(inputs.embedding_bf16(wl))
+    bud = dev(inputs.budgets(wl))
+    st = SamplerStep(Wd, wl.n_req, wl.L_c, wl.V, wl.gamma, device="cuda")
+    eager = {k: v.clone() for k, v in st(x, bud).items()}
+    torch.cuda.synchronize()
+    for v in st.out.values():
+        v.zero_()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        st(x, bud)
+    torch.cuda.current_stream().wait_stream(cap)
+    torch.cuda.synchronize()
+    for v in st.out.values():
+        v.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        st(x, bud)
+    g.replay()
+    torch.cuda.synchronize()
+    B.dg_get_device_status()
+    for k, v in eager.items():
+        assert torch.equal(st.out[k], v), k
+
+
 # --------------------------------------------------------------------------- failure detection
 
 def test_wait_timeout_is_reported_and_the_context_stays_usable(B):
