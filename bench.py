@@ -263,12 +263,16 @@ def main() -> None:
     # (same inputs, same shapes), the mean over the loop
     out = step.out
     nrep = max(args.steps, 10)
+    sample_out = {"candidate": torch.empty(wl.R, dtype=torch.int32, device=dev),
+                  "log_p": torch.empty(wl.R, dtype=torch.float32, device=dev)}
     calls = {
         "row_stats": lambda: B.dg_row_stats(xd, stream=stream, out=out),
         "accept": lambda: B.dg_entropy_accept(out["H"], out["kappa"], wl.n_req, wl.L_c, bd,
                                               stream=stream, out=out),
         "soft_embed": lambda: B.dg_soft_embed(xd, out["lse"], 0, wl.V, Wd, wl.gamma, out=out["E"],
                                               ws=step.ws, stream=stream),
+        # the stochastic-candidate pass (not part of the argmax step; reported alongside)
+        "row_sample": lambda: B.dg_row_sample(xd, 1.0, seed=1, offset=0, stream=stream, out=sample_out),
     }
     comp = {}
     k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -44,6 +44,8 @@ lib.dg_sampler_step.argtypes = [_p, _i32, _i32, _i64, _i64, _p, _i64, _i64, _i64
 lib.dg_sampler_step.restype = ctypes.c_int
 lib.dg_get_device_status.argtypes = [_p]
 lib.dg_get_device_status.restype = ctypes.c_int
+lib.dg_row_sample.argtypes = [_p, _i64, _i64, _i64, _f32, ctypes.c_uint64, ctypes.c_uint64, _p, _p, _p]
+lib.dg_row_sample.restype = ctypes.c_int
 lib.dg_check_wait_timeout.argtypes = [ctypes.c_uint32, _p]
 lib.dg_check_wait_timeout.restype = ctypes.c_int
 
@@ -92,6 +94,21 @@ def dg_row_stats(logits: torch.Tensor, V: int | None = None, stream=None, out: d
         o["argmax"] = _new(R, torch.int32, dev)
     _check(lib.dg_row_stats(_ptr(logits), R, V, _ld(logits), _ptr(o["m"]), _ptr(o["lse"]), _ptr(o["H"]),
                             _ptr(o["kappa"]), _ptr(o["argmax"]), _stream(stream)), "dg_row_stats")
+    return o
+
+
+def dg_row_sample(logits: torch.Tensor, temperature: float = 1.0, seed: int = 0, offset: int = 0,
+                  V: int | None = None, stream=None, out: dict | None = None) -> dict:
+    """Gumbel-max candidate per row of fp32 logits [R, >=V] at `temperature`, uniforms from
+    Philox4x32-10 keyed by `seed` at step `offset` -> dict candidate (int32), log_p (fp32)."""
+    R = logits.shape[0]
+    V = logits.shape[1] if V is None else V
+    dev = logits.device
+    o = out
+    if o is None:
+        o = {"candidate": _new(R, torch.int32, dev), "log_p": _new(R, torch.float32, dev)}
+    _check(lib.dg_row_sample(_ptr(logits), R, V, _ld(logits), float(temperature), int(seed), int(offset),
+                             _ptr(o["candidate"]), _ptr(o["log_p"]), _stream(stream)), "dg_row_sample")
     return o
 
 

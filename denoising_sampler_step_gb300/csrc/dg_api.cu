@@ -160,6 +160,19 @@ dg_status dg_row_stats(const float *logits, int64_t R, int64_t V, int64_t ldl, f
     return e == cudaSuccess ? DG_OK : cuda_fail(e, "row stats launch");
 }
 
+dg_status dg_row_sample(const float *logits, int64_t R, int64_t V, int64_t ldl, float temperature, uint64_t seed,
+                        uint64_t offset, int32_t *candidate, float *log_p, dg_stream_t stream) {
+    t_last_error[0] = 0;
+    dg_status st = check_stats_args(logits, R, V, ldl);
+    if (st != DG_OK || R == 0) return st;
+    if (!(temperature > 0.0f) || !(temperature < INFINITY))
+        return fail(DG_ERR_INVALID_ARG, "row sample: temperature must be positive and finite");
+    if (!candidate || !log_p) return fail(DG_ERR_INVALID_ARG, "row sample: an output pointer is NULL");
+    cudaError_t e = launch_row_sample(logits, R, V, ldl, temperature, seed, offset, candidate, log_p,
+                                      (cudaStream_t)stream);
+    return e == cudaSuccess ? DG_OK : cuda_fail(e, "row sample launch");
+}
+
 size_t dg_soft_embed_workspace_size(int64_t R, int64_t vocab_len, int64_t d) {
     if (R <= 0 || vocab_len <= 0 || d <= 0) return 0;
     const int sms = device_sm_count();

@@ -48,6 +48,11 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
 
 int device_sm_count();
 
+// Gumbel-max candidates and their tempered log-probabilities (row_sample.cu).
+cudaError_t launch_row_sample(const float *logits, int64_t R, int64_t V, int64_t ldl, float temperature,
+                              uint64_t seed, uint64_t offset, int32_t *candidate, float *log_p,
+                              cudaStream_t stream);
+
 // One thread waits on a barrier nothing completes and records a timeout after limit_us.
 cudaError_t launch_wait_timeout_check(uint32_t limit_us, cudaStream_t stream);
 

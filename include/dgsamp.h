@@ -208,6 +208,27 @@ dg_status dg_sampler_step(const float *logits, int32_t n_req, int32_t L_c, int64
 dg_status dg_get_device_status(dg_stream_t stream);
 
 /*
+ * Stochastic candidates ([P2] sampling loop: candidate tokens are sampled at every
+ * position).  For each row i, a categorical draw from softmax(l_i / temperature), taken
+ * as the Gumbel-max  candidate_i = argmax_v (l_{i,v} / temperature - ln(-ln u_{i,v})),
+ * the lowest index on ties, with uniforms from Philox4x32-10 (Salmon et al., SC 2011):
+ * entry v of row i uses word v % 4 of the block with counter
+ * (v / 4, i, offset mod 2^32, offset / 2^32) and key (seed mod 2^32, seed / 2^32), and
+ * u = ((word >> 9) + 1/2) * 2^-23.  The same (seed, offset) gives the same draws; a
+ * sampling loop advances `offset` once per step.
+ *
+ *   logits     [R, ldl] fp32, ldl >= V (as dg_row_stats)
+ *   candidate  [R] int32  the drawn token
+ *   log_p      [R] fp32   ln of its probability under softmax(l_i / temperature)
+ * -inf entries are never drawn; a row that is all -inf gives candidate 0 and NaN log_p.
+ * Requires: temperature > 0 and finite (else DG_ERR_INVALID_ARG); the layout rules of
+ * dg_row_stats.  R == 0 queues nothing.
+ */
+dg_status dg_row_sample(const float *logits, int64_t R, int64_t V, int64_t ldl, float temperature,
+                        uint64_t seed, uint64_t offset, int32_t *candidate, float *log_p,
+                        dg_stream_t stream);
+
+/*
  * Diagnostic of the timeout path (no counterpart on the pages): queues on `stream` one
  * thread that waits on a device barrier nothing ever completes, gives up after
  * `limit_us` microseconds (1 .. 1,000,000) and records the timeout exactly as the

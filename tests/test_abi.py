@@ -97,6 +97,15 @@ def test_sum_partials_rejects_bad_arguments(lib):
     assert L.dg_sum_partials(arr2, 2, 4, 4, 4, 1.0, ctypes.c_void_p(256), 4, None) == 1
 
 
+def test_row_sample_rejects_bad_temperatures(lib):
+    L = lib.lib
+    p = ctypes.c_void_p(256)
+    for t in (0.0, -1.0, float("inf"), float("nan")):
+        assert L.dg_row_sample(p, 4, 16, 16, t, 1, 0, p, p, None) == 1, t
+    assert b"temperature" in L.dg_last_error()
+    assert L.dg_row_sample(p, 4, 16, 18, 1.0, 1, 0, p, p, None) == 2  # ldl % 4 != 0
+
+
 def test_wait_timeout_check_rejects_bad_limits(lib):
     L = lib.lib
     assert L.dg_check_wait_timeout(0, None) == 1

@@ -350,3 +350,52 @@ def test_wait_timeout_is_reported_and_the_context_stays_usable(B):
     x = inputs.logits(wl)
     check_stats(B.dg_row_stats(dev(x)), row_stats(x))
     B.dg_get_device_status()
+
+
+# --------------------------------------------------------------------------- stochastic candidates
+
+def check_sample(g, o, tol=1e-3):
+    """The candidate is unique where the oracle's two best perturbed scores are more than
+    `tol` apart; elsewhere the GPU's pick must score within `tol` of the best."""
+    cand = g["candidate"].cpu().numpy()
+    lp = g["log_p"].cpu().numpy().astype(np.float64)
+    clear = o["margin"] > tol
+    assert np.array_equal(cand[clear], o["candidate"][clear])
+    rows = np.arange(len(cand))
+    top = o["score"][rows, o["candidate"]]
+    assert np.all(o["score"][rows, cand] >= top - tol)
+    fin = np.isfinite(o["log_p"])
+    assert np.array_equal(np.isnan(lp), ~fin)
+    assert np.all(np.abs(lp[fin] - o["log_p"][fin]) <= 1e-4 * np.maximum(1.0, np.abs(o["log_p"][fin])))
+
+
+@pytest.mark.parametrize("V,ld,temperature", [(4096, 4096, 1.0), (4093, 4096, 0.5), (1000, 1000, 2.0),
+                                              (70001, 70004, 1.0), (262144, 262144, 0.7)])
+def test_row_sample_matches_oracle(B, V, ld, temperature):
+    from oracle import row_sample
+    wl = inputs.WORKLOADS["tiny"].with_(V=V, L_c=12, seed=V + 3)
+    x = inputs.logits(wl, ld=ld)
+    g = B.dg_row_sample(dev(x), temperature, seed=1234, offset=7, V=V)
+    check_sample(g, row_sample(x[:, :V], temperature, 1234, 7))
+
+
+def test_row_sample_special_rows_and_determinism(B):
+    from oracle import row_sample
+    V = 50000
+    rng = np.random.default_rng(8)
+    x = (rng.standard_normal((6, V)) * 2).astype(np.float32)
+    x[1, :] = -np.inf
+    x[1, [7, 77, 40000]] = 3.0       # three allowed entries
+    x[2, 12345] = 1e4                # one-hot: always drawn
+    x[3, ::2] = -np.inf              # half masked
+    x[4] = -np.inf                   # empty: candidate 0, NaN log_p
+    xd = dev(x)
+    g = B.dg_row_sample(xd, 1.0, seed=99, offset=3)
+    check_sample(g, row_sample(x, 1.0, 99, 3))
+    c = g["candidate"].cpu().numpy()
+    assert c[1] in (7, 77, 40000) and c[2] == 12345 and c[3] % 2 == 1 and c[4] == 0
+    h = B.dg_row_sample(xd, 1.0, seed=99, offset=3)
+    for k in g:  # bit patterns (NaN compares unequal to itself)
+        assert torch.equal(g[k].view(torch.int32), h[k].view(torch.int32)), k
+    o = B.dg_row_sample(dev(np.tile(x[0], (64, 1))), 1.0, seed=99, offset=4)
+    assert len(set(o["candidate"].cpu().numpy().tolist())) > 1  # other counters, other draws
