@@ -12,6 +12,9 @@
 //      per-warp totals);
 //   4. n = the first k whose running sum is not <= B (NaN counts as passing it),
 //      raised to min(min_accept, L_c); mask[order_j] = j < n.
+// With an eligibility mask (a denoising loop: kept positions are not offered again) the
+// ineligible positions sort after every eligible one, in position order, carry no
+// entropy into the sum, are never kept, and the counts above use the eligible ones.
 #include "dg_common.cuh"
 #include "dg_internal.h"
 
@@ -28,8 +31,8 @@ __device__ __forceinline__ uint32_t order_bits(float x) {
 }
 
 __global__ void __launch_bounds__(1024)
-    accept_kernel(const float *__restrict__ H, const float *__restrict__ kappa, int L_c,
-                  const float *__restrict__ budgets, int min_accept, int32_t *__restrict__ order,
+    accept_kernel(const float *__restrict__ H, const float *__restrict__ kappa, const uint8_t *__restrict__ eligible,
+                  int L_c, const float *__restrict__ budgets, int min_accept, int32_t *__restrict__ order,
                   uint8_t *__restrict__ mask, int32_t *__restrict__ n_accepted) {
     extern __shared__ unsigned long long keys[];  // blockDim.x entries
     __shared__ float H_s[1024];
@@ -41,10 +44,14 @@ __global__ void __launch_bounds__(1024)
     const int NT = blockDim.x;
     const int64_t base = (int64_t)q * L_c;
 
-    unsigned long long key =
-        (tid < L_c) ? (((unsigned long long)order_bits(kappa[base + tid]) << 32) | (unsigned)tid) : ~0ull;
+    const bool el = tid < L_c && (!eligible || eligible[base + tid]);
+    // ineligible: above every eligible key (NaN included), in position order
+    unsigned long long key = (tid >= L_c) ? ~0ull
+                             : el ? (((unsigned long long)order_bits(kappa[base + tid]) << 32) | (unsigned)tid)
+                                  : ((0xffffffffull << 32) | 0x80000000u | (unsigned)tid);
     if (tid < L_c) H_s[tid] = H[base + tid];  // gathered in sorted order below
-    if (tid == 0) first_fail = L_c;
+    const int n_el = __syncthreads_count(el);
+    if (tid == 0) first_fail = n_el;
 
     // bitonic sort: partners within a warp exchange by shuffle, farther ones through shared memory
     for (int k = 2; k <= NT; k <<= 1) {
@@ -67,8 +74,8 @@ __global__ void __launch_bounds__(1024)
     }
     __syncthreads();  // H_s and first_fail visible
 
-    const int pos = (int)(key & 0xffffffffu);
-    double h = (tid < L_c) ? (double)H_s[pos] : 0.0;
+    const int pos = (int)(key & 0x7fffffffu);
+    double h = (tid < n_el) ? (double)H_s[pos] : 0.0;
     // inclusive scan in fp64
     const int lane = tid & 31, warp = tid >> 5;
 #pragma unroll
@@ -91,10 +98,10 @@ __global__ void __launch_bounds__(1024)
     if (warp > 0) h += warp_tot[warp - 1];
 
     const double B = (double)budgets[q];
-    if (tid < L_c && !(h <= B)) atomicMin(&first_fail, tid);
+    if (tid < n_el && !(h <= B)) atomicMin(&first_fail, tid);
     __syncthreads();
     int n = first_fail;
-    const int floor_n = min(min_accept, L_c);
+    const int floor_n = min(min_accept, n_el);
     if (n < floor_n) n = floor_n;
     if (tid < L_c) {
         order[base + tid] = pos;
@@ -107,7 +114,8 @@ __global__ void __launch_bounds__(1024)
 
 cudaError_t launch_entropy_accept(const float *H, const float *kappa, int32_t n_req, int32_t L_c,
                                   const float *budgets, int32_t min_accept, int32_t *order,
-                                  uint8_t *mask, int32_t *n_accepted, cudaStream_t stream, bool overlap_previous) {
+                                  uint8_t *mask, int32_t *n_accepted, cudaStream_t stream, bool overlap_previous,
+                                  const uint8_t *eligible) {
     int nt = 32;
     while (nt < L_c) nt <<= 1;
     cudaLaunchConfig_t cfg = {};
@@ -122,8 +130,8 @@ cudaError_t launch_entropy_accept(const float *H, const float *kappa, int32_t n_
     attr[0].val.programmaticStreamSerializationAllowed = overlap_previous ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, accept_kernel, H, kappa, (int)L_c, budgets, (int)min_accept, order, mask,
-                              n_accepted);
+    return cudaLaunchKernelEx(&cfg, accept_kernel, H, kappa, eligible, (int)L_c, budgets, (int)min_accept, order,
+                              mask, n_accepted);
 }
 
 }  // namespace dg

@@ -118,12 +118,36 @@ struct AcceptArgs {
     int32_t *order;
     uint8_t *mask;
     int32_t *n_accepted;
+    const uint8_t *eligible;  // NULL: every position
 };
 
 cudaError_t accept_hook(void *ctx, cudaStream_t stream) {
     const AcceptArgs *a = static_cast<const AcceptArgs *>(ctx);
     return launch_entropy_accept(a->H, a->kappa, a->n_req, a->L_c, a->budgets, a->min_accept, a->order, a->mask,
-                                 a->n_accepted, stream, /*overlap_previous=*/true);
+                                 a->n_accepted, stream, /*overlap_previous=*/true, a->eligible);
+}
+
+// The denoising-loop state a loop step updates after its acceptance (NULL: a plain step).
+struct LoopArgs {
+    int32_t stable_steps;
+    float entropy_threshold;
+    int32_t step_limit;
+    int32_t *canvas;
+    uint8_t *eligible;
+    int32_t *prev_candidate, *stable, *steps;
+    uint8_t *converged;
+};
+
+dg_status check_loop_args(int32_t n_req, int32_t L_c, int32_t stable_steps, float entropy_threshold,
+                          int32_t step_limit, const void *canvas, const void *eligible, const void *prev,
+                          const void *stable, const void *steps, const void *converged) {
+    if (n_req < 0 || L_c < 1) return fail(DG_ERR_INVALID_ARG, "loop: need n_req >= 0 and L_c >= 1");
+    if (L_c > 1024) return fail(DG_ERR_UNSUPPORTED, "loop: L_c = %d is above 1024", L_c);
+    if (stable_steps < 0 || step_limit < 1 || entropy_threshold != entropy_threshold)
+        return fail(DG_ERR_INVALID_ARG, "loop: need stable_steps >= 0, step_limit >= 1 and a threshold");
+    if (n_req > 0 && (!canvas || !eligible || !prev || !stable || !steps || !converged))
+        return fail(DG_ERR_INVALID_ARG, "loop: a state pointer is NULL");
+    return DG_OK;
 }
 
 }  // namespace
@@ -220,12 +244,15 @@ dg_status dg_sum_partials(const float *const *partials, int32_t T, int64_t R, in
     return e == cudaSuccess ? DG_OK : cuda_fail(e, "sum partials launch");
 }
 
-dg_status dg_sampler_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, int64_t ldl, const uint16_t *W,
-                          int64_t vocab_start, int64_t vocab_end, int64_t rows_pad, int64_t ldw, int64_t d,
-                          float gamma, const float *budgets, int32_t min_accept, float *m, float *lse, float *H,
-                          float *kappa, int32_t *argmax, int32_t *order, uint8_t *mask, int32_t *n_accepted, float *E,
-                          int64_t ldo, void *workspace, size_t workspace_bytes, dg_stream_t stream) {
-    t_last_error[0] = 0;
+namespace {
+
+// The fused step, optionally restricted to eligible positions and followed by the
+// loop-state update (a denoising-loop step).
+dg_status run_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, int64_t ldl, const uint16_t *W,
+                   int64_t vocab_start, int64_t vocab_end, int64_t rows_pad, int64_t ldw, int64_t d, float gamma,
+                   const float *budgets, int32_t min_accept, float *m, float *lse, float *H, float *kappa,
+                   int32_t *argmax, int32_t *order, uint8_t *mask, int32_t *n_accepted, float *E, int64_t ldo,
+                   void *workspace, size_t workspace_bytes, cudaStream_t s, const LoopArgs *loop) {
     if (n_req < 0 || L_c < 1) return fail(DG_ERR_INVALID_ARG, "step: need n_req >= 0 and L_c >= 1");
     const int64_t R = (int64_t)n_req * L_c;
     dg_status st = check_stats_args(logits, R, V, ldl);
@@ -237,21 +264,89 @@ dg_status dg_sampler_step(const float *logits, int32_t n_req, int32_t L_c, int64
     st = check_embed_args(logits, ldl, lse, R, vocab_start, vocab_end, W, rows_pad, ldw, d, E, ldo);
     if (st != DG_OK) return st;
     if (R > 0 && (!m || !lse || !H || !kappa || !argmax)) return fail(DG_ERR_INVALID_ARG, "step: a pointer is NULL");
+    if (loop) {
+        st = check_loop_args(n_req, L_c, loop->stable_steps, loop->entropy_threshold, loop->step_limit, loop->canvas,
+                             loop->eligible, loop->prev_candidate, loop->stable, loop->steps, loop->converged);
+        if (st != DG_OK) return st;
+    }
     if (R == 0) return DG_OK;
-    cudaStream_t s = (cudaStream_t)stream;
+    const uint8_t *eligible = loop ? loop->eligible : nullptr;
     cudaError_t e = launch_row_stats(logits, R, V, ldl, m, lse, H, kappa, argmax, s);
     if (e != cudaSuccess) return cuda_fail(e, "step: row stats launch");
     if (vocab_end == vocab_start) {
-        e = launch_entropy_accept(H, kappa, n_req, L_c, budgets, min_accept, order, mask, n_accepted, s);
+        e = launch_entropy_accept(H, kappa, n_req, L_c, budgets, min_accept, order, mask, n_accepted, s, false,
+                                  eligible);
         if (e != cudaSuccess) return cuda_fail(e, "step: accept launch");
-        return run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, ldw, d, gamma, E, ldo, workspace,
-                              workspace_bytes, s);
+        st = run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, ldw, d, gamma, E, ldo, workspace,
+                            workspace_bytes, s);
+    } else {
+        AcceptArgs acc{H, kappa, budgets, n_req, L_c, min_accept, order, mask, n_accepted, eligible};
+        // the product overlaps the tail of the statistics kernel (its W and logits loads do
+        // not depend on it), the acceptance overlaps the product
+        st = run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, ldw, d, gamma, E, ldo, workspace,
+                            workspace_bytes, s, accept_hook, &acc, /*overlap_previous=*/true);
     }
-    AcceptArgs acc{H, kappa, budgets, n_req, L_c, min_accept, order, mask, n_accepted};
-    // the product overlaps the tail of the statistics kernel (its W and logits loads do not
-    // depend on it), the acceptance overlaps the product
-    return run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, ldw, d, gamma, E, ldo, workspace,
-                          workspace_bytes, s, accept_hook, &acc, /*overlap_previous=*/true);
+    if (st != DG_OK || !loop) return st;
+    e = launch_loop_update(argmax, H, mask, n_req, L_c, loop->stable_steps, loop->entropy_threshold,
+                           loop->step_limit, loop->canvas, loop->eligible, loop->prev_candidate, loop->stable,
+                           loop->steps, loop->converged, s);
+    return e == cudaSuccess ? DG_OK : cuda_fail(e, "step: loop update launch");
+}
+
+}  // namespace
+
+dg_status dg_sampler_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, int64_t ldl, const uint16_t *W,
+                          int64_t vocab_start, int64_t vocab_end, int64_t rows_pad, int64_t ldw, int64_t d,
+                          float gamma, const float *budgets, int32_t min_accept, float *m, float *lse, float *H,
+                          float *kappa, int32_t *argmax, int32_t *order, uint8_t *mask, int32_t *n_accepted, float *E,
+                          int64_t ldo, void *workspace, size_t workspace_bytes, dg_stream_t stream) {
+    t_last_error[0] = 0;
+    return run_step(logits, n_req, L_c, V, ldl, W, vocab_start, vocab_end, rows_pad, ldw, d, gamma, budgets,
+                    min_accept, m, lse, H, kappa, argmax, order, mask, n_accepted, E, ldo, workspace,
+                    workspace_bytes, (cudaStream_t)stream, nullptr);
+}
+
+dg_status dg_sampler_loop_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, int64_t ldl,
+                               const uint16_t *W, int64_t vocab_start, int64_t vocab_end, int64_t rows_pad,
+                               int64_t ldw, int64_t d, float gamma, const float *budgets, int32_t min_accept,
+                               int32_t stable_steps, float entropy_threshold, int32_t step_limit, float *m,
+                               float *lse, float *H, float *kappa, int32_t *argmax, int32_t *order, uint8_t *mask,
+                               int32_t *n_accepted, float *E, int64_t ldo, int32_t *canvas, uint8_t *eligible,
+                               int32_t *prev_candidate, int32_t *stable, int32_t *steps, uint8_t *converged,
+                               void *workspace, size_t workspace_bytes, dg_stream_t stream) {
+    t_last_error[0] = 0;
+    LoopArgs loop{stable_steps, entropy_threshold, step_limit, canvas, eligible, prev_candidate, stable, steps,
+                  converged};
+    return run_step(logits, n_req, L_c, V, ldl, W, vocab_start, vocab_end, rows_pad, ldw, d, gamma, budgets,
+                    min_accept, m, lse, H, kappa, argmax, order, mask, n_accepted, E, ldo, workspace,
+                    workspace_bytes, (cudaStream_t)stream, &loop);
+}
+
+dg_status dg_entropy_accept_eligible(const float *H, const float *kappa, const uint8_t *eligible, int32_t n_req,
+                                     int32_t L_c, const float *budgets, int32_t min_accept, int32_t *order,
+                                     uint8_t *mask, int32_t *n_accepted, dg_stream_t stream) {
+    t_last_error[0] = 0;
+    dg_status st = check_accept_args(H, kappa, n_req, L_c, budgets, min_accept, order, mask, n_accepted);
+    if (st != DG_OK || n_req == 0) return st;
+    if (!eligible) return fail(DG_ERR_INVALID_ARG, "accept: eligible is NULL");
+    cudaError_t e = launch_entropy_accept(H, kappa, n_req, L_c, budgets, min_accept, order, mask, n_accepted,
+                                          (cudaStream_t)stream, false, eligible);
+    return e == cudaSuccess ? DG_OK : cuda_fail(e, "accept launch");
+}
+
+dg_status dg_loop_update(const int32_t *candidate, const float *H, const uint8_t *mask, int32_t n_req, int32_t L_c,
+                         int32_t stable_steps, float entropy_threshold, int32_t step_limit, int32_t *canvas,
+                         uint8_t *eligible, int32_t *prev_candidate, int32_t *stable, int32_t *steps,
+                         uint8_t *converged, dg_stream_t stream) {
+    t_last_error[0] = 0;
+    dg_status st = check_loop_args(n_req, L_c, stable_steps, entropy_threshold, step_limit, canvas, eligible,
+                                   prev_candidate, stable, steps, converged);
+    if (st != DG_OK || n_req == 0) return st;
+    if (!candidate || !H || !mask) return fail(DG_ERR_INVALID_ARG, "loop: an input pointer is NULL");
+    cudaError_t e = launch_loop_update(candidate, H, mask, n_req, L_c, stable_steps, entropy_threshold, step_limit,
+                                       canvas, eligible, prev_candidate, stable, steps, converged,
+                                       (cudaStream_t)stream);
+    return e == cudaSuccess ? DG_OK : cuda_fail(e, "loop update launch");
 }
 
 dg_status dg_check_wait_timeout(uint32_t limit_us, dg_stream_t stream) {

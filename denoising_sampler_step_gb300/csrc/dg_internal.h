@@ -16,7 +16,14 @@ cudaError_t launch_row_stats(const float *logits, int64_t R, int64_t V, int64_t 
 cudaError_t launch_entropy_accept(const float *H, const float *kappa, int32_t n_req, int32_t L_c,
                                   const float *budgets, int32_t min_accept, int32_t *order,
                                   uint8_t *mask, int32_t *n_accepted, cudaStream_t stream,
-                                  bool overlap_previous = false);
+                                  bool overlap_previous = false, const uint8_t *eligible = nullptr);
+
+// Denoising-loop state after a step (loop.cu): kept tokens, stable-candidate count,
+// step count and convergence per request.
+cudaError_t launch_loop_update(const int32_t *candidate, const float *H, const uint8_t *mask, int32_t n_req,
+                               int32_t L_c, int32_t stable_steps, float entropy_threshold, int32_t step_limit,
+                               int32_t *canvas, uint8_t *eligible, int32_t *prev_candidate, int32_t *stable,
+                               int32_t *steps, uint8_t *converged, cudaStream_t stream);
 
 constexpr int kMaxPartials = 16;
 cudaError_t launch_sum_partials(const float *const *partials, int32_t T, int64_t R, int64_t d, int64_t ldp,

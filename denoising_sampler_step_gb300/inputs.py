@@ -32,6 +32,7 @@ TAG_ROW_Z = 1        # per-row N(0,1) draws of the logits
 TAG_ROW_PARAMS = 2   # per-request row scale, boost index and boost size
 TAG_W = 3            # per-block N(0,1) draws of the embedding table
 TAG_BUDGET = 4       # per-request entropy budgets
+TAG_LOOP_NOISE = 5   # per-step, per-row noise of a denoising-loop sequence
 
 W_BLOCK_ROWS = 4096  # embedding rows drawn per Philox stream
 
@@ -205,3 +206,24 @@ def padded_shard(W_bits: np.ndarray, s: int, e: int, multiple: int = 128, pad_va
     if pad_value == "nan":
         out[rows:] = 0x7FC0
     return out
+
+
+def loop_logits(wl: Workload, step: int, settle: int = 4, noise: float = 1.0, base: np.ndarray | None = None) -> np.ndarray:
+    """fp32 logits [R, V] of step ``step`` of a synthetic denoising loop whose predictions
+    settle: the workload's logits plus N(0, sigma_t^2) noise per entry, with
+    sigma_t = noise * row scale * (1 - step / settle) for step < settle and no noise from
+    step ``settle`` on (the logits of every later step are the workload's own)."""
+    x = logits(wl) if base is None else base.copy()
+    if step >= settle:
+        return x
+    frac = np.float32(noise * (1.0 - step / settle))
+
+    def one(i: int) -> None:
+        g = philox(wl.seed, stream_id(TAG_LOOP_NOISE, i, step))
+        row = x[i]
+        sd = np.float32(row.std())
+        row += g.standard_normal(wl.V, dtype=np.float32) * (frac * sd)
+
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(one, range(wl.R)))
+    return x

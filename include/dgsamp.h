@@ -238,6 +238,73 @@ dg_status dg_row_sample(const float *logits, int64_t R, int64_t V, int64_t ldl, 
  */
 dg_status dg_check_wait_timeout(uint32_t limit_us, dg_stream_t stream);
 
+/*
+ * Entropy-bound acceptance over the positions still open ([P2] sampling loop: kept
+ * tokens stay kept while the rest of the canvas is resampled).  As dg_entropy_accept,
+ * restricted to the positions with eligible[q*L_c + j] != 0:
+ *   order  the eligible positions from most to least confident (kappa ascending, equal
+ *          kappa: lower position first, NaN statistics last among them), then the
+ *          ineligible positions in position order;
+ *   the running entropy sum runs over the eligible positions only; min_accept is
+ *          capped at the number eligible; an ineligible position is never accepted.
+ *   eligible  [n_req * L_c] uint8, required when n_req > 0.
+ * Argument rules and errors as dg_entropy_accept.
+ */
+dg_status dg_entropy_accept_eligible(const float *H, const float *kappa, const uint8_t *eligible,
+                                     int32_t n_req, int32_t L_c, const float *budgets,
+                                     int32_t min_accept, int32_t *order, uint8_t *mask,
+                                     int32_t *n_accepted, dg_stream_t stream);
+
+/*
+ * Denoising-loop state after one step ([P2] sampling loop: accepted tokens are kept; a
+ * canvas has converged when its argmax predictions have been stable for several steps
+ * and the mean entropy per token is below a threshold, or when the step limit is
+ * reached).  Per request q, one CTA:
+ *   canvas[p] = candidate[p] and eligible[p] = 0 where mask[p] != 0;
+ *   stable[q] = stable[q] + 1 if candidate[p] == prev_candidate[p] at every position
+ *               of the request, else 0;
+ *   prev_candidate[p] = candidate[p];  steps[q] += 1;
+ *   converged[q] = (stable[q] >= stable_steps && mean_H < entropy_threshold)
+ *                  || steps[q] >= step_limit,
+ *   mean_H = (sum of H over the request's L_c positions, in fp64) / L_c, compared with
+ *   the threshold widened to fp64.
+ *
+ *   candidate [R] int32 (the step's argmax or drawn tokens); H [R] fp32; mask [R] uint8
+ *   canvas [R] int32, eligible [R] uint8, prev_candidate [R] int32: read and written
+ *   stable, steps [n_req] int32, converged [n_req] uint8: read and written
+ * The caller owns the state and starts it as: prev_candidate = -1 (every byte 0xFF),
+ * stable = steps = 0, eligible = 1, canvas = the starting canvas.
+ * Requires n_req >= 0, 1 <= L_c <= 1024 (above: DG_ERR_UNSUPPORTED), stable_steps >= 0,
+ * step_limit >= 1, a threshold that is not NaN, non-NULL pointers when n_req > 0
+ * (else DG_ERR_INVALID_ARG).  n_req == 0 queues nothing.  Asynchronous.
+ */
+dg_status dg_loop_update(const int32_t *candidate, const float *H, const uint8_t *mask,
+                         int32_t n_req, int32_t L_c, int32_t stable_steps,
+                         float entropy_threshold, int32_t step_limit,
+                         int32_t *canvas, uint8_t *eligible, int32_t *prev_candidate,
+                         int32_t *stable, int32_t *steps, uint8_t *converged,
+                         dg_stream_t stream);
+
+/*
+ * One step of the denoising loop on one stream: dg_sampler_step with its acceptance
+ * restricted to the eligible positions (dg_entropy_accept_eligible), followed by
+ * dg_loop_update with the step's argmax as the candidate.  Arguments as those calls;
+ * the loop state (canvas, eligible, prev_candidate, stable, steps, converged) is read
+ * and written in place, so successive calls on one stream (or one captured graph,
+ * replayed) run successive steps.
+ */
+dg_status dg_sampler_loop_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V,
+                               int64_t ldl, const uint16_t *W, int64_t vocab_start,
+                               int64_t vocab_end, int64_t rows_pad, int64_t ldw, int64_t d,
+                               float gamma, const float *budgets, int32_t min_accept,
+                               int32_t stable_steps, float entropy_threshold, int32_t step_limit,
+                               float *m, float *lse, float *H, float *kappa, int32_t *argmax,
+                               int32_t *order, uint8_t *mask, int32_t *n_accepted,
+                               float *E, int64_t ldo,
+                               int32_t *canvas, uint8_t *eligible, int32_t *prev_candidate,
+                               int32_t *stable, int32_t *steps, uint8_t *converged,
+                               void *workspace, size_t workspace_bytes, dg_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
