@@ -13,8 +13,9 @@ page is silent the readings are:
 
 * a kept (accepted) position keeps its token and is no longer offered for acceptance
   (it is not eligible) until the canvas commits;
-* "stable for several steps": every position's candidate equals the previous step's,
-  counted in consecutive steps;
+* "stable for several steps": every position's argmax prediction equals the previous
+  step's, counted in consecutive steps (the page speaks of the argmax predictions; the
+  canvas may take sampled candidates, which need not be stable);
 * "mean entropy per token": the mean of H over all L_c positions of the canvas.
 
 Pinned by tests/test_loop_pins.py: acceptance over the eligible positions equals the
@@ -68,7 +69,7 @@ def entropy_accept_eligible(H, kappa, eligible, n_req: int, L_c: int, budgets, m
 
 
 def new_loop_state(n_req: int, L_c: int, canvas0=None) -> dict:
-    """The state a canvas starts from: no previous candidate (-1), no stable step, no step
+    """The state a canvas starts from: no previous argmax (-1), no stable step, no step
     taken, every position eligible, the canvas as given (zeros if not)."""
     R = n_req * L_c
     return {"canvas": np.zeros(R, np.int64) if canvas0 is None else np.array(canvas0, np.int64),
@@ -78,22 +79,24 @@ def new_loop_state(n_req: int, L_c: int, canvas0=None) -> dict:
 
 
 def loop_update(state: dict, candidate, H, mask, n_req: int, L_c: int, stable_steps: int,
-                entropy_threshold: float, step_limit: int) -> dict:
+                entropy_threshold: float, step_limit: int, argmax=None) -> dict:
     """One step of the loop state, per request q (positions q*L_c .. q*L_c + L_c - 1):
       canvas[pos] = candidate[pos] and eligible[pos] = 0 where mask[pos] (kept tokens);
-      stable[q] = stable[q] + 1 if every candidate equals prev at its position, else 0;
-      prev = candidate;  steps[q] += 1;
+      stable[q] = stable[q] + 1 if every argmax prediction equals prev at its position,
+                  else 0 (argmax defaults to the candidates: an argmax loop);
+      prev = argmax;  steps[q] += 1;
       mean_H = (sum of H over the request's positions, in position order) / L_c;
       converged[q] = (stable[q] >= stable_steps and mean_H < entropy_threshold)
                      or steps[q] >= step_limit.
     Returns a new state dict."""
     cand = np.asarray(candidate, np.int64)
+    am = cand if argmax is None else np.asarray(argmax, np.int64)
     H = np.asarray(H, np.float64)
     m = np.asarray(mask).astype(bool)
     s = {k: v.copy() for k, v in state.items()}
     for q in range(n_req):
         sl = slice(q * L_c, (q + 1) * L_c)
-        same = bool(np.all(cand[sl] == s["prev"][sl]))
+        same = bool(np.all(am[sl] == s["prev"][sl]))
         s["stable"][q] = s["stable"][q] + 1 if same else 0
         s["steps"][q] += 1
         mean_H = math.fsum(float(h) for h in H[sl]) / L_c
@@ -101,5 +104,5 @@ def loop_update(state: dict, candidate, H, mask, n_req: int, L_c: int, stable_st
                                   or s["steps"][q] >= step_limit) else 0
     s["canvas"] = np.where(m, cand, s["canvas"])
     s["eligible"] = np.where(m, 0, s["eligible"]).astype(np.uint8)
-    s["prev"] = cand.copy()
+    s["prev"] = am.copy()
     return s

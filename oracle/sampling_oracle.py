@@ -25,10 +25,14 @@ Also returned: ln p_tau(candidate) = l_c / tau - logsumexp_v(l_v / tau), the
 candidate's log-probability under the tempered softmax.  Entries at -inf are never
 drawn; a row with every entry at -inf gives candidate 0 and a NaN log-probability.
 
+Also: kappa of a drawn candidate, -ln p(c) under the untempered softmax, the confidence
+by which a sampling loop orders its positions (most confident first).  For the argmax
+it is ln Z, the row statistics' kappa.
+
 Pinned by tests/test_sampling_pins.py: the published known-answer vectors of
 Philox4x32-10, a chi-square test of the draw frequencies against the softmax, the
-tau -> 0 limit (the argmax), masked entries never drawn, and the log-probability
-against its closed form.
+tau -> 0 limit (the argmax), masked entries never drawn, the log-probability against
+its closed form, and sum_v exp(-kappa_v) = 1 over every candidate of a row.
 """
 from __future__ import annotations
 
@@ -98,3 +102,15 @@ def row_sample(logits: np.ndarray, temperature: float, seed: int, offset: int) -
     with np.errstate(invalid="ignore"):
         margin = top - second
     return {"candidate": cand.astype(np.int32), "log_p": log_p, "score": score, "margin": margin}
+
+
+def candidate_kappa(logits: np.ndarray, candidate) -> np.ndarray:
+    """-ln p(candidate_i) under softmax(l_i) (temperature 1), in float64: lse_i - l_{i,c};
+    NaN for a row with every entry at -inf."""
+    x = np.asarray(logits, dtype=np.float64)
+    c = np.asarray(candidate, dtype=np.int64)
+    m = x.max(axis=1)
+    with np.errstate(invalid="ignore", divide="ignore", over="ignore"):
+        lse = m + np.log(np.exp(x - m[:, None]).sum(axis=1))
+        k = lse - x[np.arange(x.shape[0]), c]
+    return np.where(np.isneginf(m), np.nan, k)

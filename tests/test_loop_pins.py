@@ -98,3 +98,22 @@ def test_loop_update_entropy_threshold_and_step_limit():
     for step in range(1, 3):
         st = loop_update(st, c[:3], H[:3], none[:3], 1, 3, 1, 0.5000001, 10)
     assert st["converged"][0] == 1   # stable once and mean H 0.5 < 0.5000001
+
+
+def test_stability_is_judged_on_the_argmax_and_the_canvas_takes_the_candidates():
+    """Sampled candidates that change every step while the argmax predictions stay put:
+    the stable count grows; the kept positions take the sampled tokens."""
+    st = new_loop_state(1, 3, canvas0=[0, 0, 0])
+    am = np.array([7, 8, 9])
+    H = np.full(3, 0.1)
+    draws = [np.array([1, 2, 3]), np.array([4, 5, 6]), np.array([1, 5, 9])]
+    masks = [np.array([1, 0, 0], np.uint8), np.array([0, 1, 0], np.uint8), np.zeros(3, np.uint8)]
+    for t in range(3):
+        st = loop_update(st, draws[t], H, masks[t], 1, 3, 2, 0.5, 10, argmax=am)
+        assert st["stable"][0] == t and list(st["prev"]) == [7, 8, 9]
+    assert list(st["canvas"]) == [1, 5, 0] and st["converged"][0] == 1
+    # the same candidates with no argmax given: judged on the candidates, never stable
+    st2 = new_loop_state(1, 3)
+    for t in range(3):
+        st2 = loop_update(st2, draws[t], H, masks[t], 1, 3, 2, 0.5, 10)
+    assert st2["stable"][0] == 0 and st2["converged"][0] == 0

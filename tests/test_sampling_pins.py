@@ -7,7 +7,7 @@ import math
 import numpy as np
 import pytest
 
-from oracle.sampling_oracle import philox4x32_10, row_sample, uniforms
+from oracle.sampling_oracle import candidate_kappa, philox4x32_10, row_sample, uniforms
 
 
 # Known-answer vectors of Philox4x32-10 published with the generator (Random123):
@@ -88,3 +88,22 @@ def test_log_probability_closed_form():
         z = [float(v) / t for v in x[i]]
         lse = math.log(math.fsum(math.exp(v - max(z)) for v in z)) + max(z)
         assert abs(out["log_p"][i] - (z[out["candidate"][i]] - lse)) < 1e-12
+
+
+def test_candidate_kappa_sums_to_one_over_every_candidate():
+    """exp(-kappa_v) is p_v: summed over every candidate of a row it is 1; the uniform row
+    gives ln V for every candidate; the argmax gives ln Z (its probability is 1/Z)."""
+    rng = np.random.default_rng(5)
+    V = 37
+    x = (rng.standard_normal((3, V)) * [[0.5], [3.0], [9.0]]).astype(np.float32)
+    for i in range(3):
+        row = np.repeat(x[i:i + 1], V, axis=0)
+        k = candidate_kappa(row, np.arange(V))
+        assert math.isclose(math.fsum(np.exp(-k)), 1.0, rel_tol=1e-12)
+        a = int(np.argmax(x[i]))
+        Z = math.fsum(math.exp(float(v) - float(x[i, a])) for v in x[i])
+        assert math.isclose(float(k[a]), math.log(Z), rel_tol=1e-12)
+    u = np.zeros((1, V), np.float32)
+    assert np.allclose(candidate_kappa(np.repeat(u, V, axis=0), np.arange(V)), math.log(V), rtol=1e-14)
+    empty = np.full((1, 4), -np.inf, np.float32)
+    assert np.isnan(candidate_kappa(empty, [0])[0])
