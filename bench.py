@@ -268,12 +268,13 @@ def main() -> None:
 
     # the denoising loop: LOOP_STEPS loop steps (the step over the eligible positions,
     # then the loop-state update) captured in one CUDA graph and replayed; the loop state
-    # advances across replays, the work per step does not change
-    loop = {"ms_per_step": None}
-    try:
+    # advances across replays, the work per step does not change.  Timed twice: with the
+    # argmax on the canvas, and with candidates drawn at temperature 1 (the statistics and
+    # the draw in one pass over the logits)
+    def time_loop(temperature):
         from denoising_sampler_step_gb300.step import SamplerLoop
         lp = SamplerLoop(Wd, wl.n_req, wl.L_c, wl.V, wl.gamma, LOOP_STABLE_STEPS, LOOP_THRESHOLD,
-                         LOOP_STEP_LIMIT, min_accept=1, device=dev)
+                         LOOP_STEP_LIMIT, temperature=temperature, seed=1, min_accept=1, device=dev)
         cap = torch.cuda.Stream(dev)
         cap.wait_stream(stream)
         with torch.cuda.stream(cap):
@@ -297,16 +298,24 @@ def main() -> None:
         lms = replicas.max_over_ranks([l0.elapsed_time(l1)], device=dev)[0]
         B.dg_get_device_status()
         n_loop = reps * LOOP_STEPS
-        loop = {"ms_per_step": lms / n_loop, "steps": n_loop,
-                "value": world * wl.R * n_loop / (lms * 1e-3),
-                "converged_requests": int(lp.state["converged"].sum().item()),
-                "params": {"stable_steps": LOOP_STABLE_STEPS, "entropy_threshold": LOOP_THRESHOLD,
-                           "step_limit": LOOP_STEP_LIMIT, "min_accept": 1},
-                "how": f"{LOOP_STEPS} dg_sampler_loop_step calls captured in one CUDA graph, replayed "
-                       f"{reps} times on the same logits"}
+        res = {"ms_per_step": lms / n_loop, "steps": n_loop,
+               "value": world * wl.R * n_loop / (lms * 1e-3),
+               "converged_requests": int(lp.state["converged"].sum().item()),
+               "params": {"stable_steps": LOOP_STABLE_STEPS, "entropy_threshold": LOOP_THRESHOLD,
+                          "step_limit": LOOP_STEP_LIMIT, "min_accept": 1, "temperature": temperature},
+               "how": f"{LOOP_STEPS} dg_sampler_loop_step calls captured in one CUDA graph, replayed "
+                      f"{reps} times on the same logits"}
         del lp, lg
+        return res
+
+    loop, loop_sampled = {"ms_per_step": None}, {"ms_per_step": None}
+    try:
+        loop = time_loop(0.0)
+        loop_sampled = time_loop(1.0)
     except Exception as ex:
-        loop = {"ms_per_step": None, "error": str(ex)[:200]}
+        err = {"ms_per_step": None, "error": str(ex)[:200]}
+        loop = loop if loop.get("ms_per_step") else err
+        loop_sampled = err
 
     # per-call durations on the launching stream: each entry point called back to back
     # (same inputs, same shapes), the mean over the loop
@@ -322,6 +331,11 @@ def main() -> None:
                                               ws=step.ws, stream=stream),
         # the stochastic-candidate pass (not part of the argmax step; reported alongside)
         "row_sample": lambda: B.dg_row_sample(xd, 1.0, seed=1, offset=0, stream=stream, out=sample_out),
+        # the statistics and the draw in one pass (the sampling loop's first kernel)
+        "row_stats_sample": lambda: B.dg_row_stats_sample(xd, 1.0, seed=1, offset=0, stream=stream,
+                                                          out=dict(sample_out, **{k: out[k] for k in
+                                                                                  ("m", "lse", "H", "kappa",
+                                                                                   "argmax")})),
     }
     comp = {}
     k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -393,6 +407,7 @@ def main() -> None:
                        "(overlapping the previous step's kernels) and reads every result back"},
         "graph": graph,
         "loop": loop,
+        "loop_sampled": loop_sampled,
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "clocks": clk,
     }

@@ -50,11 +50,15 @@ lib.dg_check_wait_timeout.argtypes = [ctypes.c_uint32, _p]
 lib.dg_check_wait_timeout.restype = ctypes.c_int
 lib.dg_entropy_accept_eligible.argtypes = [_p, _p, _p, _i32, _i32, _p, _i32, _p, _p, _p, _p]
 lib.dg_entropy_accept_eligible.restype = ctypes.c_int
-lib.dg_loop_update.argtypes = [_p, _p, _p, _i32, _i32, _i32, _f32, _i32, _p, _p, _p, _p, _p, _p, _p]
+lib.dg_loop_update.argtypes = [_p, _p, _p, _p, _i32, _i32, _i32, _f32, _i32, _p, _p, _p, _p, _p, _p, _p]
 lib.dg_loop_update.restype = ctypes.c_int
 lib.dg_sampler_loop_step.argtypes = [_p, _i32, _i32, _i64, _i64, _p, _i64, _i64, _i64, _i64, _i64, _f32, _p, _i32,
-                                     _i32, _f32, _i32, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i64,
+                                     _i32, _f32, _i32, _f32, ctypes.c_uint64, ctypes.c_uint64,
+                                     _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i64,
                                      _p, _p, _p, _p, _p, _p, _p, _sz, _p]
+lib.dg_row_stats_sample.argtypes = [_p, _i64, _i64, _i64, _f32, ctypes.c_uint64, ctypes.c_uint64,
+                                    _p, _p, _p, _p, _p, _p, _p, _p]
+lib.dg_row_stats_sample.restype = ctypes.c_int
 lib.dg_sampler_loop_step.restype = ctypes.c_int
 
 STATUS = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED", 3: "DG_ERR_CUDA", 4: "DG_ERR_TIMEOUT"}
@@ -117,6 +121,23 @@ def dg_row_sample(logits: torch.Tensor, temperature: float = 1.0, seed: int = 0,
         o = {"candidate": _new(R, torch.int32, dev), "log_p": _new(R, torch.float32, dev)}
     _check(lib.dg_row_sample(_ptr(logits), R, V, _ld(logits), float(temperature), int(seed), int(offset),
                              _ptr(o["candidate"]), _ptr(o["log_p"]), _stream(stream)), "dg_row_sample")
+    return o
+
+
+def dg_row_stats_sample(logits: torch.Tensor, temperature: float = 1.0, seed: int = 0, offset: int = 0,
+                        V: int | None = None, stream=None, out: dict | None = None) -> dict:
+    """Row statistics and a drawn candidate in one pass; kappa = -ln p(candidate)."""
+    R = logits.shape[0]
+    V = logits.shape[1] if V is None else V
+    dev = logits.device
+    o = out if out is not None else {
+        "m": _new(R, torch.float32, dev), "lse": _new(R, torch.float32, dev), "H": _new(R, torch.float32, dev),
+        "kappa": _new(R, torch.float32, dev), "argmax": _new(R, torch.int32, dev),
+        "candidate": _new(R, torch.int32, dev), "log_p": _new(R, torch.float32, dev)}
+    _check(lib.dg_row_stats_sample(_ptr(logits), R, V, _ld(logits), temperature, seed, offset, _ptr(o.get("m")),
+                                   _ptr(o.get("lse")), _ptr(o.get("H")), _ptr(o.get("kappa")),
+                                   _ptr(o.get("argmax")), _ptr(o["candidate"]), _ptr(o.get("log_p")),
+                                   _stream(stream)), "dg_row_stats_sample")
     return o
 
 
@@ -222,26 +243,30 @@ def dg_entropy_accept_eligible(H: torch.Tensor, kappa: torch.Tensor, eligible: t
     return o
 
 
-LOOP_STATE_KEYS = ("canvas", "eligible", "prev_candidate", "stable", "steps", "converged")
+LOOP_STATE_KEYS = ("canvas", "eligible", "prev_argmax", "stable", "steps", "converged")
 
 
 def new_loop_state(n_req: int, L_c: int, device, canvas0: torch.Tensor | None = None) -> dict:
     """The state buffers a denoising loop starts from, as the C API documents them:
-    prev_candidate -1, stable and steps 0, every position eligible, the canvas as given."""
+    prev_argmax -1, stable and steps 0, every position eligible, the canvas as given."""
     R = n_req * L_c
     canvas = torch.zeros(R, dtype=torch.int32, device=device) if canvas0 is None else \
         canvas0.to(device=device, dtype=torch.int32).reshape(R).clone()
     return {"canvas": canvas, "eligible": torch.ones(R, dtype=torch.uint8, device=device),
-            "prev_candidate": torch.full((R,), -1, dtype=torch.int32, device=device),
+            "prev_argmax": torch.full((R,), -1, dtype=torch.int32, device=device),
             "stable": torch.zeros(n_req, dtype=torch.int32, device=device),
             "steps": torch.zeros(n_req, dtype=torch.int32, device=device),
             "converged": torch.zeros(n_req, dtype=torch.uint8, device=device)}
 
 
 def dg_loop_update(candidate: torch.Tensor, H: torch.Tensor, mask: torch.Tensor, n_req: int, L_c: int,
-                   state: dict, stable_steps: int, entropy_threshold: float, step_limit: int, stream=None) -> dict:
-    """Updates `state` (see new_loop_state) in place after one step; returns it."""
-    _check(lib.dg_loop_update(_ptr(candidate), _ptr(H), _ptr(mask), n_req, L_c, stable_steps, entropy_threshold,
+                   state: dict, stable_steps: int, entropy_threshold: float, step_limit: int,
+                   argmax: torch.Tensor | None = None, stream=None) -> dict:
+    """Updates `state` (see new_loop_state) in place after one step; returns it.  The
+    canvas takes `candidate`; stability is judged on `argmax` (default: the candidates)."""
+    am = candidate if argmax is None else argmax
+    _check(lib.dg_loop_update(_ptr(candidate), _ptr(am), _ptr(H), _ptr(mask), n_req, L_c, stable_steps,
+                              entropy_threshold,
                               step_limit, *[_ptr(state[k]) for k in LOOP_STATE_KEYS], _stream(stream)),
            "dg_loop_update")
     return state
@@ -251,9 +276,10 @@ def dg_sampler_loop_step(logits: torch.Tensor, n_req: int, L_c: int, W: torch.Te
                          budgets: torch.Tensor, state: dict, stable_steps: int, entropy_threshold: float,
                          step_limit: int, min_accept: int = 0, vocab_start: int = 0, vocab_end: int | None = None,
                          V: int | None = None, out: dict | None = None, ws: torch.Tensor | None = None,
-                         stream=None) -> dict:
+                         temperature: float = 0.0, seed: int = 0, offset: int = 0, stream=None) -> dict:
     """One denoising-loop step: the fused step over the eligible positions, then the loop
-    update of `state` in place.  Returns the step outputs as dg_sampler_step does."""
+    update of `state` in place.  Returns the step outputs as dg_sampler_step does, plus
+    `candidate` (the drawn tokens) when temperature > 0."""
     R = n_req * L_c
     V = logits.shape[1] if V is None else V
     vocab_end = V if vocab_end is None else vocab_end
@@ -264,12 +290,15 @@ def dg_sampler_loop_step(logits: torch.Tensor, n_req: int, L_c: int, W: torch.Te
         o = {k: _new(R, torch.float32, dev) for k in ("m", "lse", "H", "kappa")}
         o.update(argmax=_new(R, torch.int32, dev), order=_new(R, torch.int32, dev), mask=_new(R, torch.uint8, dev),
                  n_accepted=_new(n_req, torch.int32, dev), E=_new((R, d), torch.float32, dev))
+    if temperature != 0.0 and "candidate" not in o:
+        o["candidate"] = _new(R, torch.int32, dev)
     if ws is None:
         ws = workspace(R, max(1, vocab_end - vocab_start), d, dev)
     _check(lib.dg_sampler_loop_step(_ptr(logits), n_req, L_c, V, _ld(logits), _ptr(W), vocab_start, vocab_end,
                                     W.shape[0], _ld(W), d, gamma, _ptr(budgets), min_accept, stable_steps,
-                                    entropy_threshold, step_limit, _ptr(o["m"]), _ptr(o["lse"]), _ptr(o["H"]),
-                                    _ptr(o["kappa"]), _ptr(o["argmax"]), _ptr(o["order"]), _ptr(o["mask"]),
+                                    entropy_threshold, step_limit, temperature, seed, offset, _ptr(o["m"]),
+                                    _ptr(o["lse"]), _ptr(o["H"]), _ptr(o["kappa"]), _ptr(o["argmax"]),
+                                    _ptr(o.get("candidate")), _ptr(o["order"]), _ptr(o["mask"]),
                                     _ptr(o["n_accepted"]), _ptr(o["E"]), _ld(o["E"]),
                                     *[_ptr(state[k]) for k in LOOP_STATE_KEYS], _ptr(ws), ws.numel(),
                                     _stream(stream)), "dg_sampler_loop_step")

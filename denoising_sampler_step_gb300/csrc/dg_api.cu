@@ -132,9 +132,12 @@ struct LoopArgs {
     int32_t stable_steps;
     float entropy_threshold;
     int32_t step_limit;
+    float temperature;  // 0: the candidate is the argmax; > 0: drawn at this temperature
+    uint64_t seed, offset;
+    int32_t *candidate;  // the drawn tokens (temperature > 0)
     int32_t *canvas;
     uint8_t *eligible;
-    int32_t *prev_candidate, *stable, *steps;
+    int32_t *prev_argmax, *stable, *steps;
     uint8_t *converged;
 };
 
@@ -195,6 +198,20 @@ dg_status dg_row_sample(const float *logits, int64_t R, int64_t V, int64_t ldl, 
     cudaError_t e = launch_row_sample(logits, R, V, ldl, temperature, seed, offset, candidate, log_p,
                                       (cudaStream_t)stream);
     return e == cudaSuccess ? DG_OK : cuda_fail(e, "row sample launch");
+}
+
+dg_status dg_row_stats_sample(const float *logits, int64_t R, int64_t V, int64_t ldl, float temperature,
+                              uint64_t seed, uint64_t offset, float *m, float *lse, float *H, float *kappa,
+                              int32_t *argmax, int32_t *candidate, float *log_p, dg_stream_t stream) {
+    t_last_error[0] = 0;
+    dg_status st = check_stats_args(logits, R, V, ldl);
+    if (st != DG_OK || R == 0) return st;
+    if (!(temperature > 0.0f) || !(temperature < INFINITY))
+        return fail(DG_ERR_INVALID_ARG, "row stats + sample: temperature must be positive and finite");
+    if (!candidate) return fail(DG_ERR_INVALID_ARG, "row stats + sample: candidate is NULL");
+    cudaError_t e = launch_row_stats_sample(logits, R, V, ldl, temperature, seed, offset, m, lse, H, kappa, argmax,
+                                            candidate, log_p, (cudaStream_t)stream);
+    return e == cudaSuccess ? DG_OK : cuda_fail(e, "row stats + sample launch");
 }
 
 size_t dg_soft_embed_workspace_size(int64_t R, int64_t vocab_len, int64_t d) {
@@ -264,14 +281,20 @@ dg_status run_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, i
     st = check_embed_args(logits, ldl, lse, R, vocab_start, vocab_end, W, rows_pad, ldw, d, E, ldo);
     if (st != DG_OK) return st;
     if (R > 0 && (!m || !lse || !H || !kappa || !argmax)) return fail(DG_ERR_INVALID_ARG, "step: a pointer is NULL");
+    const bool sampled = loop && loop->temperature != 0.0f;
     if (loop) {
         st = check_loop_args(n_req, L_c, loop->stable_steps, loop->entropy_threshold, loop->step_limit, loop->canvas,
-                             loop->eligible, loop->prev_candidate, loop->stable, loop->steps, loop->converged);
+                             loop->eligible, loop->prev_argmax, loop->stable, loop->steps, loop->converged);
         if (st != DG_OK) return st;
+        if (sampled && (!(loop->temperature > 0.0f) || !(loop->temperature < INFINITY)))
+            return fail(DG_ERR_INVALID_ARG, "loop step: temperature must be 0 (argmax) or positive and finite");
+        if (sampled && R > 0 && !loop->candidate) return fail(DG_ERR_INVALID_ARG, "loop step: candidate is NULL");
     }
     if (R == 0) return DG_OK;
     const uint8_t *eligible = loop ? loop->eligible : nullptr;
-    cudaError_t e = launch_row_stats(logits, R, V, ldl, m, lse, H, kappa, argmax, s);
+    cudaError_t e = sampled ? launch_row_stats_sample(logits, R, V, ldl, loop->temperature, loop->seed, loop->offset,
+                                                      m, lse, H, kappa, argmax, loop->candidate, nullptr, s)
+                            : launch_row_stats(logits, R, V, ldl, m, lse, H, kappa, argmax, s);
     if (e != cudaSuccess) return cuda_fail(e, "step: row stats launch");
     if (vocab_end == vocab_start) {
         e = launch_entropy_accept(H, kappa, n_req, L_c, budgets, min_accept, order, mask, n_accepted, s, false,
@@ -287,9 +310,9 @@ dg_status run_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, i
                             workspace_bytes, s, accept_hook, &acc, /*overlap_previous=*/true);
     }
     if (st != DG_OK || !loop) return st;
-    e = launch_loop_update(argmax, H, mask, n_req, L_c, loop->stable_steps, loop->entropy_threshold,
-                           loop->step_limit, loop->canvas, loop->eligible, loop->prev_candidate, loop->stable,
-                           loop->steps, loop->converged, s);
+    e = launch_loop_update(sampled ? loop->candidate : argmax, argmax, H, mask, n_req, L_c, loop->stable_steps,
+                           loop->entropy_threshold, loop->step_limit, loop->canvas, loop->eligible,
+                           loop->prev_argmax, loop->stable, loop->steps, loop->converged, s);
     return e == cudaSuccess ? DG_OK : cuda_fail(e, "step: loop update launch");
 }
 
@@ -309,14 +332,15 @@ dg_status dg_sampler_step(const float *logits, int32_t n_req, int32_t L_c, int64
 dg_status dg_sampler_loop_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, int64_t ldl,
                                const uint16_t *W, int64_t vocab_start, int64_t vocab_end, int64_t rows_pad,
                                int64_t ldw, int64_t d, float gamma, const float *budgets, int32_t min_accept,
-                               int32_t stable_steps, float entropy_threshold, int32_t step_limit, float *m,
-                               float *lse, float *H, float *kappa, int32_t *argmax, int32_t *order, uint8_t *mask,
+                               int32_t stable_steps, float entropy_threshold, int32_t step_limit,
+                               float temperature, uint64_t seed, uint64_t offset, float *m, float *lse, float *H,
+                               float *kappa, int32_t *argmax, int32_t *candidate, int32_t *order, uint8_t *mask,
                                int32_t *n_accepted, float *E, int64_t ldo, int32_t *canvas, uint8_t *eligible,
-                               int32_t *prev_candidate, int32_t *stable, int32_t *steps, uint8_t *converged,
+                               int32_t *prev_argmax, int32_t *stable, int32_t *steps, uint8_t *converged,
                                void *workspace, size_t workspace_bytes, dg_stream_t stream) {
     t_last_error[0] = 0;
-    LoopArgs loop{stable_steps, entropy_threshold, step_limit, canvas, eligible, prev_candidate, stable, steps,
-                  converged};
+    LoopArgs loop{stable_steps, entropy_threshold, step_limit, temperature, seed, offset, candidate, canvas,
+                  eligible, prev_argmax, stable, steps, converged};
     return run_step(logits, n_req, L_c, V, ldl, W, vocab_start, vocab_end, rows_pad, ldw, d, gamma, budgets,
                     min_accept, m, lse, H, kappa, argmax, order, mask, n_accepted, E, ldo, workspace,
                     workspace_bytes, (cudaStream_t)stream, &loop);
@@ -334,17 +358,17 @@ dg_status dg_entropy_accept_eligible(const float *H, const float *kappa, const u
     return e == cudaSuccess ? DG_OK : cuda_fail(e, "accept launch");
 }
 
-dg_status dg_loop_update(const int32_t *candidate, const float *H, const uint8_t *mask, int32_t n_req, int32_t L_c,
-                         int32_t stable_steps, float entropy_threshold, int32_t step_limit, int32_t *canvas,
-                         uint8_t *eligible, int32_t *prev_candidate, int32_t *stable, int32_t *steps,
-                         uint8_t *converged, dg_stream_t stream) {
+dg_status dg_loop_update(const int32_t *candidate, const int32_t *argmax, const float *H, const uint8_t *mask,
+                         int32_t n_req, int32_t L_c, int32_t stable_steps, float entropy_threshold,
+                         int32_t step_limit, int32_t *canvas, uint8_t *eligible, int32_t *prev_argmax,
+                         int32_t *stable, int32_t *steps, uint8_t *converged, dg_stream_t stream) {
     t_last_error[0] = 0;
     dg_status st = check_loop_args(n_req, L_c, stable_steps, entropy_threshold, step_limit, canvas, eligible,
-                                   prev_candidate, stable, steps, converged);
+                                   prev_argmax, stable, steps, converged);
     if (st != DG_OK || n_req == 0) return st;
-    if (!candidate || !H || !mask) return fail(DG_ERR_INVALID_ARG, "loop: an input pointer is NULL");
-    cudaError_t e = launch_loop_update(candidate, H, mask, n_req, L_c, stable_steps, entropy_threshold, step_limit,
-                                       canvas, eligible, prev_candidate, stable, steps, converged,
+    if (!candidate || !argmax || !H || !mask) return fail(DG_ERR_INVALID_ARG, "loop: an input pointer is NULL");
+    cudaError_t e = launch_loop_update(candidate, argmax, H, mask, n_req, L_c, stable_steps, entropy_threshold,
+                                       step_limit, canvas, eligible, prev_argmax, stable, steps, converged,
                                        (cudaStream_t)stream);
     return e == cudaSuccess ? DG_OK : cuda_fail(e, "loop update launch");
 }

@@ -18,12 +18,12 @@ cudaError_t launch_entropy_accept(const float *H, const float *kappa, int32_t n_
                                   uint8_t *mask, int32_t *n_accepted, cudaStream_t stream,
                                   bool overlap_previous = false, const uint8_t *eligible = nullptr);
 
-// Denoising-loop state after a step (loop.cu): kept tokens, stable-candidate count,
+// Denoising-loop state after a step (loop.cu): kept tokens, stable-argmax count,
 // step count and convergence per request.
-cudaError_t launch_loop_update(const int32_t *candidate, const float *H, const uint8_t *mask, int32_t n_req,
-                               int32_t L_c, int32_t stable_steps, float entropy_threshold, int32_t step_limit,
-                               int32_t *canvas, uint8_t *eligible, int32_t *prev_candidate, int32_t *stable,
-                               int32_t *steps, uint8_t *converged, cudaStream_t stream);
+cudaError_t launch_loop_update(const int32_t *candidate, const int32_t *argmax, const float *H, const uint8_t *mask,
+                               int32_t n_req, int32_t L_c, int32_t stable_steps, float entropy_threshold,
+                               int32_t step_limit, int32_t *canvas, uint8_t *eligible, int32_t *prev_argmax,
+                               int32_t *stable, int32_t *steps, uint8_t *converged, cudaStream_t stream);
 
 constexpr int kMaxPartials = 16;
 cudaError_t launch_sum_partials(const float *const *partials, int32_t T, int64_t R, int64_t d, int64_t ldp,
@@ -59,6 +59,11 @@ int device_sm_count();
 cudaError_t launch_row_sample(const float *logits, int64_t R, int64_t V, int64_t ldl, float temperature,
                               uint64_t seed, uint64_t offset, int32_t *candidate, float *log_p,
                               cudaStream_t stream);
+// The same draw fused with the row statistics (one read of the logits); kappa is
+// -ln p(candidate) at temperature 1.
+cudaError_t launch_row_stats_sample(const float *logits, int64_t R, int64_t V, int64_t ldl, float temperature,
+                                    uint64_t seed, uint64_t offset, float *m, float *lse, float *H, float *kappa,
+                                    int32_t *argmax, int32_t *candidate, float *log_p, cudaStream_t stream);
 
 // One thread waits on a barrier nothing completes and records a timeout after limit_us.
 cudaError_t launch_wait_timeout_check(uint32_t limit_us, cudaStream_t stream);

@@ -106,16 +106,25 @@ class SamplerStep:
 
 class SamplerLoop(SamplerStep):
     """A resident denoising loop: the step's buffers plus the loop state (canvas, eligible
-    positions, previous candidates, stable count, step count, converged flag) that each
-    call of dg_sampler_loop_step reads and updates in place.  Successive calls on one
-    stream, or a CUDA graph of several calls replayed, run successive steps."""
+    positions, previous argmax predictions, stable count, step count, converged flag) that
+    each call of dg_sampler_loop_step reads and updates in place.  Successive calls on one
+    stream, or a CUDA graph of several calls replayed, run successive steps.
+
+    temperature 0 puts the argmax on the canvas; temperature > 0 draws the candidates
+    (Philox key `seed`, counter offset advanced by one per call; a captured graph replays
+    the offsets it was captured with)."""
 
     def __init__(self, W: torch.Tensor, n_req: int, L_c: int, V: int, gamma: float, stable_steps: int,
-                 entropy_threshold: float, step_limit: int, **kw):
+                 entropy_threshold: float, step_limit: int, temperature: float = 0.0, seed: int = 0, **kw):
         super().__init__(W, n_req, L_c, V, gamma, **kw)
         self.stable_steps = int(stable_steps)
         self.entropy_threshold = float(entropy_threshold)
         self.step_limit = int(step_limit)
+        self.temperature = float(temperature)
+        self.seed = int(seed)
+        self.offset = 0
+        if self.temperature != 0.0:
+            self.out["candidate"] = torch.empty(self.R, dtype=torch.int32, device=self.device)
         self.state = B.new_loop_state(n_req, L_c, self.device)
 
     def reset(self, canvas0: torch.Tensor | None = None) -> None:
@@ -125,13 +134,17 @@ class SamplerLoop(SamplerStep):
         else:
             self.state["canvas"].copy_(canvas0.reshape(-1))
         self.state["eligible"].fill_(1)
-        self.state["prev_candidate"].fill_(-1)
+        self.state["prev_argmax"].fill_(-1)
         for k in ("stable", "steps", "converged"):
             self.state[k].zero_()
+        self.offset = 0
 
     def __call__(self, logits: torch.Tensor, budgets: torch.Tensor, stream=None) -> dict:
-        return B.dg_sampler_loop_step(logits, self.n_req, self.L_c, self.W, self.gamma, budgets, self.state,
-                                      self.stable_steps, self.entropy_threshold, self.step_limit,
-                                      min_accept=self.min_accept, vocab_start=self.vocab_start,
-                                      vocab_end=self.vocab_end, V=self.V, out=self.out, ws=self.ws,
-                                      stream=stream)
+        o = B.dg_sampler_loop_step(logits, self.n_req, self.L_c, self.W, self.gamma, budgets, self.state,
+                                   self.stable_steps, self.entropy_threshold, self.step_limit,
+                                   min_accept=self.min_accept, vocab_start=self.vocab_start,
+                                   vocab_end=self.vocab_end, V=self.V, out=self.out, ws=self.ws,
+                                   temperature=self.temperature, seed=self.seed, offset=self.offset,
+                                   stream=stream)
+        self.offset += 1
+        return o

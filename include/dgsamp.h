@@ -256,52 +256,81 @@ dg_status dg_entropy_accept_eligible(const float *H, const float *kappa, const u
                                      int32_t *n_accepted, dg_stream_t stream);
 
 /*
+ * Row statistics and a stochastic candidate in one read of the logits ([P2] sampling
+ * loop: candidates are sampled at every position, and kept from most to least
+ * confident).  m, lse, H and argmax are those of dg_row_stats (bit for bit); candidate
+ * and log_p those of dg_row_sample with the same (temperature, seed, offset), bit for
+ * bit; and
+ *   kappa[i] = -ln p_i(candidate_i) under the untempered softmax: ln Z_i (dg_row_stats'
+ *              kappa) when the candidate is the argmax, (m_i - l_{i,c}) + ln Z_i otherwise,
+ * the confidence by which a sampling loop orders its positions.
+ *   candidate  required; m, lse, H, kappa, argmax, log_p may each be NULL (not written).
+ * Requires: temperature > 0 and finite (else DG_ERR_INVALID_ARG); the layout rules of
+ * dg_row_stats.  R == 0 queues nothing.
+ */
+dg_status dg_row_stats_sample(const float *logits, int64_t R, int64_t V, int64_t ldl,
+                              float temperature, uint64_t seed, uint64_t offset,
+                              float *m, float *lse, float *H, float *kappa, int32_t *argmax,
+                              int32_t *candidate, float *log_p, dg_stream_t stream);
+
+/*
  * Denoising-loop state after one step ([P2] sampling loop: accepted tokens are kept; a
  * canvas has converged when its argmax predictions have been stable for several steps
  * and the mean entropy per token is below a threshold, or when the step limit is
  * reached).  Per request q, one CTA:
  *   canvas[p] = candidate[p] and eligible[p] = 0 where mask[p] != 0;
- *   stable[q] = stable[q] + 1 if candidate[p] == prev_candidate[p] at every position
- *               of the request, else 0;
- *   prev_candidate[p] = candidate[p];  steps[q] += 1;
+ *   stable[q] = stable[q] + 1 if argmax[p] == prev_argmax[p] at every position of the
+ *               request, else 0;
+ *   prev_argmax[p] = argmax[p];  steps[q] += 1;
  *   converged[q] = (stable[q] >= stable_steps && mean_H < entropy_threshold)
  *                  || steps[q] >= step_limit,
  *   mean_H = (sum of H over the request's L_c positions, in fp64) / L_c, compared with
  *   the threshold widened to fp64.
  *
- *   candidate [R] int32 (the step's argmax or drawn tokens); H [R] fp32; mask [R] uint8
- *   canvas [R] int32, eligible [R] uint8, prev_candidate [R] int32: read and written
+ *   candidate [R] int32: the tokens the step puts on the canvas (drawn, or the argmax)
+ *   argmax [R] int32: the step's argmax predictions; H [R] fp32; mask [R] uint8
+ *   canvas [R] int32, eligible [R] uint8, prev_argmax [R] int32: read and written
  *   stable, steps [n_req] int32, converged [n_req] uint8: read and written
- * The caller owns the state and starts it as: prev_candidate = -1 (every byte 0xFF),
- * stable = steps = 0, eligible = 1, canvas = the starting canvas.
+ * The caller owns the state and starts it as: prev_argmax = -1 (every byte 0xFF),
+ * stable = steps = 0, eligible = 1, canvas = the starting canvas.  The flag is
+ * recomputed at every step; the caller retires a converged canvas.
  * Requires n_req >= 0, 1 <= L_c <= 1024 (above: DG_ERR_UNSUPPORTED), stable_steps >= 0,
  * step_limit >= 1, a threshold that is not NaN, non-NULL pointers when n_req > 0
  * (else DG_ERR_INVALID_ARG).  n_req == 0 queues nothing.  Asynchronous.
  */
-dg_status dg_loop_update(const int32_t *candidate, const float *H, const uint8_t *mask,
-                         int32_t n_req, int32_t L_c, int32_t stable_steps,
+dg_status dg_loop_update(const int32_t *candidate, const int32_t *argmax, const float *H,
+                         const uint8_t *mask, int32_t n_req, int32_t L_c, int32_t stable_steps,
                          float entropy_threshold, int32_t step_limit,
-                         int32_t *canvas, uint8_t *eligible, int32_t *prev_candidate,
+                         int32_t *canvas, uint8_t *eligible, int32_t *prev_argmax,
                          int32_t *stable, int32_t *steps, uint8_t *converged,
                          dg_stream_t stream);
 
 /*
- * One step of the denoising loop on one stream: dg_sampler_step with its acceptance
+ * One step of the denoising loop on one stream: the fused step with its acceptance
  * restricted to the eligible positions (dg_entropy_accept_eligible), followed by
- * dg_loop_update with the step's argmax as the candidate.  Arguments as those calls;
- * the loop state (canvas, eligible, prev_candidate, stable, steps, converged) is read
- * and written in place, so successive calls on one stream (or one captured graph,
- * replayed) run successive steps.
+ * dg_loop_update.
+ *   temperature == 0: the candidate is the argmax and kappa is dg_row_stats' (ln Z);
+ *                     `candidate` may be NULL.
+ *   temperature > 0:  dg_row_stats_sample draws the candidates (seed, offset; advance
+ *                     the offset every step) into `candidate`, kappa is -ln p of the
+ *                     drawn token, and the canvas takes the drawn tokens; stability is
+ *                     still judged on the argmax.
+ * Other arguments as dg_sampler_step, dg_entropy_accept_eligible and dg_loop_update;
+ * the loop state (canvas, eligible, prev_argmax, stable, steps, converged) is read and
+ * written in place, so successive calls on one stream (or one captured graph,
+ * replayed) run successive steps.  A negative, infinite or NaN temperature is
+ * DG_ERR_INVALID_ARG.
  */
 dg_status dg_sampler_loop_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V,
                                int64_t ldl, const uint16_t *W, int64_t vocab_start,
                                int64_t vocab_end, int64_t rows_pad, int64_t ldw, int64_t d,
                                float gamma, const float *budgets, int32_t min_accept,
                                int32_t stable_steps, float entropy_threshold, int32_t step_limit,
+                               float temperature, uint64_t seed, uint64_t offset,
                                float *m, float *lse, float *H, float *kappa, int32_t *argmax,
-                               int32_t *order, uint8_t *mask, int32_t *n_accepted,
-                               float *E, int64_t ldo,
-                               int32_t *canvas, uint8_t *eligible, int32_t *prev_candidate,
+                               int32_t *candidate, int32_t *order, uint8_t *mask,
+                               int32_t *n_accepted, float *E, int64_t ldo,
+                               int32_t *canvas, uint8_t *eligible, int32_t *prev_argmax,
                                int32_t *stable, int32_t *steps, uint8_t *converged,
                                void *workspace, size_t workspace_bytes, dg_stream_t stream);
 

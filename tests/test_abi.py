@@ -28,7 +28,8 @@ def test_header_declares_the_boundary():
     names = declared_symbols()
     for n in ["dg_row_stats", "dg_soft_embed", "dg_entropy_accept", "dg_sum_partials", "dg_sampler_step",
               "dg_soft_embed_workspace_size", "dg_get_device_status", "dg_last_error", "dg_version",
-              "dg_row_sample", "dg_entropy_accept_eligible", "dg_loop_update", "dg_sampler_loop_step"]:
+              "dg_row_sample", "dg_entropy_accept_eligible", "dg_loop_update", "dg_sampler_loop_step",
+              "dg_row_stats_sample"]:
         assert n in names
 
 
@@ -136,25 +137,42 @@ def test_loop_update_rejects_bad_arguments(lib):
     L = lib.lib
     p = ctypes.c_void_p(256)
     state = [p] * 6
-    assert L.dg_loop_update(p, p, p, -1, 16, 2, 0.5, 10, *state, None) == 1
-    assert L.dg_loop_update(p, p, p, 1, 0, 2, 0.5, 10, *state, None) == 1
-    assert L.dg_loop_update(p, p, p, 1, 1025, 2, 0.5, 10, *state, None) == 2
-    assert L.dg_loop_update(p, p, p, 1, 16, -1, 0.5, 10, *state, None) == 1
-    assert L.dg_loop_update(p, p, p, 1, 16, 2, 0.5, 0, *state, None) == 1
-    assert L.dg_loop_update(p, p, p, 1, 16, 2, float("nan"), 10, *state, None) == 1
-    assert L.dg_loop_update(p, p, p, 1, 16, 2, 0.5, 10, p, p, None, p, p, p, None) == 1
-    assert L.dg_loop_update(None, p, p, 1, 16, 2, 0.5, 10, *state, None) == 1
-    assert L.dg_loop_update(None, None, None, 0, 16, 2, 0.5, 10, *([None] * 6), None) == 0
+    assert L.dg_loop_update(p, p, p, p, -1, 16, 2, 0.5, 10, *state, None) == 1
+    assert L.dg_loop_update(p, p, p, p, 1, 0, 2, 0.5, 10, *state, None) == 1
+    assert L.dg_loop_update(p, p, p, p, 1, 1025, 2, 0.5, 10, *state, None) == 2
+    assert L.dg_loop_update(p, p, p, p, 1, 16, -1, 0.5, 10, *state, None) == 1
+    assert L.dg_loop_update(p, p, p, p, 1, 16, 2, 0.5, 0, *state, None) == 1
+    assert L.dg_loop_update(p, p, p, p, 1, 16, 2, float("nan"), 10, *state, None) == 1
+    assert L.dg_loop_update(p, p, p, p, 1, 16, 2, 0.5, 10, p, p, None, p, p, p, None) == 1
+    assert L.dg_loop_update(None, p, p, p, 1, 16, 2, 0.5, 10, *state, None) == 1
+    assert L.dg_loop_update(p, None, p, p, 1, 16, 2, 0.5, 10, *state, None) == 1
+    assert L.dg_loop_update(None, None, None, None, 0, 16, 2, 0.5, 10, *([None] * 6), None) == 0
 
 
 def test_loop_step_checks_its_loop_arguments(lib):
     L = lib.lib
     p = ctypes.c_void_p(256)
     step = [p, 1, 16, 4096, 4096, p, 0, 4096, 4096, 256, 256, 16.0, p, 0]
-    outs = [p] * 9 + [256]
+    outs = [p] * 10 + [256]
     ws = [p, 1 << 20, None]
-    assert L.dg_sampler_loop_step(*step, 2, 0.5, 0, *outs, *([p] * 6), *ws) == 1       # step_limit 0
-    assert L.dg_sampler_loop_step(*step, 2, 0.5, 10, *outs, p, None, p, p, p, p, *ws) == 1  # no eligible
+    argmax_mode = [0.0, 0, 0]
+    assert L.dg_sampler_loop_step(*step, 2, 0.5, 0, *argmax_mode, *outs, *([p] * 6), *ws) == 1   # step_limit 0
+    assert L.dg_sampler_loop_step(*step, 2, 0.5, 10, *argmax_mode, *outs, p, None, p, p, p, p, *ws) == 1
     bad = list(step)
-    bad[7] = 8192                                                                       # slice past V
-    assert L.dg_sampler_loop_step(*bad, 2, 0.5, 10, *outs, *([p] * 6), *ws) == 1
+    bad[7] = 8192                                                                              # slice past V
+    assert L.dg_sampler_loop_step(*bad, 2, 0.5, 10, *argmax_mode, *outs, *([p] * 6), *ws) == 1
+    for t in (-1.0, float("inf"), float("nan")):
+        assert L.dg_sampler_loop_step(*step, 2, 0.5, 10, t, 1, 0, *outs, *([p] * 6), *ws) == 1, t
+    no_cand = [p] * 5 + [None] + [p] * 4 + [256]                                               # candidate NULL
+    assert L.dg_sampler_loop_step(*step, 2, 0.5, 10, 1.0, 1, 0, *no_cand, *([p] * 6), *ws) == 1
+    assert b"candidate" in L.dg_last_error()
+
+
+def test_row_stats_sample_rejects_bad_arguments(lib):
+    L = lib.lib
+    p = ctypes.c_void_p(256)
+    for t in (0.0, -1.0, float("inf"), float("nan")):
+        assert L.dg_row_stats_sample(p, 4, 16, 16, t, 1, 0, p, p, p, p, p, p, p, None) == 1, t
+    assert L.dg_row_stats_sample(p, 4, 16, 16, 1.0, 1, 0, p, p, p, p, p, None, p, None) == 1
+    assert L.dg_row_stats_sample(p, 4, 16, 18, 1.0, 1, 0, p, p, p, p, p, p, p, None) == 2  # ldl % 4 != 0
+    assert L.dg_row_stats_sample(None, 0, 16, 16, 1.0, 1, 0, *([None] * 7), None) == 0

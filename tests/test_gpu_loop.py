@@ -21,7 +21,7 @@ BUDGET_MARGIN = 1e-4   # nats, as the guarded step workloads
 KAPPA_REL = 1e-5
 MEAN_H_MARGIN = 1e-3   # nats: the mean of fp32 entropies within 1e-4 of fp64 ones
 
-STATE_KEYS = {"canvas": "canvas", "eligible": "eligible", "prev_candidate": "prev", "stable": "stable",
+STATE_KEYS = {"canvas": "canvas", "eligible": "eligible", "prev_argmax": "prev", "stable": "stable",
               "steps": "steps", "converged": "converged"}
 
 
@@ -241,3 +241,79 @@ def test_loop_steps_in_a_cuda_graph_match_eager_steps(B):
     for k, v in eager.items():
         assert torch.equal(now[k], v), k
     assert lp.state["steps"].tolist() == [4, 4] and lp.state["converged"].tolist() == [1, 1]
+
+
+def test_loop_update_judges_stability_on_the_argmax(B):
+    """Candidates (drawn tokens) that change every step, argmax predictions that settle:
+    the canvas takes the candidates, the stable count follows the argmax."""
+    rng = np.random.default_rng(11)
+    n_req, L_c = 3, 50
+    R = n_req * L_c
+    o = new_loop_state(n_req, L_c)
+    g = B.new_loop_state(n_req, L_c, "cuda")
+    am = rng.integers(0, 100, R).astype(np.int32)
+    for t in range(8):
+        if t < 3:
+            am = np.where(rng.random(R) < 0.3, rng.integers(0, 100, R), am).astype(np.int32)
+        cand = rng.integers(0, 100, R).astype(np.int32)
+        H = rng.uniform(0.0, 0.4, R).astype(np.float32)
+        mask = ((rng.random(R) < 0.3) & (o["eligible"] == 1)).astype(np.uint8)
+        B.dg_loop_update(dev(cand), dev(H), dev(mask), n_req, L_c, g, 3, 1.0, 20, argmax=dev(am))
+        o = loop_update(o, cand, H, mask, n_req, L_c, 3, 1.0, 20, argmax=am)
+        torch.cuda.synchronize()
+        compare_state(g, o, f"step {t}")
+    assert o["converged"].all() and (o["stable"] >= 3).all()
+
+
+SAMPLE_MARGIN = 1e-4   # top-two perturbed scores: the GPU's fp32 scores are within 1e-5
+SAMPLED_WL = LOOP_WL.with_(seed=43)
+
+
+def sampled_chain_inputs(wl, steps, temperature, seed):
+    """The oracle chain of a sampling loop, with the margins its exact comparison needs."""
+    from oracle import candidate_kappa, row_sample
+    base = inputs.logits(wl)
+    budgets = inputs.budgets(wl)
+    thr = loop_threshold(row_stats(base), wl)
+    o = new_loop_state(wl.n_req, wl.L_c)
+    chain = []
+    for t in range(steps):
+        x = inputs.loop_logits(wl, t, base=base)
+        st = row_stats(x)
+        sm = row_sample(x, temperature, seed, t)
+        kc = candidate_kappa(x, sm["candidate"])
+        assert np.all(sm["margin"] > SAMPLE_MARGIN), ("near-tie draw", t)
+        assert decision_margins_ok(st["H"], kc, o["eligible"], wl.n_req, wl.L_c, budgets), t
+        for q in range(wl.n_req):
+            assert abs(st["H"][q * wl.L_c:(q + 1) * wl.L_c].mean() - thr) >= MEAN_H_MARGIN, (t, q)
+        acc = entropy_accept_eligible(st["H"], kc, o["eligible"], wl.n_req, wl.L_c, budgets, min_accept=1)
+        o = loop_update(o, sm["candidate"], st["H"], acc["mask"], wl.n_req, wl.L_c, STABLE_STEPS, thr, STEP_LIMIT,
+                        argmax=st["argmax"])
+        chain.append((x, st, sm, kc, acc, o))
+    return budgets, thr, chain
+
+
+def test_sampled_loop_chain_matches_oracle(B):
+    """A sampling loop (temperature 1, Philox offset = step): at every step the fused
+    statistics + draw, the acceptance by -ln p of the drawn token over the eligible
+    positions, the canvas of drawn tokens and the argmax-judged state, bit-exact against
+    the oracle chain."""
+    from denoising_sampler_step_gb300.step import SamplerLoop
+    wl, temperature, seed = SAMPLED_WL, 1.0, 2024
+    budgets, thr, chain = sampled_chain_inputs(wl, N_STEPS, temperature, seed)
+    Wb = inputs.embedding_bf16(wl)
+    lp = SamplerLoop(w_dev(Wb), wl.n_req, wl.L_c, wl.V, wl.gamma, STABLE_STEPS, thr, STEP_LIMIT,
+                     temperature=temperature, seed=seed, min_accept=1)
+    bud = dev(budgets)
+    for t, (x, st, sm, kc, acc, o) in enumerate(chain):
+        out = lp(dev(x), bud)
+        torch.cuda.synchronize()
+        check_stats(out, dict(st, kappa=kc))   # kappa: -ln p of the drawn token
+        assert np.array_equal(out["candidate"].cpu().numpy(), sm["candidate"]), t
+        for key in ("order", "mask", "n_accepted"):
+            assert np.array_equal(out[key].cpu().numpy(), acc[key]), (t, key)
+        compare_state(lp.state, o, f"step {t}")
+    B.dg_get_device_status()
+    assert chain[-1][5]["converged"].all()
+    # the chain keeps drawn tokens that are not the argmax of their step
+    assert any(np.any((sm["candidate"] != st["argmax"]) & (acc["mask"] == 1)) for _, st, sm, _, acc, _ in chain)

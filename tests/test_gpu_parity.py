@@ -399,3 +399,54 @@ def test_row_sample_special_rows_and_determinism(B):
         assert torch.equal(g[k].view(torch.int32), h[k].view(torch.int32)), k
     o = B.dg_row_sample(dev(np.tile(x[0], (64, 1))), 1.0, seed=99, offset=4)
     assert len(set(o["candidate"].cpu().numpy().tolist())) > 1  # other counters, other draws
+
+
+@pytest.mark.parametrize("V,ld,temperature", [(4096, 4096, 1.0), (4093, 4096, 0.5), (70001, 70004, 1.0),
+                                              (262144, 262144, 0.7)])
+def test_row_stats_sample_is_the_two_passes_in_one(B, V, ld, temperature):
+    """The fused pass: statistics bit-identical to dg_row_stats, the draw and its
+    log-probability bit-identical to dg_row_sample, both against the oracle; kappa is
+    -ln p of the drawn token (ln Z where it is the argmax)."""
+    from oracle import candidate_kappa, row_sample
+    wl = inputs.WORKLOADS["tiny"].with_(V=V, L_c=12, seed=V + 5)
+    x = inputs.logits(wl, ld=ld)
+    xd = dev(x)
+    f = B.dg_row_stats_sample(xd, temperature, seed=77, offset=2, V=V)
+    s = B.dg_row_stats(xd, V=V)
+    r = B.dg_row_sample(xd, temperature, seed=77, offset=2, V=V)
+    for k in ("m", "lse", "H", "argmax"):
+        assert torch.equal(f[k].view(torch.int32), s[k].view(torch.int32)), k
+    for k in ("candidate", "log_p"):
+        assert torch.equal(f[k].view(torch.int32), r[k].view(torch.int32)), k
+    ost = row_stats(x[:, :V])
+    check_stats({k: s[k] for k in s}, ost)
+    check_sample(f, row_sample(x[:, :V], temperature, 77, 2))
+    cand = f["candidate"].cpu().numpy()
+    kc = f["kappa"].cpu().numpy().astype(np.float64)
+    ref = candidate_kappa(x[:, :V], cand)
+    assert np.all(np.abs(kc - ref) <= 1e-5 * np.maximum(1.0, ref))
+    at_argmax = cand == f["argmax"].cpu().numpy()
+    assert np.array_equal(f["kappa"].cpu().numpy()[at_argmax], s["kappa"].cpu().numpy()[at_argmax])
+
+
+def test_row_stats_sample_special_rows(B):
+    from oracle import candidate_kappa, row_sample
+    V = 50000
+    rng = np.random.default_rng(9)
+    x = (rng.standard_normal((5, V)) * 2).astype(np.float32)
+    x[1, :] = -np.inf
+    x[1, [7, 77, 40000]] = 3.0
+    x[2, 12345] = 1e4
+    x[4] = -np.inf
+    xd = dev(x)
+    f = B.dg_row_stats_sample(xd, 1.0, seed=5, offset=0)
+    check_sample(f, row_sample(x, 1.0, 5, 0))
+    s = B.dg_row_stats(xd)
+    for k in ("m", "lse", "H", "argmax"):
+        assert torch.equal(f[k].view(torch.int32), s[k].view(torch.int32)), k
+    kc = f["kappa"].cpu().numpy().astype(np.float64)
+    ref = candidate_kappa(x, f["candidate"].cpu().numpy())
+    assert np.array_equal(np.isnan(kc), np.isnan(ref))
+    fin = np.isfinite(ref)
+    assert np.all(np.abs(kc[fin] - ref[fin]) <= 1e-5 * np.maximum(1.0, ref[fin]))
+    assert f["candidate"][2].item() == 12345 and f["kappa"][2].item() == 0.0
