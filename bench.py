@@ -79,15 +79,16 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 100):
         self.proc = None
         self.gpu = gpu_index
+        self.period_ms = period_ms
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
         time.sleep(0.3)
@@ -99,12 +100,13 @@ class ClockSampler:
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
         rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
-        sm, mx, reasons = [], None, set()
+        sm, mx, reasons, pw = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
             try:
                 sm.append(float(r[1]))
                 mx = float(r[2])
+                pw.append(float(r[3]))
             except ValueError:
                 continue
             for n, v in zip(names, r[5:9]):
@@ -112,6 +114,7 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
                 "reasons": sorted(reasons), "samples": len(sm),
+                "power_w": statistics.median(pw) if pw else None,
                 "window": "from warm-up start to the end of the end-to-end loop"}
 
 
@@ -181,6 +184,9 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sustained", type=float, default=0.0,
+                    help="also run the step and the soft-embed call back to back for this many seconds "
+                         "each, sampling clocks and power every 20 ms")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
@@ -366,6 +372,26 @@ def main() -> None:
 
     ms, e2e_ms = replicas.max_over_ranks([ms, e2e_ms], device=dev)
 
+    # sustained operation: the clock the power cap allows when a call runs for seconds
+    sustained = None
+    if args.sustained > 0:
+        sustained = {}
+        for name, call, t_ms in (("step", lambda: step(xd, bd), ms / args.steps),
+                                 ("soft_embed", calls["soft_embed"], comp["soft_embed"])):
+            n = max(10, int(args.sustained * 1e3 / t_ms))
+            sampler = ClockSampler(local, period_ms=20)
+            sampler.start()
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            for _ in range(n):
+                call()
+            s1.record(stream)
+            torch.cuda.synchronize(dev)
+            c = sampler.stop()
+            sustained[name] = {"ms_per_call": s0.elapsed_time(s1) / n, "calls": n, "sm_mhz": c["sm_mhz"],
+                               "power_w": c["power_w"], "reasons": c["reasons"], "samples": c["samples"]}
+        B.dg_get_device_status()
+
     pk = peaks()
     sc = cost.StepCost(rows=wl.R, V=wl.V, d=wl.d, vocab=wl.V)
     t_roof = sc.roofline_seconds(pk["hbm_gbs"], pk["bf16_tflops"])
@@ -411,6 +437,8 @@ def main() -> None:
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "clocks": clk,
     }
+    if sustained is not None:
+        line["sustained"] = sustained
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(x, Wb, wl)
     if rank == 0:
