@@ -59,6 +59,10 @@ lib.dg_sampler_loop_step.argtypes = [_p, _i32, _i32, _i64, _i64, _p, _i64, _i64,
 lib.dg_row_stats_sample.argtypes = [_p, _i64, _i64, _i64, _f32, ctypes.c_uint64, ctypes.c_uint64,
                                     _p, _p, _p, _p, _p, _p, _p, _p]
 lib.dg_row_stats_sample.restype = ctypes.c_int
+lib.dg_row_stats_partial.argtypes = [_p, _i64, _i64, _i64, _i64, _p, _p]
+lib.dg_row_stats_partial.restype = ctypes.c_int
+lib.dg_row_stats_combine.argtypes = [_p, _i32, _i64, _p, _p, _p, _p, _p, _p]
+lib.dg_row_stats_combine.restype = ctypes.c_int
 lib.dg_sampler_loop_step.restype = ctypes.c_int
 
 STATUS = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED", 3: "DG_ERR_CUDA", 4: "DG_ERR_TIMEOUT"}
@@ -121,6 +125,31 @@ def dg_row_sample(logits: torch.Tensor, temperature: float = 1.0, seed: int = 0,
         o = {"candidate": _new(R, torch.int32, dev), "log_p": _new(R, torch.float32, dev)}
     _check(lib.dg_row_sample(_ptr(logits), R, V, _ld(logits), float(temperature), int(seed), int(offset),
                              _ptr(o["candidate"]), _ptr(o["log_p"]), _stream(stream)), "dg_row_sample")
+    return o
+
+
+def dg_row_stats_partial(shard: torch.Tensor, vocab_offset: int, n: int | None = None, stream=None,
+                         out: torch.Tensor | None = None) -> torch.Tensor:
+    """The shard's 16-byte summary per row: a [R, 4] float32 tensor whose column 1 holds the
+    int32 bits of the global argmax (view it with .view(torch.int32))."""
+    R = shard.shape[0]
+    n = shard.shape[1] if n is None else n
+    o = out if out is not None else _new((R, 4), torch.float32, shard.device)
+    _check(lib.dg_row_stats_partial(_ptr(shard), R, n, _ld(shard), vocab_offset, _ptr(o), _stream(stream)),
+           "dg_row_stats_partial")
+    return o
+
+
+def dg_row_stats_combine(states: torch.Tensor, stream=None, out: dict | None = None) -> dict:
+    """Full-row statistics from [T, R, 4] shard summaries in shard order."""
+    T, R = states.shape[0], states.shape[1]
+    dev = states.device
+    o = out if out is not None else {"m": _new(R, torch.float32, dev), "lse": _new(R, torch.float32, dev),
+                                     "H": _new(R, torch.float32, dev), "kappa": _new(R, torch.float32, dev),
+                                     "argmax": _new(R, torch.int32, dev)}
+    _check(lib.dg_row_stats_combine(_ptr(states), T, R, _ptr(o.get("m")), _ptr(o.get("lse")), _ptr(o.get("H")),
+                                    _ptr(o.get("kappa")), _ptr(o.get("argmax")), _stream(stream)),
+           "dg_row_stats_combine")
     return o
 
 

@@ -9,6 +9,7 @@
 
 #include "dg_common.cuh"
 #include "dg_internal.h"
+#include <cstdint>
 
 namespace dg {
 
@@ -185,6 +186,32 @@ dg_status dg_row_stats(const float *logits, int64_t R, int64_t V, int64_t ldl, f
     if (st != DG_OK || R == 0) return st;
     cudaError_t e = launch_row_stats(logits, R, V, ldl, m, lse, H, kappa, argmax, (cudaStream_t)stream);
     return e == cudaSuccess ? DG_OK : cuda_fail(e, "row stats launch");
+}
+
+dg_status dg_row_stats_partial(const float *logits, int64_t R, int64_t n, int64_t ldl, int64_t vocab_offset,
+                               float *state, dg_stream_t stream) {
+    t_last_error[0] = 0;
+    dg_status st = check_stats_args(logits, R, n, ldl);
+    if (st != DG_OK || R == 0) return st;
+    if (vocab_offset < 0 || vocab_offset + n > INT32_MAX - 1)
+        return fail(DG_ERR_INVALID_ARG, "row stats partial: the shard must lie in [0, 2^31 - 1)");
+    if (!state) return fail(DG_ERR_INVALID_ARG, "row stats partial: state is NULL");
+    if (reinterpret_cast<uintptr_t>(state) % 16 != 0)
+        return fail(DG_ERR_UNSUPPORTED, "row stats partial: state must be 16-byte aligned");
+    cudaError_t e = launch_row_stats_partial(logits, R, n, ldl, vocab_offset, state, (cudaStream_t)stream);
+    return e == cudaSuccess ? DG_OK : cuda_fail(e, "row stats partial launch");
+}
+
+dg_status dg_row_stats_combine(const float *states, int32_t T, int64_t R, float *m, float *lse, float *H,
+                               float *kappa, int32_t *argmax, dg_stream_t stream) {
+    t_last_error[0] = 0;
+    if (R < 0 || T < 1 || T > 1024) return fail(DG_ERR_INVALID_ARG, "row stats combine: need R >= 0, 1 <= T <= 1024");
+    if (R == 0) return DG_OK;
+    if (!states) return fail(DG_ERR_INVALID_ARG, "row stats combine: states is NULL");
+    if (reinterpret_cast<uintptr_t>(states) % 16 != 0)
+        return fail(DG_ERR_UNSUPPORTED, "row stats combine: states must be 16-byte aligned");
+    cudaError_t e = launch_row_stats_combine(states, T, R, m, lse, H, kappa, argmax, (cudaStream_t)stream);
+    return e == cudaSuccess ? DG_OK : cuda_fail(e, "row stats combine launch");
 }
 
 dg_status dg_row_sample(const float *logits, int64_t R, int64_t V, int64_t ldl, float temperature, uint64_t seed,

@@ -59,6 +59,13 @@ int device_sm_count();
 cudaError_t launch_row_sample(const float *logits, int64_t R, int64_t V, int64_t ldl, float temperature,
                               uint64_t seed, uint64_t offset, int32_t *candidate, float *log_p,
                               cudaStream_t stream);
+// Vocabulary-sharded statistics (row_stats.cu): a shard's 16-byte summary per row, and the
+// full-row statistics from the summaries of all shards, merged in shard order.
+cudaError_t launch_row_stats_partial(const float *logits, int64_t R, int64_t V, int64_t ldl, int64_t vocab_offset,
+                                     float *state, cudaStream_t stream);
+cudaError_t launch_row_stats_combine(const float *states, int32_t T, int64_t R, float *m, float *lse, float *H,
+                                     float *kappa, int32_t *argmax, cudaStream_t stream);
+
 // The same draw fused with the row statistics (one read of the logits); kappa is
 // -ln p(candidate) at temperature 1.
 cudaError_t launch_row_stats_sample(const float *logits, int64_t R, int64_t V, int64_t ldl, float temperature,

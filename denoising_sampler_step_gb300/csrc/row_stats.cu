@@ -44,7 +44,8 @@ template <int CLUSTER>
 __global__ void __launch_bounds__(kStatsThreads, 4)
     row_stats_kernel(const float *__restrict__ logits, int64_t V, int64_t ldl, float *__restrict__ out_m,
                      float *__restrict__ out_lse, float *__restrict__ out_H,
-                     float *__restrict__ out_kappa, int32_t *__restrict__ out_argmax) {
+                     float *__restrict__ out_kappa, int32_t *__restrict__ out_argmax,
+                     float4 *__restrict__ out_state, int64_t vocab_offset) {
     __shared__ RowState warp_state[kStatsThreads / 32];
     __shared__ RowState cta_state[CLUSTER];
 
@@ -142,6 +143,12 @@ __global__ void __launch_bounds__(kStatsThreads, 4)
         }
     }
 
+    if (threadIdx.x == 0 && out_state) {
+        // a shard's summary: (m, global argmax as int32 bits, rest, t)
+        const int a = st.m == -INFINITY ? 0x7fffffff : (int)(st.a + vocab_offset);
+        out_state[row] = make_float4(st.m, __int_as_float(a), st.rest, st.t);
+        return;
+    }
     if (threadIdx.x == 0) {
         float lse, H, kappa;
         int a = st.a;
@@ -162,9 +169,41 @@ __global__ void __launch_bounds__(kStatsThreads, 4)
     }
 }
 
+// Full-row statistics from per-shard summaries [T][R] (float4: m, argmax bits, rest, t),
+// merged in shard order with the statistics kernel's own merge.
+__global__ void __launch_bounds__(256)
+    stats_combine_kernel(const float4 *__restrict__ states, int T, int64_t R, float *__restrict__ out_m,
+                         float *__restrict__ out_lse, float *__restrict__ out_H, float *__restrict__ out_kappa,
+                         int32_t *__restrict__ out_argmax) {
+    const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (row >= R) return;
+    RowState st = empty_row_state();
+    for (int r = 0; r < T; ++r) {
+        const float4 v = states[(int64_t)r * R + row];
+        merge(st, RowState{v.x, __float_as_int(v.y), v.z, v.w});
+    }
+    float lse, H, kappa;
+    int a = st.a;
+    if (st.m == -INFINITY) {
+        lse = H = kappa = __int_as_float(0x7fc00000);
+        a = 0;
+    } else {
+        const float lnZ = log1pf(st.rest);
+        lse = st.m + lnZ;
+        H = lnZ - st.t / (1.0f + st.rest);
+        kappa = lnZ;
+    }
+    if (out_m) out_m[row] = st.m;
+    if (out_lse) out_lse[row] = lse;
+    if (out_H) out_H[row] = H;
+    if (out_kappa) out_kappa[row] = kappa;
+    if (out_argmax) out_argmax[row] = a;
+}
+
 template <int CLUSTER>
 cudaError_t launch_stats(const float *logits, int64_t R, int64_t V, int64_t ldl, float *m, float *lse,
-                         float *H, float *kappa, int32_t *argmax, cudaStream_t stream) {
+                         float *H, float *kappa, int32_t *argmax, cudaStream_t stream, float4 *state = nullptr,
+                         int64_t vocab_offset = 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(R * CLUSTER), 1, 1);
     cfg.blockDim = dim3(kStatsThreads, 1, 1);
@@ -177,7 +216,8 @@ cudaError_t launch_stats(const float *logits, int64_t R, int64_t V, int64_t ldl,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, row_stats_kernel<CLUSTER>, logits, V, ldl, m, lse, H, kappa, argmax);
+    return cudaLaunchKernelEx(&cfg, row_stats_kernel<CLUSTER>, logits, V, ldl, m, lse, H, kappa, argmax, state,
+                              vocab_offset);
 }
 
 }  // namespace
@@ -204,6 +244,33 @@ cudaError_t launch_row_stats(const float *logits, int64_t R, int64_t V, int64_t 
         case 4: return launch_stats<4>(logits, R, V, ldl, m, lse, H, kappa, argmax, stream);
         default: return launch_stats<8>(logits, R, V, ldl, m, lse, H, kappa, argmax, stream);
     }
+}
+
+}  // namespace dg
+
+namespace dg {
+
+cudaError_t launch_row_stats_partial(const float *logits, int64_t R, int64_t V, int64_t ldl, int64_t vocab_offset,
+                                     float *state, cudaStream_t stream) {
+    float4 *st = reinterpret_cast<float4 *>(state);
+    switch (stats_cluster_size(R, V)) {
+        case 1: return launch_stats<1>(logits, R, V, ldl, nullptr, nullptr, nullptr, nullptr, nullptr, stream, st,
+                                       vocab_offset);
+        case 2: return launch_stats<2>(logits, R, V, ldl, nullptr, nullptr, nullptr, nullptr, nullptr, stream, st,
+                                       vocab_offset);
+        case 4: return launch_stats<4>(logits, R, V, ldl, nullptr, nullptr, nullptr, nullptr, nullptr, stream, st,
+                                       vocab_offset);
+        default: return launch_stats<8>(logits, R, V, ldl, nullptr, nullptr, nullptr, nullptr, nullptr, stream, st,
+                                        vocab_offset);
+    }
+}
+
+cudaError_t launch_row_stats_combine(const float *states, int32_t T, int64_t R, float *m, float *lse, float *H,
+                                     float *kappa, int32_t *argmax, cudaStream_t stream) {
+    const unsigned blocks = (unsigned)((R + 255) / 256);
+    stats_combine_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4 *>(states), (int)T, R, m, lse, H,
+                                                     kappa, argmax);
+    return cudaGetLastError();
 }
 
 }  // namespace dg

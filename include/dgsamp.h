@@ -208,6 +208,34 @@ dg_status dg_sampler_step(const float *logits, int32_t n_req, int32_t L_c, int64
 dg_status dg_get_device_status(dg_stream_t stream);
 
 /*
+ * Vocabulary-sharded row statistics ([P1] "The fix": the vocabulary is split into
+ * contiguous ranges, one per rank, while the softmax stays over all V entries).  A rank
+ * holding the logit columns [vocab_offset, vocab_offset + n) summarises each row in 16
+ * bytes; the summaries of all shards, gathered in shard order, give dg_row_stats'
+ * statistics of the whole row.
+ *
+ * dg_row_stats_partial:
+ *   logits  [R, ldl] fp32, the shard's n columns (layout rules of dg_row_stats with V = n)
+ *   state   [R] x 16 bytes, 16-byte aligned: per row {m fp32, a int32, rest fp32, t fp32}
+ *           m = max over the shard, a = vocab_offset + the first column attaining it
+ *           (2^31 - 1 if the shard row has no finite logit), rest = sum over the shard's
+ *           other entries of exp(l - m), t = sum over the shard of exp(l - m)(l - m)
+ *   Requires 0 <= vocab_offset and vocab_offset + n < 2^31 - 1.
+ * dg_row_stats_combine:
+ *   states  [T][R] summaries (the shards' arrays one after another, shard order =
+ *           vocabulary order), 1 <= T <= 1024, 16-byte aligned
+ *   m, lse, H, kappa [R] fp32, argmax [R] int32: as dg_row_stats (each may be NULL);
+ *   the maxima are merged in shard order, so a maximum tied across shards takes the
+ *   lowest index.  The result equals dg_row_stats of the whole row up to the order of
+ *   the fp32 additions.
+ * Both asynchronous; R == 0 queues nothing.
+ */
+dg_status dg_row_stats_partial(const float *logits, int64_t R, int64_t n, int64_t ldl,
+                               int64_t vocab_offset, float *state, dg_stream_t stream);
+dg_status dg_row_stats_combine(const float *states, int32_t T, int64_t R, float *m, float *lse,
+                               float *H, float *kappa, int32_t *argmax, dg_stream_t stream);
+
+/*
  * Stochastic candidates ([P2] sampling loop: candidate tokens are sampled at every
  * position).  For each row i, a categorical draw from softmax(l_i / temperature), taken
  * as the Gumbel-max  candidate_i = argmax_v (l_{i,v} / temperature - ln(-ln u_{i,v})),

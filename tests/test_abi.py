@@ -29,7 +29,7 @@ def test_header_declares_the_boundary():
     for n in ["dg_row_stats", "dg_soft_embed", "dg_entropy_accept", "dg_sum_partials", "dg_sampler_step",
               "dg_soft_embed_workspace_size", "dg_get_device_status", "dg_last_error", "dg_version",
               "dg_row_sample", "dg_entropy_accept_eligible", "dg_loop_update", "dg_sampler_loop_step",
-              "dg_row_stats_sample"]:
+              "dg_row_stats_sample", "dg_row_stats_partial", "dg_row_stats_combine"]:
         assert n in names
 
 
@@ -176,3 +176,18 @@ def test_row_stats_sample_rejects_bad_arguments(lib):
     assert L.dg_row_stats_sample(p, 4, 16, 16, 1.0, 1, 0, p, p, p, p, p, None, p, None) == 1
     assert L.dg_row_stats_sample(p, 4, 16, 18, 1.0, 1, 0, p, p, p, p, p, p, p, None) == 2  # ldl % 4 != 0
     assert L.dg_row_stats_sample(None, 0, 16, 16, 1.0, 1, 0, *([None] * 7), None) == 0
+
+
+def test_sharded_statistics_reject_bad_arguments(lib):
+    L = lib.lib
+    p = ctypes.c_void_p(256)
+    assert L.dg_row_stats_partial(p, 4, 16, 16, -1, p, None) == 1            # negative offset
+    assert L.dg_row_stats_partial(p, 4, 16, 16, 2**31 - 10, p, None) == 1    # past int32 indices
+    assert L.dg_row_stats_partial(p, 4, 16, 16, 0, None, None) == 1
+    assert L.dg_row_stats_partial(p, 4, 16, 16, 0, ctypes.c_void_p(264), None) == 2   # state not 16-byte aligned
+    assert L.dg_row_stats_partial(p, 4, 16, 18, 0, p, None) == 2             # ldl % 4 != 0
+    assert L.dg_row_stats_combine(p, 0, 4, p, p, p, p, p, None) == 1
+    assert L.dg_row_stats_combine(p, 1025, 4, p, p, p, p, p, None) == 1
+    assert L.dg_row_stats_combine(None, 2, 4, p, p, p, p, p, None) == 1
+    assert L.dg_row_stats_combine(ctypes.c_void_p(264), 2, 4, p, p, p, p, p, None) == 2
+    assert L.dg_row_stats_combine(None, 2, 0, None, None, None, None, None, None) == 0

@@ -1,0 +1,99 @@
+"""Parity of the vocabulary-sharded path on one device (through the C ABI): the shard
+summaries, their combination, and the whole sharded step emulated with all shards on
+one GPU, against the oracle and the unsharded calls."""
+import numpy as np
+import pytest
+import torch
+
+from denoising_sampler_step_gb300 import inputs
+from denoising_sampler_step_gb300.vocab_parallel import ShardedStep, shard_bounds
+from oracle import entropy_accept, row_stats, soft_embed
+from oracle.partition_oracle import row_stats_partial
+from tests.test_gpu_parity import E_TOL, check_stats, dev, rel_l2, w_dev
+from tests.workloads import guarded
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from denoising_sampler_step_gb300 import build
+    build.build()
+    from denoising_sampler_step_gb300 import binding
+    return binding
+
+
+def shard_tensor(x, s, e):
+    """Columns [s, e) in their own buffer, rows padded to a multiple of 4 with NaN (never read)."""
+    n = e - s
+    ld = (n + 3) // 4 * 4
+    buf = np.full((x.shape[0], ld), np.nan, np.float32)
+    buf[:, :n] = x[:, s:e]
+    return dev(buf)[:, :n]
+
+
+def test_one_shard_is_the_row_statistics_bit_for_bit(B):
+    wl = inputs.WORKLOADS["tiny"].with_(V=40000, L_c=24, seed=12)
+    xd = dev(inputs.logits(wl))
+    st = B.dg_row_stats(xd)
+    c = B.dg_row_stats_combine(B.dg_row_stats_partial(xd, 0)[None])
+    for k in ("m", "lse", "H", "kappa", "argmax"):
+        assert torch.equal(c[k].view(torch.int32), st[k].view(torch.int32)), k
+
+
+@pytest.mark.parametrize("V,T", [(4096, 2), (40001, 4), (70003, 7)])
+def test_shard_summaries_and_their_combination(B, V, T):
+    wl = inputs.WORKLOADS["tiny"].with_(V=V, L_c=20, seed=V + T)
+    x = inputs.logits(wl)
+    x[2, :] = -np.inf
+    x[2, V - 1] = 0.5                                  # mass only in the last shard
+    x[3, :] = -np.inf                                  # no distribution
+    x[4, [5, V - 3]] = x[4].max() + 3.0                # a maximum tied across shards
+    bounds = shard_bounds(V, T)
+    parts = [B.dg_row_stats_partial(shard_tensor(x, s, e), s) for s, e in bounds]
+    for (s, e), p in zip(bounds, parts):
+        o = row_stats_partial(x[:, s:e], s)
+        g = p.cpu().numpy()
+        assert np.array_equal(g[:, 1].view(np.int32), o["a"].astype(np.int32))
+        assert np.array_equal(g[:, 0], o["m"].astype(np.float32))
+        fin = np.isfinite(o["m"])
+        for col, k in ((2, "rest"), (3, "t")):
+            err = np.abs(g[fin, col] - o[k][fin]) / np.maximum(1.0, np.abs(o[k][fin]))
+            assert err.max() <= 1e-5, k
+    c = B.dg_row_stats_combine(torch.stack(parts))
+    check_stats(c, row_stats(x))
+    assert c["argmax"][4].item() == 5 and c["argmax"][2].item() == V - 1
+
+
+def test_sharded_step_on_one_device(B):
+    """Four uneven shards in one process: statistics, acceptance and E against the oracle;
+    E against the unsharded product (the partition identity)."""
+    wl = inputs.WORKLOADS["tiny"].with_(n_req=3, L_c=32, V=40001, d=256, seed=77, budget=("uniform", 2.0, 20.0))
+    x, budgets, ost, _ = guarded(wl, ld=40004)       # the unsharded calls need ldl % 4 == 0
+    Wb = inputs.embedding_bf16(wl)
+    Wd = w_dev(Wb)
+    bounds = shard_bounds(wl.V, 4)
+    step = ShardedStep(wl.n_req, wl.L_c, wl.gamma)
+    out = step.local_step([shard_tensor(x, s, e) for s, e in bounds], [s for s, _ in bounds],
+                          [Wd[s:e] for s, e in bounds], dev(budgets))
+    torch.cuda.synchronize()
+    B.dg_get_device_status()
+    check_stats(out, ost)
+    acc = entropy_accept(ost["H"], ost["kappa"], wl.n_req, wl.L_c, budgets)
+    for k in ("order", "mask", "n_accepted"):
+        assert np.array_equal(out[k].cpu().numpy(), acc[k]), k
+    E = out["E"].cpu().numpy()
+    assert rel_l2(E, soft_embed(x[:, :wl.V], ost["lse"], 0, wl.V, Wb, wl.gamma)).max() <= E_TOL
+    xd = dev(x)
+    full = B.dg_soft_embed(xd, B.dg_row_stats(xd, V=wl.V)["lse"], 0, wl.V, Wd, wl.gamma).cpu().numpy()
+    assert rel_l2(E, full.astype(np.float64)).max() <= 1e-3
+
+
+@pytest.mark.slow
+def test_sharded_statistics_full_size(B):
+    """The vocab_tp4 workload (V = 262,144, four shards): every row against the oracle."""
+    wl = inputs.WORKLOADS["vocab_tp4"]
+    x = inputs.logits(wl)
+    bounds = shard_bounds(wl.V, 4)
+    c = B.dg_row_stats_combine(torch.stack([B.dg_row_stats_partial(shard_tensor(x, s, e), s) for s, e in bounds]))
+    check_stats(c, row_stats(x))
