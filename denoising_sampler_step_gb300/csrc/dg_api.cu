@@ -5,6 +5,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 #include "dg_common.cuh"
@@ -90,7 +91,8 @@ namespace {
 dg_status run_soft_embed(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t s, int64_t e,
                          const uint16_t *W, int64_t ldw, int64_t d, float gamma, float *out, int64_t ldo,
                          void *ws, size_t ws_bytes, cudaStream_t stream, StreamHook between = nullptr,
-                         void *ctx = nullptr, bool overlap_previous = false) {
+                         void *ctx = nullptr, bool overlap_previous = false,
+                         const SinglePassOut *single = nullptr) {
     if (R == 0) return DG_OK;
     if (e == s) {
         cudaError_t err = launch_fill_zero(out, R, d, ldo, stream);
@@ -100,14 +102,14 @@ dg_status run_soft_embed(const float *logits, int64_t ldl, const float *lse, int
     if (sms <= 0) return fail(DG_ERR_CUDA, "soft embed: no CUDA device");
     SoftEmbedPlan plan;
     if (!plan_soft_embed(R, s, e, d, sms, &plan)) return fail(DG_ERR_INVALID_ARG, "soft embed: no plan for shape");
-    if (!ws || ws_bytes < plan.workspace_bytes)
-        return fail(DG_ERR_INVALID_ARG, "soft embed: workspace of %zu bytes is below the %zu needed", ws_bytes,
-                    plan.workspace_bytes);
+    const size_t need = single ? plan.single_pass_bytes : plan.workspace_bytes;
+    if (!ws || ws_bytes < need)
+        return fail(DG_ERR_INVALID_ARG, "soft embed: workspace of %zu bytes is below the %zu needed", ws_bytes, need);
     if (!aligned16(ws)) return fail(DG_ERR_UNSUPPORTED, "soft embed: workspace must be 16-byte aligned");
     const char *msg = "soft embed";
     cudaError_t err =
         launch_soft_embed(logits, ldl, lse, R, s, e, W, ldw, d, gamma, out, ldo, ws, plan, stream, &msg, between, ctx,
-                          overlap_previous);
+                          overlap_previous, single);
     return err == cudaSuccess ? DG_OK : cuda_fail(err, msg);
 }
 
@@ -246,6 +248,8 @@ size_t dg_soft_embed_workspace_size(int64_t R, int64_t vocab_len, int64_t d) {
     const int sms = device_sm_count();
     SoftEmbedPlan plan;
     if (!plan_soft_embed(R, 0, vocab_len, d, sms, &plan)) return 0;
+    // room for the single-pass step (its statistics and redo list after the partial tiles)
+    plan.workspace_bytes = plan.single_pass_bytes;
     // a slice that starts off a multiple of 4 reads up to one more block
     SoftEmbedPlan plan2;
     if (plan_soft_embed(R, 3, vocab_len + 3, d, sms, &plan2) && plan2.workspace_bytes > plan.workspace_bytes)
@@ -290,6 +294,19 @@ dg_status dg_sum_partials(const float *const *partials, int32_t T, int64_t R, in
 
 namespace {
 
+// The step reads the logits once (the product folds the row statistics) when the slice is
+// the whole vocabulary and the workspace has room; DGSAMP_TWO_PASS=1 forces the statistics
+// pass before the product (for comparisons).
+bool use_single_pass(int64_t R, int64_t V, int64_t vocab_start, int64_t vocab_end, int64_t d, size_t ws_bytes) {
+    if (vocab_start != 0 || vocab_end != V) return false;
+    if (const char *env = getenv("DGSAMP_TWO_PASS"))
+        if (env[0] == '1') return false;
+    const int sms = device_sm_count();
+    SoftEmbedPlan plan;
+    if (sms <= 0 || !plan_soft_embed(R, vocab_start, vocab_end, d, sms, &plan)) return false;
+    return ws_bytes >= plan.single_pass_bytes;
+}
+
 // The fused step, optionally restricted to eligible positions and followed by the
 // loop-state update (a denoising-loop step).
 dg_status run_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, int64_t ldl, const uint16_t *W,
@@ -319,6 +336,19 @@ dg_status run_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, i
     }
     if (R == 0) return DG_OK;
     const uint8_t *eligible = loop ? loop->eligible : nullptr;
+    if (!sampled && use_single_pass(R, V, vocab_start, vocab_end, d, workspace_bytes)) {
+        // one read of the logits: the product folds the statistics; the acceptance runs on
+        // them between the product and its reduce
+        AcceptArgs acc{H, kappa, budgets, n_req, L_c, min_accept, order, mask, n_accepted, eligible};
+        SinglePassOut so{m, lse, H, kappa, argmax};
+        st = run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, ldw, d, gamma, E, ldo, workspace,
+                            workspace_bytes, s, accept_hook, &acc, false, &so);
+        if (st != DG_OK || !loop) return st;
+        cudaError_t e = launch_loop_update(argmax, argmax, H, mask, n_req, L_c, loop->stable_steps,
+                                           loop->entropy_threshold, loop->step_limit, loop->canvas, loop->eligible,
+                                           loop->prev_argmax, loop->stable, loop->steps, loop->converged, s);
+        return e == cudaSuccess ? DG_OK : cuda_fail(e, "step: loop update launch");
+    }
     cudaError_t e = sampled ? launch_row_stats_sample(logits, R, V, ldl, loop->temperature, loop->seed, loop->offset,
                                                       m, lse, H, kappa, argmax, loop->candidate, nullptr, s)
                             : launch_row_stats(logits, R, V, ldl, m, lse, H, kappa, argmax, s);

@@ -35,7 +35,14 @@ struct SoftEmbedPlan {
     int64_t k_begin;   // first vocabulary column read (vocab_start rounded down to a multiple of 4)
     int64_t nkb;       // vocabulary blocks of the product
     int m_tiles, n_tiles, splits;
-    size_t workspace_bytes;
+    size_t workspace_bytes;    // the product and its reduce
+    size_t single_pass_bytes;  // the same with the single pass's statistics (launch_soft_embed `single`)
+};
+// Single pass: the product also folds the row statistics (no lse needed before it); they are
+// written here after it, before `between` runs.
+struct SinglePassOut {
+    float *m, *lse, *H, *kappa;
+    int32_t *argmax;
 };
 bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t d, int num_sms,
                      SoftEmbedPlan *plan);
@@ -51,7 +58,8 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
                               int64_t vocab_start, int64_t vocab_end, const uint16_t *W, int64_t ldw,
                               int64_t d, float gamma, float *out, int64_t ldo, void *workspace,
                               const SoftEmbedPlan &plan, cudaStream_t stream, const char **msg,
-                              StreamHook between = nullptr, void *ctx = nullptr, bool overlap_previous = false);
+                              StreamHook between = nullptr, void *ctx = nullptr, bool overlap_previous = false,
+                              const SinglePassOut *single = nullptr);
 
 int device_sm_count();
 

@@ -38,6 +38,7 @@
 
 #include "dg_common.cuh"
 #include "dg_internal.h"
+#include "row_state.cuh"
 
 namespace dg {
 
@@ -113,7 +114,21 @@ struct Params {
     int tail_halves;     // 1 if the last n-tile is 256 wide or less, else 0
     int splits, tail_splits;
     int w3d;             // 1: the W map is 3-D (64 columns x rows x 64-column atoms), one load per CTA and block
+    // single pass (no lse yet): each split's probabilities are taken against a reference
+    // c per row, exp(l - c), and the column-tile-0 clusters also fold the row statistics
+    int fused;
+    const float *logits; // the reference's source (the split's first four entries)
+    int64_t ldl;
+    float *ref;          // [splits][R] c, then (after the statistics) exp(c - lse)
+    float4 *state;       // [splits][n_tiles][R] row summaries (m, argmax bits, rest, t) of the blocks
+                         // i of the split with (i / PGROUPS) % n_tiles == the column tile
+    int *counts;         // [0] (split, row) pairs to redo: the reference was too far from the maximum
+    int2 *redo;          // [splits * R] the pairs
 };
+
+// A split's probabilities exp(l - c) stay finite and their sums far from overflow while the
+// split's maximum lies within this many nats of c; other (split, row) pairs are redone.
+constexpr float kRefSpan = 64.0f;
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
@@ -147,6 +162,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // lets it start once its own wait has returned.
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
+    // single pass: the redo count starts at zero (the statistics kernel after this one counts)
+    if (p.fused && blockIdx.x == 0 && threadIdx.x == 0) p.counts[0] = 0;
 
     // work of this cluster (or CTA): (n-tile, row block, split)
     const int pair = blockIdx.x / kCtasPerUnit;
@@ -207,6 +224,24 @@ __global__ void __launch_bounds__(THREADS, 1)
     cluster_sync_all();
     const uint32_t tmem_base = *tmem_slot;
     bool ok = true;  // false once this thread gave up on a wait
+    // single pass: the producers' reference per row and their row statistics; column tile
+    // nt folds the split's blocks i with (i / PGROUPS) % n_tiles == nt (every block is folded
+    // by one column tile, and evenly by the producer groups), after handing the block's A
+    // tile over, so that the fold stays off the product's critical path; in three levels (a
+    // block, 16 blocks, all) so that no fp32 sum runs over more than a few dozen terms: rest
+    // keeps kappa = log1p(rest) accurate near one-hot
+    int my_grp = -1;
+    int my_rows[ROWS_PER_LANE];
+    float my_ref[ROWS_PER_LANE];
+    rowstate::RowState my_st[ROWS_PER_LANE], my_st16[ROWS_PER_LANE];
+    int my_folded = 0;
+#pragma unroll
+    for (int q = 0; q < ROWS_PER_LANE; ++q) {
+        my_rows[q] = 0;
+        my_ref[q] = 0.0f;
+        my_st[q] = rowstate::empty_row_state();
+        my_st16[q] = rowstate::empty_row_state();
+    }
 
     if (warp == 11) {
         // ------------------------------------------------------------ W TMA
@@ -386,16 +421,40 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int pw = 3 * (warp >> 2) + (warp & 3) - 1;  // producer 0..7 (warps 1-3, 5-7, 9, 10)
         const int grp = pw / GROUP_WARPS;
         const int wig = pw % GROUP_WARPS;
-        grid_dependency_wait();  // lse comes from the grid queued before this one
-        grid_launch_dependents();
+        my_grp = grp;
         int rr[ROWS_PER_LANE];
         float neg_lse2[ROWS_PER_LANE];
+        if (p.fused) {
+            // reference c: the largest of the split's first four entries inside the slice
+            // (0 if none is finite); every column tile takes the same c
+            const int64_t k0 = p.k_begin + kb0 * BK;
 #pragma unroll
-        for (int q = 0; q < ROWS_PER_LANE; ++q) {
-            rr[q] = (wig * ROWS_PER_LANE + q) * 32 + lane;  // row of the tile
-            const int row = row0 + rr[q];
-            // rows past R are zero-filled by the TMA: an offset of -inf makes their entries 0
-            neg_lse2[q] = row < p.R ? -p.lse[row] * kLog2e : -INFINITY;
+            for (int q = 0; q < ROWS_PER_LANE; ++q) {
+                rr[q] = (wig * ROWS_PER_LANE + q) * 32 + lane;
+                const int row = row0 + rr[q];
+                float c = -INFINITY;
+                if (row < p.R && nkb > 0) {
+                    const float4 f = __ldg(reinterpret_cast<const float4 *>(p.logits + (int64_t)row * p.ldl + k0));
+                    const float fv[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        if (k0 + t >= p.vocab_start && k0 + t < p.vocab_end) c = fmaxf(c, fv[t]);
+                }
+                if (!(c > -INFINITY)) c = 0.0f;
+                my_rows[q] = rr[q];
+                my_ref[q] = c;
+                neg_lse2[q] = row < p.R ? -c * kLog2e : -INFINITY;
+            }
+        } else {
+            grid_dependency_wait();  // lse comes from the grid queued before this one
+            grid_launch_dependents();
+#pragma unroll
+            for (int q = 0; q < ROWS_PER_LANE; ++q) {
+                rr[q] = (wig * ROWS_PER_LANE + q) * 32 + lane;  // row of the tile
+                const int row = row0 + rr[q];
+                // rows past R are zero-filled by the TMA: an offset of -inf makes their entries 0
+                neg_lse2[q] = row < p.R ? -p.lse[row] * kLog2e : -INFINITY;
+            }
         }
         for (int i = grp; i < nkb; i += PGROUPS) {
             const int sl = i % LSTAGES;
@@ -411,14 +470,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int64_t k = p.k_begin + (kb0 + i) * BK;
             const bool edge = (k < p.vocab_start) || (k + BK > p.vocab_end);
             uint32_t packed[ROWS_PER_LANE][16];
+            const bool fold = p.fused && (i / PGROUPS) % p.n_tiles == nt;
+            float4 vk[ROWS_PER_LANE][8];  // the logits, kept for the fold
 #pragma unroll
             for (int q = 0; q < ROWS_PER_LANE; ++q) {
                 const int r = rr[q];
                 // all eight 16-byte loads first, then the exponentials, then the packing
                 float4 v[8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c)  // 16-byte chunk of the 128-byte row
+                for (int c = 0; c < 8; ++c) {  // 16-byte chunk of the 128-byte row
                     v[c] = *reinterpret_cast<const float4 *>(lt + r * 128 + ((c ^ (r & 7)) << 4));
+                    vk[q][c] = v[c];
+                }
                 float e[32];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -432,6 +495,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int t = 0; t < 32; ++t)
                         if (k + t < p.vocab_start || k + t >= p.vocab_end) e[t] = 0.f;
                 }
+
 #pragma unroll
                 for (int t = 0; t < 16; ++t) packed[q][t] = pack_bf16x2(e[2 * t], e[2 * t + 1]);
             }
@@ -462,7 +526,45 @@ __global__ void __launch_bounds__(THREADS, 1)
                 else
                     mbar_arrive(smem_u32(&full_a[s]));
             }
+            if (fold) {
+                // the statistics kernel's fold over this row's 32 entries, in two halves
+#pragma unroll
+                for (int q = 0; q < ROWS_PER_LANE; ++q) {
+                    rowstate::RowState blk = rowstate::empty_row_state();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        float xs[16];
+                        int bs[4];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const float4 w = vk[q][4 * h + c];
+                            bs[c] = (int)((k >> 2) + 4 * h + c);
+                            xs[4 * c + 0] = w.x;
+                            xs[4 * c + 1] = w.y;
+                            xs[4 * c + 2] = w.z;
+                            xs[4 * c + 3] = w.w;
+                        }
+                        if (edge) {
+#pragma unroll
+                            for (int t = 0; t < 16; ++t)
+                                if (k + 16 * h + t < p.vocab_start || k + 16 * h + t >= p.vocab_end) xs[t] = -INFINITY;
+                        }
+                        rowstate::absorb<16>(blk, xs, bs);
+                    }
+                    rowstate::merge(my_st16[q], blk);
+                }
+                if (++my_folded % 16 == 0) {
+#pragma unroll
+                    for (int q = 0; q < ROWS_PER_LANE; ++q) {
+                        rowstate::merge(my_st[q], my_st16[q]);
+                        my_st16[q] = rowstate::empty_row_state();
+                    }
+                }
+            }
         }
+        if (p.fused)
+#pragma unroll
+            for (int q = 0; q < ROWS_PER_LANE; ++q) rowstate::merge(my_st[q], my_st16[q]);
     }
 
     // threads without a role in the main loop (warp 0, warp 11 and lanes 1-31 of the
@@ -509,6 +611,28 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (p.fused) {
+        // single pass: merge the producer groups' row states in group order (the A ring is
+        // idle: every MMA has completed or been drained), write the summary of this tile's
+        // share of the split's blocks per row, and (column tile 0) the reference
+        rowstate::RowState *scratch = reinterpret_cast<rowstate::RowState *>(a_ring);
+        if (my_grp > 0)
+#pragma unroll
+            for (int q = 0; q < ROWS_PER_LANE; ++q) scratch[(my_grp - 1) * BM + my_rows[q]] = my_st[q];
+        __syncthreads();
+        if (my_grp == 0 && !*abort_flag) {
+#pragma unroll
+            for (int q = 0; q < ROWS_PER_LANE; ++q) {
+                const int row = row0 + my_rows[q];
+                if (row >= p.R) continue;
+                rowstate::RowState st = my_st[q];
+                for (int g = 1; g < PGROUPS; ++g) rowstate::merge(st, scratch[(g - 1) * BM + my_rows[q]]);
+                const int a = st.m == -INFINITY ? 0x7fffffff : st.a;
+                p.state[((int64_t)j * p.n_tiles + nt) * p.R + row] = make_float4(st.m, __int_as_float(a), st.rest, st.t);
+                if (nt == 0) p.ref[(int64_t)j * p.R + row] = my_ref[q];
+            }
+        }
+    }
     // neither CTA leaves while the other may still multicast into it or commit to it
     cluster_sync_all();
     if (warp == 0) {
@@ -522,8 +646,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // E[i, c] = gamma * sum over the splits of column c's tile, in split order.
+// Single pass: each split's partial is scaled by f[split][row] = exp(c - lse) first.
 __global__ void splitk_reduce_kernel(const float4 *__restrict__ ws, const Params p, int d, float gamma,
-                                     float *__restrict__ out, int64_t ldo, int vec_out) {
+                                     float *__restrict__ out, int64_t ldo, int vec_out,
+                                     const float *__restrict__ scale) {
+    // the kernel queued next (the single pass's acceptance) reads nothing this one writes
+    grid_launch_dependents();
     const int64_t groups = ((int64_t)d + 3) / 4;  // column groups of 4
     const int64_t total = (int64_t)p.R * groups;
     const int64_t tile_elems = (int64_t)(BN / 4) * BM;  // float4 per partial tile
@@ -540,25 +668,34 @@ __global__ void splitk_reduce_kernel(const float4 *__restrict__ ws, const Params
         const float4 *src = ws + ((int64_t)mt * p.n_tiles + nt) * tile_elems + (int64_t)cg * BM + r;
         // loads issued four at a time, added strictly in split order
         float4 acc = src[0];
+        if (scale) {
+            const float f = scale[i];
+            acc = make_float4(f * acc.x, f * acc.y, f * acc.z, f * acc.w);
+        }
         int s = 1;
         for (; s + 4 <= S; s += 4) {
             float4 v[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) v[q] = src[(s + q) * split_stride];
+            float f[4] = {1.0f, 1.0f, 1.0f, 1.0f};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                acc.x += v[q].x;
-                acc.y += v[q].y;
-                acc.z += v[q].z;
-                acc.w += v[q].w;
+                v[q] = src[(s + q) * split_stride];
+                if (scale) f[q] = scale[(int64_t)(s + q) * p.R + i];
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                acc.x = fmaf(f[q], v[q].x, acc.x);
+                acc.y = fmaf(f[q], v[q].y, acc.y);
+                acc.z = fmaf(f[q], v[q].z, acc.z);
+                acc.w = fmaf(f[q], v[q].w, acc.w);
             }
         }
         for (; s < S; ++s) {
             const float4 v = src[s * split_stride];
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+            const float f = scale ? scale[(int64_t)s * p.R + i] : 1.0f;
+            acc.x = fmaf(f, v.x, acc.x);
+            acc.y = fmaf(f, v.y, acc.y);
+            acc.z = fmaf(f, v.z, acc.z);
+            acc.w = fmaf(f, v.w, acc.w);
         }
         float *o = out + (int64_t)i * ldo + c;
         if (vec_out && c + 4 <= d) {
@@ -567,6 +704,92 @@ __global__ void splitk_reduce_kernel(const float4 *__restrict__ ws, const Params
             const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
             for (int e = 0; e < 4 && c + e < d; ++e) o[e] = gamma * a4[e];
         }
+    }
+}
+
+// Single pass, after the product: per row, the split summaries merged in split order give
+// the statistics (written to the step's outputs), and each split's reference c becomes its
+// scale exp(c - lse); the (split, row) pairs whose maximum lies more than kRefSpan from the
+// reference are listed for the redo pass.
+__global__ void __launch_bounds__(256)
+    single_pass_stats_kernel(const Params p, float *__restrict__ out_m, float *__restrict__ out_lse,
+                             float *__restrict__ out_H, float *__restrict__ out_kappa,
+                             int32_t *__restrict__ out_argmax) {
+    const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (row >= p.R) return;
+    rowstate::RowState st = rowstate::empty_row_state();
+    for (int s = 0; s < p.splits; ++s) {
+        rowstate::RowState sp = rowstate::empty_row_state();
+        for (int t = 0; t < p.n_tiles; ++t) {
+            const float4 v = p.state[((int64_t)s * p.n_tiles + t) * p.R + row];
+            rowstate::merge(sp, rowstate::RowState{v.x, __float_as_int(v.y), v.z, v.w});
+        }
+        // the split's maximum against its reference: list the pair for the redo pass
+        const float gap = sp.m - p.ref[(int64_t)s * p.R + row];
+        if (sp.m > -INFINITY && !(gap <= kRefSpan && gap >= -kRefSpan)) {
+            const int slot = atomicAdd(&p.counts[0], 1);
+            p.redo[slot] = make_int2(s, (int)row);
+        }
+        rowstate::merge(st, sp);
+    }
+    float lse, H, kappa;
+    int a = st.a;
+    if (st.m == -INFINITY) {
+        lse = H = kappa = __int_as_float(0x7fc00000);
+        a = 0;
+    } else {
+        const float lnZ = log1pf(st.rest);
+        lse = st.m + lnZ;
+        H = lnZ - st.t / (1.0f + st.rest);
+        kappa = lnZ;
+    }
+    for (int s = 0; s < p.splits; ++s) {
+        float *r = p.ref + (int64_t)s * p.R + row;
+        // c <= m <= lse: at most 1; a row without a distribution gets NaN, as in the two-pass step
+        *r = st.m == -INFINITY ? __int_as_float(0x7fc00000) : ex2_approx((*r - lse) * kLog2e);
+    }
+    if (out_m) out_m[row] = st.m;
+    if (out_lse) out_lse[row] = lse;
+    if (out_H) out_H[row] = H;
+    if (out_kappa) out_kappa[row] = kappa;
+    if (out_argmax) out_argmax[row] = a;
+}
+
+// Single pass, the rare (split, row) pairs whose reference was too far from the maximum:
+// their partial, sum over the split of exp(l - lse) W[v, :], is recomputed on the CUDA
+// cores (fp32, vocabulary in order) for every column tile, and the scale set to 1.  One CTA
+// per listed pair, in turn; nothing to do when the list is empty.
+__global__ void __launch_bounds__(256)
+    single_pass_redo_kernel(const Params p, const uint16_t *__restrict__ W, int64_t ldw, int d,
+                            const float *__restrict__ lse) {
+    const int n = p.counts[0];
+    for (int e = blockIdx.x; e < n; e += gridDim.x) {
+        const int2 sr = p.redo[e];
+        const int j = sr.x, row = sr.y;
+        const int64_t kb0 = (int64_t)j * p.nkb / p.splits, kb1 = (int64_t)(j + 1) * p.nkb / p.splits;
+        int64_t v0 = p.k_begin + kb0 * BK, v1 = p.k_begin + kb1 * BK;
+        if (v0 < p.vocab_start) v0 = p.vocab_start;
+        if (v1 > p.vocab_end) v1 = p.vocab_end;
+        const float l2 = lse[row] * kLog2e;
+        const float *lrow = p.logits + (int64_t)row * p.ldl;
+        const int mt = row / BM, r = row % BM;
+        const int64_t tile_elems = (int64_t)(BN / 4) * BM;
+        float4 *ws = reinterpret_cast<float4 *>(p.ws);
+        for (int c4 = threadIdx.x; c4 * 4 < d; c4 += blockDim.x) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int64_t v = v0; v < v1; ++v) {
+                const float pv = ex2_approx(fmaf(lrow[v], kLog2e, -l2));
+                const uint16_t *wr = W + (v - p.vocab_start) * ldw + 4 * c4;
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    if (4 * c4 + t < d) acc[t] = fmaf(pv, __uint_as_float((uint32_t)wr[t] << 16), acc[t]);
+            }
+            const int c = 4 * c4;
+            const int nt = c / BN, cg = (c % BN) / 4;
+            ws[((int64_t)j * p.m_tiles * p.n_tiles + (int64_t)mt * p.n_tiles + nt) * tile_elems + (int64_t)cg * BM + r] =
+                make_float4(acc[0], acc[1], acc[2], acc[3]);
+        }
+        if (threadIdx.x == 0) p.ref[(int64_t)j * p.R + row] = 1.0f;
     }
 }
 
@@ -601,6 +824,14 @@ int tail_splits_of(int splits, int tail) { return tail ? splits : 0; }
 
 size_t soft_embed_workspace_bytes(const SoftEmbedPlan &plan, int splits) {
     return (size_t)splits * (size_t)plan.m_tiles * (size_t)plan.n_tiles * BM * BN * sizeof(float);
+}
+
+// The single pass's extra workspace, after the partial tiles: references / scales
+// [splits][R] fp32, summaries [splits][R] x 16 B, two counters, the redo list [splits][R] x 8 B.
+static size_t align16(size_t b) { return (b + 15) & ~size_t(15); }
+size_t single_pass_extra_bytes(const SoftEmbedPlan &plan, int64_t R) {
+    const size_t n = (size_t)plan.splits * (size_t)R;
+    return align16(n * 4) + n * (size_t)plan.n_tiles * 16 + 16 + align16(n * 8);
 }
 
 bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t d, int num_sms,
@@ -642,6 +873,7 @@ bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t 
     }
     pl.splits = best;
     pl.workspace_bytes = soft_embed_workspace_bytes(pl, pl.splits);
+    pl.single_pass_bytes = pl.workspace_bytes + single_pass_extra_bytes(pl, R);
     *plan = pl;
     return true;
 }
@@ -649,7 +881,8 @@ bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t 
 cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t vocab_start,
                               int64_t vocab_end, const uint16_t *W, int64_t ldw, int64_t d, float gamma, float *out,
                               int64_t ldo, void *workspace, const SoftEmbedPlan &plan, cudaStream_t stream,
-                              const char **msg, StreamHook between, void *ctx, bool overlap_previous) {
+                              const char **msg, StreamHook between, void *ctx, bool overlap_previous,
+                              const SinglePassOut *single) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
     if (!encode) {
         *msg = "cuTensorMapEncodeTiled is not available from the driver";
@@ -719,6 +952,25 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     p.splits = plan.splits;
     p.tail_splits = tail_splits_of(plan.splits, tail);
     p.w3d = w3d;
+    p.fused = single ? 1 : 0;
+    p.logits = logits;
+    p.ldl = ldl;
+    p.ref = nullptr;
+    p.state = nullptr;
+    p.counts = nullptr;
+    p.redo = nullptr;
+    if (single) {
+        const size_t n = (size_t)plan.splits * (size_t)R;
+        uint8_t *x = static_cast<uint8_t *>(workspace) + soft_embed_workspace_bytes(plan, plan.splits);
+        p.ref = reinterpret_cast<float *>(x);
+        x += align16(n * 4);
+        p.state = reinterpret_cast<float4 *>(x);
+        x += n * (size_t)plan.n_tiles * 16;
+        p.counts = reinterpret_cast<int *>(x);
+        x += 16;
+        p.redo = reinterpret_cast<int2 *>(x);
+        overlap_previous = false;  // nothing before it to wait for
+    }
     const int64_t pairs = (int64_t)(plan.m_tiles / kCtasPerUnit) * (n_full * (int64_t)p.splits + p.tail_splits);
 
     cudaLaunchConfig_t cfg = {};
@@ -740,7 +992,21 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
         *msg = "soft-embed kernel launch failed";
         return e;
     }
-    if (between) {
+    if (single) {
+        single_pass_stats_kernel<<<(unsigned)((R + 255) / 256), 256, 0, stream>>>(p, single->m, single->lse,
+                                                                                  single->H, single->kappa,
+                                                                                  single->argmax);
+        single_pass_redo_kernel<<<64, 256, 0, stream>>>(p, W, ldw, (int)d, single->lse);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            *msg = "single pass: statistics or redo launch failed";
+            return e;
+        }
+    }
+    // two passes: the acceptance overlaps the product, then the reduce; single pass: the
+    // acceptance needs the statistics that follow the product, so the reduce goes first
+    // and lets the acceptance start at once
+    if (between && !single) {
         e = between(ctx, stream);
         if (e != cudaSuccess) {
             *msg = "launch between the product and the reduce failed";
@@ -754,9 +1020,16 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const float4 *>(workspace), p, (int)d,
-                                                               gamma, out, ldo, vec_out);
+                                                               gamma, out, ldo, vec_out, single ? p.ref : nullptr);
     e = cudaGetLastError();
-    if (e != cudaSuccess) *msg = "split-K reduce launch failed";
+    if (e != cudaSuccess) {
+        *msg = "split-K reduce launch failed";
+        return e;
+    }
+    if (between && single) {
+        e = between(ctx, stream);
+        if (e != cudaSuccess) *msg = "launch after the reduce failed";
+    }
     return e;
 }
 

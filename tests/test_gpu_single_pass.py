@@ -1,0 +1,98 @@
+"""The single-pass step (the product folds the row statistics, the logits are read once)
+against the oracle, against the two-pass step, and on the rows it must redo (a split
+whose maximum lies far from its reference)."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from denoising_sampler_step_gb300 import inputs
+from oracle import entropy_accept, row_stats, soft_embed
+from tests.test_gpu_parity import E_TOL, check_stats, dev, rel_l2, sampled_rows, w_dev
+from tests.workloads import guarded
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from denoising_sampler_step_gb300 import build
+    build.build()
+    from denoising_sampler_step_gb300 import binding
+    return binding
+
+
+def two_pass(fn):
+    os.environ["DGSAMP_TWO_PASS"] = "1"
+    try:
+        return fn()
+    finally:
+        del os.environ["DGSAMP_TWO_PASS"]
+
+
+def run_step(B, x, wl, Wd, budgets, V=None):
+    out = B.dg_sampler_step(dev(x), wl.n_req, wl.L_c, Wd, wl.gamma, dev(budgets), V=V)
+    torch.cuda.synchronize()
+    B.dg_get_device_status()
+    return out
+
+
+@pytest.mark.parametrize("V,d,L_c,n_req", [(4096, 256, 16, 1), (40001, 256, 64, 2), (70000, 640, 100, 3)])
+def test_single_pass_matches_oracle_and_two_pass(B, V, d, L_c, n_req):
+    wl = inputs.WORKLOADS["tiny"].with_(V=V, d=d, L_c=L_c, n_req=n_req, seed=V + d, budget=("uniform", 1.0, 12.0))
+    ld = (V + 3) // 4 * 4
+    x, budgets, ost, _ = guarded(wl, ld=ld)
+    Wb = inputs.embedding_bf16(wl)
+    Wd = w_dev(Wb)
+    one = run_step(B, x, wl, Wd, budgets, V=V)
+    check_stats(one, ost)
+    acc = entropy_accept(ost["H"], ost["kappa"], wl.n_req, wl.L_c, budgets)
+    for k in ("order", "mask", "n_accepted"):
+        assert np.array_equal(one[k].cpu().numpy(), acc[k]), k
+    E = one["E"].cpu().numpy()
+    assert rel_l2(E, soft_embed(x[:, :V], ost["lse"], 0, V, Wb, wl.gamma)).max() <= E_TOL
+    two = two_pass(lambda: run_step(B, x, wl, Wd, budgets, V=V))
+    assert torch.equal(one["argmax"], two["argmax"])
+    for k in ("order", "mask", "n_accepted"):
+        assert torch.equal(one[k], two[k]), k
+    # the two passes round different bf16 probabilities (exp(l - c) against exp(l - lse)),
+    # so they agree to the tolerance, not to the rounding
+    assert rel_l2(E, two["E"].cpu().numpy().astype(np.float64)).max() <= E_TOL
+
+
+def test_single_pass_redoes_rows_far_from_their_reference(B):
+    """Rows whose maximum lies more than 64 nats above a split's first entries (one-hot
+    rows), rows whose splits start masked, rows with nothing finite: the redo pass must give
+    the oracle's statistics and embedding."""
+    wl = inputs.WORKLOADS["tiny"].with_(V=40000, d=256, L_c=16, n_req=1, seed=3, budget=5.0)
+    x = inputs.logits(wl)
+    x[0, 12345] = 1.0e4                     # one-hot: overflow against any reference
+    x[1, 30000] = 90.0                      # 90 nats above the rest
+    x[2, :8192] = -np.inf                   # the first splits start masked
+    x[3, :] = -np.inf                       # no distribution
+    x[4, :] -= 300.0                        # far below the default reference
+    Wb = inputs.embedding_bf16(wl)
+    out = run_step(B, x, wl, w_dev(Wb), np.array([5.0], np.float32))
+    ost = row_stats(x)
+    check_stats(out, ost)
+    assert out["argmax"][0].item() == 12345 and out["argmax"][1].item() == 30000
+    E = out["E"].cpu().numpy()
+    rows = np.array([0, 1, 2, 4, 5, 15])
+    assert rel_l2(E[rows], soft_embed(x, ost["lse"], 0, wl.V, Wb, wl.gamma, rows=rows)).max() <= E_TOL
+    assert np.all(np.isnan(E[3]))           # a row without a distribution, as in the two-pass step
+
+
+@pytest.mark.slow
+def test_single_pass_canvas256_full_size(B):
+    wl = inputs.WORKLOADS["canvas256"]
+    x, budgets, ost, _ = guarded(wl)
+    Wb = inputs.embedding_bf16(wl)
+    out = run_step(B, x, wl, w_dev(Wb), budgets)
+    check_stats(out, ost)
+    acc = entropy_accept(ost["H"], ost["kappa"], wl.n_req, wl.L_c, budgets)
+    for k in ("order", "mask", "n_accepted"):
+        assert np.array_equal(out[k].cpu().numpy(), acc[k]), k
+    rows = sampled_rows(wl.R, 14, 5)
+    ref = soft_embed(x, ost["lse"], 0, wl.V, Wb, wl.gamma, rows=rows)
+    assert rel_l2(out["E"].cpu().numpy()[rows], ref).max() <= E_TOL
