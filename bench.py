@@ -184,6 +184,9 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["soft_embed", "step"], default=None,
+                    help="profiling target: run only this call (warm-up, then --steps calls) and print "
+                         "its mean duration; no JSON line")
     ap.add_argument("--sustained", type=float, default=0.0,
                     help="also run the step and the soft-embed call back to back for this many seconds "
                          "each, sampling clocks and power every 20 ms")
@@ -221,6 +224,30 @@ def main() -> None:
     bd = torch.from_numpy(budgets).to(dev)
     step = SamplerStep(Wd, wl.n_req, wl.L_c, wl.V, wl.gamma, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    if args.only:
+        # a short, fixed launch sequence for a profiler: warm-up calls, then --steps calls
+        if args.only == "soft_embed":
+            lse = B.dg_row_stats(xd)["lse"]
+            call = lambda: B.dg_soft_embed(xd, lse, 0, wl.V, Wd, wl.gamma, out=step.out["E"], ws=step.ws)
+        else:
+            call = lambda: step(xd, bd)
+        for _ in range(args.warmup):
+            call()
+        torch.cuda.synchronize(dev)
+        o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        o0.record(stream)
+        for _ in range(args.steps):
+            call()
+        o1.record(stream)
+        torch.cuda.synchronize(dev)
+        B.dg_get_device_status()
+        if rank == 0:
+            print(f"{args.only}: {o0.elapsed_time(o1) / args.steps * 1e3:.1f} us per call "
+                  f"({args.warmup} warm-up + {args.steps} calls)", flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     def barrier():
         if world > 1:

@@ -707,24 +707,25 @@ __global__ void splitk_reduce_kernel(const float4 *__restrict__ ws, const Params
     }
 }
 
-// Single pass, after the product: per row, the split summaries merged in split order give
-// the statistics (written to the step's outputs), and each split's reference c becomes its
-// scale exp(c - lse); the (split, row) pairs whose maximum lies more than kRefSpan from the
-// reference are listed for the redo pass.
+// Single pass, after the product: per row (one warp), lane l merges the tile summaries of
+// splits l, l + 32, ... (tile order), checks each split's maximum against its reference
+// (pairs more than kRefSpan apart are listed for the redo pass), the lanes' states merge in a
+// fixed shuffle tree, lane 0 writes the statistics, and each split's reference becomes its
+// scale exp(c - lse).
 __global__ void __launch_bounds__(256)
     single_pass_stats_kernel(const Params p, float *__restrict__ out_m, float *__restrict__ out_lse,
                              float *__restrict__ out_H, float *__restrict__ out_kappa,
                              int32_t *__restrict__ out_argmax) {
-    const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (row >= p.R) return;
+    const int lane = threadIdx.x & 31;
+    const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (row >= p.R) return;  // warp-uniform
     rowstate::RowState st = rowstate::empty_row_state();
-    for (int s = 0; s < p.splits; ++s) {
+    for (int s = lane; s < p.splits; s += 32) {
         rowstate::RowState sp = rowstate::empty_row_state();
         for (int t = 0; t < p.n_tiles; ++t) {
             const float4 v = p.state[((int64_t)s * p.n_tiles + t) * p.R + row];
             rowstate::merge(sp, rowstate::RowState{v.x, __float_as_int(v.y), v.z, v.w});
         }
-        // the split's maximum against its reference: list the pair for the redo pass
         const float gap = sp.m - p.ref[(int64_t)s * p.R + row];
         if (sp.m > -INFINITY && !(gap <= kRefSpan && gap >= -kRefSpan)) {
             const int slot = atomicAdd(&p.counts[0], 1);
@@ -732,27 +733,31 @@ __global__ void __launch_bounds__(256)
         }
         rowstate::merge(st, sp);
     }
-    float lse, H, kappa;
-    int a = st.a;
-    if (st.m == -INFINITY) {
-        lse = H = kappa = __int_as_float(0x7fc00000);
-        a = 0;
-    } else {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) rowstate::merge(st, rowstate::shfl_down(st, off));
+    float lse = __int_as_float(0x7fc00000), H = lse, kappa = lse;
+    int a = 0;
+    if (lane == 0 && st.m != -INFINITY) {
         const float lnZ = log1pf(st.rest);
         lse = st.m + lnZ;
         H = lnZ - st.t / (1.0f + st.rest);
         kappa = lnZ;
+        a = st.a;
     }
-    for (int s = 0; s < p.splits; ++s) {
+    lse = __shfl_sync(0xffffffffu, lse, 0);
+    const float m = __shfl_sync(0xffffffffu, st.m, 0);
+    for (int s = lane; s < p.splits; s += 32) {
         float *r = p.ref + (int64_t)s * p.R + row;
         // c <= m <= lse: at most 1; a row without a distribution gets NaN, as in the two-pass step
-        *r = st.m == -INFINITY ? __int_as_float(0x7fc00000) : ex2_approx((*r - lse) * kLog2e);
+        *r = m == -INFINITY ? __int_as_float(0x7fc00000) : ex2_approx((*r - lse) * kLog2e);
     }
-    if (out_m) out_m[row] = st.m;
-    if (out_lse) out_lse[row] = lse;
-    if (out_H) out_H[row] = H;
-    if (out_kappa) out_kappa[row] = kappa;
-    if (out_argmax) out_argmax[row] = a;
+    if (lane == 0) {
+        if (out_m) out_m[row] = st.m;
+        if (out_lse) out_lse[row] = lse;
+        if (out_H) out_H[row] = H;
+        if (out_kappa) out_kappa[row] = kappa;
+        if (out_argmax) out_argmax[row] = a;
+    }
 }
 
 // Single pass, the rare (split, row) pairs whose reference was too far from the maximum:
@@ -993,7 +998,7 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
         return e;
     }
     if (single) {
-        single_pass_stats_kernel<<<(unsigned)((R + 255) / 256), 256, 0, stream>>>(p, single->m, single->lse,
+        single_pass_stats_kernel<<<(unsigned)((R * 32 + 255) / 256), 256, 0, stream>>>(p, single->m, single->lse,
                                                                                   single->H, single->kappa,
                                                                                   single->argmax);
         single_pass_redo_kernel<<<64, 256, 0, stream>>>(p, W, ldw, (int)d, single->lse);
