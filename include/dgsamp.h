@@ -190,6 +190,17 @@ dg_status dg_sum_partials(const float *const *partials, int32_t T, int64_t R, in
  *            n_accepted [n_req] int32; E [R, ldo] fp32
  *   workspace  >= dg_soft_embed_workspace_size(R, vocab_end - vocab_start, d) bytes
  * All output pointers are required.  The argument rules of the three calls above apply.
+ *
+ * When the slice is the whole vocabulary (vocab_start == 0, vocab_end == V) and the
+ * workspace is that size, the step reads the logits once: each vocabulary split of the
+ * product takes its probabilities against a per-row reference c (the largest of the
+ * split's first four entries), exp(l - c), while it folds the row statistics; the split
+ * summaries then give the statistics (as dg_row_stats, up to the order of the fp32
+ * additions) and each split's partial is scaled by exp(c - lse) in the reduce.  A
+ * (split, row) whose maximum lies more than 64 nats from c is recomputed against lse on
+ * the CUDA cores (exact, slow, rare: one-hot rows).  E then equals the two-pass result up
+ * to the bf16 rounding of different probabilities.  The environment variable
+ * DGSAMP_TWO_PASS=1 forces the statistics pass before the product.
  */
 dg_status dg_sampler_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, int64_t ldl,
                           const uint16_t *W, int64_t vocab_start, int64_t vocab_end,
