@@ -1,7 +1,8 @@
 """Pins of the sampling oracle against facts that do not come from the oracle itself:
 the published known-answer vectors of Philox4x32-10, the categorical distribution of
-the Gumbel-max draw (chi-square), its zero-temperature limit (the argmax), masked
-entries, and the closed form of the log-probability."""
+the two-level Gumbel-max draw (chi-square, within one group and across groups), its
+zero-temperature limit (the argmax), masked entries and groups, and the closed form of
+the log-probability."""
 import math
 
 import numpy as np
@@ -107,3 +108,34 @@ def test_candidate_kappa_sums_to_one_over_every_candidate():
     assert np.allclose(candidate_kappa(np.repeat(u, V, axis=0), np.arange(V)), math.log(V), rtol=1e-14)
     empty = np.full((1, 4), -np.inf, np.float32)
     assert np.isnan(candidate_kappa(empty, [0])[0])
+
+
+@pytest.mark.parametrize("temperature", [1.0, 0.6])
+def test_draws_across_groups_follow_the_tempered_softmax(temperature):
+    # 60,000 draws of one 40-entry row: three groups (16, 16, 8), both levels at work;
+    # chi-square with 39 degrees of freedom, bound far in the tail (false alarm << 1e-6)
+    rng = np.random.default_rng(21)
+    l = (rng.standard_normal(40) * 1.3).astype(np.float32)
+    l[33] = 2.5                                   # the short last group holds the most mass
+    n = 60000
+    out = row_sample(np.tile(l, (n, 1)), temperature, seed=12, offset=1)
+    counts = np.bincount(out["candidate"], minlength=40)
+    z = l.astype(np.float64) / temperature
+    p = np.exp(z - z.max())
+    p /= p.sum()
+    chi2 = ((counts - n * p) ** 2 / (n * p)).sum()
+    assert chi2 < 110.0, (chi2, counts, n * p)
+    # the group choice alone follows the group masses
+    gc = np.bincount(out["group"], minlength=3)
+    pg = np.array([p[:16].sum(), p[16:32].sum(), p[32:].sum()])
+    assert ((gc - n * pg) ** 2 / (n * pg)).sum() < 40.0
+
+
+def test_masked_groups_are_never_chosen():
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((3000, 64)).astype(np.float32)
+    x[:, 16:32] = -np.inf                          # group 1 entirely masked
+    x[:, 50] = -np.inf
+    out = row_sample(x, 1.0, seed=4, offset=0)
+    assert np.all(out["group"] != 1) and np.all(out["candidate"] != 50)
+    assert np.all(out["candidate"] // 16 == out["group"])
