@@ -1,29 +1,28 @@
-// Stochastic candidate per canvas position: a categorical draw from softmax(l / tau)
-// taken as the Gumbel-max, argmax_v (l_v / tau - ln(-ln u_v)), with its tempered
-// log-probability; optionally fused with the row statistics (one read of the logits
-// for both).
+// Stochastic candidate per canvas position: a categorical draw from softmax(l / tau) with
+// its tempered log-probability; optionally fused with the row statistics (one read of
+// the logits for both).
 //
 // What it computes: agentlenshq.com, "サンプリングループとエントロピー境界デノイジング"
-// (candidate tokens are sampled at every position).  The uniforms are Philox4x32-10
-// (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011):
-// entry v of row i uses word v % 4 of the block with counter (v / 4, i, offset low,
-// offset high) and key (seed low, seed high); u = ((x >> 9) + 1/2) 2^-23.
+// (candidate tokens are sampled at every position).  The draw is a two-level Gumbel-max,
+// an exact categorical sampler: the vocabulary is cut into groups of 16 consecutive
+// entries; the group g* = argmax_g (L_g + G_g), L_g the group's log-mass logsumexp(l/tau)
+// and G_g = -ln(-ln u_g); then the candidate = argmax over g*'s entries of l/tau + G_v.
+// The uniforms are Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers:
+// as easy as 1, 2, 3", SC 2011) with key (seed low, seed high): entry v uses word v % 4 of
+// the block with counter (v / 4, row, offset low, offset high), group g word g % 4 of the
+// block with counter (2^31 + g / 4, row, offset low, offset high); u = ((x >> 9) + 1/2) 2^-23.
 //
-// Design (HBM-bound like the row statistics: one cluster of CTAs per row, 128-bit loads,
-// fixed-order warp / CTA / cluster merges).  The draw is kept as an exponential race,
-// the same argmax written without the outer logarithm: with E_v = -ln u_v and
-// e_v = exp(z_v - m) (z = l / tau, m the running max), the winner minimises E_v / e_v,
-// and e_v is the term the tempered log-sum-exp adds anyway.  So each entry costs one
-// exp, one logarithm and a multiply-compare; a division only when a thread's best
-// changes.  Each thread keeps
-//   m, s   : running max of z and sum of exp(z - m)  (for lse_tau);
-//   R      : its best ratio E / e, relative to its m (R scales by exp(m' - m) when m grows);
-//   idx, l : the best entry's index (lowest on ties) and its logit.
-// Threads merge in the log domain, score = m - ln R = z + g of the best entry.
-// Since u <= 1 - 2^-24, g <= -ln(2^-24) < 16.7: a group of four entries whose z all lie
-// more than that below a score the warp already holds cannot win, and its Philox block
-// and logarithms are skipped (the warp shares its best score after every batch of loads).
-// Near-uniform rows, where every entry can still win, pay for every draw.
+// Design (HBM-bound like the row statistics: one cluster of CTAs per row, fixed-order warp /
+// CTA / cluster merges).  A thread takes one group (four contiguous float4) per batch and
+// keeps
+//   m, s       : running max of z = l / tau and sum of exp(z - m)  (for lse_tau);
+//   best, grp  : the best group score m + ln(sum of the group's exp(z - m)) + G_g and its
+//                group (lowest on ties);
+// so a group costs its 16 exponentials (which the tempered sum needs anyway), one Philox
+// block and two logarithms.  Since u <= 1 - 2^-24, G < 16.7: a group whose largest z lies
+// more than ln 16 + 16.7 below a score the warp already holds cannot win and skips its
+// Philox block and logarithms.  After the merges, 16 lanes of the first CTA draw inside the
+// chosen group (four Philox blocks) and the lowest-index best entry is the candidate.
 #include <cooperative_groups.h>
 #include <float.h>
 
@@ -38,8 +37,10 @@ namespace dg {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kVec = 4;              // float4 loads per thread per batch
-constexpr float kGumbelMax = 16.7f;  // above every g the 23-bit uniforms can give
+constexpr int kGroup = 16;           // vocabulary entries per group (four float4)
+constexpr uint32_t kGroupCounter = 0x80000000u;  // counter word 0 of the group uniforms
+constexpr float kGumbelMax = 16.7f;  // above every G the 23-bit uniforms can give
+constexpr float kLn16 = 2.7725887222397811f;
 constexpr float kLn2 = 0.69314718055994531f;
 
 struct Philox {
@@ -76,47 +77,39 @@ __device__ __forceinline__ float neg_log_uniform(uint32_t x) {
     return t < 0.015625f ? t * fmaf(t, fmaf(t, 0.333333343f, 0.5f), 1.0f) : -kLn2 * __log2f(u);
 }
 
-struct SampleState {
-    float m, s;  // max of z and sum of exp(z - m)
-    float R;     // best E / exp(z - m) (+inf: none yet)
-    int idx;     // its index
-    float l;     // its logit
-};
-
-__device__ __forceinline__ SampleState empty_state() { return {-INFINITY, 0.0f, INFINITY, 0x7fffffff, 0.0f}; }
-
-// the best entry's perturbed score z + g, -inf if none
-__device__ __forceinline__ float score(const SampleState &a) {
-    return a.R == INFINITY ? -INFINITY : a.m - kLn2 * __log2f(a.R);
+__device__ __forceinline__ uint32_t philox_word(const Philox &w, int j) {
+    return j == 0 ? w.x0 : j == 1 ? w.x1 : j == 2 ? w.x2 : w.x3;
 }
 
-// A := A merged with B: the larger max carries the rescaled sums; the better score wins,
-// equal scores keep the lower index; the winner's ratio is restated against the new max.
+struct SampleState {
+    float m, s;  // max of z and sum of exp(z - m)
+    float best;  // best group score (-inf: none yet)
+    int grp;     // its group (INT_MAX: none)
+};
+
+__device__ __forceinline__ SampleState empty_state() { return {-INFINITY, 0.0f, -INFINITY, 0x7fffffff}; }
+
+// A := A merged with B: the larger max carries the rescaled sums; the better group score
+// wins, equal scores keep the lower group.
 __device__ __forceinline__ void merge(SampleState &A, const SampleState &B) {
-    const float sa = score(A), sb = score(B);
-    const bool b_best = sb > sa || (sb == sa && B.idx < A.idx);
-    float m = A.m, s = A.s;
     if (B.m > A.m) {
-        s = (A.m == -INFINITY ? 0.0f : A.s * ex2_approx((A.m - B.m) * kLog2e)) + B.s;
-        m = B.m;
+        A.s = (A.m == -INFINITY ? 0.0f : A.s * ex2_approx((A.m - B.m) * kLog2e)) + B.s;
+        A.m = B.m;
     } else if (B.m != -INFINITY) {
-        s += B.s * ex2_approx((B.m - A.m) * kLog2e);
+        A.s += B.s * ex2_approx((B.m - A.m) * kLog2e);
     }
-    const float wR = b_best ? B.R : A.R, wm = b_best ? B.m : A.m;
-    A.R = wR == INFINITY ? INFINITY : wR * ex2_approx((m - wm) * kLog2e);
-    A.idx = b_best ? B.idx : A.idx;
-    A.l = b_best ? B.l : A.l;
-    A.m = m;
-    A.s = s;
+    if (B.best > A.best || (B.best == A.best && B.grp < A.grp)) {
+        A.best = B.best;
+        A.grp = B.grp;
+    }
 }
 
 __device__ __forceinline__ SampleState shfl_down(const SampleState &a, int off) {
     SampleState o;
     o.m = __shfl_down_sync(0xffffffffu, a.m, off);
     o.s = __shfl_down_sync(0xffffffffu, a.s, off);
-    o.R = __shfl_down_sync(0xffffffffu, a.R, off);
-    o.idx = __shfl_down_sync(0xffffffffu, a.idx, off);
-    o.l = __shfl_down_sync(0xffffffffu, a.l, off);
+    o.best = __shfl_down_sync(0xffffffffu, a.best, off);
+    o.grp = __shfl_down_sync(0xffffffffu, a.grp, off);
     return o;
 }
 
@@ -125,47 +118,40 @@ struct SampleArgs {
     uint32_t k0, k1, o0, o1;  // key and the counter's offset words
 };
 
-// Folds the four entries 4q .. 4q+3 of row `row` (values v, -inf past V) into st.
+// Folds group g of row `row` (entries 16g .. 16g + 15: z, -inf past V) into st.
 // `bound`: a score some thread of the warp already holds.
-__device__ __forceinline__ void absorb4(SampleState &st, const float4 v, int64_t q, uint32_t row, const SampleArgs &a,
-                                        float bound) {
-    const float l[4] = {v.x, v.y, v.z, v.w};
-    float z[4];
+__device__ __forceinline__ void absorb_group(SampleState &st, const float (&z)[kGroup], int g, uint32_t row,
+                                             const SampleArgs &a, float bound) {
+    float gm = z[0];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) z[j] = l[j] * a.inv_tau;
-    const float bm = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
-    if (bm == -INFINITY) return;  // four masked entries: nothing to add, nothing to draw
-    if (bm > st.m) {
-        if (st.m == -INFINITY) {
-            st.s = 0.0f;
-        } else {
-            const float c = ex2_approx((st.m - bm) * kLog2e);
-            st.s *= c;
-            st.R = st.R == INFINITY ? INFINITY : __fdividef(st.R, c);  // c == 0: the old best cannot win
-        }
-        st.m = bm;
+    for (int j = 1; j < kGroup; ++j) gm = fmaxf(gm, z[j]);
+    if (gm == -INFINITY) return;  // a masked group: no mass, never drawn
+    if (gm > st.m) {
+        st.s = st.m == -INFINITY ? 0.0f : st.s * ex2_approx((st.m - gm) * kLog2e);
+        st.m = gm;
     }
-    float e[4];
+    const float nm = -st.m * kLog2e;
+    float gs = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        e[j] = ex2_approx((z[j] - st.m) * kLog2e);  // st.m is finite here; -inf entries give 0
-        st.s += e[j];
+    for (int j = 0; j < kGroup; ++j) gs += ex2_approx(fmaf(z[j], kLog2e, nm));  // -inf entries: 0
+    st.s += gs;
+    // no group here can beat `bound`: its score is at most gm + ln 16 + 16.7
+    if (gm + (kLn16 + kGumbelMax) < bound) return;
+    const Philox w = philox4x32_10(kGroupCounter + (uint32_t)(g >> 2), row, a.o0, a.o1, a.k0, a.k1);
+    // score = ln(sum of exp(z)) + G = m + ln(gs) - ln(-ln u)
+    const float sc = st.m + kLn2 * __log2f(gs) - kLn2 * __log2f(neg_log_uniform(philox_word(w, g & 3)));
+    if (sc > st.best) {  // groups arrive in increasing order: ties keep the lower
+        st.best = sc;
+        st.grp = g;
     }
-    // no entry here can beat `bound`
-    if (bm + kGumbelMax < bound) return;
-    const Philox w = philox4x32_10((uint32_t)q, row, a.o0, a.o1, a.k0, a.k1);
-    const uint32_t words[4] = {w.x0, w.x1, w.x2, w.x3};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float E = neg_log_uniform(words[j]);
-        // E / e < R, written without the division (e == 0 gives NaN or 0: never a win;
-        // R == inf: any e > 0 wins)
-        if (E < st.R * e[j]) {
-            st.R = __fdividef(E, e[j]);
-            st.idx = (int)(4 * q + j);
-            st.l = l[j];
-        }
-    }
+}
+
+__device__ __forceinline__ float4 ld_stream(const float4 *p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
 }
 
 // Per-row outputs of the fused kernel (statistics at temperature 1 and the draw).
@@ -184,6 +170,8 @@ __global__ void __launch_bounds__(kThreads, 3)
     __shared__ SampleState cta_state[CLUSTER];
     __shared__ RowState warp_stats[STATS ? kThreads / 32 : 1];
     __shared__ RowState cta_stats[STATS ? CLUSTER : 1];
+    __shared__ float draw_lse;
+    __shared__ int draw_grp;
 
     // the kernel queued next (the soft-embed product of a step) may start its CTAs now: it
     // waits for this grid to complete before it reads anything this grid writes
@@ -192,70 +180,69 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int64_t row = blockIdx.x / CLUSTER;
     const float *rowp = logits + row * ldl;
     const float4 *rowv = reinterpret_cast<const float4 *>(rowp);
-    const int64_t nv = V >> 2;
-    const int64_t per = (nv + CLUSTER - 1) / CLUSTER;
-    const int64_t v_begin = min(nv, (int64_t)rank * per);
-    const int64_t v_end = min(nv, v_begin + per);
+    // float4s holding the row (the last one partial when V % 4 != 0: ldl % 4 == 0 keeps it
+    // inside the row), groups, and this CTA's contiguous share of the groups
+    const int64_t nv = (V + 3) >> 2;
+    const int64_t G = (V + kGroup - 1) / kGroup;
+    const int64_t per = (G + CLUSTER - 1) / CLUSTER;
+    const int64_t g_begin = min(G, (int64_t)rank * per);
+    const int64_t g_end = min(G, g_begin + per);
 
     if constexpr (CLUSTER > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
     SampleState st = empty_state();
     RowState rs = rowstate::empty_row_state();
-    constexpr int64_t kStep = (int64_t)kThreads * kVec;
-    float4 cur[kVec], nxt[kVec];
-    auto load_batch = [&](int64_t b, float4(&v)[kVec]) {
+    float4 cur[4], nxt[4];
+    auto load_group = [&](int64_t g, float4(&v)[4]) {
 #pragma unroll
-        for (int k = 0; k < kVec; ++k) {
-            const int64_t vi = b + (int64_t)k * kThreads;
-            v[k] = (vi < v_end) ? rowstate::ld_stream_v4(rowv + vi)
-                                : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        for (int k = 0; k < 4; ++k) {
+            const int64_t q = 4 * g + k;
+            v[k] = (g < g_end && q < nv) ? ld_stream(rowv + q)
+                                         : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         }
     };
-    int64_t b = v_begin + threadIdx.x;
-    if (b < v_end) load_batch(b, cur);
+    int64_t g = g_begin + threadIdx.x;
+    load_group(g, cur);
     float bound = -INFINITY;  // the best score in the warp after the previous batch
-    // every lane of a warp runs the same number of batches (the bounds are warp-uniform
-    // up to the last batch, where lanes past v_end only skip their entries)
-    for (int64_t b0 = v_begin; b0 < v_end; b0 += kStep, b += kStep) {
-        const bool more = b + kStep < v_end;
-        if (more) load_batch(b + kStep, nxt);
-        if constexpr (STATS) {
-            // the statistics kernel's fold, on the same batches (lanes past v_end hold -inf)
-            float x[4 * kVec];
-            int base[kVec];
+    // every lane of a warp runs the same number of batches (lanes past g_end skip their group)
+    for (int64_t g0 = g_begin; g0 < g_end; g0 += kThreads, g += kThreads) {
+        const bool more = g0 + kThreads < g_end;
+        if (more) load_group(g + kThreads, nxt);
+        if (g < g_end) {
+            float x[kGroup];
 #pragma unroll
-            for (int k = 0; k < kVec; ++k) {
-                base[k] = (int)(b + (int64_t)k * kThreads);
+            for (int k = 0; k < 4; ++k) {
                 x[4 * k + 0] = cur[k].x;
                 x[4 * k + 1] = cur[k].y;
                 x[4 * k + 2] = cur[k].z;
                 x[4 * k + 3] = cur[k].w;
             }
-            if (b < v_end) rowstate::absorb<4 * kVec>(rs, x, base);
-        }
+            if (kGroup * (g + 1) > V) {  // the row's last group: entries past V are not part of it
 #pragma unroll
-        for (int k = 0; k < kVec; ++k) {
-            const int64_t vi = b + (int64_t)k * kThreads;
-            if (vi < v_end) absorb4(st, cur[k], vi, (uint32_t)row, a, bound);
+                for (int j = 0; j < kGroup; ++j)
+                    if (kGroup * g + j >= V) x[j] = -INFINITY;
+            }
+            if constexpr (STATS) {
+                float xs[kGroup];
+                int bs[4];
+#pragma unroll
+                for (int j = 0; j < kGroup; ++j) xs[j] = x[j];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) bs[k] = (int)(4 * g + k);
+                rowstate::absorb<kGroup>(rs, xs, bs);
+            }
+            float z[kGroup];
+#pragma unroll
+            for (int j = 0; j < kGroup; ++j) z[j] = x[j] * a.inv_tau;
+            absorb_group(st, z, (int)g, (uint32_t)row, a, bound);
         }
-        float wb = score(st);
+        float wb = st.best;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) wb = fmaxf(wb, __shfl_xor_sync(0xffffffffu, wb, off));
         bound = wb;
         if (more) {
 #pragma unroll
-            for (int k = 0; k < kVec; ++k) cur[k] = nxt[k];
-        }
-    }
-    // ragged tail (V % 4 entries), taken by the last piece's first thread
-    if (rank == CLUSTER - 1 && threadIdx.x == 0 && (V & 3)) {
-        float t[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) t[c] = (4 * nv + c < V) ? rowp[4 * nv + c] : -INFINITY;
-        absorb4(st, make_float4(t[0], t[1], t[2], t[3]), nv, (uint32_t)row, a, -INFINITY);
-        if constexpr (STATS) {
-            int base[1] = {(int)nv};
-            rowstate::absorb<4>(rs, t, base);
+            for (int k = 0; k < 4; ++k) cur[k] = nxt[k];
         }
     }
 
@@ -300,11 +287,41 @@ __global__ void __launch_bounds__(kThreads, 3)
             }
         }
     }
-    if (threadIdx.x == 0) {
+    if (warp != 0) return;
+    // the second level: lanes 0-15 draw inside the chosen group
+    const bool none = st.m == -INFINITY || st.grp == 0x7fffffff;
+    if (lane == 0) {
+        draw_lse = none ? __int_as_float(0x7fc00000) : st.m + kLn2 * __log2f(st.s);
+        draw_grp = none ? -1 : st.grp;
+    }
+    __syncwarp();
+    const int gs = draw_grp;
+    const int64_t v = (int64_t)kGroup * gs + lane;
+    const bool valid = gs >= 0 && lane < kGroup && v < V;
+    const float l = valid ? rowp[v] : -INFINITY;
+    float sc = -INFINITY;
+    if (valid && l != -INFINITY) {
+        const Philox w = philox4x32_10((uint32_t)(v >> 2), (uint32_t)row, a.o0, a.o1, a.k0, a.k1);
+        sc = l * a.inv_tau - kLn2 * __log2f(neg_log_uniform(philox_word(w, (int)(v & 3))));
+    }
+    int bi = valid ? (int)v : 0x7fffffff;
+    float bl = l;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float os = __shfl_down_sync(0xffffffffu, sc, off);
+        const int oi = __shfl_down_sync(0xffffffffu, bi, off);
+        const float ol = __shfl_down_sync(0xffffffffu, bl, off);
+        if (os > sc || (os == sc && oi < bi)) {
+            sc = os;
+            bi = oi;
+            bl = ol;
+        }
+    }
+    if (lane == 0) {
         const float qnan = __int_as_float(0x7fc00000);
-        const bool none = st.m == -INFINITY || st.R == INFINITY;
-        candidate[row] = none ? 0 : st.idx;
-        if (log_p) log_p[row] = none ? qnan : st.l * a.inv_tau - (st.m + logf(st.s));
+        const bool drawn = !none && sc > -INFINITY;
+        candidate[row] = drawn ? bi : 0;
+        if (log_p) log_p[row] = drawn ? bl * a.inv_tau - draw_lse : qnan;
         if constexpr (STATS) {
             // statistics at temperature 1, and kappa = -ln p(candidate): ln Z for the
             // argmax itself, (m - l_c) + ln Z otherwise
@@ -315,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                 lse = rs.m + lnZ;
                 H = lnZ - rs.t / (1.0f + rs.rest);
                 am = rs.a;
-                kappa = none ? qnan : (st.idx == rs.a ? lnZ : (rs.m - st.l) + lnZ);
+                kappa = !drawn ? qnan : (bi == rs.a ? lnZ : (rs.m - bl) + lnZ);
             }
             if (fo.m) fo.m[row] = rs.m;
             if (fo.lse) fo.lse[row] = lse;

@@ -249,14 +249,19 @@ dg_status dg_row_stats_combine(const float *states, int32_t T, int64_t R, float 
 /*
  * Stochastic candidates ([P2] sampling loop: candidate tokens are sampled at every
  * position).  For each row i, a categorical draw from softmax(l_i / temperature), taken
- * as the Gumbel-max  candidate_i = argmax_v (l_{i,v} / temperature - ln(-ln u_{i,v})),
- * the lowest index on ties, with uniforms from Philox4x32-10 (Salmon et al., SC 2011):
- * entry v of row i uses word v % 4 of the block with counter
- * (v / 4, i, offset mod 2^32, offset / 2^32) and key (seed mod 2^32, seed / 2^32), and
- * u = ((word >> 9) + 1/2) * 2^-23.  The same (seed, offset) gives the same draws; a
- * sampling loop advances `offset` once per step.
+ * as a two-level Gumbel-max (an exact categorical sampler): with z = l_i / temperature,
+ * groups of 16 consecutive entries g = v / 16 and G(u) = -ln(-ln u),
+ *   g* = argmax_g (logsumexp_{v in g} z_v + G(u_{i,g}))          (lowest g on ties),
+ *   candidate_i = argmax_{v in g*} (z_v + G(u_{i,v}))           (lowest v on ties),
+ * with uniforms from Philox4x32-10 (Salmon et al., SC 2011), key (seed mod 2^32,
+ * seed / 2^32): entry v of row i uses word v % 4 of the block with counter
+ * (v / 4, i, offset mod 2^32, offset / 2^32), group g word g % 4 of the block with counter
+ * (2^31 + g / 4, i, offset mod 2^32, offset / 2^32), and u = ((word >> 9) + 1/2) * 2^-23.
+ * The same (seed, offset) gives the same draws; a sampling loop advances `offset` once
+ * per step.
  *
- *   logits     [R, ldl] fp32, ldl >= V (as dg_row_stats)
+ *   logits     [R, ldl] fp32, ldl >= V (as dg_row_stats; the padding columns up to the next
+ *              multiple of 4 are read and ignored)
  *   candidate  [R] int32  the drawn token
  *   log_p      [R] fp32   ln of its probability under softmax(l_i / temperature)
  * -inf entries are never drawn; a row that is all -inf gives candidate 0 and NaN log_p.
@@ -297,9 +302,9 @@ dg_status dg_entropy_accept_eligible(const float *H, const float *kappa, const u
 /*
  * Row statistics and a stochastic candidate in one read of the logits ([P2] sampling
  * loop: candidates are sampled at every position, and kept from most to least
- * confident).  m, lse, H and argmax are those of dg_row_stats (bit for bit); candidate
- * and log_p those of dg_row_sample with the same (temperature, seed, offset), bit for
- * bit; and
+ * confident).  m and argmax are those of dg_row_stats, lse and H too up to the order of
+ * the fp32 additions; candidate and log_p are those of dg_row_sample with the same
+ * (temperature, seed, offset), bit for bit; and
  *   kappa[i] = -ln p_i(candidate_i) under the untempered softmax: ln Z_i (dg_row_stats'
  *              kappa) when the candidate is the argmax, (m_i - l_{i,c}) + ln Z_i otherwise,
  * the confidence by which a sampling loop orders its positions.

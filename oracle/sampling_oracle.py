@@ -154,7 +154,7 @@ def row_sample(logits: np.ndarray, temperature: float, seed: int, offset: int) -
     cand = np.where(empty, 0, cand)
     log_p = np.where(empty, np.nan, log_p)
     return {"candidate": cand.astype(np.int32), "log_p": log_p, "group": gstar, "group_score": gscore,
-            "group_margin": gmargin, "score": escore_in, "margin": emargin}
+            "group_margin": gmargin, "entry_score": escore, "score": escore_in, "margin": emargin}
 
 
 def candidate_kappa(logits: np.ndarray, candidate) -> np.ndarray:
