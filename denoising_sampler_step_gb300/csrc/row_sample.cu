@@ -19,10 +19,10 @@
 //   best, grp  : the best group score m + ln(sum of the group's exp(z - m)) + G_g and its
 //                group (lowest on ties);
 // so a group costs its 16 exponentials (which the tempered sum needs anyway), one Philox
-// block and two logarithms.  Since u <= 1 - 2^-24, G < 16.7: a group whose largest z lies
-// more than ln 16 + 16.7 below a score the warp already holds cannot win and skips its
-// Philox block and logarithms.  After the merges, 16 lanes of the first CTA draw inside the
-// chosen group (four Philox blocks) and the lowest-index best entry is the candidate.
+// block and two logarithms.  (Skipping groups that cannot win, as G < 16.7, measured slower:
+// the warp-wide bound costs more than the rare skips save.)  After the merges, 16 lanes of
+// the first CTA draw inside the chosen group (four Philox blocks) and the lowest-index best
+// entry is the candidate.
 #include <cooperative_groups.h>
 #include <float.h>
 
@@ -39,8 +39,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kGroup = 16;           // vocabulary entries per group (four float4)
 constexpr uint32_t kGroupCounter = 0x80000000u;  // counter word 0 of the group uniforms
-constexpr float kGumbelMax = 16.7f;  // above every G the 23-bit uniforms can give
-constexpr float kLn16 = 2.7725887222397811f;
 constexpr float kLn2 = 0.69314718055994531f;
 
 struct Philox {
@@ -119,9 +117,8 @@ struct SampleArgs {
 };
 
 // Folds group g of row `row` (entries 16g .. 16g + 15: z, -inf past V) into st.
-// `bound`: a score some thread of the warp already holds.
 __device__ __forceinline__ void absorb_group(SampleState &st, const float (&z)[kGroup], int g, uint32_t row,
-                                             const SampleArgs &a, float bound) {
+                                             const SampleArgs &a) {
     float gm = z[0];
 #pragma unroll
     for (int j = 1; j < kGroup; ++j) gm = fmaxf(gm, z[j]);
@@ -135,8 +132,6 @@ __device__ __forceinline__ void absorb_group(SampleState &st, const float (&z)[k
 #pragma unroll
     for (int j = 0; j < kGroup; ++j) gs += ex2_approx(fmaf(z[j], kLog2e, nm));  // -inf entries: 0
     st.s += gs;
-    // no group here can beat `bound`: its score is at most gm + ln 16 + 16.7
-    if (gm + (kLn16 + kGumbelMax) < bound) return;
     const Philox w = philox4x32_10(kGroupCounter + (uint32_t)(g >> 2), row, a.o0, a.o1, a.k0, a.k1);
     // score = ln(sum of exp(z)) + G = m + ln(gs) - ln(-ln u)
     const float sc = st.m + kLn2 * __log2f(gs) - kLn2 * __log2f(neg_log_uniform(philox_word(w, g & 3)));
@@ -203,7 +198,6 @@ __global__ void __launch_bounds__(kThreads, 3)
     };
     int64_t g = g_begin + threadIdx.x;
     load_group(g, cur);
-    float bound = -INFINITY;  // the best score in the warp after the previous batch
     // every lane of a warp runs the same number of batches (lanes past g_end skip their group)
     for (int64_t g0 = g_begin; g0 < g_end; g0 += kThreads, g += kThreads) {
         const bool more = g0 + kThreads < g_end;
@@ -234,12 +228,8 @@ __global__ void __launch_bounds__(kThreads, 3)
             float z[kGroup];
 #pragma unroll
             for (int j = 0; j < kGroup; ++j) z[j] = x[j] * a.inv_tau;
-            absorb_group(st, z, (int)g, (uint32_t)row, a, bound);
+            absorb_group(st, z, (int)g, (uint32_t)row, a);
         }
-        float wb = st.best;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) wb = fmaxf(wb, __shfl_xor_sync(0xffffffffu, wb, off));
-        bound = wb;
         if (more) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) cur[k] = nxt[k];
