@@ -96,3 +96,29 @@ def test_single_pass_canvas256_full_size(B):
     rows = sampled_rows(wl.R, 14, 5)
     ref = soft_embed(x, ost["lse"], 0, wl.V, Wb, wl.gamma, rows=rows)
     assert rel_l2(out["E"].cpu().numpy()[rows], ref).max() <= E_TOL
+
+
+def test_single_pass_largest_canvas(B):
+    """1024 positions per request (the acceptance's limit): statistics and E against the
+    oracle; the acceptance against the oracle's rule applied to the step's own fp32
+    statistics (1024 kappas cannot all be kept 1e-5 apart, so the order is decided on the
+    same fp32 values on both sides)."""
+    wl = inputs.WORKLOADS["tiny"].with_(V=8192, d=256, L_c=1024, n_req=2, seed=99, budget=("uniform", 5.0, 60.0))
+    x = inputs.logits(wl)
+    budgets = inputs.budgets(wl)
+    Wb = inputs.embedding_bf16(wl)
+    out = run_step(B, x, wl, w_dev(Wb), budgets)
+    ost = row_stats(x)
+    check_stats(out, ost)
+    H = out["H"].cpu().numpy().astype(np.float64)
+    kappa = out["kappa"].cpu().numpy().astype(np.float64)
+    acc = entropy_accept(H, kappa, wl.n_req, wl.L_c, budgets)
+    for q in range(wl.n_req):                # the budget decision keeps a margin over the sum order
+        sl = slice(q * wl.L_c, (q + 1) * wl.L_c)
+        C = np.cumsum(H[sl][acc["order"][sl]])
+        assert np.all(np.abs(C - budgets[q]) > 1e-9)
+    for k in ("order", "mask", "n_accepted"):
+        assert np.array_equal(out[k].cpu().numpy(), acc[k]), k
+    rows = np.array([0, 511, 1023, 1024, 2047])
+    ref = soft_embed(x, ost["lse"], 0, wl.V, Wb, wl.gamma, rows=rows)
+    assert rel_l2(out["E"].cpu().numpy()[rows], ref).max() <= E_TOL
