@@ -471,7 +471,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             const bool edge = (k < p.vocab_start) || (k + BK > p.vocab_end);
             uint32_t packed[ROWS_PER_LANE][16];
             const bool fold = p.fused && (i / PGROUPS) % p.n_tiles == nt;
-            float4 vk[ROWS_PER_LANE][8];  // the logits, kept for the fold
+            float4 vk[ROWS_PER_LANE][8];  // the logits and their exponentials, kept for the fold
+            float ek[ROWS_PER_LANE][32];
 #pragma unroll
             for (int q = 0; q < ROWS_PER_LANE; ++q) {
                 const int r = rr[q];
@@ -498,6 +499,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 #pragma unroll
                 for (int t = 0; t < 16; ++t) packed[q][t] = pack_bf16x2(e[2 * t], e[2 * t + 1]);
+#pragma unroll
+                for (int t = 0; t < 32; ++t) ek[q][t] = e[t];
             }
             // the logits slot is free once the group's warps have read it
             __syncwarp();
@@ -527,10 +530,46 @@ __global__ void __launch_bounds__(THREADS, 1)
                     mbar_arrive(smem_u32(&full_a[s]));
             }
             if (fold) {
-                // the statistics kernel's fold over this row's 32 entries, in two halves
 #pragma unroll
                 for (int q = 0; q < ROWS_PER_LANE; ++q) {
+                    // the block's summary from the probabilities' own exponentials e = exp(l - c):
+                    // relative to the block max bm, exp(l - bm) = e exp(c - bm); a block whose max
+                    // lies more than 60 nats from c (e or exp(c - bm) may overflow) takes the
+                    // statistics kernel's fold instead.  Entries that underflow in e lie more than
+                    // 87 nats below c, so below every row maximum by as much: they add nothing
+                    // the fp32 statistics could hold.
+                    float xb[32];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        xb[4 * c + 0] = vk[q][c].x;
+                        xb[4 * c + 1] = vk[q][c].y;
+                        xb[4 * c + 2] = vk[q][c].z;
+                        xb[4 * c + 3] = vk[q][c].w;
+                    }
+                    if (edge) {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            if (k + t < p.vocab_start || k + t >= p.vocab_end) xb[t] = -INFINITY;
+                    }
+                    float bm = xb[0];
+#pragma unroll
+                    for (int t = 1; t < 32; ++t) bm = fmaxf(bm, xb[t]);
                     rowstate::RowState blk = rowstate::empty_row_state();
+                    if (bm > -INFINITY && fabsf(bm - my_ref[q]) <= 60.0f) {
+                        int ja = 31;
+#pragma unroll
+                        for (int t = 31; t >= 0; --t)
+                            if (xb[t] == bm) ja = t;
+                        float se = 0.0f, sd = 0.0f;
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) {
+                            se += t == ja ? 0.0f : ek[q][t];
+                            sd = fmaf(ek[q][t], fmaxf(xb[t] - bm, -FLT_MAX), sd);
+                        }
+                        const float inv = ex2_approx((my_ref[q] - bm) * kLog2e);
+                        blk = rowstate::RowState{bm, (int)(k + ja), se * inv, sd * inv};
+                    } else if (bm > -INFINITY) {
+                    // the statistics kernel's fold over this row's 32 entries, in two halves
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         float xs[16];
@@ -550,6 +589,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 if (k + 16 * h + t < p.vocab_start || k + 16 * h + t >= p.vocab_end) xs[t] = -INFINITY;
                         }
                         rowstate::absorb<16>(blk, xs, bs);
+                    }
                     }
                     rowstate::merge(my_st16[q], blk);
                 }
