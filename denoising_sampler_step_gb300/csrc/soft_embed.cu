@@ -690,8 +690,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 __global__ void splitk_reduce_kernel(const float4 *__restrict__ ws, const Params p, int d, float gamma,
                                      float *__restrict__ out, int64_t ldo, int vec_out,
                                      const float *__restrict__ scale) {
-    // the kernel queued next (the single pass's acceptance) reads nothing this one writes
+    // the kernel queued next (the single pass's acceptance) reads nothing this one writes;
+    // when this one overlaps the kernel before it (the single pass's redo), it reads the
+    // partials only after that one has completed
     grid_launch_dependents();
+    grid_dependency_wait();
     const int64_t groups = ((int64_t)d + 3) / 4;  // column groups of 4
     const int64_t total = (int64_t)p.R * groups;
     const int64_t tile_elems = (int64_t)(BN / 4) * BM;  // float4 per partial tile
@@ -756,6 +759,9 @@ __global__ void __launch_bounds__(256)
     single_pass_stats_kernel(const Params p, float *__restrict__ out_m, float *__restrict__ out_lse,
                              float *__restrict__ out_H, float *__restrict__ out_kappa,
                              int32_t *__restrict__ out_argmax) {
+    // launched to overlap the product's tail: the summaries are read after it completes
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (row >= p.R) return;  // warp-uniform
@@ -807,6 +813,8 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256)
     single_pass_redo_kernel(const Params p, const uint16_t *__restrict__ W, int64_t ldw, int d,
                             const float *__restrict__ lse) {
+    grid_dependency_wait();  // the list is complete once the statistics kernel is
+    grid_launch_dependents();
     const int n = p.counts[0];
     for (int e = blockIdx.x; e < n; e += gridDim.x) {
         const int2 sr = p.redo[e];
@@ -1037,12 +1045,28 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
         *msg = "soft-embed kernel launch failed";
         return e;
     }
+    // the single pass's small kernels each start while the one before finishes (programmatic
+    // dependent launch); each waits for its predecessor before it reads what that one wrote
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    auto small_cfg = [&](unsigned grid) {
+        cudaLaunchConfig_t c = {};
+        c.gridDim = dim3(grid, 1, 1);
+        c.blockDim = dim3(256, 1, 1);
+        c.stream = stream;
+        c.attrs = pdl;
+        c.numAttrs = 1;
+        return c;
+    };
     if (single) {
-        single_pass_stats_kernel<<<(unsigned)((R * 32 + 255) / 256), 256, 0, stream>>>(p, single->m, single->lse,
-                                                                                  single->H, single->kappa,
-                                                                                  single->argmax);
-        single_pass_redo_kernel<<<64, 256, 0, stream>>>(p, W, ldw, (int)d, single->lse);
-        e = cudaGetLastError();
+        cudaLaunchConfig_t c1 = small_cfg((unsigned)((R * 32 + 255) / 256));
+        e = cudaLaunchKernelEx(&c1, single_pass_stats_kernel, p, single->m, single->lse, single->H, single->kappa,
+                               single->argmax);
+        if (e == cudaSuccess) {
+            cudaLaunchConfig_t c2 = small_cfg(64);
+            e = cudaLaunchKernelEx(&c2, single_pass_redo_kernel, p, W, ldw, (int)d, (const float *)single->lse);
+        }
         if (e != cudaSuccess) {
             *msg = "single pass: statistics or redo launch failed";
             return e;
@@ -1064,9 +1088,15 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     const int64_t cap = (int64_t)device_sm_count() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const float4 *>(workspace), p, (int)d,
-                                                               gamma, out, ldo, vec_out, single ? p.ref : nullptr);
-    e = cudaGetLastError();
+    if (single) {
+        cudaLaunchConfig_t c3 = small_cfg((unsigned)blocks);
+        e = cudaLaunchKernelEx(&c3, splitk_reduce_kernel, static_cast<const float4 *>(workspace), p, (int)d, gamma,
+                               out, ldo, vec_out, (const float *)p.ref);
+    } else {
+        splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const float4 *>(workspace), p, (int)d,
+                                                                   gamma, out, ldo, vec_out, nullptr);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) {
         *msg = "split-K reduce launch failed";
         return e;
