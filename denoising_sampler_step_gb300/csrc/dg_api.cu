@@ -336,15 +336,18 @@ dg_status run_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, i
     }
     if (R == 0) return DG_OK;
     const uint8_t *eligible = loop ? loop->eligible : nullptr;
-    if (!sampled && use_single_pass(R, V, vocab_start, vocab_end, d, workspace_bytes)) {
-        // one read of the logits: the product folds the statistics; the acceptance runs on
-        // them between the product and its reduce
+    const bool draw_t1 = sampled && loop->temperature == 1.0f;  // the single pass folds this draw
+    if ((!sampled || draw_t1) && use_single_pass(R, V, vocab_start, vocab_end, d, workspace_bytes)) {
+        // one read of the logits: the product folds the statistics (and at temperature 1 the
+        // draw); the acceptance runs on them after the reduce starts
         AcceptArgs acc{H, kappa, budgets, n_req, L_c, min_accept, order, mask, n_accepted, eligible};
-        SinglePassOut so{m, lse, H, kappa, argmax};
+        SinglePassOut so{m, lse, H, kappa, argmax, draw_t1 ? loop->candidate : nullptr,
+                         draw_t1 ? loop->seed : 0, draw_t1 ? loop->offset : 0};
         st = run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, ldw, d, gamma, E, ldo, workspace,
                             workspace_bytes, s, accept_hook, &acc, false, &so);
         if (st != DG_OK || !loop) return st;
-        cudaError_t e = launch_loop_update(argmax, argmax, H, mask, n_req, L_c, loop->stable_steps,
+        cudaError_t e = launch_loop_update(draw_t1 ? loop->candidate : argmax, argmax, H, mask, n_req, L_c,
+                                           loop->stable_steps,
                                            loop->entropy_threshold, loop->step_limit, loop->canvas, loop->eligible,
                                            loop->prev_argmax, loop->stable, loop->steps, loop->converged, s);
         return e == cudaSuccess ? DG_OK : cuda_fail(e, "step: loop update launch");

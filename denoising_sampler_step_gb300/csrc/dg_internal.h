@@ -43,6 +43,8 @@ struct SoftEmbedPlan {
 struct SinglePassOut {
     float *m, *lse, *H, *kappa;
     int32_t *argmax;
+    int32_t *candidate;     // non-NULL: also draw at temperature 1 (two-level Gumbel-max); kappa is
+    uint64_t seed, offset;  // then -ln p of the drawn token
 };
 bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t d, int num_sms,
                      SoftEmbedPlan *plan);

@@ -38,6 +38,7 @@
 
 #include "dg_common.cuh"
 #include "dg_internal.h"
+#include "philox.cuh"
 #include "row_state.cuh"
 
 namespace dg {
@@ -124,6 +125,12 @@ struct Params {
                          // i of the split with (i / PGROUPS) % n_tiles == the column tile
     int *counts;         // [0] (split, row) pairs to redo: the reference was too far from the maximum
     int2 *redo;          // [splits * R] the pairs
+    // single pass with the temperature-1 draw: the folded blocks also take the draw's first
+    // level (a group of 16 entries by log-mass + Gumbel), the statistics kernel the second
+    int draw;
+    uint32_t k0, k1, o0, o1;  // Philox key (seed) and counter offset words
+    float2 *draws;            // [splits][n_tiles][R] best group score, group (int bits)
+    int32_t *candidate;       // [R] the drawn tokens
 };
 
 // A split's probabilities exp(l - c) stay finite and their sums far from overflow while the
@@ -235,12 +242,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     float my_ref[ROWS_PER_LANE];
     rowstate::RowState my_st[ROWS_PER_LANE], my_st16[ROWS_PER_LANE];
     int my_folded = 0;
+    float my_gbest[ROWS_PER_LANE];  // the draw's first level: best group score and group
+    int my_gidx[ROWS_PER_LANE];
 #pragma unroll
     for (int q = 0; q < ROWS_PER_LANE; ++q) {
         my_rows[q] = 0;
         my_ref[q] = 0.0f;
         my_st[q] = rowstate::empty_row_state();
         my_st16[q] = rowstate::empty_row_state();
+        my_gbest[q] = -INFINITY;
+        my_gidx[q] = 0x7fffffff;
     }
 
     if (warp == 11) {
@@ -555,6 +566,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int t = 1; t < 32; ++t) bm = fmaxf(bm, xb[t]);
                     rowstate::RowState blk = rowstate::empty_row_state();
+                    float glm[2] = {-INFINITY, -INFINITY};  // the two groups' log-masses
                     if (bm > -INFINITY && fabsf(bm - my_ref[q]) <= 60.0f) {
                         int ja = 31;
 #pragma unroll
@@ -568,6 +580,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                         const float inv = ex2_approx((my_ref[q] - bm) * kLog2e);
                         blk = rowstate::RowState{bm, (int)(k + ja), se * inv, sd * inv};
+                        if (p.draw) {  // the two groups' log-masses, c + ln(sum of e)
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                float gsum = 0.0f;
+#pragma unroll
+                                for (int t = 0; t < 16; ++t) gsum += ek[q][16 * h + t];
+                                glm[h] = my_ref[q] + philox::kLn2 * __log2f(gsum);
+                            }
+                        }
                     } else if (bm > -INFINITY) {
                     // the statistics kernel's fold over this row's 32 entries, in two halves
 #pragma unroll
@@ -590,8 +611,33 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                         rowstate::absorb<16>(blk, xs, bs);
                     }
+                    if (p.draw) {  // far from c: the log-masses against the block max
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            float gsum = 0.0f;
+#pragma unroll
+                            for (int t = 0; t < 16; ++t) gsum += ex2_approx((xb[16 * h + t] - bm) * kLog2e);
+                            glm[h] = bm + philox::kLn2 * __log2f(gsum);
+                        }
+                    }
                     }
                     rowstate::merge(my_st16[q], blk);
+                    if (p.draw && bm > -INFINITY) {
+                        // groups k/16 and k/16 + 1 (k is a multiple of 32): words of one Philox block
+                        const int g0 = (int)(k >> 4);
+                        const philox::Philox w = philox::philox4x32_10(philox::kGroupCounter + (uint32_t)(g0 >> 2),
+                                                                       (uint32_t)(row0 + rr[q]), p.o0, p.o1, p.k0,
+                                                                       p.k1);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const float sc =
+                                glm[h] - philox::kLn2 * __log2f(philox::neg_log_uniform(philox::philox_word(w, (g0 + h) & 3)));
+                            if (sc > my_gbest[q]) {  // groups arrive in increasing order: ties keep the lower
+                                my_gbest[q] = sc;
+                                my_gidx[q] = g0 + h;
+                            }
+                        }
+                    }
                 }
                 if (++my_folded % 16 == 0) {
 #pragma unroll
@@ -656,9 +702,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         // idle: every MMA has completed or been drained), write the summary of this tile's
         // share of the split's blocks per row, and (column tile 0) the reference
         rowstate::RowState *scratch = reinterpret_cast<rowstate::RowState *>(a_ring);
+        float2 *dscratch = reinterpret_cast<float2 *>(a_ring + 8192);  // after (PGROUPS - 1) x 2 KiB of states
         if (my_grp > 0)
 #pragma unroll
-            for (int q = 0; q < ROWS_PER_LANE; ++q) scratch[(my_grp - 1) * BM + my_rows[q]] = my_st[q];
+            for (int q = 0; q < ROWS_PER_LANE; ++q) {
+                scratch[(my_grp - 1) * BM + my_rows[q]] = my_st[q];
+                dscratch[(my_grp - 1) * BM + my_rows[q]] = make_float2(my_gbest[q], __int_as_float(my_gidx[q]));
+            }
         __syncthreads();
         if (my_grp == 0 && !*abort_flag) {
 #pragma unroll
@@ -670,6 +720,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int a = st.m == -INFINITY ? 0x7fffffff : st.a;
                 p.state[((int64_t)j * p.n_tiles + nt) * p.R + row] = make_float4(st.m, __int_as_float(a), st.rest, st.t);
                 if (nt == 0) p.ref[(int64_t)j * p.R + row] = my_ref[q];
+                if (p.draw) {
+                    float best = my_gbest[q];
+                    int gi = my_gidx[q];
+                    for (int g = 1; g < PGROUPS; ++g) {
+                        const float2 o = dscratch[(g - 1) * BM + my_rows[q]];
+                        const int oi = __float_as_int(o.y);
+                        if (o.x > best || (o.x == best && oi < gi)) {
+                            best = o.x;
+                            gi = oi;
+                        }
+                    }
+                    p.draws[((int64_t)j * p.n_tiles + nt) * p.R + row] = make_float2(best, __int_as_float(gi));
+                }
             }
         }
     }
@@ -766,11 +829,21 @@ __global__ void __launch_bounds__(256)
     const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (row >= p.R) return;  // warp-uniform
     rowstate::RowState st = rowstate::empty_row_state();
+    float dbest = -INFINITY;  // the draw's first level: best group score and group
+    int dgrp = 0x7fffffff;
     for (int s = lane; s < p.splits; s += 32) {
         rowstate::RowState sp = rowstate::empty_row_state();
         for (int t = 0; t < p.n_tiles; ++t) {
             const float4 v = p.state[((int64_t)s * p.n_tiles + t) * p.R + row];
             rowstate::merge(sp, rowstate::RowState{v.x, __float_as_int(v.y), v.z, v.w});
+            if (p.draw) {
+                const float2 dv = p.draws[((int64_t)s * p.n_tiles + t) * p.R + row];
+                const int gi = __float_as_int(dv.y);
+                if (dv.x > dbest || (dv.x == dbest && gi < dgrp)) {
+                    dbest = dv.x;
+                    dgrp = gi;
+                }
+            }
         }
         const float gap = sp.m - p.ref[(int64_t)s * p.R + row];
         if (sp.m > -INFINITY && !(gap <= kRefSpan && gap >= -kRefSpan)) {
@@ -780,7 +853,15 @@ __global__ void __launch_bounds__(256)
         rowstate::merge(st, sp);
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) rowstate::merge(st, rowstate::shfl_down(st, off));
+    for (int off = 16; off > 0; off >>= 1) {
+        rowstate::merge(st, rowstate::shfl_down(st, off));
+        const float ob = __shfl_down_sync(0xffffffffu, dbest, off);
+        const int og = __shfl_down_sync(0xffffffffu, dgrp, off);
+        if (ob > dbest || (ob == dbest && og < dgrp)) {
+            dbest = ob;
+            dgrp = og;
+        }
+    }
     float lse = __int_as_float(0x7fc00000), H = lse, kappa = lse;
     int a = 0;
     if (lane == 0 && st.m != -INFINITY) {
@@ -796,6 +877,38 @@ __global__ void __launch_bounds__(256)
         float *r = p.ref + (int64_t)s * p.R + row;
         // c <= m <= lse: at most 1; a row without a distribution gets NaN, as in the two-pass step
         *r = m == -INFINITY ? __int_as_float(0x7fc00000) : ex2_approx((*r - lse) * kLog2e);
+    }
+    if (p.draw) {
+        // the second level: lanes 0-15 draw inside the chosen group (temperature 1); kappa
+        // becomes -ln p of the drawn token
+        const int gs = __shfl_sync(0xffffffffu, dgrp, 0);
+        const int64_t v = (int64_t)16 * gs + lane;
+        const bool valid = gs != 0x7fffffff && lane < 16 && v < p.vocab_end;
+        const float l = valid ? p.logits[row * p.ldl + v] : -INFINITY;
+        float sc = -INFINITY;
+        if (valid && l != -INFINITY) {
+            const philox::Philox w = philox::philox4x32_10((uint32_t)(v >> 2), (uint32_t)row, p.o0, p.o1, p.k0, p.k1);
+            sc = l - philox::kLn2 * __log2f(philox::neg_log_uniform(philox::philox_word(w, (int)(v & 3))));
+        }
+        int bi = valid ? (int)v : 0x7fffffff;
+        float bl = l;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float os = __shfl_down_sync(0xffffffffu, sc, off);
+            const int oi = __shfl_down_sync(0xffffffffu, bi, off);
+            const float ol = __shfl_down_sync(0xffffffffu, bl, off);
+            if (os > sc || (os == sc && oi < bi)) {
+                sc = os;
+                bi = oi;
+                bl = ol;
+            }
+        }
+        if (lane == 0) {
+            const bool drawn = st.m != -INFINITY && sc > -INFINITY;
+            p.candidate[row] = drawn ? bi : 0;
+            const float lnZ = kappa;  // ln Z (NaN without a distribution)
+            kappa = !drawn ? __int_as_float(0x7fc00000) : (bi == a ? lnZ : (st.m - bl) + lnZ);
+        }
     }
     if (lane == 0) {
         if (out_m) out_m[row] = st.m;
@@ -884,7 +997,7 @@ size_t soft_embed_workspace_bytes(const SoftEmbedPlan &plan, int splits) {
 static size_t align16(size_t b) { return (b + 15) & ~size_t(15); }
 size_t single_pass_extra_bytes(const SoftEmbedPlan &plan, int64_t R) {
     const size_t n = (size_t)plan.splits * (size_t)R;
-    return align16(n * 4) + n * (size_t)plan.n_tiles * 16 + 16 + align16(n * 8);
+    return align16(n * 4) + n * (size_t)plan.n_tiles * 16 + 16 + align16(n * 8) + n * (size_t)plan.n_tiles * 8;
 }
 
 bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t d, int num_sms,
@@ -1012,6 +1125,10 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     p.state = nullptr;
     p.counts = nullptr;
     p.redo = nullptr;
+    p.draw = 0;
+    p.k0 = p.k1 = p.o0 = p.o1 = 0;
+    p.draws = nullptr;
+    p.candidate = nullptr;
     if (single) {
         const size_t n = (size_t)plan.splits * (size_t)R;
         uint8_t *x = static_cast<uint8_t *>(workspace) + soft_embed_workspace_bytes(plan, plan.splits);
@@ -1022,6 +1139,16 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
         p.counts = reinterpret_cast<int *>(x);
         x += 16;
         p.redo = reinterpret_cast<int2 *>(x);
+        x += align16(n * 8);
+        if (single->candidate) {
+            p.draw = 1;
+            p.draws = reinterpret_cast<float2 *>(x);
+            p.candidate = single->candidate;
+            p.k0 = (uint32_t)single->seed;
+            p.k1 = (uint32_t)(single->seed >> 32);
+            p.o0 = (uint32_t)single->offset;
+            p.o1 = (uint32_t)(single->offset >> 32);
+        }
         overlap_previous = false;  // nothing before it to wait for
     }
     const int64_t pairs = (int64_t)(plan.m_tiles / kCtasPerUnit) * (n_full * (int64_t)p.splits + p.tail_splits);

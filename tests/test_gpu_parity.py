@@ -55,8 +55,13 @@ def check_stats(g, o, rows=None):
     err = np.abs(kp[fin] - ref[fin]) / np.maximum(1.0, ref[fin])
     assert err.size == 0 or err.max() <= 1e-5, float(err.max())
     rel = np.abs(kp[fin] - ref[fin]) / np.maximum(ref[fin], 1e-30)
-    small = ref[fin] < 1.0
+    # near one-hot (kappa < 1) the order rests on kappa's relative precision; below 1e-30 the
+    # terms of rest fall under fp32's normal range (flushed to zero), so only an absolute
+    # bound holds there
+    small = (ref[fin] < 1.0) & (ref[fin] >= 1e-30)
     assert not np.any(small) or rel[small].max() <= 5e-6, ("kappa near one-hot", float(rel[small].max()))
+    tiny = ref[fin] < 1e-30
+    assert not np.any(tiny) or np.abs(kp[fin] - ref[fin])[tiny].max() <= 1e-33
 
 
 def rel_l2(E, ref):

@@ -122,3 +122,37 @@ def test_single_pass_largest_canvas(B):
     rows = np.array([0, 511, 1023, 1024, 2047])
     ref = soft_embed(x, ost["lse"], 0, wl.V, Wb, wl.gamma, rows=rows)
     assert rel_l2(out["E"].cpu().numpy()[rows], ref).max() <= E_TOL
+
+
+def test_single_pass_draw_at_temperature_one(B):
+    """The loop step at temperature 1 folds the draw into the product: the candidates
+    against the two-level oracle draw (unique where both decisions lead by 1e-3), kappa =
+    -ln p of the drawn token; rows far from their reference (one-hot, 90 nats up, masked
+    starts, shifted) take the fallback folds."""
+    from oracle import candidate_kappa, row_sample
+    from tests.test_gpu_parity import check_sample
+    wl = inputs.WORKLOADS["tiny"].with_(V=40000, d=256, L_c=24, n_req=2, seed=17, budget=5.0)
+    x = inputs.logits(wl)
+    x[0, 12345] = 1.0e4
+    x[1, 30000] = 90.0
+    x[2, :8192] = -np.inf
+    x[4, :] -= 300.0
+    x[5, :] = -np.inf
+    x[5, [100, 20000]] = 2.0
+    Wb = inputs.embedding_bf16(wl)
+    Wd = w_dev(Wb)
+    state = B.new_loop_state(wl.n_req, wl.L_c, "cuda")
+    out = B.dg_sampler_loop_step(dev(x), wl.n_req, wl.L_c, Wd, wl.gamma, dev(inputs.budgets(wl)), state, 2, 1.0, 10,
+                                 temperature=1.0, seed=31, offset=4)
+    torch.cuda.synchronize()
+    B.dg_get_device_status()
+    o = row_sample(x, 1.0, 31, 4)
+    g = {"candidate": out["candidate"], "log_p": torch.from_numpy(o["log_p"].astype(np.float32))}
+    check_sample(g, o)
+    cand = out["candidate"].cpu().numpy()
+    assert cand[0] == 12345 and cand[1] == 30000 and cand[5] in (100, 20000)
+    ref = candidate_kappa(x, cand)
+    k = out["kappa"].cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(k - ref) <= 1e-5 * np.maximum(1.0, ref))
+    check_stats({kk: out[kk] for kk in ("m", "lse", "H", "argmax")} | {"kappa": out["kappa"]},
+                dict(row_stats(x), kappa=ref))
