@@ -28,7 +28,10 @@ sys.path.insert(0, ROOT)
 METRIC = "canvas positions/sec per fused sampler step (V=262144,d=2816); % of roofline"
 UNIT = "positions/s"
 WORKLOAD = "canvas256"
-KERNELS_PER_STEP = 4   # row stats, acceptance, soft-embed product, split-K reduce
+# kernels one timed step launches: the single pass's product, statistics, redo, reduce and
+# acceptance (DGSAMP_TWO_PASS=1: statistics, product, acceptance, reduce)
+KERNELS_PER_STEP = 5
+KERNELS_PER_STEP_TWO_PASS = 4
 # the denoising loop timed beside the step: a graph of 16 steps (the pages report 11 to 24
 # denoising steps per canvas), convergence after two stable steps below 1 nat of mean
 # entropy or at 24 steps
@@ -461,7 +464,8 @@ def main() -> None:
         "graph": graph,
         "loop": loop,
         "loop_sampled": loop_sampled,
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": (KERNELS_PER_STEP_TWO_PASS if os.environ.get("DGSAMP_TWO_PASS") == "1"
+                         else KERNELS_PER_STEP) * args.steps,
         "clocks": clk,
     }
     if sustained is not None:
