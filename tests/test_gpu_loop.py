@@ -293,13 +293,15 @@ def sampled_chain_inputs(wl, steps, temperature, seed):
     return budgets, thr, chain
 
 
-def test_sampled_loop_chain_matches_oracle(B):
-    """A sampling loop (temperature 1, Philox offset = step): at every step the fused
-    statistics + draw, the acceptance by -ln p of the drawn token over the eligible
+@pytest.mark.parametrize("temperature", [1.0, 0.7])
+def test_sampled_loop_chain_matches_oracle(B, temperature):
+    """A sampling loop (Philox offset = step): at every step the statistics and the draw
+    (folded into the single pass at temperature 1, the fused statistics + draw pass before
+    the product otherwise), the acceptance by -ln p of the drawn token over the eligible
     positions, the canvas of drawn tokens and the argmax-judged state, bit-exact against
     the oracle chain."""
     from denoising_sampler_step_gb300.step import SamplerLoop
-    wl, temperature, seed = SAMPLED_WL, 1.0, 2024
+    wl, seed = SAMPLED_WL, 2024
     budgets, thr, chain = sampled_chain_inputs(wl, N_STEPS, temperature, seed)
     Wb = inputs.embedding_bf16(wl)
     lp = SamplerLoop(w_dev(Wb), wl.n_req, wl.L_c, wl.V, wl.gamma, STABLE_STEPS, thr, STEP_LIMIT,
@@ -317,3 +319,42 @@ def test_sampled_loop_chain_matches_oracle(B):
     assert chain[-1][5]["converged"].all()
     # the chain keeps drawn tokens that are not the argmax of their step
     assert any(np.any((sm["candidate"] != st["argmax"]) & (acc["mask"] == 1)) for _, st, sm, _, acc, _ in chain)
+
+
+def test_sampled_loop_steps_in_a_cuda_graph_match_eager_steps(B):
+    """Four loop steps at temperature 1 (the draw folded into the single pass) captured in
+    one CUDA graph: replayed from the starting state they give the eager steps' state,
+    draws and outputs bit for bit (the graph keeps the offsets it was captured with)."""
+    from denoising_sampler_step_gb300.step import SamplerLoop
+    wl = LOOP_WL.with_(n_req=2, V=30000)
+    x = dev(inputs.logits(wl))
+    bud = dev(inputs.budgets(wl))
+    lp = SamplerLoop(w_dev(inputs.embedding_bf16(wl)), wl.n_req, wl.L_c, wl.V, wl.gamma, 1, 9.0, 3,
+                     temperature=1.0, seed=5, min_accept=1)
+    for _ in range(4):
+        lp(x, bud)
+    torch.cuda.synchronize()
+    eager = {k: v.clone() for k, v in list(lp.out.items()) + list(lp.state.items())}
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        lp.reset()
+        lp(x, bud)
+    torch.cuda.current_stream().wait_stream(cap)
+    torch.cuda.synchronize()
+    lp.reset()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        for _ in range(4):
+            lp(x, bud)
+    lp.reset()
+    for v in lp.out.values():
+        v.zero_()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    B.dg_get_device_status()
+    now = dict(list(lp.out.items()) + list(lp.state.items()))
+    for k, v in eager.items():
+        assert torch.equal(now[k].view(torch.int32) if now[k].dtype == torch.float32 else now[k],
+                           v.view(torch.int32) if v.dtype == torch.float32 else v), k

@@ -156,3 +156,20 @@ def test_single_pass_draw_at_temperature_one(B):
     assert np.all(np.abs(k - ref) <= 1e-5 * np.maximum(1.0, ref))
     check_stats({kk: out[kk] for kk in ("m", "lse", "H", "argmax")} | {"kappa": out["kappa"]},
                 dict(row_stats(x), kappa=ref))
+
+
+@pytest.mark.slow
+def test_two_pass_canvas256_full_size(B):
+    """The two-pass step (statistics before the product) at full size, as DGSAMP_TWO_PASS=1
+    selects it."""
+    wl = inputs.WORKLOADS["canvas256"]
+    x, budgets, ost, _ = guarded(wl)
+    Wb = inputs.embedding_bf16(wl)
+    out = two_pass(lambda: run_step(B, x, wl, w_dev(Wb), budgets))
+    check_stats(out, ost)
+    acc = entropy_accept(ost["H"], ost["kappa"], wl.n_req, wl.L_c, budgets)
+    for k in ("order", "mask", "n_accepted"):
+        assert np.array_equal(out[k].cpu().numpy(), acc[k]), k
+    rows = sampled_rows(wl.R, 14, 6)
+    ref = soft_embed(x, ost["lse"], 0, wl.V, Wb, wl.gamma, rows=rows)
+    assert rel_l2(out["E"].cpu().numpy()[rows], ref).max() <= E_TOL
