@@ -118,7 +118,7 @@ struct Params {
     // single pass (no lse yet): each split's probabilities are taken against a reference
     // c per row, exp(l - c), and the column-tile-0 clusters also fold the row statistics
     int fused;
-    const float *logits; // the reference's source (the split's first four entries)
+    const float *logits; // the reference's source (the split's first kRefEntries entries)
     int64_t ldl;
     float *ref;          // [splits][R] c, then (after the statistics) exp(c - lse)
     float4 *state;       // [splits][n_tiles][R] row summaries (m, argmax bits, rest, t) of the blocks
@@ -133,9 +133,14 @@ struct Params {
     int32_t *candidate;       // [R] the drawn tokens
 };
 
-// A split's probabilities exp(l - c) stay finite and their sums far from overflow while the
-// split's maximum lies within this many nats of c; other (split, row) pairs are redone.
-constexpr float kRefSpan = 64.0f;
+// A (split, row) is redone when its probabilities against c could overflow: when the sum
+// of exp(l - c) over the split passes e^kRefSumLog (about 4e35, so that with |W| <= 100 the
+// fp32 partial stays below 4e37), or when the split's maximum lies more than kRefBelow nats
+// below c (everything would underflow).
+constexpr float kRefSumLog = 82.0f;
+constexpr float kRefBelow = 64.0f;
+// The reference is the largest of a split's first kRefEntries logits.
+constexpr int kRefEntries = 32;
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
@@ -436,8 +441,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         int rr[ROWS_PER_LANE];
         float neg_lse2[ROWS_PER_LANE];
         if (p.fused) {
-            // reference c: the largest of the split's first four entries inside the slice
-            // (0 if none is finite); every column tile takes the same c
+            // reference c: the largest of the split's first 32 entries inside the slice (0 if
+            // none is finite); every column tile takes the same c.  A float4 that starts below
+            // vocab_end ends inside the row (ldl is a multiple of 4).
             const int64_t k0 = p.k_begin + kb0 * BK;
 #pragma unroll
             for (int q = 0; q < ROWS_PER_LANE; ++q) {
@@ -445,11 +451,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int row = row0 + rr[q];
                 float c = -INFINITY;
                 if (row < p.R && nkb > 0) {
-                    const float4 f = __ldg(reinterpret_cast<const float4 *>(p.logits + (int64_t)row * p.ldl + k0));
-                    const float fv[4] = {f.x, f.y, f.z, f.w};
+                    const float *lr = p.logits + (int64_t)row * p.ldl;
+#pragma unroll 8
+                    for (int c4 = 0; c4 < kRefEntries / 4; ++c4) {
+                        const int64_t kk = k0 + 4 * c4;
+                        if (kk >= p.vocab_end) break;
+                        const float4 f = __ldg(reinterpret_cast<const float4 *>(lr + kk));
+                        const float fv[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        if (k0 + t >= p.vocab_start && k0 + t < p.vocab_end) c = fmaxf(c, fv[t]);
+                        for (int t = 0; t < 4; ++t)
+                            if (kk + t >= p.vocab_start && kk + t < p.vocab_end) c = fmaxf(c, fv[t]);
+                    }
                 }
                 if (!(c > -INFINITY)) c = 0.0f;
                 my_rows[q] = rr[q];
@@ -815,7 +827,7 @@ __global__ void splitk_reduce_kernel(const float4 *__restrict__ ws, const Params
 
 // Single pass, after the product: per row (one warp), lane l merges the tile summaries of
 // splits l, l + 32, ... (tile order), checks each split's maximum against its reference
-// (pairs more than kRefSpan apart are listed for the redo pass), the lanes' states merge in a
+// (pairs whose probabilities could overflow are listed for the redo pass), the lanes' states merge in a
 // fixed shuffle tree, lane 0 writes the statistics, and each split's reference becomes its
 // scale exp(c - lse).
 __global__ void __launch_bounds__(256)
@@ -845,8 +857,10 @@ __global__ void __launch_bounds__(256)
                 }
             }
         }
+        // the split's probabilities against its reference: ln of their sum is
+        // (m - c) + ln Z_split; list the pair for the redo pass if they could overflow
         const float gap = sp.m - p.ref[(int64_t)s * p.R + row];
-        if (sp.m > -INFINITY && !(gap <= kRefSpan && gap >= -kRefSpan)) {
+        if (sp.m > -INFINITY && !(gap + log1pf(sp.rest) <= kRefSumLog && gap >= -kRefBelow)) {
             const int slot = atomicAdd(&p.counts[0], 1);
             p.redo[slot] = make_int2(s, (int)row);
         }

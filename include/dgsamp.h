@@ -194,11 +194,12 @@ dg_status dg_sum_partials(const float *const *partials, int32_t T, int64_t R, in
  * When the slice is the whole vocabulary (vocab_start == 0, vocab_end == V) and the
  * workspace is that size, the step reads the logits once: each vocabulary split of the
  * product takes its probabilities against a per-row reference c (the largest of the
- * split's first four entries), exp(l - c), while it folds the row statistics; the split
+ * split's first 32 entries), exp(l - c), while it folds the row statistics; the split
  * summaries then give the statistics (as dg_row_stats, up to the order of the fp32
  * additions) and each split's partial is scaled by exp(c - lse) in the reduce.  A
- * (split, row) whose maximum lies more than 64 nats from c is recomputed against lse on
- * the CUDA cores (exact, slow, rare: one-hot rows).  E then equals the two-pass result up
+ * (split, row) whose probabilities against c could overflow (their sum above e^82, or the
+ * split's maximum 64 nats below c) is recomputed against lse on the CUDA cores (exact,
+ * slow, rare: one-hot rows).  E then equals the two-pass result up
  * to the bf16 rounding of different probabilities.  The environment variable
  * DGSAMP_TWO_PASS=1 forces the statistics pass before the product.
  */

@@ -62,9 +62,10 @@ def test_single_pass_matches_oracle_and_two_pass(B, V, d, L_c, n_req):
 
 
 def test_single_pass_redoes_rows_far_from_their_reference(B):
-    """Rows whose maximum lies more than 64 nats above a split's first entries (one-hot
-    rows), rows whose splits start masked, rows with nothing finite: the redo pass must give
-    the oracle's statistics and embedding."""
+    """Rows whose probabilities against a split's reference could overflow (a one-hot row,
+    a logit 90 nats above the rest) go through the redo pass; rows whose splits start
+    masked, shifted rows and rows with nothing finite stay in the product: all must give the
+    oracle's statistics and embedding."""
     wl = inputs.WORKLOADS["tiny"].with_(V=40000, d=256, L_c=16, n_req=1, seed=3, budget=5.0)
     x = inputs.logits(wl)
     x[0, 12345] = 1.0e4                     # one-hot: overflow against any reference
