@@ -180,6 +180,45 @@ def run_reference(args) -> None:
 
 # --------------------------------------------------------------------------- GPU arm
 
+def other_configs(args, dev, B, inputs, SamplerStep) -> dict:
+    """The step at further workloads (fresh inputs each): ms per step and the product's
+    tensor rate, single pass and two passes (DGSAMP_TWO_PASS=1)."""
+    import numpy as np
+    import torch
+    res = {}
+    for name in [n for n in args.also.split(",") if n]:
+        wl = inputs.WORKLOADS[name]
+        xd = torch.from_numpy(inputs.logits(wl)).to(dev)
+        Wd = torch.from_numpy(inputs.embedding_bf16(wl).view(np.int16)).to(dev).view(torch.bfloat16)
+        bd = torch.from_numpy(inputs.budgets(wl)).to(dev)
+        st = SamplerStep(Wd, wl.n_req, wl.L_c, wl.V, wl.gamma, device=dev)
+        n = max(3, min(args.steps, int(2000 // max(1, wl.R // 256))))
+        out = {"rows": wl.R, "steps": n}
+        for mode in ("single_pass", "two_pass"):
+            if mode == "two_pass":
+                os.environ["DGSAMP_TWO_PASS"] = "1"
+            try:
+                for _ in range(3):
+                    st(xd, bd)
+                torch.cuda.synchronize(dev)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(n):
+                    st(xd, bd)
+                e1.record()
+                torch.cuda.synchronize(dev)
+                B.dg_get_device_status()
+            finally:
+                os.environ.pop("DGSAMP_TWO_PASS", None)
+            ms = e0.elapsed_time(e1) / n
+            out[mode] = {"ms_per_step": ms, "positions_per_s": wl.R / (ms * 1e-3),
+                         "tflops": 2.0 * wl.R * wl.V * wl.d / (ms * 1e-3) / 1e12}
+        res[name] = out
+        del st, xd, Wd
+        torch.cuda.empty_cache()
+    return res
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -187,6 +226,10 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--also", default="",
+                    help="comma-separated further workloads (e.g. batch8,late_batch32) whose step is "
+                         "timed after the main one and reported under other_configs (single pass and "
+                         "two passes)")
     ap.add_argument("--only", choices=["soft_embed", "step"], default=None,
                     help="profiling target: run only this call (warm-up, then --steps calls) and print "
                          "its mean duration; no JSON line")
@@ -470,6 +513,8 @@ def main() -> None:
     }
     if sustained is not None:
         line["sustained"] = sustained
+    if args.also:
+        line["other_configs"] = other_configs(args, dev, B, inputs, SamplerStep)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(x, Wb, wl)
     if rank == 0:
