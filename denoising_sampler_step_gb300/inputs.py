@@ -33,6 +33,7 @@ TAG_ROW_PARAMS = 2   # per-request row scale, boost index and boost size
 TAG_W = 3            # per-block N(0,1) draws of the embedding table
 TAG_BUDGET = 4       # per-request entropy budgets
 TAG_LOOP_NOISE = 5   # per-step, per-row noise of a denoising-loop sequence
+TAG_W8 = 6           # per-block draws of an 8-bit (E4M3) embedding table
 
 W_BLOCK_ROWS = 4096  # embedding rows drawn per Philox stream
 
@@ -172,6 +173,30 @@ def embedding_bf16(wl: Workload) -> np.ndarray:
     with ThreadPoolExecutor(_threads()) as ex:
         list(ex.map(one, range(nblk)))
     return out
+
+
+def embedding_e4m3(wl: Workload) -> tuple:
+    """An 8-bit embedding table drawn directly: codes Q [V, d] (uint8) and per-row fp32 scales
+    [V].  Magnitude codes are uniform over 0x40..0x7E (E4M3 values 2 to 448), signs uniform,
+    and one entry per row holds the code of 448 (the row maximum a per-row quantiser
+    produces); scales are uniform in [1e-4, 3e-4], so entries lie within about 0.13 of 0."""
+    V, d = wl.V, wl.d
+    Q = np.empty((V, d), np.uint8)
+    scale = np.empty(V, np.float32)
+    nblk = (V + W_BLOCK_ROWS - 1) // W_BLOCK_ROWS
+
+    def one(b: int) -> None:
+        r0, r1 = b * W_BLOCK_ROWS, min(V, (b + 1) * W_BLOCK_ROWS)
+        g = philox(wl.seed, stream_id(TAG_W8, b))
+        mag = g.integers(0x40, 0x7F, (r1 - r0, d), dtype=np.uint8)
+        sign = g.integers(0, 2, (r1 - r0, d), dtype=np.uint8) << np.uint8(7)
+        mag[np.arange(r1 - r0), g.integers(0, d, r1 - r0)] = 0x7E
+        Q[r0:r1] = mag | sign
+        scale[r0:r1] = g.uniform(1e-4, 3e-4, r1 - r0).astype(np.float32)
+
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(one, range(nblk)))
+    return Q, scale
 
 
 def budgets(wl: Workload) -> np.ndarray:
