@@ -64,6 +64,16 @@ lib.dg_row_stats_partial.restype = ctypes.c_int
 lib.dg_row_stats_combine.argtypes = [_p, _i32, _i64, _p, _p, _p, _p, _p, _p]
 lib.dg_row_stats_combine.restype = ctypes.c_int
 lib.dg_sampler_loop_step.restype = ctypes.c_int
+lib.dg_quantize_e4m3.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _p]
+lib.dg_quantize_e4m3.restype = ctypes.c_int
+lib.dg_soft_embed_workspace_size_e4m3.argtypes = [_i64, _i64, _i64]
+lib.dg_soft_embed_workspace_size_e4m3.restype = _sz
+lib.dg_soft_embed_e4m3.argtypes = [_p, _i64, _p, _i64, _i64, _i64, _p, _p, _i64, _i64, _i64, _f32, _p, _i64, _p,
+                                   _sz, _p]
+lib.dg_soft_embed_e4m3.restype = ctypes.c_int
+lib.dg_sampler_step_e4m3.argtypes = [_p, _i32, _i32, _i64, _i64, _p, _p, _i64, _i64, _i64, _i64, _i64, _f32, _p,
+                                     _i32, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i64, _p, _sz, _p]
+lib.dg_sampler_step_e4m3.restype = ctypes.c_int
 
 STATUS = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED", 3: "DG_ERR_CUDA", 4: "DG_ERR_TIMEOUT"}
 
@@ -209,6 +219,73 @@ def dg_soft_embed_no_alloc(logits: torch.Tensor, lse: torch.Tensor, vocab_start:
                                       _ptr(W_shard), W_shard.shape[0], _ld(W_shard), d, gamma, _ptr(out), _ld(out),
                                       _stream(stream)), "dg_soft_embed_no_alloc")
     return out
+
+
+def dg_quantize_e4m3(W: torch.Tensor, stream=None) -> tuple:
+    """Per-row E4M3 quantisation of a bf16 table [V, >=d] -> (Q, scale): Q a uint8 [V, d] view
+    of a buffer whose rows are padded to a multiple of 16 bytes, scale fp32 [V]."""
+    if W.dtype not in (torch.bfloat16, torch.int16):
+        raise TypeError("W must hold bfloat16 values")
+    V, d = W.shape
+    ldq = (d + 15) // 16 * 16
+    Q = _new((V, ldq), torch.uint8, W.device)
+    scale = _new(V, torch.float32, W.device)
+    _check(lib.dg_quantize_e4m3(_ptr(W), V, d, _ld(W), _ptr(Q), ldq, _ptr(scale), _stream(stream)),
+           "dg_quantize_e4m3")
+    return Q[:, :d], scale
+
+
+def dg_soft_embed_workspace_size_e4m3(R: int, vocab_len: int, d: int) -> int:
+    return int(lib.dg_soft_embed_workspace_size_e4m3(R, vocab_len, d))
+
+
+def workspace_e4m3(R: int, vocab_len: int, d: int, device) -> torch.Tensor:
+    """A workspace tensor large enough for dg_soft_embed_e4m3 / dg_sampler_step_e4m3."""
+    n = max(16, dg_soft_embed_workspace_size_e4m3(R, vocab_len, d))
+    return torch.empty((n + 15) // 16 * 16, dtype=torch.uint8, device=device)
+
+
+def dg_soft_embed_e4m3(logits: torch.Tensor, lse: torch.Tensor, vocab_start: int, vocab_end: int,
+                       Q_shard: torch.Tensor, scale_shard: torch.Tensor, gamma: float, out: torch.Tensor | None = None,
+                       ws: torch.Tensor | None = None, stream=None, R: int | None = None) -> torch.Tensor:
+    """E = gamma * softmax(logits)[:, s:e] @ (scale * e4m3(Q_shard))[0:e-s] (Q_shard uint8 [rows_pad, d])."""
+    R = logits.shape[0] if R is None else R
+    d = Q_shard.shape[1]
+    if Q_shard.dtype != torch.uint8 or scale_shard.dtype != torch.float32:
+        raise TypeError("Q_shard must be uint8 codes and scale_shard fp32")
+    if out is None:
+        out = _new((R, d), torch.float32, logits.device)
+    if ws is None:
+        ws = workspace_e4m3(R, max(1, vocab_end - vocab_start), d, logits.device)
+    _check(lib.dg_soft_embed_e4m3(_ptr(logits), _ld(logits), _ptr(lse), R, vocab_start, vocab_end, _ptr(Q_shard),
+                                  _ptr(scale_shard), Q_shard.shape[0], _ld(Q_shard), d, gamma, _ptr(out), _ld(out),
+                                  _ptr(ws), ws.numel(), _stream(stream)), "dg_soft_embed_e4m3")
+    return out
+
+
+def dg_sampler_step_e4m3(logits: torch.Tensor, n_req: int, L_c: int, Q: torch.Tensor, scale: torch.Tensor,
+                         gamma: float, budgets: torch.Tensor, min_accept: int = 0, vocab_start: int = 0,
+                         vocab_end: int | None = None, V: int | None = None, out: dict | None = None,
+                         ws: torch.Tensor | None = None, stream=None) -> dict:
+    """dg_sampler_step with the 8-bit table (Q uint8 [rows_pad, d], scale fp32 [rows_pad])."""
+    R = n_req * L_c
+    V = logits.shape[1] if V is None else V
+    vocab_end = V if vocab_end is None else vocab_end
+    d = Q.shape[1]
+    dev = logits.device
+    o = out
+    if o is None:
+        o = {k: _new(R, torch.float32, dev) for k in ("m", "lse", "H", "kappa")}
+        o.update(argmax=_new(R, torch.int32, dev), order=_new(R, torch.int32, dev), mask=_new(R, torch.uint8, dev),
+                 n_accepted=_new(n_req, torch.int32, dev), E=_new((R, d), torch.float32, dev))
+    if ws is None:
+        ws = workspace_e4m3(R, max(1, vocab_end - vocab_start), d, dev)
+    _check(lib.dg_sampler_step_e4m3(_ptr(logits), n_req, L_c, V, _ld(logits), _ptr(Q), _ptr(scale), vocab_start,
+                                    vocab_end, Q.shape[0], _ld(Q), d, gamma, _ptr(budgets), min_accept,
+                                    _ptr(o["m"]), _ptr(o["lse"]), _ptr(o["H"]), _ptr(o["kappa"]), _ptr(o["argmax"]),
+                                    _ptr(o["order"]), _ptr(o["mask"]), _ptr(o["n_accepted"]), _ptr(o["E"]),
+                                    _ld(o["E"]), _ptr(ws), ws.numel(), _stream(stream)), "dg_sampler_step_e4m3")
+    return o
 
 
 def dg_entropy_accept(H: torch.Tensor, kappa: torch.Tensor, n_req: int, L_c: int, budgets: torch.Tensor,

@@ -59,9 +59,10 @@ dg_status check_accept_args(const float *H, const float *kappa, int32_t n_req, i
 
 }  // namespace
 
-dg_status check_embed_args(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t s, int64_t e,
-                           const uint16_t *W, int64_t rows_pad, int64_t ldw, int64_t d, const float *out,
-                           int64_t ldo) {
+dg_status check_table_args(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t s, int64_t e,
+                           const EmbedTable &tab, int64_t rows_pad, int64_t d, const float *out, int64_t ldo) {
+    const void *W = tab.W;
+    const int64_t ldw = tab.ldw;
     if (R < 0 || d < 1) return fail(DG_ERR_INVALID_ARG, "soft embed: need R >= 0 and d >= 1");
     if (s < 0 || e < s)
         return fail(DG_ERR_INVALID_ARG, "soft embed: slice [%lld, %lld) is reversed or negative", (long long)s,
@@ -80,16 +81,29 @@ dg_status check_embed_args(const float *logits, int64_t ldl, const float *lse, i
     if (R > 0 && e > s) {
         if (!aligned16(logits) || (ldl & 3))
             return fail(DG_ERR_UNSUPPORTED, "soft embed: logits must be 16-byte aligned with ldl %% 4 == 0");
-        if (!aligned16(W) || (ldw & 7))
+        if (tab.fmt == kTableBf16 && (!aligned16(W) || (ldw & 7)))
             return fail(DG_ERR_UNSUPPORTED, "soft embed: W must be 16-byte aligned with ldw %% 8 == 0");
+        if (tab.fmt == kTableE4m3) {
+            if (!aligned16(W) || (ldw & 15))
+                return fail(DG_ERR_UNSUPPORTED, "soft embed: Q must be 16-byte aligned with ldq %% 16 == 0");
+            if (!tab.scale) return fail(DG_ERR_INVALID_ARG, "soft embed: scale is NULL");
+            if (reinterpret_cast<uintptr_t>(tab.scale) & 3)
+                return fail(DG_ERR_UNSUPPORTED, "soft embed: scale must be 4-byte aligned");
+        }
     }
     return DG_OK;
+}
+
+dg_status check_embed_args(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t s, int64_t e,
+                           const uint16_t *W, int64_t rows_pad, int64_t ldw, int64_t d, const float *out,
+                           int64_t ldo) {
+    return check_table_args(logits, ldl, lse, R, s, e, EmbedTable{kTableBf16, W, ldw, nullptr}, rows_pad, d, out, ldo);
 }
 
 namespace {
 
 dg_status run_soft_embed(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t s, int64_t e,
-                         const uint16_t *W, int64_t ldw, int64_t d, float gamma, float *out, int64_t ldo,
+                         const EmbedTable &W, int64_t d, float gamma, float *out, int64_t ldo,
                          void *ws, size_t ws_bytes, cudaStream_t stream, StreamHook between = nullptr,
                          void *ctx = nullptr, bool overlap_previous = false,
                          const SinglePassOut *single = nullptr) {
@@ -101,14 +115,15 @@ dg_status run_soft_embed(const float *logits, int64_t ldl, const float *lse, int
     const int sms = device_sm_count();
     if (sms <= 0) return fail(DG_ERR_CUDA, "soft embed: no CUDA device");
     SoftEmbedPlan plan;
-    if (!plan_soft_embed(R, s, e, d, sms, &plan)) return fail(DG_ERR_INVALID_ARG, "soft embed: no plan for shape");
+    if (!plan_soft_embed(R, s, e, d, sms, &plan, W.fmt))
+        return fail(DG_ERR_INVALID_ARG, "soft embed: no plan for shape");
     const size_t need = single ? plan.single_pass_bytes : plan.workspace_bytes;
     if (!ws || ws_bytes < need)
         return fail(DG_ERR_INVALID_ARG, "soft embed: workspace of %zu bytes is below the %zu needed", ws_bytes, need);
     if (!aligned16(ws)) return fail(DG_ERR_UNSUPPORTED, "soft embed: workspace must be 16-byte aligned");
     const char *msg = "soft embed";
     cudaError_t err =
-        launch_soft_embed(logits, ldl, lse, R, s, e, W, ldw, d, gamma, out, ldo, ws, plan, stream, &msg, between, ctx,
+        launch_soft_embed(logits, ldl, lse, R, s, e, W, d, gamma, out, ldo, ws, plan, stream, &msg, between, ctx,
                           overlap_previous, single);
     return err == cudaSuccess ? DG_OK : cuda_fail(err, msg);
 }
@@ -157,6 +172,20 @@ dg_status check_loop_args(int32_t n_req, int32_t L_c, int32_t stable_steps, floa
 }
 
 }  // namespace
+
+// Bytes of workspace for the product and the single-pass step over a slice of vocab_len
+// entries of a table of format fmt (a slice that starts off a multiple of 4 reads up to
+// one more block).
+size_t workspace_size(int64_t R, int64_t vocab_len, int64_t d, int fmt) {
+    if (R <= 0 || vocab_len <= 0 || d <= 0) return 0;
+    const int sms = device_sm_count();
+    SoftEmbedPlan plan, plan2;
+    if (!plan_soft_embed(R, 0, vocab_len, d, sms, &plan, fmt)) return 0;
+    size_t bytes = plan.single_pass_bytes;
+    if (plan_soft_embed(R, 3, vocab_len + 3, d, sms, &plan2, fmt) && plan2.single_pass_bytes > bytes)
+        bytes = plan2.single_pass_bytes;
+    return bytes;
+}
 
 int device_sm_count() {
     int dev = 0;
@@ -244,17 +273,11 @@ dg_status dg_row_stats_sample(const float *logits, int64_t R, int64_t V, int64_t
 }
 
 size_t dg_soft_embed_workspace_size(int64_t R, int64_t vocab_len, int64_t d) {
-    if (R <= 0 || vocab_len <= 0 || d <= 0) return 0;
-    const int sms = device_sm_count();
-    SoftEmbedPlan plan;
-    if (!plan_soft_embed(R, 0, vocab_len, d, sms, &plan)) return 0;
-    // room for the single-pass step (its statistics and redo list after the partial tiles)
-    plan.workspace_bytes = plan.single_pass_bytes;
-    // a slice that starts off a multiple of 4 reads up to one more block
-    SoftEmbedPlan plan2;
-    if (plan_soft_embed(R, 3, vocab_len + 3, d, sms, &plan2) && plan2.workspace_bytes > plan.workspace_bytes)
-        return plan2.workspace_bytes;
-    return plan.workspace_bytes;
+    return workspace_size(R, vocab_len, d, kTableBf16);
+}
+
+size_t dg_soft_embed_workspace_size_e4m3(int64_t R, int64_t vocab_len, int64_t d) {
+    return workspace_size(R, vocab_len, d, kTableE4m3);
 }
 
 dg_status dg_soft_embed(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t vocab_start,
@@ -262,10 +285,36 @@ dg_status dg_soft_embed(const float *logits, int64_t ldl, const float *lse, int6
                         float gamma, float *out, int64_t ldo, void *workspace, size_t workspace_bytes,
                         dg_stream_t stream) {
     t_last_error[0] = 0;
-    dg_status st = check_embed_args(logits, ldl, lse, R, vocab_start, vocab_end, W_shard, rows_pad, ldw, d, out, ldo);
+    const EmbedTable tab{kTableBf16, W_shard, ldw, nullptr};
+    dg_status st = check_table_args(logits, ldl, lse, R, vocab_start, vocab_end, tab, rows_pad, d, out, ldo);
     if (st != DG_OK) return st;
-    return run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W_shard, ldw, d, gamma, out, ldo, workspace,
+    return run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, tab, d, gamma, out, ldo, workspace,
                           workspace_bytes, (cudaStream_t)stream);
+}
+
+dg_status dg_soft_embed_e4m3(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t vocab_start,
+                             int64_t vocab_end, const uint8_t *Q_shard, const float *scale_shard, int64_t rows_pad,
+                             int64_t ldq, int64_t d, float gamma, float *out, int64_t ldo, void *workspace,
+                             size_t workspace_bytes, dg_stream_t stream) {
+    t_last_error[0] = 0;
+    const EmbedTable tab{kTableE4m3, Q_shard, ldq, scale_shard};
+    dg_status st = check_table_args(logits, ldl, lse, R, vocab_start, vocab_end, tab, rows_pad, d, out, ldo);
+    if (st != DG_OK) return st;
+    return run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, tab, d, gamma, out, ldo, workspace,
+                          workspace_bytes, (cudaStream_t)stream);
+}
+
+dg_status dg_quantize_e4m3(const uint16_t *W, int64_t V, int64_t d, int64_t ldw, uint8_t *Q, int64_t ldq,
+                           float *scale, dg_stream_t stream) {
+    t_last_error[0] = 0;
+    if (V < 0 || d < 1 || ldw < d || ldq < d) return fail(DG_ERR_INVALID_ARG, "quantize: need V >= 0, d >= 1, ldw and ldq >= d");
+    if (V == 0) return DG_OK;
+    if (!W || !Q || !scale) return fail(DG_ERR_INVALID_ARG, "quantize: a pointer is NULL");
+    if (V > (1LL << 31) || d > (1LL << 30)) return fail(DG_ERR_UNSUPPORTED, "quantize: a size is too large");
+    if ((reinterpret_cast<uintptr_t>(W) & 3) || (ldw & 1) || (reinterpret_cast<uintptr_t>(Q) & 1) || (ldq & 1))
+        return fail(DG_ERR_UNSUPPORTED, "quantize: W must be 4-byte aligned and Q 2-byte aligned, ldw and ldq even");
+    cudaError_t e = launch_quantize_e4m3(W, V, d, ldw, Q, ldq, scale, (cudaStream_t)stream);
+    return e == cudaSuccess ? DG_OK : cuda_fail(e, "quantize launch");
 }
 
 dg_status dg_entropy_accept(const float *H, const float *kappa, int32_t n_req, int32_t L_c, const float *budgets,
@@ -297,20 +346,21 @@ namespace {
 // The step reads the logits once (the product folds the row statistics) when the slice is
 // the whole vocabulary and the workspace has room; DGSAMP_TWO_PASS=1 forces the statistics
 // pass before the product (for comparisons).
-bool use_single_pass(int64_t R, int64_t V, int64_t vocab_start, int64_t vocab_end, int64_t d, size_t ws_bytes) {
+bool use_single_pass(int64_t R, int64_t V, int64_t vocab_start, int64_t vocab_end, int64_t d, size_t ws_bytes,
+                     int fmt) {
     if (vocab_start != 0 || vocab_end != V) return false;
     if (const char *env = getenv("DGSAMP_TWO_PASS"))
         if (env[0] == '1') return false;
     const int sms = device_sm_count();
     SoftEmbedPlan plan;
-    if (sms <= 0 || !plan_soft_embed(R, vocab_start, vocab_end, d, sms, &plan)) return false;
+    if (sms <= 0 || !plan_soft_embed(R, vocab_start, vocab_end, d, sms, &plan, fmt)) return false;
     return ws_bytes >= plan.single_pass_bytes;
 }
 
 // The fused step, optionally restricted to eligible positions and followed by the
 // loop-state update (a denoising-loop step).
-dg_status run_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, int64_t ldl, const uint16_t *W,
-                   int64_t vocab_start, int64_t vocab_end, int64_t rows_pad, int64_t ldw, int64_t d, float gamma,
+dg_status run_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, int64_t ldl, const EmbedTable &W,
+                   int64_t vocab_start, int64_t vocab_end, int64_t rows_pad, int64_t d, float gamma,
                    const float *budgets, int32_t min_accept, float *m, float *lse, float *H, float *kappa,
                    int32_t *argmax, int32_t *order, uint8_t *mask, int32_t *n_accepted, float *E, int64_t ldo,
                    void *workspace, size_t workspace_bytes, cudaStream_t s, const LoopArgs *loop) {
@@ -322,7 +372,7 @@ dg_status run_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, i
     if (st != DG_OK) return st;
     if (vocab_end > V)
         return fail(DG_ERR_INVALID_ARG, "step: slice end %lld is past V %lld", (long long)vocab_end, (long long)V);
-    st = check_embed_args(logits, ldl, lse, R, vocab_start, vocab_end, W, rows_pad, ldw, d, E, ldo);
+    st = check_table_args(logits, ldl, lse, R, vocab_start, vocab_end, W, rows_pad, d, E, ldo);
     if (st != DG_OK) return st;
     if (R > 0 && (!m || !lse || !H || !kappa || !argmax)) return fail(DG_ERR_INVALID_ARG, "step: a pointer is NULL");
     const bool sampled = loop && loop->temperature != 0.0f;
@@ -337,13 +387,13 @@ dg_status run_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, i
     if (R == 0) return DG_OK;
     const uint8_t *eligible = loop ? loop->eligible : nullptr;
     const bool draw_t1 = sampled && loop->temperature == 1.0f;  // the single pass folds this draw
-    if ((!sampled || draw_t1) && use_single_pass(R, V, vocab_start, vocab_end, d, workspace_bytes)) {
+    if ((!sampled || draw_t1) && use_single_pass(R, V, vocab_start, vocab_end, d, workspace_bytes, W.fmt)) {
         // one read of the logits: the product folds the statistics (and at temperature 1 the
         // draw); the acceptance runs on them after the reduce starts
         AcceptArgs acc{H, kappa, budgets, n_req, L_c, min_accept, order, mask, n_accepted, eligible};
         SinglePassOut so{m, lse, H, kappa, argmax, draw_t1 ? loop->candidate : nullptr,
                          draw_t1 ? loop->seed : 0, draw_t1 ? loop->offset : 0};
-        st = run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, ldw, d, gamma, E, ldo, workspace,
+        st = run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, d, gamma, E, ldo, workspace,
                             workspace_bytes, s, accept_hook, &acc, false, &so);
         if (st != DG_OK || !loop) return st;
         cudaError_t e = launch_loop_update(draw_t1 ? loop->candidate : argmax, argmax, H, mask, n_req, L_c,
@@ -360,13 +410,13 @@ dg_status run_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, i
         e = launch_entropy_accept(H, kappa, n_req, L_c, budgets, min_accept, order, mask, n_accepted, s, false,
                                   eligible);
         if (e != cudaSuccess) return cuda_fail(e, "step: accept launch");
-        st = run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, ldw, d, gamma, E, ldo, workspace,
+        st = run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, d, gamma, E, ldo, workspace,
                             workspace_bytes, s);
     } else {
         AcceptArgs acc{H, kappa, budgets, n_req, L_c, min_accept, order, mask, n_accepted, eligible};
         // the product overlaps the tail of the statistics kernel (its W and logits loads do
         // not depend on it), the acceptance overlaps the product
-        st = run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, ldw, d, gamma, E, ldo, workspace,
+        st = run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, d, gamma, E, ldo, workspace,
                             workspace_bytes, s, accept_hook, &acc, /*overlap_previous=*/true);
     }
     if (st != DG_OK || !loop) return st;
@@ -384,9 +434,21 @@ dg_status dg_sampler_step(const float *logits, int32_t n_req, int32_t L_c, int64
                           float *kappa, int32_t *argmax, int32_t *order, uint8_t *mask, int32_t *n_accepted, float *E,
                           int64_t ldo, void *workspace, size_t workspace_bytes, dg_stream_t stream) {
     t_last_error[0] = 0;
-    return run_step(logits, n_req, L_c, V, ldl, W, vocab_start, vocab_end, rows_pad, ldw, d, gamma, budgets,
-                    min_accept, m, lse, H, kappa, argmax, order, mask, n_accepted, E, ldo, workspace,
-                    workspace_bytes, (cudaStream_t)stream, nullptr);
+    return run_step(logits, n_req, L_c, V, ldl, EmbedTable{kTableBf16, W, ldw, nullptr}, vocab_start, vocab_end,
+                    rows_pad, d, gamma, budgets, min_accept, m, lse, H, kappa, argmax, order, mask, n_accepted, E,
+                    ldo, workspace, workspace_bytes, (cudaStream_t)stream, nullptr);
+}
+
+dg_status dg_sampler_step_e4m3(const float *logits, int32_t n_req, int32_t L_c, int64_t V, int64_t ldl,
+                               const uint8_t *Q, const float *scale, int64_t vocab_start, int64_t vocab_end,
+                               int64_t rows_pad, int64_t ldq, int64_t d, float gamma, const float *budgets,
+                               int32_t min_accept, float *m, float *lse, float *H, float *kappa, int32_t *argmax,
+                               int32_t *order, uint8_t *mask, int32_t *n_accepted, float *E, int64_t ldo,
+                               void *workspace, size_t workspace_bytes, dg_stream_t stream) {
+    t_last_error[0] = 0;
+    return run_step(logits, n_req, L_c, V, ldl, EmbedTable{kTableE4m3, Q, ldq, scale}, vocab_start, vocab_end,
+                    rows_pad, d, gamma, budgets, min_accept, m, lse, H, kappa, argmax, order, mask, n_accepted, E,
+                    ldo, workspace, workspace_bytes, (cudaStream_t)stream, nullptr);
 }
 
 dg_status dg_sampler_loop_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, int64_t ldl,
@@ -401,9 +463,9 @@ dg_status dg_sampler_loop_step(const float *logits, int32_t n_req, int32_t L_c, 
     t_last_error[0] = 0;
     LoopArgs loop{stable_steps, entropy_threshold, step_limit, temperature, seed, offset, candidate, canvas,
                   eligible, prev_argmax, stable, steps, converged};
-    return run_step(logits, n_req, L_c, V, ldl, W, vocab_start, vocab_end, rows_pad, ldw, d, gamma, budgets,
-                    min_accept, m, lse, H, kappa, argmax, order, mask, n_accepted, E, ldo, workspace,
-                    workspace_bytes, (cudaStream_t)stream, &loop);
+    return run_step(logits, n_req, L_c, V, ldl, EmbedTable{kTableBf16, W, ldw, nullptr}, vocab_start, vocab_end,
+                    rows_pad, d, gamma, budgets, min_accept, m, lse, H, kappa, argmax, order, mask, n_accepted, E,
+                    ldo, workspace, workspace_bytes, (cudaStream_t)stream, &loop);
 }
 
 dg_status dg_entropy_accept_eligible(const float *H, const float *kappa, const uint8_t *eligible, int32_t n_req,

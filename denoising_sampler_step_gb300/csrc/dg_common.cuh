@@ -35,6 +35,13 @@ __device__ __forceinline__ void grid_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// max(a, b, c) in one instruction (sm_100 family); NaN inputs are ignored as by fmaxf.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -368,6 +375,73 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_maj
            | ((uint32_t)b_mn_major << 16)  // B major
            | ((uint32_t)(N >> 3) << 17)    // N / 8
            | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// Instruction descriptor of the block-scaled kind::mxf8f6f4 with E4M3 A and B, fp32
+// accumulator and UE8M0 scale factors (one per 32 entries of K).  sfa_id / sfb_id: the byte
+// of the 32-bit scale-factor word that this MMA uses.
+__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N, int a_mn_major, int b_mn_major, int sfa_id,
+                                                       int sfb_id) {
+    return ((uint32_t)sfb_id << 4)         // B scale-factor byte
+           | (0u << 7)                     // A format: E4M3
+           | (0u << 10)                    // B format: E4M3
+           | ((uint32_t)a_mn_major << 15)  // A major
+           | ((uint32_t)b_mn_major << 16)  // B major
+           | ((uint32_t)(N >> 3) << 17)    // N / 8
+           | (1u << 23)                    // scale-factor format: UE8M0
+           | ((uint32_t)(M >> 4) << 24)    // M / 16
+           | ((uint32_t)sfa_id << 29);     // A scale-factor byte
+}
+
+// D[tmem] (+)= (A * 2^sfa) (B * 2^sfb), block-scaled E4M3 x E4M3, one CTA.  The scale factors
+// live in TMEM (M = 128: row m's word at lane m, column sfa + m / 32).
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Copies 32 rows x 16 bytes of shared memory (the matrix described by sdesc) into four TMEM
+// columns of every 32-lane quarter (the same data in each quarter).  Ordered before the
+// tcgen05.mma the same thread issues after it.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// As tmem_cp_32x128b_warpx4 for 128 rows x 16 bytes: row m's four words go to lane m.
+__device__ __forceinline__ void tmem_cp_128x128b(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from this CTA's
+// shared memory to shared memory of a CTA of the cluster (dst, bar: shared::cluster
+// addresses); the bytes complete a transaction on that CTA's barrier.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "r"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Two fp32 values as E4M3 codes (round to nearest even, magnitudes past 448 saturate):
+// lo in the low byte.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// The value of one E4M3 code (exact; 0x7F and 0xFF are NaN).
+__device__ __forceinline__ float e4m3_to_f32(uint8_t code) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)code));
+    float f;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"((uint16_t)(h2 & 0xFFFFu)));
+    return f;
 }
 
 }  // namespace dg

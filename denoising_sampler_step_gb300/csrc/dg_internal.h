@@ -30,8 +30,20 @@ cudaError_t launch_sum_partials(const float *const *partials, int32_t T, int64_t
                                 float gamma, float *out, int64_t ldo, cudaStream_t stream);
 cudaError_t launch_fill_zero(float *out, int64_t R, int64_t d, int64_t ldo, cudaStream_t stream);
 
+// The embedding table of the product: bf16 entries, or E4M3 codes with one fp32 scale per
+// row (W[v, j] = scale[v] * e4m3(Q[v, j])).
+enum { kTableBf16 = 0, kTableE4m3 = 1 };
+struct EmbedTable {
+    int fmt;              // kTableBf16 (W: uint16 bit patterns) or kTableE4m3 (W: uint8 codes)
+    const void *W;        // [rows, ldw] entries; row j is vocabulary entry vocab_start + j
+    int64_t ldw;          // entries per row
+    const float *scale;   // kTableE4m3: [rows] row scales; else NULL
+};
+
 // Plan of the split-K soft-embed product for one shape on one device.
 struct SoftEmbedPlan {
+    int fmt;           // the table format it was made for
+    int bn;            // output columns per tile
     int64_t k_begin;   // first vocabulary column read (vocab_start rounded down to a multiple of 4)
     int64_t nkb;       // vocabulary blocks of the product
     int m_tiles, n_tiles, splits;
@@ -47,7 +59,7 @@ struct SinglePassOut {
     uint64_t seed, offset;  // then -ln p of the drawn token
 };
 bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t d, int num_sms,
-                     SoftEmbedPlan *plan);
+                     SoftEmbedPlan *plan, int fmt = kTableBf16);
 // Workspace bytes a plan needs with a given number of splits.
 size_t soft_embed_workspace_bytes(const SoftEmbedPlan &plan, int splits);
 // Queues the product, then `between(ctx, stream)` if given (work that may overlap the
@@ -57,13 +69,18 @@ size_t soft_embed_workspace_bytes(const SoftEmbedPlan &plan, int splits);
 // only after that kernel has completed.  On failure *msg names the step.
 typedef cudaError_t (*StreamHook)(void *ctx, cudaStream_t stream);
 cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse, int64_t R,
-                              int64_t vocab_start, int64_t vocab_end, const uint16_t *W, int64_t ldw,
+                              int64_t vocab_start, int64_t vocab_end, const EmbedTable &W,
                               int64_t d, float gamma, float *out, int64_t ldo, void *workspace,
                               const SoftEmbedPlan &plan, cudaStream_t stream, const char **msg,
                               StreamHook between = nullptr, void *ctx = nullptr, bool overlap_previous = false,
                               const SinglePassOut *single = nullptr);
 
 int device_sm_count();
+size_t workspace_size(int64_t R, int64_t vocab_len, int64_t d, int fmt);
+
+// Per-row E4M3 quantisation of a bf16 table (quantize.cu).
+cudaError_t launch_quantize_e4m3(const uint16_t *W, int64_t V, int64_t d, int64_t ldw, uint8_t *Q, int64_t ldq,
+                                 float *scale, cudaStream_t stream);
 
 // Gumbel-max candidates and their tempered log-probabilities (row_sample.cu).
 cudaError_t launch_row_sample(const float *logits, int64_t R, int64_t V, int64_t ldl, float temperature,

@@ -46,7 +46,6 @@ namespace dg {
 namespace {
 
 constexpr int BM = 128;          // rows per CTA (TMEM lanes)
-constexpr int BN = 512;          // output columns per cluster tile (two MMAs of N = 256)
 constexpr int BK = 32;           // vocabulary entries per block
 #ifndef DG_SE_LSTAGES
 #define DG_SE_LSTAGES 4
@@ -70,7 +69,10 @@ constexpr int ROWS_PER_LANE = 128 / (32 * GROUP_WARPS);
 // shared-memory work of the other warps on its scheduler (warp % 4), so: warp 4 issues the
 // MMAs and warp 8 the logits TMA (scheduler 0, no producers); warp 11 issues the W TMA
 // (scheduler 3, two producers); warps 1-3, 5-7, 9 and 10 produce A.  Every warp takes part
-// in the epilogue.
+// in the epilogue.  The 8-bit table's producers have about three times the work per entry
+// and set the pace, so there each producer group spans all four schedulers: warps 4-7 and
+// 8-11 produce A, warp 0 issues the MMAs, warp 1 the logits TMA, warp 2 the W TMA and warp 3
+// stages the row scales.
 constexpr int THREADS = 384;
 constexpr int TMEM_COLS = 512;
 constexpr uint16_t kPairMask = 0x3;
@@ -84,19 +86,60 @@ constexpr bool kPair = DG_SE_PAIR != 0;
 constexpr int kCtasPerUnit = 2;
 
 constexpr int L_BYTES = BM * BK * 4;      // logits tile, rows of 128 B (128-byte swizzle)
-constexpr int W_BOX_BYTES = BK * 64 * 2;  // one TMA box: 32 rows x 64 columns
-constexpr int W_HALF_BYTES = 4 * W_BOX_BYTES;
-constexpr int W_BYTES = BK * BN * 2;      // a block's whole W tile: 8 boxes
-constexpr int W_SLOT = kPair ? W_BYTES / 2 : W_BYTES;  // the part of it one CTA holds
-constexpr int W_ATOMS = W_SLOT / W_BOX_BYTES;          // 64-column atoms per CTA and block
-constexpr int A_BYTES = BM * BK * 2;      // bf16 probabilities, rows of 64 B (64-byte swizzle)
+constexpr int W_BOX_BYTES = BK * 128;     // one TMA box: 32 rows x 128 bytes (64 bf16 or 128 e4m3 columns)
+// A operand, rows of 64 B (64-byte swizzle): 32 bf16 probabilities, or for the 8-bit table
+// the 32 e4m3 high parts then the 32 low parts
+constexpr int A_BYTES = BM * 64;
 constexpr int L_RING = LSTAGES * L_BYTES;
-constexpr int W_RING = STAGES * W_SLOT;
-constexpr int A_RING = STAGES * A_BYTES;
-constexpr int SMEM_BYTES = L_RING + W_RING + A_RING + 1024 /*align*/ + 256 /*barriers*/;
 
-static_assert(L_BYTES % 1024 == 0 && W_SLOT % 1024 == 0 && A_BYTES % 1024 == 0, "1 KiB alignment");
-static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+// The embedding table's format.  kBf16: bf16 entries, kind::f16 MMAs (bf16 x bf16).
+// kE4m3: E4M3 codes with one fp32 scale per vocabulary row; the producers fold the row scale
+// into the probabilities and split each into two E4M3 parts with a power-of-two scale per
+// (row, block), and the MMAs are block-scaled kind::mxf8f6f4 (e4m3 x e4m3).
+enum { kBf16 = kTableBf16, kE4m3 = kTableE4m3 };
+template <int F>
+struct Fmt;
+template <>
+struct Fmt<kBf16> {
+    static constexpr int BN = 512;                // output columns per cluster tile: halves of 256 + 256
+    static constexpr int WST = STAGES;            // W ring depth (the A ring's: one index for both)
+    static constexpr int AST = STAGES;            // A ring depth
+    static constexpr int W_SLOT = (kPair ? BK * BN : BK * BN * 2);  // the part of a block's W tile one CTA holds
+    static constexpr int SF_BYTES = 0;
+};
+template <>
+struct Fmt<kE4m3> {
+    // 24 TMEM columns hold the per-slot A scales and 8 the B scales, so the accumulator keeps
+    // 480: halves of 256 + 224
+    static constexpr int BN = 480;
+    static constexpr int N1 = 224;                // N of the second half
+    // A block's time is bounded by each ring's round trip over its depth: half-size W slots
+    // let the W ring run six deep, and the A ring's slots alternate between the cluster's two
+    // CTAs, so six of them let each producer group store its next block while both CTAs'
+    // MMAs of its previous one are still in flight
+    static constexpr int WST = 6;
+    static constexpr int AST = 6;
+    static constexpr int W_SLOT = 4 * W_BOX_BYTES;  // four 128-column atoms (the last one's final 32 unused)
+    // per-stage A scale matrices (128 rows x 16 bytes), the B scale chunk, then the staged
+    // row scales (one slot per logits stage: 32 normalised scales and their exponent)
+    static constexpr int SF_STAGE = 2048;
+    static constexpr int SF_BYTES = AST * SF_STAGE + 512 + LSTAGES * 160;
+};
+constexpr int S_SLOT = 160;
+// TMEM columns of the scale factors (8-bit table): four per A slot (lane m's word in column
+// m / 32), then eight for the B scales (two 128-column groups of N)
+constexpr uint32_t kSfaCol = 480, kSfbCol = 504;
+template <int F>
+constexpr int smem_bytes() {
+    return L_RING + Fmt<F>::WST * Fmt<F>::W_SLOT + Fmt<F>::AST * A_BYTES + Fmt<F>::SF_BYTES + 1024 /*align*/ +
+           512 /*barriers*/;
+}
+
+static_assert(L_BYTES % 1024 == 0 && Fmt<kBf16>::W_SLOT % 1024 == 0 && Fmt<kE4m3>::W_SLOT % 1024 == 0 &&
+                  A_BYTES % 1024 == 0,
+              "1 KiB alignment");
+static_assert(smem_bytes<kBf16>() <= 232448 && smem_bytes<kE4m3>() <= 232448, "shared memory per CTA");
+static_assert(kSfaCol + 4 * Fmt<kE4m3>::AST <= kSfbCol && kSfbCol + 8 <= TMEM_COLS, "scale-factor columns");
 // each producer group keeps to every other slot of the logits and A rings
 // a group waits only for phases its own blocks need, and no slot can run two phases ahead
 // of its waiter, so the depths need not be multiples of the group count
@@ -114,7 +157,9 @@ struct Params {
     int n_full;          // n-tiles of full width (two halves)
     int tail_halves;     // 1 if the last n-tile is 256 wide or less, else 0
     int splits, tail_splits;
-    int w3d;             // 1: the W map is 3-D (64 columns x rows x 64-column atoms), one load per CTA and block
+    int w3d;             // 1: the W map is 3-D (atom columns x rows x atoms), one load per CTA and block
+    // 8-bit table: the fp32 scale of vocabulary entry v is w_scale[v - vocab_start]
+    const float *w_scale;
     // single pass (no lse yet): each split's probabilities are taken against a reference
     // c per row, exp(l - c), and the column-tile-0 clusters also fold the row statistics
     int fused;
@@ -142,28 +187,57 @@ constexpr float kRefBelow = 64.0f;
 // The reference is the largest of a split's first kRefEntries logits.
 constexpr int kRefEntries = 32;
 
+// The largest of 32 values (NaN ignored), as a tree of three-input maxima: 16 instructions
+// and five levels of dependency.
+__device__ __forceinline__ float max32(const float (&v)[32]) {
+    float a[11];
+#pragma unroll
+    for (int t = 0; t < 10; ++t) a[t] = max3f(v[3 * t], v[3 * t + 1], v[3 * t + 2]);
+    a[10] = fmaxf(v[30], v[31]);
+    const float b0 = max3f(a[0], a[1], a[2]), b1 = max3f(a[3], a[4], a[5]), b2 = max3f(a[6], a[7], a[8]);
+    const float b3 = fmaxf(a[9], a[10]);
+    return fmaxf(max3f(b0, b1, b2), b3);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
 
+template <int F>
 __global__ void __launch_bounds__(THREADS, 1)
     soft_embed_kernel(const __grid_constant__ CUtensorMap tm_logits, const __grid_constant__ CUtensorMap tm_w,
                       const Params p) {
+    static_assert(F == kBf16 || !kPair, "the 8-bit table runs in multicast mode");
+    constexpr int BN = Fmt<F>::BN;
+    constexpr int W_SLOT = Fmt<F>::W_SLOT;
+    constexpr int WST = Fmt<F>::WST;
+    constexpr int AST = Fmt<F>::AST;
+    constexpr bool kSplitRings = F == kE4m3;  // W released on its own barriers (8-bit table)
+    constexpr int W_RING = WST * W_SLOT;
+    constexpr int A_RING = AST * A_BYTES;
+    static_assert(F == kBf16 || (AST % 2 == 0 && ROWS_PER_LANE == 1),
+                  "8-bit table: A slots alternate between the two CTAs; a warp copies 32 whole rows");
+    static_assert(AST >= PGROUPS, "an A slot per producer group at least");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *l_ring = smem;
     uint8_t *w_ring = smem + L_RING;
     uint8_t *a_ring = smem + L_RING + W_RING;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L_RING + W_RING + A_RING);
+    uint8_t *sf_ring = smem + L_RING + W_RING + A_RING;  // 8-bit table: per-stage A scale chunks, B scale chunk
+    uint8_t *sfb_chunk = sf_ring + AST * 2048;           // 8-bit table: the B scale chunk
+    uint8_t *s_ring = sfb_chunk + 512;                   // 8-bit table: staged row scales
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L_RING + W_RING + A_RING + Fmt<F>::SF_BYTES);
     uint64_t *full_l = bars;                   // logits tile landed
     uint64_t *empty_l = full_l + LSTAGES;      // the producer warps have read it
     uint64_t *full_w = empty_l + LSTAGES;      // W tile landed (both halves)
-    uint64_t *full_a = full_w + STAGES;        // A operand written by a producer group
-    uint64_t *empty = full_a + STAGES;         // both CTAs' MMAs done with the W + A slot
-    uint64_t *acc_full = empty + STAGES;       // accumulator complete
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
+    uint64_t *full_a = full_w + WST;           // A operand written by a producer group
+    uint64_t *empty = full_a + AST;            // MMAs done with the A slot (and, one ring, the W slot: both CTAs')
+    uint64_t *acc_full = empty + AST;          // accumulator complete
+    uint64_t *full_s = acc_full + 1;           // 8-bit table: a block's row scales staged
+    uint64_t *empty_w = full_s + LSTAGES;      // 8-bit table: this CTA's MMAs done with the W slot
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(empty_w + WST);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     // Overlap with the neighbours on the stream (programmatic dependent launch): this grid
@@ -181,8 +255,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int pair = blockIdx.x / kCtasPerUnit;
     const int m_pairs = p.m_tiles / kCtasPerUnit;
     const int full_pairs = p.splits * m_pairs * p.n_full;
-    int nt, mp, j, S, halves;
-    if (pair < full_pairs) {
+    int nt, mp, j, S, halves, mt;
+    // 8-bit table: a cluster is one row block and two adjacent column tiles (CTA c takes
+    // tile 2 ntp + c; n_tiles is even, a last odd tile's partner lies past d and reads zeros)
+    const int ntp_count = p.n_tiles / 2;
+    int ntp = 0;
+    if (F == kE4m3) {
+        ntp = pair % ntp_count;
+        mt = (pair / ntp_count) % p.m_tiles;
+        j = pair / (ntp_count * p.m_tiles);
+        S = p.splits;
+        nt = 2 * ntp + (int)rank;
+        halves = nt < p.n_full ? 2 : 1;
+        mp = 0;
+    } else if (pair < full_pairs) {
         nt = pair % p.n_full;
         mp = (pair / p.n_full) % m_pairs;
         j = pair / (p.n_full * m_pairs);
@@ -196,7 +282,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         S = p.tail_splits;
         halves = 1;
     }
-    const int mt = kCtasPerUnit * mp + (int)rank;
+    if (F != kE4m3) mt = kCtasPerUnit * mp + (int)rank;
+    // 8-bit table: CTA c produces (loads the logits of, stages the scales of, computes the A
+    // operand of) the blocks i with i % 2 == c and copies each A operand to its partner
+    const int i0 = F == kE4m3 ? (int)rank : 0, di = F == kE4m3 ? 2 : 1;
     const int64_t kb0 = (int64_t)j * p.nkb / S;
     const int64_t kb1 = (int64_t)(j + 1) * p.nkb / S;
     const int nkb = (int)(kb1 - kb0);
@@ -207,20 +296,34 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int s = 0; s < LSTAGES; ++s) {
             mbar_init(smem_u32(&full_l[s]), 1);
             mbar_init(smem_u32(&empty_l[s]), GROUP_WARPS);
+            mbar_init(smem_u32(&full_s[s]), 1);
         }
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < AST; ++s) {
             // pair: the even CTA's full_w counts both CTAs' W bytes, its full_a both CTAs'
             // producer groups; one commit reaches each CTA's empty.  Multicast: each CTA's
-            // full_w counts the whole tile, and both CTAs' commits reach each empty.
-            mbar_init(smem_u32(&full_w[s]), 1);
-            mbar_init(smem_u32(&full_a[s]), kPair ? 2 * GROUP_WARPS : GROUP_WARPS);
+            // full_w counts the whole tile, and both CTAs' commits reach each empty.  8-bit
+            // table: an A slot this CTA fills counts its producer group's warps, one its
+            // partner fills counts the MMA thread's arrival (with the copied bytes); both
+            // CTAs' commits reach each empty (the slot is read in both)
+            int fa = kPair ? 2 * GROUP_WARPS : GROUP_WARPS;
+            if (F == kE4m3) fa = (s % 2 == (int)rank) ? GROUP_WARPS : 1;
+            mbar_init(smem_u32(&full_a[s]), fa);
             mbar_init(smem_u32(&empty[s]), kPair ? 1 : kCtasPerUnit);
+        }
+        for (int s = 0; s < WST; ++s) {
+            mbar_init(smem_u32(&full_w[s]), 1);
+            mbar_init(smem_u32(&empty_w[s]), 1);  // 8-bit table: this CTA's own W tile
         }
         mbar_init(smem_u32(acc_full), 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tm_logits);
         prefetch_tmap(&tm_w);
+    }
+    if constexpr (F == kE4m3) {
+        // the B scale chunk: every byte 127, a factor of 1 (the table's row scales go into A)
+        if (threadIdx.x < 128) reinterpret_cast<uint32_t *>(sfb_chunk)[threadIdx.x] = 0x7F7F7F7Fu;
+        fence_proxy_async_smem();
     }
     __syncwarp();
     if (warp == 0) {
@@ -259,14 +362,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         my_gidx[q] = 0x7fffffff;
     }
 
-    if (warp == 11) {
+    constexpr int kWarpW = F == kE4m3 ? 2 : 11, kWarpL = F == kE4m3 ? 1 : 8, kWarpMma = F == kE4m3 ? 0 : 4;
+    constexpr int kWarpStage = 3;
+    const bool producer = F == kE4m3 ? warp >= 4 : ((warp & 3) != 0 && warp < 11);
+    if (warp == kWarpW) {
         // ------------------------------------------------------------ W TMA
         // pair: this CTA's 128 columns of each 256-column half (atoms 4h + 2 rank, +1), the
         //   bytes counted on the even CTA's full_w, which that CTA arms for both;
         // multicast: this CTA's half of the boxes, delivered to both CTAs.
         if (lane == 0) {
-            int issued[STAGES];
-            for (int s = 0; s < STAGES; ++s) issued[s] = 0;
+            int issued[WST];
+            for (int s = 0; s < WST; ++s) issued[s] = 0;
             const int nbox = 4 * halves / kCtasPerUnit;  // multicast: this CTA's share of the 4 * halves boxes
             const uint64_t w_policy = l2_policy_evict_first();
             // 3-D map: one load per CTA (pair: per 256-column half) fetches W_ATOMS or 2
@@ -274,22 +380,31 @@ __global__ void __launch_bounds__(THREADS, 1)
             // zero-filled and are not used
             const bool w3d = p.w3d;
             const uint32_t w_bytes = kPair ? (uint32_t)halves * 2 * 2 * W_BOX_BYTES
-                                           : (w3d ? (uint32_t)W_BYTES : (uint32_t)halves * W_HALF_BYTES);
+                                           : (w3d ? (uint32_t)W_SLOT : (uint32_t)halves * W_SLOT / 2);
             const uint32_t lead = map_to_cta(smem_u32(&full_w[0]), 0);  // the even CTA's full_w[0]
             for (int i = 0; i < nkb; ++i) {
-                const int s = i % STAGES;
-                const uint32_t u = (uint32_t)(i / STAGES);
-                if (i == STAGES) {  // the first round of W loads is out
+                const int s = i % WST;
+                const uint32_t u = (uint32_t)(i / WST);
+                if (i == WST) {  // the first round of W loads is out
                     grid_dependency_wait();
                     grid_launch_dependents();
                 }
-                if (u > 0 && !mbar_wait(smem_u32(&empty[s]), (u - 1) & 1, abort_flag)) {
+                if (u > 0 && !mbar_wait(smem_u32(kSplitRings ? &empty_w[s] : &empty[s]), (u - 1) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
                 const int64_t k = p.k_begin + (kb0 + i) * BK;
                 const uint32_t bw = smem_u32(&full_w[s]);
                 const int wy = (int)(k - p.vocab_start);
+                if constexpr (F == kE4m3) {
+                    // this CTA's own tile: four 128-column atoms (two for a half-width tile)
+                    mbar_arrive_expect_tx(bw, (uint32_t)halves * 2 * W_BOX_BYTES);
+                    for (int a = 0; a < 2 * halves; ++a)
+                        tma_load_2d_hint(smem_u32(w_ring + s * W_SLOT + a * W_BOX_BYTES), &tm_w, bw, col0 + 128 * a, wy,
+                                         w_policy);
+                    issued[s] = (int)u + 1;
+                    continue;
+                }
                 if (kPair) {
                     if (rank == 0) mbar_arrive_expect_tx(bw, w_bytes);
                     const uint32_t bl = lead + 8u * (uint32_t)s;
@@ -317,7 +432,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 issued[s] = (int)u + 1;
             }
-            if (nkb <= STAGES) {
+            if (nkb <= WST) {
                 grid_dependency_wait();
                 grid_launch_dependents();
             }
@@ -325,18 +440,19 @@ __global__ void __launch_bounds__(THREADS, 1)
             // counts both CTAs' loads, and the odd CTA leaves only after the final cluster
             // barrier, which the even CTA reaches after this drain)
             if (!ok && (!kPair || rank == 0))
-                for (int s = 0; s < STAGES; ++s)
+                for (int s = 0; s < WST; ++s)
                     if (issued[s] > 0) drain_wait(smem_u32(&full_w[s]), (issued[s] - 1) & 1);
         }
-    } else if (warp == 8) {
+    } else if (warp == kWarpL) {
         // ------------------------------------------------------------ logits TMA
         if (lane == 0) {
             int issued[LSTAGES];
             for (int s = 0; s < LSTAGES; ++s) issued[s] = 0;
-            for (int i = 0; i < nkb; ++i) {
-                const int s = i % LSTAGES;
-                const uint32_t u = (uint32_t)(i / LSTAGES);
-                if (i == LSTAGES) {  // the first round of logits loads is out
+            int nl = 0;  // logits tiles this CTA loads
+            for (int li = 0, i = i0; i < nkb; ++li, i += di, ++nl) {
+                const int s = li % LSTAGES;
+                const uint32_t u = (uint32_t)(li / LSTAGES);
+                if (li == LSTAGES) {  // the first round of logits loads is out
                     grid_dependency_wait();
                     grid_launch_dependents();
                 }
@@ -350,7 +466,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tma_load_2d(smem_u32(l_ring + s * L_BYTES), &tm_logits, bl, (int)k, row0);
                 issued[s] = (int)u + 1;
             }
-            if (nkb <= LSTAGES) {
+            if (nl <= LSTAGES) {
                 grid_dependency_wait();
                 grid_launch_dependents();
             }
@@ -358,7 +474,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int s = 0; s < LSTAGES; ++s)
                     if (issued[s] > 0) drain_wait(smem_u32(&full_l[s]), (issued[s] - 1) & 1);
         }
-    } else if (warp == 4) {
+    } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
         // (pair: the even CTA's thread issues for both CTAs; the odd CTA's has no role)
         if (lane == 0 && (!kPair || rank == 0)) {
@@ -374,6 +490,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t b_desc0 = smem_desc(smem_u32(w_ring), W_BOX_BYTES, 1024, 2);
             // a CTA's part of one 256-column half: 4 atoms (multicast) or 2 (pair)
             constexpr uint64_t kA_K16 = 32 >> 4, kB_K16 = 2048 >> 4, kB_HALF = (W_SLOT / 2) >> 4;
+            // 8-bit table: the B scale factors (all 1) go into their columns once; per block the
+            // stage's A scale chunk goes into its four columns ahead of the block's MMAs (the copy
+            // and the MMAs run in issue order; the commit covers both)
+            if constexpr (F == kE4m3) {
+                const uint64_t sfb_desc = smem_desc(smem_u32(sfb_chunk), 16, 128, 0);
+                for (int q = 0; q < 8; q += 4) tmem_cp_32x128b_warpx4(tmem_base + kSfbCol + q, sfb_desc);
+            }
             bool issued_any = false;
             // a block's two tiles are tested together (their latencies overlap), and right
             // after the previous block's MMAs are issued, ahead of its commit; the bounded
@@ -389,17 +512,36 @@ __global__ void __launch_bounds__(THREADS, 1)
             bool a_in = nkb > 0 && test(smem_u32(&full_a[0]), 0);
             bool w_in = nkb > 0 && test(smem_u32(&full_w[0]), 0);
             for (int i = 0; i < nkb; ++i) {
-                const int s = i % STAGES;
-                const uint32_t ph = (uint32_t)(i / STAGES) & 1;
-                if (!(a_in && w_in) && (!wait(smem_u32(&full_a[s]), ph) || !wait(smem_u32(&full_w[s]), ph))) {
+                const int s = i % AST, sw = i % WST;
+                const uint32_t ph = (uint32_t)(i / AST) & 1, phw = (uint32_t)(i / WST) & 1;
+                // 8-bit table: a slot the partner fills completes on its copies' bytes and this
+                // arrival (the bytes may land first)
+                if (F == kE4m3 && (i & 1) != (int)rank)
+                    mbar_arrive_expect_tx(smem_u32(&full_a[s]), GROUP_WARPS * (2048u + 512u));
+                if (!(a_in && w_in) && (!wait(smem_u32(&full_a[s]), ph) || !wait(smem_u32(&full_w[sw]), phw))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint64_t ad = a_desc0 + (uint64_t)((s * A_BYTES) >> 4);
-                const uint64_t bd = b_desc0 + (uint64_t)((s * W_SLOT) >> 4);
+                const uint64_t bd = b_desc0 + (uint64_t)((sw * W_SLOT) >> 4);
                 const uint32_t acc = i > 0 ? 1u : 0u;
-                if (kPair) {
+                if constexpr (F == kE4m3) {
+                    // high parts, then low parts (the word's four bytes are the same scale)
+                    constexpr uint32_t id_h0 = idesc_mxf8_e4m3(BM, 256, 0, 1, 0, 0);
+                    constexpr uint32_t id_h1 = idesc_mxf8_e4m3(BM, Fmt<F>::N1, 0, 1, 0, 0);
+                    constexpr uint32_t id_l0 = idesc_mxf8_e4m3(BM, 256, 0, 1, 1, 0);
+                    constexpr uint32_t id_l1 = idesc_mxf8_e4m3(BM, Fmt<F>::N1, 0, 1, 1, 0);
+                    constexpr uint64_t kB_HALF8 = (2 * W_BOX_BYTES) >> 4;
+                    // the A slot's TMEM scale slot: free, as the A slot is, once both CTAs' MMAs of
+                    // the block before in this slot are done (its producers waited for that)
+                    const uint32_t sfa = tmem_base + kSfaCol + 4 * (uint32_t)s, sfb = tmem_base + kSfbCol;
+                    tmem_cp_128x128b(sfa, smem_desc(smem_u32(sf_ring + s * Fmt<kE4m3>::SF_STAGE), 16, 128, 0));
+                    umma_mxf8(tmem_base, ad, bd, id_h0, sfa, sfb, acc);
+                    if (halves == 2) umma_mxf8(tmem_base + 256, ad, bd + kB_HALF8, id_h1, sfa, sfb, acc);
+                    umma_mxf8(tmem_base, ad + kA_K16, bd, id_l0, sfa, sfb, 1u);
+                    if (halves == 2) umma_mxf8(tmem_base + 256, ad + kA_K16, bd + kB_HALF8, id_l1, sfa, sfb, 1u);
+                } else if (kPair) {
                     umma_bf16_pair(tmem_base, ad, bd, idesc, acc);
                     if (halves == 2) umma_bf16_pair(tmem_base + 256, ad, bd + kB_HALF, idesc, acc);
                     umma_bf16_pair(tmem_base, ad + kA_K16, bd + kB_K16, idesc, 1u);
@@ -411,16 +553,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (halves == 2) umma_bf16(tmem_base + 256, ad + kA_K16, bd + kB_HALF + kB_K16, idesc, 1u);
                 }
                 if (i + 1 < nkb) {
-                    const int s1 = (i + 1) % STAGES;
-                    const uint32_t ph1 = (uint32_t)((i + 1) / STAGES) & 1;
-                    a_in = test(smem_u32(&full_a[s1]), ph1);
-                    w_in = test(smem_u32(&full_w[s1]), ph1);
+                    a_in = test(smem_u32(&full_a[(i + 1) % AST]), (uint32_t)((i + 1) / AST) & 1);
+                    w_in = test(smem_u32(&full_w[(i + 1) % WST]), (uint32_t)((i + 1) / WST) & 1);
                 }
                 // one commit releases the W and A slots once both CTAs' MMAs have read them
-                if (kPair)
-                    umma_commit_pair_multicast(smem_u32(&empty[s]), kPairMask);
-                else
+                // (8-bit table: the W slot, this CTA's own, on this commit; the A slot, read
+                // in both CTAs, on both)
+                if (kSplitRings) {
+                    umma_commit(smem_u32(&empty_w[sw]));
                     umma_commit_multicast(smem_u32(&empty[s]), kPairMask);
+                } else if (kPair) {
+                    umma_commit_pair_multicast(smem_u32(&empty[s]), kPairMask);
+                } else {
+                    umma_commit_multicast(smem_u32(&empty[s]), kPairMask);
+                }
                 issued_any = true;
             }
             if (kPair)
@@ -429,12 +575,60 @@ __global__ void __launch_bounds__(THREADS, 1)
                 umma_commit(smem_u32(acc_full));
             if (*abort_flag && issued_any) drain_wait(smem_u32(acc_full), 0);
         }
-    } else if ((warp & 3) != 0 && warp < 11) {
+    } else if (F == kE4m3 && warp == kWarpStage) {
+        // ------------------------------------------------------------ row-scale staging
+        // (8-bit table) per block: lane t holds the row scale of entry k + t (0 outside the
+        // slice); the warp writes u = scale 2^-E with E chosen so that the largest u lies in
+        // [0.5, 1), and E.  A block whose scales are all zero (or below 2^-126) stages zeros.
+        // The loads run kScalePrefetch blocks ahead of the stores, so that their latency
+        // overlaps (the slots themselves follow the logits ring).
+        constexpr int kScalePrefetch = 8;
+        const int nl = nkb > i0 ? (nkb - i0 + di - 1) / di : 0;  // this CTA's blocks
+        auto load_scale = [&](int li) {
+            const int64_t v = p.k_begin + (kb0 + i0 + (int64_t)di * li) * BK + lane;
+            return (li < nl && v >= p.vocab_start && v < p.vocab_end) ? __ldg(p.w_scale + (v - p.vocab_start)) : 0.0f;
+        };
+        float pre[kScalePrefetch];
+#pragma unroll
+        for (int jj = 0; jj < kScalePrefetch; ++jj) pre[jj] = load_scale(jj);
+        for (int l0 = 0; l0 < nl && ok; l0 += kScalePrefetch) {
+#pragma unroll
+            for (int jj = 0; jj < kScalePrefetch; ++jj) {
+                const int li = l0 + jj;
+                if (li >= nl) break;
+                const float sv = pre[jj];
+                pre[jj] = load_scale(li + kScalePrefetch);
+                const int sl = li % LSTAGES;
+                const uint32_t ul = (uint32_t)(li / LSTAGES);
+                // the slot is free once the producers of this CTA's block li - LSTAGES have read it
+                if (ul > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty_l[sl]), (ul - 1) & 1, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                float mx = sv;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                const uint32_t eb = __float_as_uint(mx) >> 23;  // biased exponent of the largest scale (>= 0)
+                float uu = 0.0f;
+                int E = 0;
+                if (eb >= 1u && eb <= 252u) {
+                    uu = sv * __uint_as_float((253u - eb) << 23);  // times 2^(126 - eb)
+                    E = (int)eb - 126;
+                }
+                float *slot = reinterpret_cast<float *>(s_ring + sl * S_SLOT);
+                slot[lane] = uu;
+                if (lane == 0) reinterpret_cast<int *>(slot)[32] = E;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&full_s[sl]));
+            }
+        }
+    } else if (producer) {
         // ------------------------------------------------------------ A producers
         // PGROUPS groups take the blocks in turn, so a warp has PGROUPS block times for the
         // dependent chain of one block (barrier waits, stores, proxy fence, arrival); a
         // warp converts ROWS_PER_LANE * 32 rows x all 32 entries of its group's block
-        const int pw = 3 * (warp >> 2) + (warp & 3) - 1;  // producer 0..7 (warps 1-3, 5-7, 9, 10)
+        // producer 0..7 (warps 1-3, 5-7, 9, 10; 8-bit table: warps 4-11)
+        const int pw = F == kE4m3 ? warp - 4 : 3 * (warp >> 2) + (warp & 3) - 1;
         const int grp = pw / GROUP_WARPS;
         const int wig = pw % GROUP_WARPS;
         my_grp = grp;
@@ -479,13 +673,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                 neg_lse2[q] = row < p.R ? -p.lse[row] * kLog2e : -INFINITY;
             }
         }
-        for (int i = grp; i < nkb; i += PGROUPS) {
-            const int sl = i % LSTAGES;
-            const int s = i % STAGES;
-            const uint32_t ul = (uint32_t)(i / LSTAGES);
-            const uint32_t u = (uint32_t)(i / STAGES);
-            // every lane waits (acquire), the warp decides together
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_l[sl]), ul & 1, abort_flag))) {
+        // the group's blocks: this CTA's li-th block is i = i0 + di li (all blocks, or for the
+        // 8-bit table every other); logits and staged scales by li, the A ring by i
+        for (int li = grp, i = i0 + di * grp; i < nkb; li += PGROUPS, i += di * PGROUPS) {
+            const int sl = li % LSTAGES;
+            const int s = i % AST;
+            const uint32_t ul = (uint32_t)(li / LSTAGES);
+            const uint32_t u = (uint32_t)(i / AST);
+            // every lane waits (acquire), the warp decides together; the 8-bit table's staged
+            // row scales share the logits slot's index and phase
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_l[sl]), ul & 1, abort_flag) &&
+                                             (F != kE4m3 || mbar_wait(smem_u32(&full_s[sl]), ul & 1, abort_flag)))) {
                 ok = false;
                 break;
             }
@@ -493,42 +691,150 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int64_t k = p.k_begin + (kb0 + i) * BK;
             const bool edge = (k < p.vocab_start) || (k + BK > p.vocab_end);
             uint32_t packed[ROWS_PER_LANE][16];
-            const bool fold = p.fused && (i / PGROUPS) % p.n_tiles == nt;
-            float4 vk[ROWS_PER_LANE][8];  // the logits and their exponentials, kept for the fold
-            float ek[ROWS_PER_LANE][32];
-#pragma unroll
-            for (int q = 0; q < ROWS_PER_LANE; ++q) {
-                const int r = rr[q];
-                // all eight 16-byte loads first, then the exponentials, then the packing
-                float4 v[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {  // 16-byte chunk of the 128-byte row
-                    v[c] = *reinterpret_cast<const float4 *>(lt + r * 128 + ((c ^ (r & 7)) << 4));
-                    vk[q][c] = v[c];
-                }
-                float e[32];
+            uint32_t sf_word[ROWS_PER_LANE];  // 8-bit table: the (row, block) scale bytes
+            // every block is folded once per row block: (bf16) by column tile (i / PGROUPS) %
+            // n_tiles, (8-bit table) by the CTA producing it in cluster (i / 4) % (n_tiles / 2)
+            const bool fold = p.fused && (F == kE4m3 ? (i >> 2) % ntp_count == ntp : (i / PGROUPS) % p.n_tiles == nt);
+            // 8-bit table: the block's normalised row scales u (0 outside the slice) and their
+            // exponent E (row scale = u 2^E), staged by warp 0
+            float us[F == kE4m3 ? 32 : 1];
+            int ue = 0;
+            if constexpr (F == kE4m3) {
+                const float *slot = reinterpret_cast<const float *>(s_ring + sl * S_SLOT);
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    e[4 * c + 0] = ex2_approx(fmaf(v[c].x, kLog2e, neg_lse2[q]));
-                    e[4 * c + 1] = ex2_approx(fmaf(v[c].y, kLog2e, neg_lse2[q]));
-                    e[4 * c + 2] = ex2_approx(fmaf(v[c].z, kLog2e, neg_lse2[q]));
-                    e[4 * c + 3] = ex2_approx(fmaf(v[c].w, kLog2e, neg_lse2[q]));
+                    const float4 f = *reinterpret_cast<const float4 *>(slot + 4 * c);
+                    us[4 * c + 0] = f.x;
+                    us[4 * c + 1] = f.y;
+                    us[4 * c + 2] = f.z;
+                    us[4 * c + 3] = f.w;
                 }
-                if (edge) {  // a block that straddles an end of the slice (warp-uniform, rare)
+                ue = reinterpret_cast<const int *>(slot)[32];
+            }
+            float4 vk[ROWS_PER_LANE][8];  // the logits and their exponentials, kept for the fold
+            float ek[ROWS_PER_LANE][32];
+            float bmq[ROWS_PER_LANE], kfq[ROWS_PER_LANE];  // 8-bit table: block maximum and k (below)
+            // every 16-byte load of the block's rows first; the logits slot (and the staged scales)
+            // go back to the TMA at once, so that the next tile's load overlaps this block's work
 #pragma unroll
-                    for (int t = 0; t < 32; ++t)
-                        if (k + t < p.vocab_start || k + t >= p.vocab_end) e[t] = 0.f;
+            for (int q = 0; q < ROWS_PER_LANE; ++q)
+#pragma unroll
+                for (int c = 0; c < 8; ++c)  // 16-byte chunk of the 128-byte row
+                    vk[q][c] = *reinterpret_cast<const float4 *>(lt + rr[q] * 128 + ((c ^ (rr[q] & 7)) << 4));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&empty_l[sl]));
+#pragma unroll
+            for (int q = 0; q < ROWS_PER_LANE; ++q) {
+                // the exponentials, then the packing
+                float4 v[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) v[c] = vk[q][c];
+                float e[32];
+                if constexpr (F == kE4m3) {
+                    // Each block's exponentials are taken against its own maximum bm: with
+                    // k = floor((bm - c) log2 e), e'' = 2^((l - c) log2 e - k + 7) =
+                    // exp(l - c) 2^(7 - k) lies in (0, 256), its maximum in [128, 256).  With the
+                    // staged scales x = e'' u < 256, and p(l) scale = x 2^(k - 7 + E): the
+                    // block's power-of-two scale 2^S, S = k - 7 + E, goes to the MMA (scale byte
+                    // 127 + S).  x is split as x = h + l (h = x rounded to E4M3 through fp16, l =
+                    // the rest, exact in fp16, rounded to E4M3 too): both MMAs take 2^S, and
+                    // together h and l carry about eight significant bits, as bf16 does (a rest
+                    // below E4M3's normal range, 2^-6, only occurs for x < 2^-2, under 2^-9 of
+                    // the block maximum, and keeps an absolute error under 2^-10).
+                    float xb[32];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        xb[4 * c + 0] = v[c].x;
+                        xb[4 * c + 1] = v[c].y;
+                        xb[4 * c + 2] = v[c].z;
+                        xb[4 * c + 3] = v[c].w;
+                    }
+                    if (edge) {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            if (k + t < p.vocab_start || k + t >= p.vocab_end) xb[t] = -INFINITY;
+                    }
+                    const float bm = max32(xb);
+                    // a block with nothing finite keeps k = 0: its exponentials are all 0
+                    const float kf = bm > -INFINITY ? floorf(fmaf(bm, kLog2e, neg_lse2[q])) : 0.0f;
+                    const float off = neg_lse2[q] - kf + 7.0f;
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) e[t] = ex2_approx(fmaf(xb[t], kLog2e, off));
+                    bmq[q] = bm;
+                    kfq[q] = kf;
+                    int S = (int)kf - 7 + ue;
+                    // the largest x: when the largest exponential and the largest scale sit on
+                    // different entries it can fall far below 128; then x goes up by 2^j (and
+                    // S down) so that it lies in [128, 256) again
+                    float x[32];
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) x[t] = e[t] * us[t];
+                    const float xm = max32(x);
+                    bool live = bm > -INFINITY && xm > 0.0f;
+                    if (live && xm < 32.0f) {
+                        const int eb = (int)(__float_as_uint(xm) >> 23);  // xm > 0
+                        const int j = 134 - eb;                           // 2^j xm in [128, 256)
+                        if (eb >= 7) {
+                            const float up = __uint_as_float((uint32_t)(127 + j) << 23);
+#pragma unroll
+                            for (int t = 0; t < 32; ++t) x[t] *= up;
+                            S -= j;
+                        } else {
+                            live = false;  // below 2^-120 of the reference
+                        }
+                    }
+                    if (live && S >= -127 && S <= 127) {
+#pragma unroll
+                        for (int w = 0; w < 8; ++w) {
+                            uint32_t hw = 0, lw = 0;
+#pragma unroll
+                            for (int h2 = 0; h2 < 2; ++h2) {
+                                const float x0 = x[4 * w + 2 * h2];
+                                const float x1 = x[4 * w + 2 * h2 + 1];
+                                uint32_t xh, hh, rh;
+                                uint16_t h8, l8;
+                                asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(xh) : "f"(x1), "f"(x0));
+                                asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h8) : "r"(xh));
+                                asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hh) : "h"(h8));
+                                // the rest, exact in fp16 (under half a spacing of h)
+                                asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(rh) : "r"(xh), "r"(hh));
+                                asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l8) : "r"(rh));
+                                hw |= (uint32_t)h8 << (16 * h2);
+                                lw |= (uint32_t)l8 << (16 * h2);
+                            }
+                            packed[q][w] = hw;
+                            packed[q][8 + w] = lw;
+                        }
+                        sf_word[q] = (uint32_t)(127 + S) * 0x01010101u;
+                    } else {
+                        // nothing in the slice, or a block far under the reference: zero
+#pragma unroll
+                        for (int w = 0; w < 16; ++w) packed[q][w] = 0u;
+                        sf_word[q] = 0x7F7F7F7Fu;
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        e[4 * c + 0] = ex2_approx(fmaf(v[c].x, kLog2e, neg_lse2[q]));
+                        e[4 * c + 1] = ex2_approx(fmaf(v[c].y, kLog2e, neg_lse2[q]));
+                        e[4 * c + 2] = ex2_approx(fmaf(v[c].z, kLog2e, neg_lse2[q]));
+                        e[4 * c + 3] = ex2_approx(fmaf(v[c].w, kLog2e, neg_lse2[q]));
+                    }
+                    if (edge) {  // a block that straddles an end of the slice (warp-uniform, rare)
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            if (k + t < p.vocab_start || k + t >= p.vocab_end) e[t] = 0.f;
+                    }
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) packed[q][t] = pack_bf16x2(e[2 * t], e[2 * t + 1]);
+                    sf_word[q] = 0u;
+                    bmq[q] = 0.0f;
+                    kfq[q] = 0.0f;
                 }
-
-#pragma unroll
-                for (int t = 0; t < 16; ++t) packed[q][t] = pack_bf16x2(e[2 * t], e[2 * t + 1]);
 #pragma unroll
                 for (int t = 0; t < 32; ++t) ek[q][t] = e[t];
             }
-            // the logits slot is free once the group's warps have read it
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&empty_l[sl]));
-            // the A slot is free once both CTAs' MMAs of its previous round are done
+            // the A slot is free once the MMAs of its previous round are done
             if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[s]), (u - 1) & 1, abort_flag))) {
                 ok = false;
                 break;
@@ -543,6 +849,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                                                packed[q][4 * c8 + 3]);
                     *reinterpret_cast<uint4 *>(at + r * 64 + ((c8 ^ ((r >> 1) & 3)) << 4)) = w;
                 }
+                // the scale word of row r: word r / 32 of 16-byte row r, which the MMA thread
+                // copies into TMEM lane r (the MMA reads lane r's scale from column r / 32)
+                if constexpr (F == kE4m3)
+                    reinterpret_cast<uint32_t *>(sf_ring + s * Fmt<kE4m3>::SF_STAGE)[4 * r + (r >> 5)] = sf_word[q];
             }
             fence_proxy_async_smem();
             __syncwarp();  // every lane's A stores (and proxy fence) before the arrival
@@ -551,6 +861,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                     mbar_arrive_remote(map_to_cta(smem_u32(&full_a[s]), 0));
                 else
                     mbar_arrive(smem_u32(&full_a[s]));
+                if constexpr (F == kE4m3) {
+                    // the warp's 32 A rows (2 KiB) and 32 scale rows (512 B) to the same slot of
+                    // the partner CTA, completing on its full_a
+                    const uint32_t peer = rank ^ 1u;
+                    const uint32_t pbar = map_to_cta(smem_u32(&full_a[s]), peer);
+                    const uint32_t a_src = smem_u32(a_ring + s * A_BYTES + wig * 2048);
+                    const uint32_t f_src = smem_u32(sf_ring + s * Fmt<kE4m3>::SF_STAGE + wig * 512);
+                    bulk_copy_to_cluster(map_to_cta(a_src, peer), a_src, 2048u, pbar);
+                    bulk_copy_to_cluster(map_to_cta(f_src, peer), f_src, 512u, pbar);
+                }
             }
             if (fold) {
 #pragma unroll
@@ -574,12 +894,40 @@ __global__ void __launch_bounds__(THREADS, 1)
                         for (int t = 0; t < 32; ++t)
                             if (k + t < p.vocab_start || k + t >= p.vocab_end) xb[t] = -INFINITY;
                     }
-                    float bm = xb[0];
+                    float bm = bmq[q];  // the 8-bit path's block maximum
+                    if constexpr (F == kBf16) {
+                        bm = xb[0];
 #pragma unroll
-                    for (int t = 1; t < 32; ++t) bm = fmaxf(bm, xb[t]);
+                        for (int t = 1; t < 32; ++t) bm = fmaxf(bm, xb[t]);
+                    }
                     rowstate::RowState blk = rowstate::empty_row_state();
                     float glm[2] = {-INFINITY, -INFINITY};  // the two groups' log-masses
-                    if (bm > -INFINITY && fabsf(bm - my_ref[q]) <= 60.0f) {
+                    if (F == kE4m3 && bm > -INFINITY) {
+                        // the 8-bit path's exponentials e'' = exp(l - bm) 2^(7 + f), f the
+                        // fraction (bm - c) log2 e - k: the summary takes them times 2^-(7 + f)
+                        int ja = 31;
+#pragma unroll
+                        for (int t = 31; t >= 0; --t)
+                            if (xb[t] == bm) ja = t;
+                        float se = 0.0f, sd = 0.0f;
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) {
+                            se += t == ja ? 0.0f : ek[q][t];
+                            sd = fmaf(ek[q][t], fmaxf(xb[t] - bm, -FLT_MAX), sd);
+                        }
+                        const float f = fmaf(bm, kLog2e, neg_lse2[q]) - kfq[q];
+                        const float inv = ex2_approx(-7.0f - f);
+                        blk = rowstate::RowState{bm, (int)(k + ja), se * inv, sd * inv};
+                        if (p.draw) {  // c + ln(sum of exp(l - c)) = c + ln 2 (log2(sum e'') + k - 7)
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                float gsum = 0.0f;
+#pragma unroll
+                                for (int t = 0; t < 16; ++t) gsum += ek[q][16 * h + t];
+                                glm[h] = my_ref[q] + philox::kLn2 * (__log2f(gsum) + kfq[q] - 7.0f);
+                            }
+                        }
+                    } else if (F == kBf16 && bm > -INFINITY && fabsf(bm - my_ref[q]) <= 60.0f) {
                         int ja = 31;
 #pragma unroll
                         for (int t = 31; t >= 0; --t)
@@ -601,7 +949,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 glm[h] = my_ref[q] + philox::kLn2 * __log2f(gsum);
                             }
                         }
-                    } else if (bm > -INFINITY) {
+                    } else if (F == kBf16 && bm > -INFINITY) {
                     // the statistics kernel's fold over this row's 32 entries, in two halves
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
@@ -665,8 +1013,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int q = 0; q < ROWS_PER_LANE; ++q) rowstate::merge(my_st[q], my_st16[q]);
     }
 
-    // threads without a role in the main loop (warp 0, warp 11 and lanes 1-31 of the
-    // single-thread roles) and roles whose wait came last
+    // threads without a role in the main loop (lanes 1-31 of the single-thread roles, and
+    // the bf16 kernel's warp 0) and roles whose wait came last
     grid_dependency_wait();
     grid_launch_dependents();
     // ---------------------------------------------------------------- epilogue (all warps)
@@ -679,7 +1027,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int r = quarter * 32 + lane;
         float4 *dst = reinterpret_cast<float4 *>(p.ws) +
                       ((int64_t)(j * p.m_tiles + mt) * p.n_tiles + nt) * (BN / 4) * BM;
-        const int nch = halves * 8;  // 32-column chunks of this tile
+        const int nch = halves == 2 ? BN / 32 : 8;  // 32-column chunks of this tile
         const int c_lo = third * nch / 3, c_hi = (third + 1) * nch / 3;
         // tcgen05.ld is warp-collective: the warp goes on only if every lane got here cleanly
         bool have_acc = false;
@@ -762,6 +1110,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // E[i, c] = gamma * sum over the splits of column c's tile, in split order.
 // Single pass: each split's partial is scaled by f[split][row] = exp(c - lse) first.
+template <int BN>
 __global__ void splitk_reduce_kernel(const float4 *__restrict__ ws, const Params p, int d, float gamma,
                                      float *__restrict__ out, int64_t ldo, int vec_out,
                                      const float *__restrict__ scale) {
@@ -937,9 +1286,11 @@ __global__ void __launch_bounds__(256)
 // their partial, sum over the split of exp(l - lse) W[v, :], is recomputed on the CUDA
 // cores (fp32, vocabulary in order) for every column tile, and the scale set to 1.  One CTA
 // per listed pair, in turn; nothing to do when the list is empty.
+template <int F>
 __global__ void __launch_bounds__(256)
-    single_pass_redo_kernel(const Params p, const uint16_t *__restrict__ W, int64_t ldw, int d,
+    single_pass_redo_kernel(const Params p, const void *__restrict__ Wv, int64_t ldw, int d,
                             const float *__restrict__ lse) {
+    constexpr int BN = Fmt<F>::BN;
     grid_dependency_wait();  // the list is complete once the statistics kernel is
     grid_launch_dependents();
     const int n = p.counts[0];
@@ -959,10 +1310,18 @@ __global__ void __launch_bounds__(256)
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             for (int64_t v = v0; v < v1; ++v) {
                 const float pv = ex2_approx(fmaf(lrow[v], kLog2e, -l2));
-                const uint16_t *wr = W + (v - p.vocab_start) * ldw + 4 * c4;
+                if constexpr (F == kE4m3) {
+                    const uint8_t *wr = static_cast<const uint8_t *>(Wv) + (v - p.vocab_start) * ldw + 4 * c4;
+                    const float ps = pv * p.w_scale[v - p.vocab_start];
 #pragma unroll
-                for (int t = 0; t < 4; ++t)
-                    if (4 * c4 + t < d) acc[t] = fmaf(pv, __uint_as_float((uint32_t)wr[t] << 16), acc[t]);
+                    for (int t = 0; t < 4; ++t)
+                        if (4 * c4 + t < d) acc[t] = fmaf(ps, e4m3_to_f32(wr[t]), acc[t]);
+                } else {
+                    const uint16_t *wr = static_cast<const uint16_t *>(Wv) + (v - p.vocab_start) * ldw + 4 * c4;
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        if (4 * c4 + t < d) acc[t] = fmaf(pv, __uint_as_float((uint32_t)wr[t] << 16), acc[t]);
+                }
             }
             const int c = 4 * c4;
             const int nt = c / BN, cg = (c % BN) / 4;
@@ -987,12 +1346,15 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
-// Column tiling of d: n_full tiles of 512 columns, then (if tail) one of <= 256.
-void column_tiles(int64_t d, int *n_tiles, int *n_full, int *tail) {
-    const int nt = (int)((d + BN - 1) / BN);
-    const int64_t last = d - (int64_t)(nt - 1) * BN;
+int tile_width(int fmt) { return fmt == kE4m3 ? Fmt<kE4m3>::BN : Fmt<kBf16>::BN; }
+
+// Column tiling of d: n_full tiles of bn columns (two MMA halves), then (if tail) one of
+// <= 256 (the first half alone).
+void column_tiles(int64_t d, int bn, int *n_tiles, int *n_full, int *tail) {
+    const int nt = (int)((d + bn - 1) / bn);
+    const int64_t last = d - (int64_t)(nt - 1) * bn;
     *n_tiles = nt;
-    *tail = last <= BN / 2 ? 1 : 0;
+    *tail = last <= 256 ? 1 : 0;
     *n_full = nt - *tail;
 }
 
@@ -1003,7 +1365,7 @@ int tail_splits_of(int splits, int tail) { return tail ? splits : 0; }
 }  // namespace
 
 size_t soft_embed_workspace_bytes(const SoftEmbedPlan &plan, int splits) {
-    return (size_t)splits * (size_t)plan.m_tiles * (size_t)plan.n_tiles * BM * BN * sizeof(float);
+    return (size_t)splits * (size_t)plan.m_tiles * (size_t)plan.n_tiles * BM * (size_t)plan.bn * sizeof(float);
 }
 
 // The single pass's extra workspace, after the partial tiles: references / scales
@@ -1015,15 +1377,26 @@ size_t single_pass_extra_bytes(const SoftEmbedPlan &plan, int64_t R) {
 }
 
 bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t d, int num_sms,
-                     SoftEmbedPlan *plan) {
+                     SoftEmbedPlan *plan, int fmt) {
     if (R <= 0 || d <= 0 || vocab_end <= vocab_start || vocab_start < 0 || num_sms < 2) return false;
+    if (fmt != kBf16 && fmt != kE4m3) return false;
     SoftEmbedPlan pl;
+    pl.fmt = fmt;
+    pl.bn = tile_width(fmt);
     pl.k_begin = vocab_start & ~int64_t(3);
     pl.nkb = (vocab_end - pl.k_begin + BK - 1) / BK;
-    const int64_t m_pairs = (R + kCtasPerUnit * BM - 1) / (kCtasPerUnit * BM);  // row blocks per unit
+    int64_t m_pairs = (R + kCtasPerUnit * BM - 1) / (kCtasPerUnit * BM);  // row blocks per unit
     pl.m_tiles = (int)(kCtasPerUnit * m_pairs);
     int n_full, tail;
-    column_tiles(d, &pl.n_tiles, &n_full, &tail);
+    column_tiles(d, pl.bn, &pl.n_tiles, &n_full, &tail);
+    if (fmt == kE4m3) {
+        // clusters of one row block and two column tiles: every row block, an even tile count
+        pl.m_tiles = (int)((R + BM - 1) / BM);
+        pl.n_tiles += pl.n_tiles & 1;
+        m_pairs = pl.m_tiles;
+        n_full = pl.n_tiles / 2;
+        tail = 0;
+    }
     // choose the vocabulary splits that finish soonest: whole waves of clusters times
     // the largest per-cluster work (vocabulary blocks x 256-column halves)
     const int64_t clusters = num_sms / kCtasPerUnit;
@@ -1059,10 +1432,16 @@ bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t 
 }
 
 cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t vocab_start,
-                              int64_t vocab_end, const uint16_t *W, int64_t ldw, int64_t d, float gamma, float *out,
+                              int64_t vocab_end, const EmbedTable &tab, int64_t d, float gamma, float *out,
                               int64_t ldo, void *workspace, const SoftEmbedPlan &plan, cudaStream_t stream,
                               const char **msg, StreamHook between, void *ctx, bool overlap_previous,
                               const SinglePassOut *single) {
+    if (tab.fmt != plan.fmt) {
+        *msg = "soft embed: the plan was made for another table format";
+        return cudaErrorInvalidValue;
+    }
+    const bool e4 = tab.fmt == kE4m3;
+    const int64_t ldw = tab.ldw;
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
     if (!encode) {
         *msg = "cuTensorMapEncodeTiled is not available from the driver";
@@ -1081,11 +1460,24 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
             return cudaErrorInvalidValue;
         }
     }
-    // W: a 3-D view (64 columns of an atom, rows, atoms 128 bytes apart) when every atom's
-    // 64 columns lie inside the row pitch, else 2-D boxes of 64 columns
+    // W (bf16): a 3-D view (64 columns of an atom, rows, atoms 128 bytes apart) when every
+    // atom's 64 columns lie inside the row pitch, else 2-D boxes of 64 columns.
+    // W (E4M3): 2-D boxes of 128 columns.
     int w3d = 0;
     const int64_t atoms = (d + 63) / 64;
-    if (atoms * 64 <= ldw) {
+    const uint16_t *W = static_cast<const uint16_t *>(tab.W);
+    if (e4) {
+        const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)(vocab_end - vocab_start)};
+        const cuuint64_t strides[1] = {(cuuint64_t)ldw};
+        const cuuint32_t box[2] = {128, BK};
+        const cuuint32_t estr[2] = {1, 1};
+        if (encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(tab.W), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+            *msg = "tensor map of the 8-bit embedding shard could not be encoded";
+            return cudaErrorInvalidValue;
+        }
+    } else if (atoms * 64 <= ldw) {
         const cuuint64_t dims[3] = {64, (cuuint64_t)(vocab_end - vocab_start), (cuuint64_t)atoms};
         const cuuint64_t strides[2] = {(cuuint64_t)ldw * 2, 128};
         const cuuint32_t box[3] = {64, BK, kPair ? 2u : 4u};
@@ -1094,7 +1486,7 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     }
-    if (!w3d) {
+    if (!e4 && !w3d) {
         const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)(vocab_end - vocab_start)};
         const cuuint64_t strides[1] = {(cuuint64_t)ldw * 2};
         const cuuint32_t box[2] = {64, BK};
@@ -1109,14 +1501,19 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(soft_embed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        attr_err = cudaFuncSetAttribute(soft_embed_kernel<kBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        smem_bytes<kBf16>());
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(soft_embed_kernel<kE4m3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            smem_bytes<kE4m3>());
     });
     if (attr_err != cudaSuccess) {
         *msg = "could not raise the shared-memory limit of the soft-embed kernel";
         return attr_err;
     }
     int n_tiles, n_full, tail;
-    column_tiles(d, &n_tiles, &n_full, &tail);
+    column_tiles(d, plan.bn, &n_tiles, &n_full, &tail);
+    if (e4) n_tiles = plan.n_tiles;  // rounded up to pairs of column tiles
     Params p;
     p.lse = lse;
     p.ws = static_cast<float *>(workspace);
@@ -1132,6 +1529,7 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     p.splits = plan.splits;
     p.tail_splits = tail_splits_of(plan.splits, tail);
     p.w3d = w3d;
+    p.w_scale = e4 ? tab.scale : nullptr;
     p.fused = single ? 1 : 0;
     p.logits = logits;
     p.ldl = ldl;
@@ -1165,12 +1563,13 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
         }
         overlap_previous = false;  // nothing before it to wait for
     }
-    const int64_t pairs = (int64_t)(plan.m_tiles / kCtasPerUnit) * (n_full * (int64_t)p.splits + p.tail_splits);
+    const int64_t pairs = e4 ? (int64_t)plan.m_tiles * (n_tiles / 2) * p.splits
+                             : (int64_t)(plan.m_tiles / kCtasPerUnit) * (n_full * (int64_t)p.splits + p.tail_splits);
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(kCtasPerUnit * pairs), 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.dynamicSmemBytes = e4 ? smem_bytes<kE4m3>() : smem_bytes<kBf16>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1181,7 +1580,8 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     attr[1].val.programmaticStreamSerializationAllowed = overlap_previous ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, soft_embed_kernel, tm_l, tm_w, p);
+    cudaError_t e = e4 ? cudaLaunchKernelEx(&cfg, soft_embed_kernel<kE4m3>, tm_l, tm_w, p)
+                       : cudaLaunchKernelEx(&cfg, soft_embed_kernel<kBf16>, tm_l, tm_w, p);
     if (e != cudaSuccess) {
         *msg = "soft-embed kernel launch failed";
         return e;
@@ -1206,7 +1606,10 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
                                single->argmax);
         if (e == cudaSuccess) {
             cudaLaunchConfig_t c2 = small_cfg(64);
-            e = cudaLaunchKernelEx(&c2, single_pass_redo_kernel, p, W, ldw, (int)d, (const float *)single->lse);
+            e = e4 ? cudaLaunchKernelEx(&c2, single_pass_redo_kernel<kE4m3>, p, tab.W, ldw, (int)d,
+                                        (const float *)single->lse)
+                   : cudaLaunchKernelEx(&c2, single_pass_redo_kernel<kBf16>, p, tab.W, ldw, (int)d,
+                                        (const float *)single->lse);
         }
         if (e != cudaSuccess) {
             *msg = "single pass: statistics or redo launch failed";
@@ -1231,11 +1634,17 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     if (blocks < 1) blocks = 1;
     if (single) {
         cudaLaunchConfig_t c3 = small_cfg((unsigned)blocks);
-        e = cudaLaunchKernelEx(&c3, splitk_reduce_kernel, static_cast<const float4 *>(workspace), p, (int)d, gamma,
-                               out, ldo, vec_out, (const float *)p.ref);
+        e = e4 ? cudaLaunchKernelEx(&c3, splitk_reduce_kernel<Fmt<kE4m3>::BN>, static_cast<const float4 *>(workspace),
+                                    p, (int)d, gamma, out, ldo, vec_out, (const float *)p.ref)
+               : cudaLaunchKernelEx(&c3, splitk_reduce_kernel<Fmt<kBf16>::BN>, static_cast<const float4 *>(workspace),
+                                    p, (int)d, gamma, out, ldo, vec_out, (const float *)p.ref);
     } else {
-        splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const float4 *>(workspace), p, (int)d,
-                                                                   gamma, out, ldo, vec_out, nullptr);
+        if (e4)
+            splitk_reduce_kernel<Fmt<kE4m3>::BN><<<(unsigned)blocks, 256, 0, stream>>>(
+                static_cast<const float4 *>(workspace), p, (int)d, gamma, out, ldo, vec_out, nullptr);
+        else
+            splitk_reduce_kernel<Fmt<kBf16>::BN><<<(unsigned)blocks, 256, 0, stream>>>(
+                static_cast<const float4 *>(workspace), p, (int)d, gamma, out, ldo, vec_out, nullptr);
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) {

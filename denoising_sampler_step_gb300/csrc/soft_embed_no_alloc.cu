@@ -90,7 +90,8 @@ extern "C" dg_status dg_soft_embed_no_alloc(const float *logits, int64_t ldl, co
     st = scratch_address(&scratch);
     if (st != DG_OK) return st;
     const char *msg = "soft embed (no alloc)";
-    cudaError_t e = launch_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W_shard, ldw, d, gamma, out, ldo,
-                                      scratch, plan, s, &msg);
+    const EmbedTable tab{kTableBf16, W_shard, ldw, nullptr};
+    cudaError_t e = launch_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, tab, d, gamma, out, ldo, scratch,
+                                      plan, s, &msg);
     return e == cudaSuccess ? DG_OK : cuda_fail(e, msg);
 }

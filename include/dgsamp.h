@@ -379,6 +379,66 @@ dg_status dg_sampler_loop_step(const float *logits, int32_t n_req, int32_t L_c, 
                                int32_t *stable, int32_t *steps, uint8_t *converged,
                                void *workspace, size_t workspace_bytes, dg_stream_t stream);
 
+/*
+ * ---- 8-bit embedding table (E4M3 codes with per-row scales) ----
+ *
+ * The pages run quantised checkpoints ([P2] "量子化チェックポイント": FP8 weights; [P1]
+ * "Running it": INT8) but do not say the embedding table is quantised or how.  These calls
+ * take the table as E4M3 codes Q [rows, ldq] uint8 (the OCP 8-bit format: 1 sign bit, 4
+ * exponent bits with bias 7, 3 mantissa bits, subnormals, no infinity, 0x7F/0xFF NaN, 448
+ * the largest finite magnitude) and one fp32 scale per row: W[v, j] = scale[v] e4m3(Q[v, j]).
+ * The table is half the bytes of bf16, and the product streams it.
+ */
+
+/*
+ * Per-row quantisation of a bf16 table W [V, ldw] (bit patterns) into Q [V, ldq] and
+ * scale [V]: scale[v] = amax_v / 448 (fp32, correctly rounded) with amax_v the largest
+ * |W[v, j]|; Q[v, j] = the E4M3 code nearest to W[v, j] / scale[v] (correctly rounded fp32
+ * quotient), ties to the even code, magnitudes past 448 saturated.  A zero row gets scale 0
+ * and codes 0.  Entries must be finite.  W 4-byte aligned, Q 2-byte aligned, ldw and ldq
+ * even (else DG_ERR_UNSUPPORTED); the caller owns all three buffers.
+ */
+dg_status dg_quantize_e4m3(const uint16_t *W, int64_t V, int64_t d, int64_t ldw, uint8_t *Q,
+                           int64_t ldq, float *scale, dg_stream_t stream);
+
+/*
+ * Bytes of device workspace dg_soft_embed_e4m3 and dg_sampler_step_e4m3 need (the tile
+ * width differs from the bf16 product's).  0 for an invalid shape or without a device.
+ */
+size_t dg_soft_embed_workspace_size_e4m3(int64_t R, int64_t vocab_len, int64_t d);
+
+/*
+ * dg_soft_embed with the 8-bit table: E = gamma * sum over the slice of
+ * exp(l - lse) scale[v] e4m3(Q[v - s, :]).
+ *   Q_shard      [rows_pad, ldq] E4M3 codes, row j = vocabulary entry vocab_start + j
+ *   scale_shard  [rows_pad] fp32 row scales (rows past the slice are never read)
+ * The probabilities are not cast to 8 bits: each p scale[v] is held as two E4M3 parts
+ * (high and low, about eight significant bits together, as bf16) with a power-of-two scale
+ * per row and 32-entry block, and the product runs as block-scaled E4M3 MMAs with fp32
+ * accumulation and the same fixed-order split-K reduce.  Requires Q 16-byte aligned with
+ * ldq % 16 == 0 and scale 4-byte aligned (else DG_ERR_UNSUPPORTED); other rules as
+ * dg_soft_embed, with the workspace from dg_soft_embed_workspace_size_e4m3.
+ */
+dg_status dg_soft_embed_e4m3(const float *logits, int64_t ldl, const float *lse, int64_t R,
+                             int64_t vocab_start, int64_t vocab_end, const uint8_t *Q_shard,
+                             const float *scale_shard, int64_t rows_pad, int64_t ldq, int64_t d,
+                             float gamma, float *out, int64_t ldo, void *workspace,
+                             size_t workspace_bytes, dg_stream_t stream);
+
+/*
+ * dg_sampler_step with the 8-bit table (Q, scale, ldq as dg_soft_embed_e4m3).  With the
+ * whole vocabulary and a workspace of dg_soft_embed_workspace_size_e4m3 bytes it is the
+ * single-pass step (the same references, redo rule and statistics as dg_sampler_step).
+ */
+dg_status dg_sampler_step_e4m3(const float *logits, int32_t n_req, int32_t L_c, int64_t V,
+                               int64_t ldl, const uint8_t *Q, const float *scale,
+                               int64_t vocab_start, int64_t vocab_end, int64_t rows_pad,
+                               int64_t ldq, int64_t d, float gamma, const float *budgets,
+                               int32_t min_accept, float *m, float *lse, float *H, float *kappa,
+                               int32_t *argmax, int32_t *order, uint8_t *mask,
+                               int32_t *n_accepted, float *E, int64_t ldo, void *workspace,
+                               size_t workspace_bytes, dg_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

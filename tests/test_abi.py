@@ -191,3 +191,28 @@ def test_sharded_statistics_reject_bad_arguments(lib):
     assert L.dg_row_stats_combine(None, 2, 4, p, p, p, p, p, None) == 1
     assert L.dg_row_stats_combine(ctypes.c_void_p(264), 2, 4, p, p, p, p, p, None) == 2
     assert L.dg_row_stats_combine(None, 2, 0, None, None, None, None, None, None) == 0
+
+
+def test_e4m3_calls_reject_bad_arguments(lib):
+    L = lib.lib
+    p = ctypes.c_void_p(256)
+    # quantiser: sizes, NULL pointers, alignment
+    assert L.dg_quantize_e4m3(p, 4, 0, 16, p, 16, p, None) == 1
+    assert L.dg_quantize_e4m3(p, 4, 32, 16, p, 32, p, None) == 1
+    assert L.dg_quantize_e4m3(None, 4, 16, 16, p, 16, p, None) == 1
+    assert L.dg_quantize_e4m3(ctypes.c_void_p(258), 4, 16, 16, p, 16, p, None) == 2
+    assert L.dg_quantize_e4m3(p, 4, 15, 15, p, 16, p, None) == 2
+    assert L.dg_quantize_e4m3(None, 0, 16, 16, None, 16, None, None) == 0
+    # product: the contraction mismatch, a missing scale array, unaligned codes
+    st = L.dg_soft_embed_e4m3(p, 262144, p, 256, 0, 262144, p, p, 65536, 2816, 2816, 53.0, p, 2816, p, 1 << 30, None)
+    assert st == 1 and b"shard" in L.dg_last_error()
+    assert L.dg_soft_embed_e4m3(p, 4096, p, 16, 0, 4096, p, None, 4096, 256, 256, 1.0, p, 256, p, 1 << 20, None) == 1
+    assert L.dg_soft_embed_e4m3(p, 4096, p, 16, 0, 4096, p, p, 4096, 264, 260, 1.0, p, 260, p, 1 << 20, None) == 2
+    assert L.dg_soft_embed_e4m3(p, 4096, p, 16, 0, 4096, ctypes.c_void_p(264), p, 4096, 256, 256, 1.0, p, 256, p,
+                                1 << 20, None) == 2
+    assert L.dg_soft_embed_e4m3(p, 4096, p, 16, 0, 4096, p, ctypes.c_void_p(258), 4096, 256, 256, 1.0, p, 256, p,
+                                1 << 20, None) == 2
+    # the step checks its slice against V like the bf16 step
+    st = L.dg_sampler_step_e4m3(p, 1, 16, 4096, 4096, p, p, 0, 5000, 8192, 256, 256, 1.0, p, 0, p, p, p, p, p, p, p,
+                                p, p, 256, p, 1 << 20, None)
+    assert st == 1
