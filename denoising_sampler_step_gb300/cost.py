@@ -75,6 +75,16 @@ class StepCost:
         """Soft-embed product: the logits of the slice once, W once, E once."""
         return self.rows * self.vocab * F32_BYTES + self.w_bytes + self.out_bytes
 
+    @property
+    def e4m3_table_bytes(self) -> int:
+        """The 8-bit table of the slice: one E4M3 code per entry and one fp32 scale per row."""
+        return self.vocab * self.d + self.vocab * F32_BYTES
+
+    @property
+    def e4m3_gemm_bytes(self) -> int:
+        """Soft-embed product over the 8-bit table: the logits once, the table once, E once."""
+        return self.rows * self.vocab * F32_BYTES + self.e4m3_table_bytes + self.out_bytes
+
     def roofline_seconds(self, hbm_gbs: float, bf16_tflops: float) -> float:
         """Slower of the product's FLOPs at the bf16 peak and the logits + W bytes at HBM bandwidth."""
         t_mem = (self.logits_bytes + self.w_bytes) / (hbm_gbs * 1e9)
