@@ -230,7 +230,7 @@ def main() -> None:
                     help="comma-separated further workloads (e.g. batch8,late_batch32) whose step is "
                          "timed after the main one and reported under other_configs (single pass and "
                          "two passes)")
-    ap.add_argument("--only", choices=["soft_embed", "step"], default=None,
+    ap.add_argument("--only", choices=["soft_embed", "step", "soft_embed_e4m3", "step_e4m3"], default=None,
                     help="profiling target: run only this call (warm-up, then --steps calls) and print "
                          "its mean duration; no JSON line")
     ap.add_argument("--sustained", type=float, default=0.0,
@@ -276,6 +276,15 @@ def main() -> None:
         if args.only == "soft_embed":
             lse = B.dg_row_stats(xd)["lse"]
             call = lambda: B.dg_soft_embed(xd, lse, 0, wl.V, Wd, wl.gamma, out=step.out["E"], ws=step.ws)
+        elif args.only in ("soft_embed_e4m3", "step_e4m3"):
+            # the 8-bit table: the bf16 table quantised per row once (before the calls)
+            Qd, sd = B.dg_quantize_e4m3(Wd)
+            ws8 = B.workspace_e4m3(wl.R, wl.V, wl.d, dev)
+            lse = B.dg_row_stats(xd)["lse"]
+            if args.only == "soft_embed_e4m3":
+                call = lambda: B.dg_soft_embed_e4m3(xd, lse, 0, wl.V, Qd, sd, wl.gamma, out=step.out["E"], ws=ws8)
+            else:
+                call = lambda: B.dg_sampler_step_e4m3(xd, wl.n_req, wl.L_c, Qd, sd, wl.gamma, bd, ws=ws8)
         else:
             call = lambda: step(xd, bd)
         for _ in range(args.warmup):

@@ -756,7 +756,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     const float bm = max32(xb);
                     // a block with nothing finite keeps k = 0: its exponentials are all 0
-                    const float kf = bm > -INFINITY ? floorf(fmaf(bm, kLog2e, neg_lse2[q])) : 0.0f;
+                    // (rows past R have no reference: k = 0 and exponentials of 0)
+                    const float kf =
+                        (bm > -INFINITY && neg_lse2[q] > -INFINITY) ? floorf(fmaf(bm, kLog2e, neg_lse2[q])) : 0.0f;
                     const float off = neg_lse2[q] - kf + 7.0f;
 #pragma unroll
                     for (int t = 0; t < 32; ++t) e[t] = ex2_approx(fmaf(xb[t], kLog2e, off));
