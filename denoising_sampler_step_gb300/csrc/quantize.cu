@@ -5,8 +5,9 @@
 // format (bias 7, subnormals, no infinity, 448 the largest finite value).  The pages name FP8
 // checkpoints (agentlenshq.com, "量子化チェックポイント") without a layout for the table;
 // this per-row layout is the reading the product takes.
-// One CTA per row (grid-stride): a max-reduction over the row, then the codes, two per thread
-// step.  HBM-bound and run once per table.
+// Rows of whole 16-byte groups take a warp each (below); others one CTA per row (grid-stride):
+// a max-reduction over the row, then the codes, two per thread step.  HBM-bound and run once
+// per table.
 #include "dg_common.cuh"
 #include "dg_internal.h"
 
@@ -54,14 +55,63 @@ __global__ void __launch_bounds__(kQuantThreads)
     }
 }
 
+// The same with a warp per row and 16-byte accesses (8 entries per lane and step), for rows
+// whose bases and lengths are multiples of 8 entries: the maximum over the row, then the
+// codes from a second read of the row (it is in L1 by then).
+__global__ void __launch_bounds__(kQuantThreads)
+    quantize_e4m3_vec_kernel(const uint16_t *__restrict__ W, int64_t V, int64_t d, int64_t ldw,
+                             uint8_t *__restrict__ Q, int64_t ldq, float *__restrict__ scale) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (kQuantThreads / 32);
+    for (int64_t v = (int64_t)blockIdx.x * (kQuantThreads / 32) + (threadIdx.x >> 5); v < V; v += warps) {
+        const uint4 *w = reinterpret_cast<const uint4 *>(W + v * ldw);
+        const int64_t n8 = d / 8;
+        float amax = 0.0f;
+        for (int64_t c = lane; c < n8; c += 32) {
+            const uint4 u = __ldg(w + c);
+            const uint32_t h[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                amax = fmaxf(amax, fmaxf(fabsf(bf16_value((uint16_t)(h[t] & 0xFFFFu))), fabsf(bf16_value((uint16_t)(h[t] >> 16)))));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const float s = __fdiv_rn(amax, 448.0f);
+        if (lane == 0) scale[v] = s;
+        uint2 *q = reinterpret_cast<uint2 *>(Q + v * ldq);
+        for (int64_t c = lane; c < n8; c += 32) {
+            const uint4 u = __ldg(w + c);
+            const uint32_t h[4] = {u.x, u.y, u.z, u.w};
+            uint32_t codes[2] = {0u, 0u};
+            if (s > 0.0f) {
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const float x0 = __fdiv_rn(bf16_value((uint16_t)(h[t] & 0xFFFFu)), s);
+                    const float x1 = __fdiv_rn(bf16_value((uint16_t)(h[t] >> 16)), s);
+                    codes[t >> 1] |= pack_e4m3x2(x0, x1) << (16 * (t & 1));
+                }
+            }
+            q[c] = make_uint2(codes[0], codes[1]);
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_e4m3(const uint16_t *W, int64_t V, int64_t d, int64_t ldw, uint8_t *Q, int64_t ldq,
                                  float *scale, cudaStream_t stream) {
-    int64_t blocks = V;
     const int64_t cap = (int64_t)device_sm_count() * 16;
-    if (cap > 0 && blocks > cap) blocks = cap;
-    quantize_e4m3_kernel<<<(unsigned)blocks, kQuantThreads, 0, stream>>>(W, V, d, ldw, Q, ldq, scale);
+    const bool vec = (reinterpret_cast<uintptr_t>(W) & 15) == 0 && (ldw & 7) == 0 && (d & 7) == 0 &&
+                     (reinterpret_cast<uintptr_t>(Q) & 7) == 0 && (ldq & 7) == 0;
+    if (vec) {
+        int64_t blocks = (V + kQuantThreads / 32 - 1) / (kQuantThreads / 32);
+        if (cap > 0 && blocks > cap) blocks = cap;
+        quantize_e4m3_vec_kernel<<<(unsigned)blocks, kQuantThreads, 0, stream>>>(W, V, d, ldw, Q, ldq, scale);
+    } else {
+        int64_t blocks = V;
+        if (cap > 0 && blocks > cap) blocks = cap;
+        quantize_e4m3_kernel<<<(unsigned)blocks, kQuantThreads, 0, stream>>>(W, V, d, ldw, Q, ldq, scale);
+    }
     return cudaGetLastError();
 }
 
