@@ -214,12 +214,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int W_SLOT = Fmt<F>::W_SLOT;
     constexpr int WST = Fmt<F>::WST;
     constexpr int AST = Fmt<F>::AST;
-    constexpr bool kSplitRings = F == kE4m3;  // W released on its own barriers (8-bit table)
+    constexpr bool kSplitRings = WST != AST;  // W released on its own barriers
     constexpr int W_RING = WST * W_SLOT;
     constexpr int A_RING = AST * A_BYTES;
     static_assert(F == kBf16 || (AST % 2 == 0 && ROWS_PER_LANE == 1),
                   "8-bit table: A slots alternate between the two CTAs; a warp copies 32 whole rows");
     static_assert(AST >= PGROUPS, "an A slot per producer group at least");
+    // 8-bit table: a block's W bytes complete on its A slot's barrier (one index for both
+    // rings), so the MMA thread waits on one barrier per block
+    static_assert(F == kBf16 || WST == AST, "8-bit table: one ring index");
+    constexpr bool kWOnA = F == kE4m3;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *l_ring = smem;
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // partner fills counts the MMA thread's arrival (with the copied bytes); both
             // CTAs' commits reach each empty (the slot is read in both)
             int fa = kPair ? 2 * GROUP_WARPS : GROUP_WARPS;
-            if (F == kE4m3) fa = (s % 2 == (int)rank) ? GROUP_WARPS : 1;
+            if (F == kE4m3) fa = ((s % 2 == (int)rank) ? GROUP_WARPS : 1) + 1;  // + the W TMA's arrival
             mbar_init(smem_u32(&full_a[s]), fa);
             mbar_init(smem_u32(&empty[s]), kPair ? 1 : kCtasPerUnit);
         }
@@ -394,7 +398,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 const int64_t k = p.k_begin + (kb0 + i) * BK;
-                const uint32_t bw = smem_u32(&full_w[s]);
+                const uint32_t bw = smem_u32(kWOnA ? &full_a[s] : &full_w[s]);
                 const int wy = (int)(k - p.vocab_start);
                 if constexpr (F == kE4m3) {
                     // this CTA's own tile: four 128-column atoms (two for a half-width tile)
@@ -441,7 +445,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // barrier, which the even CTA reaches after this drain)
             if (!ok && (!kPair || rank == 0))
                 for (int s = 0; s < WST; ++s)
-                    if (issued[s] > 0) drain_wait(smem_u32(&full_w[s]), (issued[s] - 1) & 1);
+                    if (issued[s] > 0) drain_wait(smem_u32(kWOnA ? &full_a[s] : &full_w[s]), (issued[s] - 1) & 1);
         }
     } else if (warp == kWarpL) {
         // ------------------------------------------------------------ logits TMA
@@ -509,16 +513,20 @@ __global__ void __launch_bounds__(THREADS, 1)
             auto wait = [&](uint32_t bar, uint32_t ph) {
                 return kPair ? mbar_wait_cluster(bar, ph, abort_flag) : mbar_wait(bar, ph, abort_flag);
             };
+            // 8-bit table: a slot the partner fills completes on its copies' bytes and one
+            // arrival of this thread (the bytes may land first), made before the slot is tested
+            auto arm = [&](int i) {
+                if (F == kE4m3 && i < nkb && (i & 1) != (int)rank)
+                    mbar_arrive_expect_tx(smem_u32(&full_a[i % AST]), GROUP_WARPS * (2048u + 512u));
+            };
+            arm(0);
             bool a_in = nkb > 0 && test(smem_u32(&full_a[0]), 0);
-            bool w_in = nkb > 0 && test(smem_u32(&full_w[0]), 0);
+            bool w_in = kWOnA || (nkb > 0 && test(smem_u32(&full_w[0]), 0));
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % AST, sw = i % WST;
                 const uint32_t ph = (uint32_t)(i / AST) & 1, phw = (uint32_t)(i / WST) & 1;
-                // 8-bit table: a slot the partner fills completes on its copies' bytes and this
-                // arrival (the bytes may land first)
-                if (F == kE4m3 && (i & 1) != (int)rank)
-                    mbar_arrive_expect_tx(smem_u32(&full_a[s]), GROUP_WARPS * (2048u + 512u));
-                if (!(a_in && w_in) && (!wait(smem_u32(&full_a[s]), ph) || !wait(smem_u32(&full_w[sw]), phw))) {
+                if (!(a_in && w_in) &&
+                    (!wait(smem_u32(&full_a[s]), ph) || (!kWOnA && !wait(smem_u32(&full_w[sw]), phw)))) {
                     ok = false;
                     break;
                 }
@@ -553,8 +561,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (halves == 2) umma_bf16(tmem_base + 256, ad + kA_K16, bd + kB_HALF + kB_K16, idesc, 1u);
                 }
                 if (i + 1 < nkb) {
+                    arm(i + 1);
                     a_in = test(smem_u32(&full_a[(i + 1) % AST]), (uint32_t)((i + 1) / AST) & 1);
-                    w_in = test(smem_u32(&full_w[(i + 1) % WST]), (uint32_t)((i + 1) / WST) & 1);
+                    w_in = kWOnA || test(smem_u32(&full_w[(i + 1) % WST]), (uint32_t)((i + 1) / WST) & 1);
                 }
                 // one commit releases the W and A slots once both CTAs' MMAs have read them
                 // (8-bit table: the W slot, this CTA's own, on this commit; the A slot, read
