@@ -220,10 +220,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     static_assert(F == kBf16 || (AST % 2 == 0 && ROWS_PER_LANE == 1),
                   "8-bit table: A slots alternate between the two CTAs; a warp copies 32 whole rows");
     static_assert(AST >= PGROUPS, "an A slot per producer group at least");
-    // 8-bit table: a block's W bytes complete on its A slot's barrier (one index for both
-    // rings), so the MMA thread waits on one barrier per block
-    static_assert(F == kBf16 || WST == AST, "8-bit table: one ring index");
-    constexpr bool kWOnA = F == kE4m3;
+    // a block's W bytes complete on its A slot's barrier (one index for both rings), so the
+    // MMA thread waits on one barrier per block (not in the CTA-pair diagnostic build)
+    static_assert(WST == AST, "one ring index");
+    constexpr bool kWOnA = !kPair;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *l_ring = smem;
@@ -310,7 +310,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             // partner fills counts the MMA thread's arrival (with the copied bytes); both
             // CTAs' commits reach each empty (the slot is read in both)
             int fa = kPair ? 2 * GROUP_WARPS : GROUP_WARPS;
-            if (F == kE4m3) fa = ((s % 2 == (int)rank) ? GROUP_WARPS : 1) + 1;  // + the W TMA's arrival
+            if (F == kE4m3) fa = (s % 2 == (int)rank) ? GROUP_WARPS : 1;
+            if (kWOnA) fa += 1;  // the W TMA's arrival
             mbar_init(smem_u32(&full_a[s]), fa);
             mbar_init(smem_u32(&empty[s]), kPair ? 1 : kCtasPerUnit);
         }
