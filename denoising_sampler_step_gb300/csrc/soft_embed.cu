@@ -30,6 +30,13 @@
 //   tile of a row block) in L2.
 //   Every barrier wait is bounded (about a second); a wait that gives up records
 //   DG_ERR_TIMEOUT, drains what is in flight and leaves the kernel.
+//
+// The same kernel, instantiated for an 8-bit table (E4M3 codes with one fp32 scale per
+// vocabulary row), runs block-scaled E4M3 MMAs (kind::mxf8f6f4): the producers take each
+// block's exponentials against its own maximum, fold in the (normalised, staged) row scales
+// and split each value into two E4M3 parts under a power-of-two scale per (row, block) that
+// the MMA applies from TMEM; a cluster holds one row block and two 480-column tiles, and each
+// CTA computes every other block's A operand and copies it to its partner.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -214,7 +221,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int W_SLOT = Fmt<F>::W_SLOT;
     constexpr int WST = Fmt<F>::WST;
     constexpr int AST = Fmt<F>::AST;
-    constexpr bool kSplitRings = WST != AST;  // W released on its own barriers
     constexpr int W_RING = WST * W_SLOT;
     constexpr int A_RING = AST * A_BYTES;
     static_assert(F == kBf16 || (AST % 2 == 0 && ROWS_PER_LANE == 1),
@@ -240,8 +246,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t *empty = full_a + AST;            // MMAs done with the A slot (and, one ring, the W slot: both CTAs')
     uint64_t *acc_full = empty + AST;          // accumulator complete
     uint64_t *full_s = acc_full + 1;           // 8-bit table: a block's row scales staged
-    uint64_t *empty_w = full_s + LSTAGES;      // 8-bit table: this CTA's MMAs done with the W slot
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(empty_w + WST);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(full_s + LSTAGES);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     // Overlap with the neighbours on the stream (programmatic dependent launch): this grid
@@ -315,10 +320,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(smem_u32(&full_a[s]), fa);
             mbar_init(smem_u32(&empty[s]), kPair ? 1 : kCtasPerUnit);
         }
-        for (int s = 0; s < WST; ++s) {
-            mbar_init(smem_u32(&full_w[s]), 1);
-            mbar_init(smem_u32(&empty_w[s]), 1);  // 8-bit table: this CTA's own W tile
-        }
+        for (int s = 0; s < WST; ++s) mbar_init(smem_u32(&full_w[s]), 1);
         mbar_init(smem_u32(acc_full), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -394,7 +396,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     grid_dependency_wait();
                     grid_launch_dependents();
                 }
-                if (u > 0 && !mbar_wait(smem_u32(kSplitRings ? &empty_w[s] : &empty[s]), (u - 1) & 1, abort_flag)) {
+                if (u > 0 && !mbar_wait(smem_u32(&empty[s]), (u - 1) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -524,16 +526,16 @@ __global__ void __launch_bounds__(THREADS, 1)
             bool a_in = nkb > 0 && test(smem_u32(&full_a[0]), 0);
             bool w_in = kWOnA || (nkb > 0 && test(smem_u32(&full_w[0]), 0));
             for (int i = 0; i < nkb; ++i) {
-                const int s = i % AST, sw = i % WST;
-                const uint32_t ph = (uint32_t)(i / AST) & 1, phw = (uint32_t)(i / WST) & 1;
+                const int s = i % AST;
+                const uint32_t ph = (uint32_t)(i / AST) & 1;
                 if (!(a_in && w_in) &&
-                    (!wait(smem_u32(&full_a[s]), ph) || (!kWOnA && !wait(smem_u32(&full_w[sw]), phw)))) {
+                    (!wait(smem_u32(&full_a[s]), ph) || (!kWOnA && !wait(smem_u32(&full_w[s]), ph)))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint64_t ad = a_desc0 + (uint64_t)((s * A_BYTES) >> 4);
-                const uint64_t bd = b_desc0 + (uint64_t)((sw * W_SLOT) >> 4);
+                const uint64_t bd = b_desc0 + (uint64_t)((s * W_SLOT) >> 4);
                 const uint32_t acc = i > 0 ? 1u : 0u;
                 if constexpr (F == kE4m3) {
                     // high parts, then low parts (the word's four bytes are the same scale)
@@ -564,15 +566,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (i + 1 < nkb) {
                     arm(i + 1);
                     a_in = test(smem_u32(&full_a[(i + 1) % AST]), (uint32_t)((i + 1) / AST) & 1);
-                    w_in = kWOnA || test(smem_u32(&full_w[(i + 1) % WST]), (uint32_t)((i + 1) / WST) & 1);
+                    w_in = kWOnA || test(smem_u32(&full_w[(i + 1) % AST]), (uint32_t)((i + 1) / AST) & 1);
                 }
                 // one commit releases the W and A slots once both CTAs' MMAs have read them
-                // (8-bit table: the W slot, this CTA's own, on this commit; the A slot, read
-                // in both CTAs, on both)
-                if (kSplitRings) {
-                    umma_commit(smem_u32(&empty_w[sw]));
-                    umma_commit_multicast(smem_u32(&empty[s]), kPairMask);
-                } else if (kPair) {
+                // (8-bit table: the A slot is read in both, the W slot is this CTA's own)
+                if (kPair) {
                     umma_commit_pair_multicast(smem_u32(&empty[s]), kPairMask);
                 } else {
                     umma_commit_multicast(smem_u32(&empty[s]), kPairMask);
