@@ -74,6 +74,11 @@ lib.dg_soft_embed_e4m3.restype = ctypes.c_int
 lib.dg_sampler_step_e4m3.argtypes = [_p, _i32, _i32, _i64, _i64, _p, _p, _i64, _i64, _i64, _i64, _i64, _f32, _p,
                                      _i32, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i64, _p, _sz, _p]
 lib.dg_sampler_step_e4m3.restype = ctypes.c_int
+lib.dg_sampler_loop_step_e4m3.argtypes = [_p, _i32, _i32, _i64, _i64, _p, _p, _i64, _i64, _i64, _i64, _i64, _f32, _p,
+                                          _i32, _i32, _f32, _i32, _f32, ctypes.c_uint64, ctypes.c_uint64,
+                                          _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i64,
+                                          _p, _p, _p, _p, _p, _p, _p, _sz, _p]
+lib.dg_sampler_loop_step_e4m3.restype = ctypes.c_int
 
 STATUS = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED", 3: "DG_ERR_CUDA", 4: "DG_ERR_TIMEOUT"}
 
@@ -408,6 +413,38 @@ def dg_sampler_loop_step(logits: torch.Tensor, n_req: int, L_c: int, W: torch.Te
                                     _ptr(o["n_accepted"]), _ptr(o["E"]), _ld(o["E"]),
                                     *[_ptr(state[k]) for k in LOOP_STATE_KEYS], _ptr(ws), ws.numel(),
                                     _stream(stream)), "dg_sampler_loop_step")
+    return o
+
+
+def dg_sampler_loop_step_e4m3(logits: torch.Tensor, n_req: int, L_c: int, Q: torch.Tensor, scale: torch.Tensor,
+                              gamma: float, budgets: torch.Tensor, state: dict, stable_steps: int,
+                              entropy_threshold: float, step_limit: int, min_accept: int = 0, vocab_start: int = 0,
+                              vocab_end: int | None = None, V: int | None = None, out: dict | None = None,
+                              ws: torch.Tensor | None = None, temperature: float = 0.0, seed: int = 0, offset: int = 0,
+                              stream=None) -> dict:
+    """dg_sampler_loop_step with the 8-bit table (Q uint8 [rows_pad, d], scale fp32 [rows_pad])."""
+    R = n_req * L_c
+    V = logits.shape[1] if V is None else V
+    vocab_end = V if vocab_end is None else vocab_end
+    d = Q.shape[1]
+    dev = logits.device
+    o = out
+    if o is None:
+        o = {k: _new(R, torch.float32, dev) for k in ("m", "lse", "H", "kappa")}
+        o.update(argmax=_new(R, torch.int32, dev), order=_new(R, torch.int32, dev), mask=_new(R, torch.uint8, dev),
+                 n_accepted=_new(n_req, torch.int32, dev), E=_new((R, d), torch.float32, dev))
+    if temperature != 0.0 and "candidate" not in o:
+        o["candidate"] = _new(R, torch.int32, dev)
+    if ws is None:
+        ws = workspace_e4m3(R, max(1, vocab_end - vocab_start), d, dev)
+    _check(lib.dg_sampler_loop_step_e4m3(_ptr(logits), n_req, L_c, V, _ld(logits), _ptr(Q), _ptr(scale), vocab_start,
+                                         vocab_end, Q.shape[0], _ld(Q), d, gamma, _ptr(budgets), min_accept,
+                                         stable_steps, entropy_threshold, step_limit, temperature, seed, offset,
+                                         _ptr(o["m"]), _ptr(o["lse"]), _ptr(o["H"]), _ptr(o["kappa"]),
+                                         _ptr(o["argmax"]), _ptr(o.get("candidate")), _ptr(o["order"]),
+                                         _ptr(o["mask"]), _ptr(o["n_accepted"]), _ptr(o["E"]), _ld(o["E"]),
+                                         *[_ptr(state[k]) for k in LOOP_STATE_KEYS], _ptr(ws), ws.numel(),
+                                         _stream(stream)), "dg_sampler_loop_step_e4m3")
     return o
 
 

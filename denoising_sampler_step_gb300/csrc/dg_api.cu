@@ -468,6 +468,24 @@ dg_status dg_sampler_loop_step(const float *logits, int32_t n_req, int32_t L_c, 
                     ldo, workspace, workspace_bytes, (cudaStream_t)stream, &loop);
 }
 
+dg_status dg_sampler_loop_step_e4m3(const float *logits, int32_t n_req, int32_t L_c, int64_t V, int64_t ldl,
+                                    const uint8_t *Q, const float *scale, int64_t vocab_start, int64_t vocab_end,
+                                    int64_t rows_pad, int64_t ldq, int64_t d, float gamma, const float *budgets,
+                                    int32_t min_accept, int32_t stable_steps, float entropy_threshold,
+                                    int32_t step_limit, float temperature, uint64_t seed, uint64_t offset, float *m,
+                                    float *lse, float *H, float *kappa, int32_t *argmax, int32_t *candidate,
+                                    int32_t *order, uint8_t *mask, int32_t *n_accepted, float *E, int64_t ldo,
+                                    int32_t *canvas, uint8_t *eligible, int32_t *prev_argmax, int32_t *stable,
+                                    int32_t *steps, uint8_t *converged, void *workspace, size_t workspace_bytes,
+                                    dg_stream_t stream) {
+    t_last_error[0] = 0;
+    LoopArgs loop{stable_steps, entropy_threshold, step_limit, temperature, seed, offset, candidate, canvas,
+                  eligible, prev_argmax, stable, steps, converged};
+    return run_step(logits, n_req, L_c, V, ldl, EmbedTable{kTableE4m3, Q, ldq, scale}, vocab_start, vocab_end,
+                    rows_pad, d, gamma, budgets, min_accept, m, lse, H, kappa, argmax, order, mask, n_accepted, E,
+                    ldo, workspace, workspace_bytes, (cudaStream_t)stream, &loop);
+}
+
 dg_status dg_entropy_accept_eligible(const float *H, const float *kappa, const uint8_t *eligible, int32_t n_req,
                                      int32_t L_c, const float *budgets, int32_t min_accept, int32_t *order,
                                      uint8_t *mask, int32_t *n_accepted, dg_stream_t stream) {

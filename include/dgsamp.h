@@ -439,6 +439,26 @@ dg_status dg_sampler_step_e4m3(const float *logits, int32_t n_req, int32_t L_c, 
                                int32_t *n_accepted, float *E, int64_t ldo, void *workspace,
                                size_t workspace_bytes, dg_stream_t stream);
 
+/*
+ * dg_sampler_loop_step with the 8-bit table (Q, scale, ldq as dg_soft_embed_e4m3; the loop
+ * state and the other arguments as dg_sampler_loop_step).  The loop's decisions depend on
+ * the statistics only, so a loop over the 8-bit table keeps the same canvas and state as one
+ * over the bf16 table it was quantised from; E differs by the table's quantisation.
+ */
+dg_status dg_sampler_loop_step_e4m3(const float *logits, int32_t n_req, int32_t L_c, int64_t V,
+                                    int64_t ldl, const uint8_t *Q, const float *scale,
+                                    int64_t vocab_start, int64_t vocab_end, int64_t rows_pad,
+                                    int64_t ldq, int64_t d, float gamma, const float *budgets,
+                                    int32_t min_accept, int32_t stable_steps,
+                                    float entropy_threshold, int32_t step_limit, float temperature,
+                                    uint64_t seed, uint64_t offset, float *m, float *lse, float *H,
+                                    float *kappa, int32_t *argmax, int32_t *candidate,
+                                    int32_t *order, uint8_t *mask, int32_t *n_accepted, float *E,
+                                    int64_t ldo, int32_t *canvas, uint8_t *eligible,
+                                    int32_t *prev_argmax, int32_t *stable, int32_t *steps,
+                                    uint8_t *converged, void *workspace, size_t workspace_bytes,
+                                    dg_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

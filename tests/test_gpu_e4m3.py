@@ -189,3 +189,51 @@ def test_step_canvas256_full_size(B):
     rows = sampled_rows(wl.R, 14, 7)
     ref = soft_embed_e4m3(x, ost["lse"], 0, wl.V, Q, scale, wl.gamma, rows=rows)
     assert rel_l2(out["E"].cpu().numpy()[rows], ref).max() <= E_TOL
+
+
+@pytest.mark.parametrize("temperature", [0.0, 1.0])
+def test_loop_over_the_8bit_table_matches_the_oracle_chain(B, temperature):
+    """Denoising-loop steps over the 8-bit table (argmax, and drawn candidates with the draw
+    folded into the single pass): statistics, candidates, acceptance and the whole loop
+    state bit-exact against the oracle chain (whose decisions keep their margins), E against
+    the 8-bit oracle."""
+    from oracle.loop_oracle import entropy_accept_eligible, loop_update, new_loop_state
+    from tests.test_gpu_loop import (LOOP_WL, SAMPLED_WL, STABLE_STEPS, STEP_LIMIT, compare_state,
+                                     decision_margins_ok, loop_threshold, sampled_chain_inputs)
+    steps, seed = 6, 2024
+    if temperature > 0:
+        wl = SAMPLED_WL
+        budgets, thr, chain = sampled_chain_inputs(wl, steps, temperature, seed)
+    else:
+        wl = LOOP_WL
+        base = inputs.logits(wl)
+        budgets = inputs.budgets(wl)
+        thr = loop_threshold(row_stats(base), wl)
+        o = new_loop_state(wl.n_req, wl.L_c)
+        chain = []
+        for t in range(steps):
+            x = inputs.loop_logits(wl, t, base=base)
+            st = row_stats(x)
+            assert decision_margins_ok(st["H"], st["kappa"], o["eligible"], wl.n_req, wl.L_c, budgets), t
+            acc = entropy_accept_eligible(st["H"], st["kappa"], o["eligible"], wl.n_req, wl.L_c, budgets,
+                                          min_accept=1)
+            o = loop_update(o, st["argmax"], st["H"], acc["mask"], wl.n_req, wl.L_c, STABLE_STEPS, thr, STEP_LIMIT)
+            chain.append((x, st, {"candidate": st["argmax"]}, st["kappa"], acc, o))
+    Q, scale = quantize_rows_e4m3(inputs.embedding_bf16(wl))
+    Qd, sd = q_dev(Q), s_dev(scale)
+    state = B.new_loop_state(wl.n_req, wl.L_c, "cuda")
+    bud = dev(budgets)
+    for t, (x, st, sm, kc, acc, o) in enumerate(chain):
+        out = B.dg_sampler_loop_step_e4m3(dev(x), wl.n_req, wl.L_c, Qd, sd, wl.gamma, bud, state, STABLE_STEPS, thr,
+                                          STEP_LIMIT, min_accept=1, temperature=temperature, seed=seed, offset=t)
+        torch.cuda.synchronize()
+        check_stats(out, dict(st, kappa=kc))
+        if temperature > 0:
+            assert np.array_equal(out["candidate"].cpu().numpy(), sm["candidate"]), t
+        for key in ("order", "mask", "n_accepted"):
+            assert np.array_equal(out[key].cpu().numpy(), acc[key]), (t, key)
+        compare_state(state, o, f"step {t}")
+    B.dg_get_device_status()
+    rows = np.array([0, 17, 130, wl.R - 1])
+    ref = soft_embed_e4m3(x, st["lse"], 0, wl.V, Q, scale, wl.gamma, rows=rows)
+    assert rel_l2(out["E"].cpu().numpy()[rows], ref).max() <= E_TOL
