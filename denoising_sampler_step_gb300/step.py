@@ -13,13 +13,16 @@ from . import binding as B
 
 
 class SamplerStep:
-    """Owns the embedding table W (bf16, resident), the workspace and the outputs."""
+    """Owns the embedding table W (resident), the workspace and the outputs.  W is bf16, or
+    with `scale` given an 8-bit table: W the E4M3 codes (uint8 [rows, d]) and `scale` the fp32
+    row scales (from dg_quantize_e4m3, or the caller's own)."""
 
     def __init__(self, W: torch.Tensor, n_req: int, L_c: int, V: int, gamma: float,
                  vocab_start: int = 0, vocab_end: int | None = None, min_accept: int = 0,
-                 device: str | torch.device = "cuda"):
+                 device: str | torch.device = "cuda", scale: torch.Tensor | None = None):
         self.device = torch.device(device)
         self.W = W
+        self.scale = scale
         self.n_req, self.L_c, self.V = n_req, L_c, V
         self.R = n_req * L_c
         self.d = W.shape[1]
@@ -34,12 +37,18 @@ class SamplerStep:
                         mask=torch.empty(R, dtype=torch.uint8, device=dev),
                         n_accepted=torch.empty(n_req, dtype=torch.int32, device=dev),
                         E=torch.empty((R, d), dtype=torch.float32, device=dev))
-        self.ws = B.workspace(R, max(1, self.vocab_end - self.vocab_start), d, dev)
+        self.ws = (B.workspace_e4m3 if scale is not None else B.workspace)(
+            R, max(1, self.vocab_end - self.vocab_start), d, dev)
         self.logits_dev = None
         self.budgets_dev = torch.empty(n_req, dtype=torch.float32, device=dev)
 
     # -- device-resident inputs
     def __call__(self, logits: torch.Tensor, budgets: torch.Tensor, stream=None) -> dict:
+        if self.scale is not None:
+            return B.dg_sampler_step_e4m3(logits, self.n_req, self.L_c, self.W, self.scale, self.gamma, budgets,
+                                          min_accept=self.min_accept, vocab_start=self.vocab_start,
+                                          vocab_end=self.vocab_end, V=self.V, out=self.out, ws=self.ws,
+                                          stream=stream)
         return B.dg_sampler_step(logits, self.n_req, self.L_c, self.W, self.gamma, budgets,
                                  min_accept=self.min_accept, vocab_start=self.vocab_start,
                                  vocab_end=self.vocab_end, V=self.V, out=self.out, ws=self.ws,
@@ -140,6 +149,15 @@ class SamplerLoop(SamplerStep):
         self.offset = 0
 
     def __call__(self, logits: torch.Tensor, budgets: torch.Tensor, stream=None) -> dict:
+        if self.scale is not None:
+            o = B.dg_sampler_loop_step_e4m3(logits, self.n_req, self.L_c, self.W, self.scale, self.gamma, budgets,
+                                            self.state, self.stable_steps, self.entropy_threshold,
+                                            self.step_limit, min_accept=self.min_accept,
+                                            vocab_start=self.vocab_start, vocab_end=self.vocab_end, V=self.V,
+                                            out=self.out, ws=self.ws, temperature=self.temperature,
+                                            seed=self.seed, offset=self.offset, stream=stream)
+            self.offset += 1
+            return o
         o = B.dg_sampler_loop_step(logits, self.n_req, self.L_c, self.W, self.gamma, budgets, self.state,
                                    self.stable_steps, self.entropy_threshold, self.step_limit,
                                    min_accept=self.min_accept, vocab_start=self.vocab_start,

@@ -237,3 +237,32 @@ def test_loop_over_the_8bit_table_matches_the_oracle_chain(B, temperature):
     rows = np.array([0, 17, 130, wl.R - 1])
     ref = soft_embed_e4m3(x, st["lse"], 0, wl.V, Q, scale, wl.gamma, rows=rows)
     assert rel_l2(out["E"].cpu().numpy()[rows], ref).max() <= E_TOL
+
+
+def test_resident_step_and_loop_hold_an_8bit_table(B):
+    """SamplerStep and SamplerLoop given an 8-bit table run the same calls as the C ABI's
+    8-bit entry points: identical outputs (the product's reduce is deterministic) and, over
+    three loop steps, identical state."""
+    from denoising_sampler_step_gb300.step import SamplerLoop, SamplerStep
+    wl = inputs.WORKLOADS["tiny"].with_(V=20000, d=512, L_c=64, n_req=2, seed=13, budget=6.0)
+    x = dev(inputs.logits(wl))
+    Q, scale = inputs.embedding_e4m3(wl)
+    Qd, sd = q_dev(Q), s_dev(scale)
+    bud = dev(inputs.budgets(wl))
+    st = SamplerStep(Qd, wl.n_req, wl.L_c, wl.V, wl.gamma, scale=sd)
+    a = {k: v.clone() for k, v in st(x, bud).items()}
+    b = B.dg_sampler_step_e4m3(x, wl.n_req, wl.L_c, Qd, sd, wl.gamma, bud)
+    torch.cuda.synchronize()
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+    lp = SamplerLoop(Qd, wl.n_req, wl.L_c, wl.V, wl.gamma, 2, 1.0, 8, temperature=1.0, seed=5, scale=sd)
+    state = B.new_loop_state(wl.n_req, wl.L_c, "cuda")
+    for t in range(3):
+        o1 = lp(x, bud)
+        o2 = B.dg_sampler_loop_step_e4m3(x, wl.n_req, wl.L_c, Qd, sd, wl.gamma, bud, state, 2, 1.0, 8,
+                                         temperature=1.0, seed=5, offset=t)
+        torch.cuda.synchronize()
+        assert torch.equal(o1["candidate"], o2["candidate"]) and torch.equal(o1["E"], o2["E"]), t
+        for k in state:
+            assert torch.equal(lp.state[k], state[k]), (t, k)
+    B.dg_get_device_status()
