@@ -1345,13 +1345,12 @@ __global__ void __launch_bounds__(256)
 // The 8-bit kernel; the CTA-pair diagnostic build has none (its launches are refused), and
 // names the bf16 kernel in its place so that nothing instantiates the 8-bit one.
 template <bool Pair>
-struct E4m3Kernel {
-    static constexpr auto fn = soft_embed_kernel<kE4m3>;
-};
-template <>
-struct E4m3Kernel<true> {
-    static constexpr auto fn = soft_embed_kernel<kBf16>;
-};
+constexpr auto e4m3_kernel() {
+    if constexpr (Pair)
+        return soft_embed_kernel<kBf16>;
+    else
+        return soft_embed_kernel<kE4m3>;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1529,7 +1528,7 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
         attr_err = cudaFuncSetAttribute(soft_embed_kernel<kBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         smem_bytes<kBf16>());
         if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(E4m3Kernel<kPair>::fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            attr_err = cudaFuncSetAttribute(e4m3_kernel<kPair>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             smem_bytes<kE4m3>());
     });
     if (attr_err != cudaSuccess) {
@@ -1605,7 +1604,7 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     attr[1].val.programmaticStreamSerializationAllowed = overlap_previous ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = e4 ? cudaLaunchKernelEx(&cfg, E4m3Kernel<kPair>::fn, tm_l, tm_w, p)
+    cudaError_t e = e4 ? cudaLaunchKernelEx(&cfg, e4m3_kernel<kPair>(), tm_l, tm_w, p)
                        : cudaLaunchKernelEx(&cfg, soft_embed_kernel<kBf16>, tm_l, tm_w, p);
     if (e != cudaSuccess) {
         *msg = "soft-embed kernel launch failed";
