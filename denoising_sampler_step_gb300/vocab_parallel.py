@@ -16,7 +16,8 @@ Per step, on every rank:
 `ops` carries the five calls (the CUDA binding by default) and `comm` the all-gather (a
 torch.distributed process group); both are parameters so that the orchestration can be
 exercised by multi-process tests on the host.  `local_step` runs all shards in one
-process, on one device, with the gathers replaced by stacking.
+process, on one device, with the gathers replaced by stacking.  A shard of an 8-bit table
+is the pair (E4M3 codes, fp32 row scales) of its rows; step 4 then runs dg_soft_embed_e4m3.
 """
 from __future__ import annotations
 
@@ -56,6 +57,9 @@ class CudaOps:
         return self.B.dg_entropy_accept(H, kappa, n_req, L_c, budgets, min_accept=min_accept)
 
     def soft_embed_shard(self, shard, lse, W_shard):
+        if isinstance(W_shard, tuple):  # an 8-bit table: (codes, row scales)
+            Q, scale = W_shard
+            return self.B.dg_soft_embed_e4m3(shard, lse, 0, shard.shape[1], Q, scale, 1.0)
         return self.B.dg_soft_embed(shard, lse, 0, shard.shape[1], W_shard, 1.0)
 
     def sum_partials(self, parts, gamma):

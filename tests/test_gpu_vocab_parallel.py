@@ -97,3 +97,32 @@ def test_sharded_statistics_full_size(B):
     bounds = shard_bounds(wl.V, 4)
     c = B.dg_row_stats_combine(torch.stack([B.dg_row_stats_partial(shard_tensor(x, s, e), s) for s, e in bounds]))
     check_stats(c, row_stats(x))
+
+
+def test_sharded_step_over_an_8bit_table(B):
+    """Four uneven shards of an 8-bit table (codes and row scales per shard) in one process:
+    statistics and acceptance against the oracle, E against the 8-bit oracle over the whole
+    table (the partition identity)."""
+    from oracle.quant_oracle import soft_embed_e4m3
+    wl = inputs.WORKLOADS["tiny"].with_(n_req=2, L_c=32, V=40001, d=512, seed=78, budget=("uniform", 2.0, 20.0))
+    x, budgets, ost, _ = guarded(wl, ld=40004)
+    Q, scale = inputs.embedding_e4m3(wl)
+    bounds = shard_bounds(wl.V, 4)
+
+    def q_shard(s, e):
+        ldq = (wl.d + 15) // 16 * 16
+        buf = np.zeros((e - s, ldq), np.uint8)
+        buf[:, :wl.d] = Q[s:e]
+        return dev(buf)[:, :wl.d], dev(scale[s:e])
+
+    step = ShardedStep(wl.n_req, wl.L_c, wl.gamma)
+    out = step.local_step([shard_tensor(x, s, e) for s, e in bounds], [s for s, _ in bounds],
+                          [q_shard(s, e) for s, e in bounds], dev(budgets))
+    torch.cuda.synchronize()
+    B.dg_get_device_status()
+    check_stats(out, ost)
+    acc = entropy_accept(ost["H"], ost["kappa"], wl.n_req, wl.L_c, budgets)
+    for k in ("order", "mask", "n_accepted"):
+        assert np.array_equal(out[k].cpu().numpy(), acc[k]), k
+    ref = soft_embed_e4m3(x[:, :wl.V], ost["lse"], 0, wl.V, Q, scale, wl.gamma)
+    assert rel_l2(out["E"].cpu().numpy(), ref).max() <= E_TOL
