@@ -111,6 +111,7 @@ struct Fmt<kBf16> {
     static constexpr int BN = 512;                // output columns per cluster tile: halves of 256 + 256
     static constexpr int WST = STAGES;            // W ring depth (the A ring's: one index for both)
     static constexpr int AST = STAGES;            // A ring depth
+    static constexpr int BPS = 1;                 // vocabulary blocks per ring slot
     static constexpr int W_SLOT = (kPair ? BK * BN : BK * BN * 2);  // the part of a block's W tile one CTA holds
     static constexpr int SF_BYTES = 0;
 };
@@ -120,16 +121,17 @@ struct Fmt<kE4m3> {
     // 480: halves of 256 + 224
     static constexpr int BN = 480;
     static constexpr int N1 = 224;                // N of the second half
-    // A block's time is bounded by each ring's round trip over its depth: half-size W slots
-    // let the W ring run six deep, and the A ring's slots alternate between the cluster's two
-    // CTAs, so six of them let each producer group store its next block while both CTAs'
-    // MMAs of its previous one are still in flight
-    static constexpr int WST = 6;
-    static constexpr int AST = 6;
-    static constexpr int W_SLOT = 4 * W_BOX_BYTES;  // four 128-column atoms (the last one's final 32 unused)
+    // three slots of two blocks: each producer group (two per CTA, one block per slot each)
+    // stores its next block while both CTAs' MMAs of its previous one are still in flight
+    static constexpr int WST = 3;
+    static constexpr int AST = 3;
+    // a ring slot holds two vocabulary blocks, one from each CTA of the cluster: the MMA
+    // thread's barrier wait, scale copy and commit then serve eight MMAs instead of four
+    static constexpr int BPS = 2;
+    static constexpr int W_SLOT = 4 * BPS * W_BOX_BYTES;  // four 128-column atoms of 64 rows (the last atom's final 32 columns unused)
     // per-stage A scale matrices (128 rows x 16 bytes), the B scale chunk, then the staged
     // row scales (one slot per logits stage: 32 normalised scales and their exponent)
-    static constexpr int SF_STAGE = 2048;
+    static constexpr int SF_STAGE = 2048 * BPS;  // a slot's blocks' A scale matrices, one after the other
     static constexpr int SF_BYTES = AST * SF_STAGE + 512 + LSTAGES * 160;
 };
 constexpr int S_SLOT = 160;
@@ -138,7 +140,7 @@ constexpr int S_SLOT = 160;
 constexpr uint32_t kSfaCol = 480, kSfbCol = 504;
 template <int F>
 constexpr int smem_bytes() {
-    return L_RING + Fmt<F>::WST * Fmt<F>::W_SLOT + Fmt<F>::AST * A_BYTES + Fmt<F>::SF_BYTES + 1024 /*align*/ +
+    return L_RING + Fmt<F>::WST * Fmt<F>::W_SLOT + Fmt<F>::AST * Fmt<F>::BPS * A_BYTES + Fmt<F>::SF_BYTES + 1024 /*align*/ +
            512 /*barriers*/;
 }
 
@@ -146,7 +148,8 @@ static_assert(L_BYTES % 1024 == 0 && Fmt<kBf16>::W_SLOT % 1024 == 0 && Fmt<kE4m3
                   A_BYTES % 1024 == 0,
               "1 KiB alignment");
 static_assert(smem_bytes<kBf16>() <= 232448 && smem_bytes<kE4m3>() <= 232448, "shared memory per CTA");
-static_assert(kSfaCol + 4 * Fmt<kE4m3>::AST <= kSfbCol && kSfbCol + 8 <= TMEM_COLS, "scale-factor columns");
+static_assert(kSfaCol + 4 * Fmt<kE4m3>::AST * Fmt<kE4m3>::BPS <= kSfbCol && kSfbCol + 8 <= TMEM_COLS,
+              "scale-factor columns");
 // each producer group keeps to every other slot of the logits and A rings
 // a group waits only for phases its own blocks need, and no slot can run two phases ahead
 // of its waiter, so the depths need not be multiples of the group count
@@ -167,6 +170,7 @@ struct Params {
     int w3d;             // 1: the W map is 3-D (atom columns x rows x atoms), one load per CTA and block
     // 8-bit table: the fp32 scale of vocabulary entry v is w_scale[v - vocab_start]
     const float *w_scale;
+    int pair_blocks;     // 8-bit table: splits hold whole pairs of blocks (two per ring slot)
     // single pass (no lse yet): each split's probabilities are taken against a reference
     // c per row, exp(l - c), and the column-tile-0 clusters also fold the row statistics
     int fused;
@@ -189,6 +193,20 @@ struct Params {
 // of exp(l - c) over the split passes e^kRefSumLog (about 4e35, so that with |W| <= 100 the
 // fp32 partial stays below 4e37), or when the split's maximum lies more than kRefBelow nats
 // below c (everything would underflow).
+// Vocabulary blocks [kb0, kb1) of split j of S.  Pair mode (the 8-bit table's two blocks per
+// ring slot): the bounds are even, and the last split may end one block past the slice (that
+// block reads zeros).
+__host__ __device__ inline void split_range(const Params &p, int j, int S, int64_t *kb0, int64_t *kb1) {
+    if (p.pair_blocks) {
+        const int64_t np = (p.nkb + 1) / 2;
+        *kb0 = 2 * ((int64_t)j * np / S);
+        *kb1 = 2 * ((int64_t)(j + 1) * np / S);
+    } else {
+        *kb0 = (int64_t)j * p.nkb / S;
+        *kb1 = (int64_t)(j + 1) * p.nkb / S;
+    }
+}
+
 constexpr float kRefSumLog = 82.0f;
 constexpr float kRefBelow = 64.0f;
 // The reference is the largest of a split's first kRefEntries logits.
@@ -222,9 +240,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int WST = Fmt<F>::WST;
     constexpr int AST = Fmt<F>::AST;
     constexpr int W_RING = WST * W_SLOT;
-    constexpr int A_RING = AST * A_BYTES;
-    static_assert(F == kBf16 || (AST % 2 == 0 && ROWS_PER_LANE == 1),
-                  "8-bit table: A slots alternate between the two CTAs; a warp copies 32 whole rows");
+    constexpr int BPS = Fmt<F>::BPS;
+    constexpr int A_SLOT = BPS * A_BYTES;
+    constexpr int A_RING = AST * A_SLOT;
+    static_assert(F == kBf16 || (BPS == 2 && ROWS_PER_LANE == 1),
+                  "8-bit table: a slot holds one block of each CTA; a warp copies 32 whole rows");
     static_assert(AST >= PGROUPS, "an A slot per producer group at least");
     // a block's W bytes complete on its A slot's barrier (one index for both rings), so the
     // MMA thread waits on one barrier per block (not in the CTA-pair diagnostic build)
@@ -236,7 +256,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t *w_ring = smem + L_RING;
     uint8_t *a_ring = smem + L_RING + W_RING;
     uint8_t *sf_ring = smem + L_RING + W_RING + A_RING;  // 8-bit table: per-stage A scale chunks, B scale chunk
-    uint8_t *sfb_chunk = sf_ring + AST * 2048;           // 8-bit table: the B scale chunk
+    uint8_t *sfb_chunk = sf_ring + (F == kE4m3 ? AST * Fmt<kE4m3>::SF_STAGE : 0);  // 8-bit table: the B scale chunk
     uint8_t *s_ring = sfb_chunk + 512;                   // 8-bit table: staged row scales
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L_RING + W_RING + A_RING + Fmt<F>::SF_BYTES);
     uint64_t *full_l = bars;                   // logits tile landed
@@ -295,8 +315,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // 8-bit table: CTA c produces (loads the logits of, stages the scales of, computes the A
     // operand of) the blocks i with i % 2 == c and copies each A operand to its partner
     const int i0 = F == kE4m3 ? (int)rank : 0, di = F == kE4m3 ? 2 : 1;
-    const int64_t kb0 = (int64_t)j * p.nkb / S;
-    const int64_t kb1 = (int64_t)(j + 1) * p.nkb / S;
+    int64_t kb0, kb1;
+    split_range(p, j, S, &kb0, &kb1);
     const int nkb = (int)(kb1 - kb0);
     const int row0 = mt * BM;
     const int col0 = nt * BN;
@@ -315,7 +335,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             // partner fills counts the MMA thread's arrival (with the copied bytes); both
             // CTAs' commits reach each empty (the slot is read in both)
             int fa = kPair ? 2 * GROUP_WARPS : GROUP_WARPS;
-            if (F == kE4m3) fa = (s % 2 == (int)rank) ? GROUP_WARPS : 1;
+            // 8-bit table: this CTA's block (its producer group), the partner's (the MMA thread's
+            // arrival with the copied bytes) and the W TMA's arrival
+            if (F == kE4m3) fa = GROUP_WARPS + 1;
             if (kWOnA) fa += 1;  // the W TMA's arrival
             mbar_init(smem_u32(&full_a[s]), fa);
             mbar_init(smem_u32(&empty[s]), kPair ? 1 : kCtasPerUnit);
@@ -389,7 +411,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t w_bytes = kPair ? (uint32_t)halves * 2 * 2 * W_BOX_BYTES
                                            : (w3d ? (uint32_t)W_SLOT : (uint32_t)halves * W_SLOT / 2);
             const uint32_t lead = map_to_cta(smem_u32(&full_w[0]), 0);  // the even CTA's full_w[0]
-            for (int i = 0; i < nkb; ++i) {
+            for (int i = 0; i < nkb / BPS; ++i) {  // ring slots (BPS blocks each)
                 const int s = i % WST;
                 const uint32_t u = (uint32_t)(i / WST);
                 if (i == WST) {  // the first round of W loads is out
@@ -400,15 +422,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                     ok = false;
                     break;
                 }
-                const int64_t k = p.k_begin + (kb0 + i) * BK;
+                const int64_t k = p.k_begin + (kb0 + (int64_t)BPS * i) * BK;
                 const uint32_t bw = smem_u32(kWOnA ? &full_a[s] : &full_w[s]);
                 const int wy = (int)(k - p.vocab_start);
                 if constexpr (F == kE4m3) {
-                    // this CTA's own tile: four 128-column atoms (two for a half-width tile)
-                    mbar_arrive_expect_tx(bw, (uint32_t)halves * 2 * W_BOX_BYTES);
+                    // this CTA's own tile for the slot's two blocks: four 128-column atoms of 64
+                    // rows (two for a half-width tile)
+                    mbar_arrive_expect_tx(bw, (uint32_t)halves * 2 * BPS * W_BOX_BYTES);
                     for (int a = 0; a < 2 * halves; ++a)
-                        tma_load_2d_hint(smem_u32(w_ring + s * W_SLOT + a * W_BOX_BYTES), &tm_w, bw, col0 + 128 * a, wy,
-                                         w_policy);
+                        tma_load_2d_hint(smem_u32(w_ring + s * W_SLOT + a * BPS * W_BOX_BYTES), &tm_w, bw,
+                                         col0 + 128 * a, wy, w_policy);
                     issued[s] = (int)u + 1;
                     continue;
                 }
@@ -439,7 +462,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 issued[s] = (int)u + 1;
             }
-            if (nkb <= WST) {
+            if (nkb / BPS <= WST) {
                 grid_dependency_wait();
                 grid_launch_dependents();
             }
@@ -494,7 +517,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t a_desc0 = smem_desc(smem_u32(a_ring), 16, 512, 4);
             // B: N-major, 64-column atoms 4 KiB apart (LBO), 8-row groups 1 KiB apart (SBO);
             // +2 KiB per K = 16 step
-            const uint64_t b_desc0 = smem_desc(smem_u32(w_ring), W_BOX_BYTES, 1024, 2);
+            const uint64_t b_desc0 = smem_desc(smem_u32(w_ring), BPS * W_BOX_BYTES, 1024, 2);
             // a CTA's part of one 256-column half: 4 atoms (multicast) or 2 (pair)
             constexpr uint64_t kA_K16 = 32 >> 4, kB_K16 = 2048 >> 4, kB_HALF = (W_SLOT / 2) >> 4;
             // 8-bit table: the B scale factors (all 1) go into their columns once; per block the
@@ -518,14 +541,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             };
             // 8-bit table: a slot the partner fills completes on its copies' bytes and one
             // arrival of this thread (the bytes may land first), made before the slot is tested
-            auto arm = [&](int i) {
-                if (F == kE4m3 && i < nkb && (i & 1) != (int)rank)
+            auto arm = [&](int i) {  // every slot holds one block of the partner's
+                if (F == kE4m3 && i < nkb / BPS)
                     mbar_arrive_expect_tx(smem_u32(&full_a[i % AST]), GROUP_WARPS * (2048u + 512u));
             };
             arm(0);
             bool a_in = nkb > 0 && test(smem_u32(&full_a[0]), 0);
             bool w_in = kWOnA || (nkb > 0 && test(smem_u32(&full_w[0]), 0));
-            for (int i = 0; i < nkb; ++i) {
+            for (int i = 0; i < nkb / BPS; ++i) {  // ring slots (BPS blocks each)
                 const int s = i % AST;
                 const uint32_t ph = (uint32_t)(i / AST) & 1;
                 if (!(a_in && w_in) &&
@@ -534,7 +557,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint64_t ad = a_desc0 + (uint64_t)((s * A_BYTES) >> 4);
+                const uint64_t ad = a_desc0 + (uint64_t)((s * A_SLOT) >> 4);
                 const uint64_t bd = b_desc0 + (uint64_t)((s * W_SLOT) >> 4);
                 const uint32_t acc = i > 0 ? 1u : 0u;
                 if constexpr (F == kE4m3) {
@@ -543,15 +566,24 @@ __global__ void __launch_bounds__(THREADS, 1)
                     constexpr uint32_t id_h1 = idesc_mxf8_e4m3(BM, Fmt<F>::N1, 0, 1, 0, 0);
                     constexpr uint32_t id_l0 = idesc_mxf8_e4m3(BM, 256, 0, 1, 1, 0);
                     constexpr uint32_t id_l1 = idesc_mxf8_e4m3(BM, Fmt<F>::N1, 0, 1, 1, 0);
-                    constexpr uint64_t kB_HALF8 = (2 * W_BOX_BYTES) >> 4;
-                    // the A slot's TMEM scale slot: free, as the A slot is, once both CTAs' MMAs of
-                    // the block before in this slot are done (its producers waited for that)
-                    const uint32_t sfa = tmem_base + kSfaCol + 4 * (uint32_t)s, sfb = tmem_base + kSfbCol;
-                    tmem_cp_128x128b(sfa, smem_desc(smem_u32(sf_ring + s * Fmt<kE4m3>::SF_STAGE), 16, 128, 0));
-                    umma_mxf8(tmem_base, ad, bd, id_h0, sfa, sfb, acc);
-                    if (halves == 2) umma_mxf8(tmem_base + 256, ad, bd + kB_HALF8, id_h1, sfa, sfb, acc);
-                    umma_mxf8(tmem_base, ad + kA_K16, bd, id_l0, sfa, sfb, 1u);
-                    if (halves == 2) umma_mxf8(tmem_base + 256, ad + kA_K16, bd + kB_HALF8, id_l1, sfa, sfb, 1u);
+                    constexpr uint64_t kB_HALF8 = (2 * BPS * W_BOX_BYTES) >> 4;
+                    const uint32_t sfb = tmem_base + kSfbCol;
+                    // the slot's TMEM scale slots: free, as the A slot is, once both CTAs' MMAs of
+                    // the blocks before in this slot are done (its producers waited for that)
+#pragma unroll
+                    for (int b = 0; b < BPS; ++b) {
+                        const uint32_t sfa = tmem_base + kSfaCol + 4 * (uint32_t)(BPS * s + b);
+                        tmem_cp_128x128b(sfa, smem_desc(smem_u32(sf_ring + s * Fmt<kE4m3>::SF_STAGE + b * 2048), 16,
+                                                        128, 0));
+                        // block b: its A tile, and its 32 rows of each W atom
+                        const uint64_t adb = ad + (uint64_t)((b * A_BYTES) >> 4);
+                        const uint64_t bdb = bd + (uint64_t)((b * BK * 128) >> 4);
+                        const uint32_t accb = (i > 0 || b > 0) ? 1u : 0u;
+                        umma_mxf8(tmem_base, adb, bdb, id_h0, sfa, sfb, accb);
+                        if (halves == 2) umma_mxf8(tmem_base + 256, adb, bdb + kB_HALF8, id_h1, sfa, sfb, accb);
+                        umma_mxf8(tmem_base, adb + kA_K16, bdb, id_l0, sfa, sfb, 1u);
+                        if (halves == 2) umma_mxf8(tmem_base + 256, adb + kA_K16, bdb + kB_HALF8, id_l1, sfa, sfb, 1u);
+                    }
                 } else if (kPair) {
                     umma_bf16_pair(tmem_base, ad, bd, idesc, acc);
                     if (halves == 2) umma_bf16_pair(tmem_base + 256, ad, bd + kB_HALF, idesc, acc);
@@ -563,7 +595,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     umma_bf16(tmem_base, ad + kA_K16, bd + kB_K16, idesc, 1u);
                     if (halves == 2) umma_bf16(tmem_base + 256, ad + kA_K16, bd + kB_HALF + kB_K16, idesc, 1u);
                 }
-                if (i + 1 < nkb) {
+                if (i + 1 < nkb / BPS) {
                     arm(i + 1);
                     a_in = test(smem_u32(&full_a[(i + 1) % AST]), (uint32_t)((i + 1) / AST) & 1);
                     w_in = kWOnA || test(smem_u32(&full_w[(i + 1) % AST]), (uint32_t)((i + 1) / AST) & 1);
@@ -685,9 +717,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         // 8-bit table every other); logits and staged scales by li, the A ring by i
         for (int li = grp, i = i0 + di * grp; i < nkb; li += PGROUPS, i += di * PGROUPS) {
             const int sl = li % LSTAGES;
-            const int s = i % AST;
+            // the A ring: slot of block i (8-bit table: slot li holds blocks 2 li and 2 li + 1,
+            // this CTA's at position rank)
+            const int s = (F == kE4m3 ? li : i) % AST;
             const uint32_t ul = (uint32_t)(li / LSTAGES);
-            const uint32_t u = (uint32_t)(i / AST);
+            const uint32_t u = (uint32_t)((F == kE4m3 ? li : i) / AST);
             // every lane waits (acquire), the warp decides together; the 8-bit table's staged
             // row scales share the logits slot's index and phase
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_l[sl]), ul & 1, abort_flag) &&
@@ -849,7 +883,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 ok = false;
                 break;
             }
-            uint8_t *at = a_ring + s * A_BYTES;
+            uint8_t *at = a_ring + s * A_SLOT + (F == kE4m3 ? (int)rank * A_BYTES : 0);
+            uint8_t *sft = sf_ring + s * Fmt<kE4m3>::SF_STAGE + (int)rank * 2048;  // 8-bit table
 #pragma unroll
             for (int q = 0; q < ROWS_PER_LANE; ++q) {
                 const int r = rr[q];
@@ -861,8 +896,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 // the scale word of row r: word r / 32 of 16-byte row r, which the MMA thread
                 // copies into TMEM lane r (the MMA reads lane r's scale from column r / 32)
-                if constexpr (F == kE4m3)
-                    reinterpret_cast<uint32_t *>(sf_ring + s * Fmt<kE4m3>::SF_STAGE)[4 * r + (r >> 5)] = sf_word[q];
+                if constexpr (F == kE4m3) reinterpret_cast<uint32_t *>(sft)[4 * r + (r >> 5)] = sf_word[q];
             }
             fence_proxy_async_smem();
             __syncwarp();  // every lane's A stores (and proxy fence) before the arrival
@@ -876,8 +910,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // the partner CTA, completing on its full_a
                     const uint32_t peer = rank ^ 1u;
                     const uint32_t pbar = map_to_cta(smem_u32(&full_a[s]), peer);
-                    const uint32_t a_src = smem_u32(a_ring + s * A_BYTES + wig * 2048);
-                    const uint32_t f_src = smem_u32(sf_ring + s * Fmt<kE4m3>::SF_STAGE + wig * 512);
+                    const uint32_t a_src = smem_u32(at + wig * 2048);
+                    const uint32_t f_src = smem_u32(sft + wig * 512);
                     bulk_copy_to_cluster(map_to_cta(a_src, peer), a_src, 2048u, pbar);
                     bulk_copy_to_cluster(map_to_cta(f_src, peer), f_src, 512u, pbar);
                 }
@@ -1307,7 +1341,8 @@ __global__ void __launch_bounds__(256)
     for (int e = blockIdx.x; e < n; e += gridDim.x) {
         const int2 sr = p.redo[e];
         const int j = sr.x, row = sr.y;
-        const int64_t kb0 = (int64_t)j * p.nkb / p.splits, kb1 = (int64_t)(j + 1) * p.nkb / p.splits;
+        int64_t kb0, kb1;
+        split_range(p, j, p.splits, &kb0, &kb1);
         int64_t v0 = p.k_begin + kb0 * BK, v1 = p.k_begin + kb1 * BK;
         if (v0 < p.vocab_start) v0 = p.vocab_start;
         if (v1 > p.vocab_end) v1 = p.vocab_end;
@@ -1493,7 +1528,7 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     if (e4) {
         const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)(vocab_end - vocab_start)};
         const cuuint64_t strides[1] = {(cuuint64_t)ldw};
-        const cuuint32_t box[2] = {128, BK};
+        const cuuint32_t box[2] = {128, (cuuint32_t)(Fmt<kE4m3>::BPS * BK)};  // a ring slot's two blocks
         const cuuint32_t estr[2] = {1, 1};
         if (encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(tab.W), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1554,6 +1589,7 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     p.tail_splits = tail_splits_of(plan.splits, tail);
     p.w3d = w3d;
     p.w_scale = e4 ? tab.scale : nullptr;
+    p.pair_blocks = e4 ? 1 : 0;
     p.fused = single ? 1 : 0;
     p.logits = logits;
     p.ldl = ldl;
