@@ -36,7 +36,9 @@
 // block's exponentials against its own maximum, fold in the (normalised, staged) row scales
 // and split each value into two E4M3 parts under a power-of-two scale per (row, block) that
 // the MMA applies from TMEM; a cluster holds one row block and two 480-column tiles, and each
-// CTA computes every other block's A operand and copies it to its partner.
+// CTA computes every other block's A operand and copies it to its partner.  Each ring slot
+// holds two blocks, one from each CTA, so the MMA thread's wait, scale copy and commit serve
+// eight MMAs.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -714,7 +716,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
         // the group's blocks: this CTA's li-th block is i = i0 + di li (all blocks, or for the
-        // 8-bit table every other); logits and staged scales by li, the A ring by i
+        // 8-bit table every other); logits and staged scales by li, the A ring by i (8-bit
+        // table: by li)
         for (int li = grp, i = i0 + di * grp; i < nkb; li += PGROUPS, i += di * PGROUPS) {
             const int sl = li % LSTAGES;
             // the A ring: slot of block i (8-bit table: slot li holds blocks 2 li and 2 li + 1,
