@@ -292,8 +292,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int ntp_count = p.n_tiles / 2;
     int ntp = 0;
     if (F == kE4m3) {
-        ntp = pair % ntp_count;
-        mt = (pair / ntp_count) % p.m_tiles;
+        // the row blocks that read the same W tiles take adjacent clusters
+        mt = pair % p.m_tiles;
+        ntp = (pair / p.m_tiles) % ntp_count;
         j = pair / (ntp_count * p.m_tiles);
         S = p.splits;
         nt = 2 * ntp + (int)rank;
