@@ -7,8 +7,12 @@ self-conditioning soft embedding.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
---impl reference times the CPU oracle as it stands on the host cores, on a bounded
-sample of canvas positions per step (the pages ship no runnable reference).
+--impl reference times the CPU oracle as it stands on the host cores, one whole canvas
+(all 256 positions, full V and d) per step (the pages ship no runnable reference).
+
+--gpus N > 1 runs one replica per GPU (independent canvases, no collective on the data
+path): under torchrun (WORLD_SIZE set) each rank is one replica; without it the script
+starts torchrun itself on 127.0.0.1.  --gpus must equal WORLD_SIZE.
 """
 from __future__ import annotations
 
@@ -29,9 +33,12 @@ METRIC = "canvas positions/sec per fused sampler step (V=262144,d=2816); % of ro
 UNIT = "positions/s"
 WORKLOAD = "canvas256"
 # kernels one timed step launches: the single pass's product, statistics, redo, reduce and
-# acceptance (DGSAMP_TWO_PASS=1: statistics, product, acceptance, reduce)
+# acceptance (the two-pass step: statistics, product, acceptance, reduce)
 KERNELS_PER_STEP = 5
 KERNELS_PER_STEP_TWO_PASS = 4
+# the tensor-bound workloads timed after the headline one (their own step, single pass and
+# two passes)
+DEFAULT_ALSO = "batch8,late_batch32"
 # the denoising loop timed beside the step: a graph of 16 steps (the pages report 11 to 24
 # denoising steps per canvas), convergence after two stable steps below 1 nat of mean
 # entropy or at 24 steps
@@ -51,15 +58,13 @@ def peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def config_of(wl, extra=None) -> dict:
-    c = {"workload": f"{wl.name}: {wl.n_req} request x {wl.L_c} positions, V={wl.V}, d={wl.d}, "
-                     f"fp32 logits, bf16 W, gamma={wl.gamma}",
-         "rows": wl.R, "V": wl.V, "d": wl.d,
-         "budget_nats": list(wl.budget) if isinstance(wl.budget, tuple) else wl.budget,
-         "l2": "no flush: each step reads 1.62 GiB of logits and W, 13x the 129 MB L2"}
-    if extra:
-        c.update(extra)
-    return c
+def config_of(wl) -> dict:
+    """The workload a line is measured on; identical for the native and the reference arm."""
+    return {"workload": f"{wl.name}: {wl.n_req} request x {wl.L_c} positions, V={wl.V}, d={wl.d}, "
+                        f"fp32 logits, bf16 W, gamma={wl.gamma}",
+            "rows": wl.R, "V": wl.V, "d": wl.d,
+            "budget_nats": list(wl.budget) if isinstance(wl.budget, tuple) else wl.budget,
+            "l2": "no flush: each step reads 1.62 GiB of logits and W, 13x the 129 MB L2"}
 
 
 def source_sha(files=("soft_embed.cu", "dg_common.cuh")) -> str:
@@ -150,25 +155,27 @@ def cpu_baseline(x, Wb, wl, min_seconds: float = 10.0) -> dict:
 
 
 def run_reference(args) -> None:
+    """The oracle as it stands, one whole canvas per step (statistics, acceptance and the
+    soft embedding of all 256 positions over the full vocabulary) on the host cores."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    import numpy as np
     from denoising_sampler_step_gb300 import inputs
     wl = inputs.WORKLOADS[WORKLOAD]
     x = inputs.logits(wl)
     Wb = inputs.embedding_bf16(wl)
-    rows_per_step = 1
-    rng = np.random.default_rng(0)
+    import numpy as np
+    rows = np.arange(wl.R)
     for _ in range(args.warmup):
-        oracle_seconds(x, Wb, wl, rng.choice(wl.R, rows_per_step, replace=False), float(wl.budget))
-    times = [oracle_seconds(x, Wb, wl, rng.choice(wl.R, rows_per_step, replace=False), float(wl.budget))
-             for _ in range(args.steps)]
+        oracle_seconds(x, Wb, wl, rows, float(wl.budget))
+    times = [oracle_seconds(x, Wb, wl, rows, float(wl.budget)) for _ in range(args.steps)]
     total = sum(times)
-    value = rows_per_step * args.steps / total
-    sample = (f"{rows_per_step} random canvas position(s) of {wl.name} per step (full V and d per row), "
-              f"fp64 oracle; {total:.1f} s over {args.steps} steps")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+    value = wl.R * args.steps / total
+    sample = (f"{args.steps} whole-canvas steps of {wl.name} ({wl.R} positions each, full V and d): fp64 "
+              f"statistics, acceptance and soft embedding, {total:.1f} s; numpy BLAS and the oracle's row "
+              f"pool on all host cores")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_of(wl),
@@ -180,43 +187,55 @@ def run_reference(args) -> None:
 
 # --------------------------------------------------------------------------- GPU arm
 
-def other_configs(args, dev, B, inputs, SamplerStep) -> dict:
-    """The step at further workloads (fresh inputs each): ms per step and the product's
-    tensor rate, single pass and two passes (DGSAMP_TWO_PASS=1)."""
+def other_configs(args, dev, B, inputs, SamplerStep, cost) -> dict:
+    """The step at further workloads (fresh inputs each): ms per step, the product's tensor
+    rate and the fraction of the step roofline, single pass and two passes."""
     import numpy as np
     import torch
+    pk = peaks()
     res = {}
     for name in [n for n in args.also.split(",") if n]:
         wl = inputs.WORKLOADS[name]
         xd = torch.from_numpy(inputs.logits(wl)).to(dev)
         Wd = torch.from_numpy(inputs.embedding_bf16(wl).view(np.int16)).to(dev).view(torch.bfloat16)
         bd = torch.from_numpy(inputs.budgets(wl)).to(dev)
-        st = SamplerStep(Wd, wl.n_req, wl.L_c, wl.V, wl.gamma, device=dev)
+        sc = cost.StepCost(rows=wl.R, V=wl.V, d=wl.d, vocab=wl.V)
+        t_roof = sc.roofline_seconds(pk["hbm_gbs"], pk["bf16_tflops"])
+        t_roof_sus = sc.roofline_seconds(pk["hbm_gbs"], pk["bf16_tflops_sustained"] or pk["bf16_tflops"])
         n = max(3, min(args.steps, int(2000 // max(1, wl.R // 256))))
-        out = {"rows": wl.R, "steps": n}
+        out = {"rows": wl.R, "steps": n, "t_roof_us": t_roof * 1e6,
+               "bound": "tensor" if sc.flops / (pk["bf16_tflops"] * 1e12) >= t_roof * 0.999 else "hbm",
+               "config": config_of(wl)}
         for mode in ("single_pass", "two_pass"):
-            if mode == "two_pass":
-                os.environ["DGSAMP_TWO_PASS"] = "1"
-            try:
-                for _ in range(3):
-                    st(xd, bd)
-                torch.cuda.synchronize(dev)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                for _ in range(n):
-                    st(xd, bd)
-                e1.record()
-                torch.cuda.synchronize(dev)
-                B.dg_get_device_status()
-            finally:
-                os.environ.pop("DGSAMP_TWO_PASS", None)
+            st = SamplerStep(Wd, wl.n_req, wl.L_c, wl.V, wl.gamma, device=dev, two_pass=mode == "two_pass")
+            for _ in range(3):
+                st(xd, bd)
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(n):
+                st(xd, bd)
+            e1.record()
+            torch.cuda.synchronize(dev)
+            B.dg_get_device_status()
             ms = e0.elapsed_time(e1) / n
             out[mode] = {"ms_per_step": ms, "positions_per_s": wl.R / (ms * 1e-3),
-                         "tflops": 2.0 * wl.R * wl.V * wl.d / (ms * 1e-3) / 1e12}
+                         "tflops": sc.flops / (ms * 1e-3) / 1e12,
+                         "frac": t_roof / (ms * 1e-3), "frac_sustained_peak": t_roof_sus / (ms * 1e-3)}
+            del st
         res[name] = out
-        del st, xd, Wd
+        del xd, Wd
         torch.cuda.empty_cache()
     return res
+
+
+def spawn_ranks(args) -> int:
+    """--gpus N > 1 without torchrun: start torchrun on 127.0.0.1 with N ranks running this
+    script (same arguments) and return its exit status."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+           "--master-addr", "127.0.0.1", "--master-port", str(args.master_port), os.path.abspath(__file__)]
+    cmd += sys.argv[1:]
+    return subprocess.call(cmd)
 
 
 def main() -> None:
@@ -226,10 +245,11 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--also", default="",
-                    help="comma-separated further workloads (e.g. batch8,late_batch32) whose step is "
-                         "timed after the main one and reported under other_configs (single pass and "
-                         "two passes)")
+    ap.add_argument("--also", default=DEFAULT_ALSO,
+                    help="comma-separated further workloads whose step is timed after the main one and "
+                         "reported under other_configs (single pass and two passes); '' for none")
+    ap.add_argument("--master-port", type=int, default=29531,
+                    help="rendezvous port when --gpus N > 1 starts its own ranks")
     ap.add_argument("--only", choices=["soft_embed", "step", "soft_embed_e4m3", "step_e4m3"], default=None,
                     help="profiling target: run only this call (warm-up, then --steps calls) and print "
                          "its mean duration; no JSON line")
@@ -238,6 +258,11 @@ def main() -> None:
                          "each, sampling clocks and power every 20 ms")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        sys.exit(spawn_ranks(args))
+    world_env = int(os.environ.get("WORLD_SIZE", "1"))
+    if world_env != args.gpus:
+        sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world_env}: start one rank per GPU")
     if args.impl == "reference":
         run_reference(args)
         return
@@ -535,15 +560,20 @@ def main() -> None:
     pk = peaks()
     sc = cost.StepCost(rows=wl.R, V=wl.V, d=wl.d, vocab=wl.V)
     t_roof = sc.roofline_seconds(pk["hbm_gbs"], pk["bf16_tflops"])
+    ms_step = ms / args.steps
+    # the kernels one step runs (the single pass: the product with the statistics folded, the
+    # statistics merge, the redo pass, the split-K reduce, the acceptance), timed together as
+    # the step, against the step's algorithmic bytes; the plain product call beside it
+    achieved_step = sc.step_bytes / (ms_step * 1e-3) / 1e9
     achieved = sc.gemm_bytes / (comp["soft_embed"] * 1e-3) / 1e9
-    traffic = None
+    traffic, traffic_step = None, None
     tpath = os.path.join(ROOT, "profiles", "soft_embed_traffic.json")
     if os.path.exists(tpath):
         with open(tpath) as f:
             tj = json.load(f)
         if tj.get("kernel_source_sha") == source_sha():
             traffic = tj.get("traffic_bytes_per_launch")
-    ms_step = ms / args.steps
+            traffic_step = tj.get("step_traffic_bytes")
     line = {
         "metric": METRIC,
         "value": replicas.whole_job_rate(wl.R, args.steps, world, ms),
@@ -557,14 +587,22 @@ def main() -> None:
         "vs_baseline": None,
         "dtype": "f32 statistics, bf16 x bf16 -> f32 tensor-core product",
         "data": "synthetic",
-        "config": config_of(wl, {"parallelism": f"replicas x{world} (independent canvases per GPU)"}),
+        "config": config_of(wl),
+        "parallelism": f"replicas x{world} (independent canvases per GPU, no collective on the data path)",
         "step_roofline": {"t_roof_us": t_roof * 1e6, "t_step_us": ms_step * 1e3,
                           "frac": t_roof / (ms_step * 1e-3), "peaks": pk["source"]},
-        "roofline": {"kernel": "soft_embed (tcgen05 product + split-K reduce)", "bound": "hbm",
-                     "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
-                     "algorithmic_bytes_per_launch": sc.gemm_bytes, "launch_us": comp["soft_embed"] * 1e3,
-                     "peak_source": pk["source"]},
+        "roofline": {"kernel": "dg_sampler_step, single pass: soft_embed_kernel<0> with the statistics "
+                               "folded (the dominant kernel) + statistics merge + redo + split-K reduce + "
+                               "acceptance, one call", "bound": "hbm",
+                     "achieved": achieved_step, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved_step / pk["hbm_gbs"], "traffic": traffic_step,
+                     "algorithmic_bytes_per_launch": sc.step_bytes, "launch_us": ms_step * 1e3,
+                     "peak_source": pk["source"], "timed": "CUDA events around the timed steps"},
+        "roofline_product": {"kernel": "dg_soft_embed (soft_embed_kernel<0> + split-K reduce), statistics given",
+                             "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                             "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+                             "algorithmic_bytes_per_launch": sc.gemm_bytes,
+                             "launch_us": comp["soft_embed"] * 1e3, "peak_source": pk["source"]},
         "kernel_us": {k: v * 1e3 for k, v in comp.items()},
         "e2e": {"value": replicas.whole_job_rate(wl.R, args.steps, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": step.h2d_bytes(h), "d2h_bytes_per_step": step.d2h_bytes(),
@@ -576,14 +614,13 @@ def main() -> None:
         "loop": loop,
         "loop_sampled": loop_sampled,
         "e4m3_table": e4m3,
-        "gpu_launches": (KERNELS_PER_STEP_TWO_PASS if os.environ.get("DGSAMP_TWO_PASS") == "1"
-                         else KERNELS_PER_STEP) * args.steps,
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
         "clocks": clk,
     }
     if sustained is not None:
         line["sustained"] = sustained
-    if args.also:
-        line["other_configs"] = other_configs(args, dev, B, inputs, SamplerStep)
+    if args.also and not args.sustained:
+        line["other_configs"] = other_configs(args, dev, B, inputs, SamplerStep, cost)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(x, Wb, wl)
     if rank == 0:

@@ -24,6 +24,10 @@ if not os.path.exists(LIB_PATH):
 lib = ctypes.CDLL(LIB_PATH)
 
 _i64, _i32, _f32, _p, _sz = ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+_u32 = ctypes.c_uint32
+
+# flags of the sampler-step calls (dg_step_flags)
+DG_STEP_TWO_PASS = 1
 
 lib.dg_version.restype = ctypes.c_int
 lib.dg_last_error.restype = ctypes.c_char_p
@@ -40,7 +44,7 @@ lib.dg_entropy_accept.restype = ctypes.c_int
 lib.dg_sum_partials.argtypes = [ctypes.POINTER(_p), _i32, _i64, _i64, _i64, _f32, _p, _i64, _p]
 lib.dg_sum_partials.restype = ctypes.c_int
 lib.dg_sampler_step.argtypes = [_p, _i32, _i32, _i64, _i64, _p, _i64, _i64, _i64, _i64, _i64, _f32, _p, _i32,
-                                _p, _p, _p, _p, _p, _p, _p, _p, _p, _i64, _p, _sz, _p]
+                                _p, _p, _p, _p, _p, _p, _p, _p, _p, _i64, _u32, _p, _sz, _p]
 lib.dg_sampler_step.restype = ctypes.c_int
 lib.dg_get_device_status.argtypes = [_p]
 lib.dg_get_device_status.restype = ctypes.c_int
@@ -55,7 +59,7 @@ lib.dg_loop_update.restype = ctypes.c_int
 lib.dg_sampler_loop_step.argtypes = [_p, _i32, _i32, _i64, _i64, _p, _i64, _i64, _i64, _i64, _i64, _f32, _p, _i32,
                                      _i32, _f32, _i32, _f32, ctypes.c_uint64, ctypes.c_uint64,
                                      _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i64,
-                                     _p, _p, _p, _p, _p, _p, _p, _sz, _p]
+                                     _p, _p, _p, _p, _p, _p, _u32, _p, _sz, _p]
 lib.dg_row_stats_sample.argtypes = [_p, _i64, _i64, _i64, _f32, ctypes.c_uint64, ctypes.c_uint64,
                                     _p, _p, _p, _p, _p, _p, _p, _p]
 lib.dg_row_stats_sample.restype = ctypes.c_int
@@ -72,12 +76,12 @@ lib.dg_soft_embed_e4m3.argtypes = [_p, _i64, _p, _i64, _i64, _i64, _p, _p, _i64,
                                    _sz, _p]
 lib.dg_soft_embed_e4m3.restype = ctypes.c_int
 lib.dg_sampler_step_e4m3.argtypes = [_p, _i32, _i32, _i64, _i64, _p, _p, _i64, _i64, _i64, _i64, _i64, _f32, _p,
-                                     _i32, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i64, _p, _sz, _p]
+                                     _i32, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i64, _u32, _p, _sz, _p]
 lib.dg_sampler_step_e4m3.restype = ctypes.c_int
 lib.dg_sampler_loop_step_e4m3.argtypes = [_p, _i32, _i32, _i64, _i64, _p, _p, _i64, _i64, _i64, _i64, _i64, _f32, _p,
                                           _i32, _i32, _f32, _i32, _f32, ctypes.c_uint64, ctypes.c_uint64,
                                           _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i64,
-                                          _p, _p, _p, _p, _p, _p, _p, _sz, _p]
+                                          _p, _p, _p, _p, _p, _p, _u32, _p, _sz, _p]
 lib.dg_sampler_loop_step_e4m3.restype = ctypes.c_int
 
 STATUS = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED", 3: "DG_ERR_CUDA", 4: "DG_ERR_TIMEOUT"}
@@ -108,6 +112,10 @@ def _ld(t: torch.Tensor) -> int:
     if t.dim() != 2 or t.stride(1) != 1:
         raise ValueError("expected a 2-D tensor with unit column stride")
     return t.stride(0)
+
+
+def _flags(two_pass: bool) -> int:
+    return DG_STEP_TWO_PASS if two_pass else 0
 
 
 def _new(shape, dtype, device):
@@ -271,7 +279,7 @@ def dg_soft_embed_e4m3(logits: torch.Tensor, lse: torch.Tensor, vocab_start: int
 def dg_sampler_step_e4m3(logits: torch.Tensor, n_req: int, L_c: int, Q: torch.Tensor, scale: torch.Tensor,
                          gamma: float, budgets: torch.Tensor, min_accept: int = 0, vocab_start: int = 0,
                          vocab_end: int | None = None, V: int | None = None, out: dict | None = None,
-                         ws: torch.Tensor | None = None, stream=None) -> dict:
+                         ws: torch.Tensor | None = None, stream=None, two_pass: bool = False) -> dict:
     """dg_sampler_step with the 8-bit table (Q uint8 [rows_pad, d], scale fp32 [rows_pad])."""
     R = n_req * L_c
     V = logits.shape[1] if V is None else V
@@ -289,7 +297,8 @@ def dg_sampler_step_e4m3(logits: torch.Tensor, n_req: int, L_c: int, Q: torch.Te
                                     vocab_end, Q.shape[0], _ld(Q), d, gamma, _ptr(budgets), min_accept,
                                     _ptr(o["m"]), _ptr(o["lse"]), _ptr(o["H"]), _ptr(o["kappa"]), _ptr(o["argmax"]),
                                     _ptr(o["order"]), _ptr(o["mask"]), _ptr(o["n_accepted"]), _ptr(o["E"]),
-                                    _ld(o["E"]), _ptr(ws), ws.numel(), _stream(stream)), "dg_sampler_step_e4m3")
+                                    _ld(o["E"]), _flags(two_pass), _ptr(ws), ws.numel(), _stream(stream)),
+           "dg_sampler_step_e4m3")
     return o
 
 
@@ -320,8 +329,9 @@ def dg_sum_partials(partials: list, gamma: float, out: torch.Tensor | None = Non
 def dg_sampler_step(logits: torch.Tensor, n_req: int, L_c: int, W: torch.Tensor, gamma: float,
                     budgets: torch.Tensor, min_accept: int = 0, vocab_start: int = 0, vocab_end: int | None = None,
                     V: int | None = None, out: dict | None = None, ws: torch.Tensor | None = None,
-                    stream=None) -> dict:
-    """One fused sampler step; returns dict m, lse, H, kappa, argmax, order, mask, n_accepted, E."""
+                    stream=None, two_pass: bool = False) -> dict:
+    """One fused sampler step; returns dict m, lse, H, kappa, argmax, order, mask, n_accepted, E.
+    two_pass: statistics before the product even over the whole vocabulary (DG_STEP_TWO_PASS)."""
     R = n_req * L_c
     V = logits.shape[1] if V is None else V
     vocab_end = V if vocab_end is None else vocab_end
@@ -337,8 +347,8 @@ def dg_sampler_step(logits: torch.Tensor, n_req: int, L_c: int, W: torch.Tensor,
     _check(lib.dg_sampler_step(_ptr(logits), n_req, L_c, V, _ld(logits), _ptr(W), vocab_start, vocab_end,
                                W.shape[0], _ld(W), d, gamma, _ptr(budgets), min_accept, _ptr(o["m"]), _ptr(o["lse"]),
                                _ptr(o["H"]), _ptr(o["kappa"]), _ptr(o["argmax"]), _ptr(o["order"]), _ptr(o["mask"]),
-                               _ptr(o["n_accepted"]), _ptr(o["E"]), _ld(o["E"]), _ptr(ws), ws.numel(),
-                               _stream(stream)), "dg_sampler_step")
+                               _ptr(o["n_accepted"]), _ptr(o["E"]), _ld(o["E"]), _flags(two_pass), _ptr(ws),
+                               ws.numel(), _stream(stream)), "dg_sampler_step")
     return o
 
 
@@ -387,7 +397,8 @@ def dg_sampler_loop_step(logits: torch.Tensor, n_req: int, L_c: int, W: torch.Te
                          budgets: torch.Tensor, state: dict, stable_steps: int, entropy_threshold: float,
                          step_limit: int, min_accept: int = 0, vocab_start: int = 0, vocab_end: int | None = None,
                          V: int | None = None, out: dict | None = None, ws: torch.Tensor | None = None,
-                         temperature: float = 0.0, seed: int = 0, offset: int = 0, stream=None) -> dict:
+                         temperature: float = 0.0, seed: int = 0, offset: int = 0, stream=None,
+                         two_pass: bool = False) -> dict:
     """One denoising-loop step: the fused step over the eligible positions, then the loop
     update of `state` in place.  Returns the step outputs as dg_sampler_step does, plus
     `candidate` (the drawn tokens) when temperature > 0."""
@@ -411,8 +422,8 @@ def dg_sampler_loop_step(logits: torch.Tensor, n_req: int, L_c: int, W: torch.Te
                                     _ptr(o["lse"]), _ptr(o["H"]), _ptr(o["kappa"]), _ptr(o["argmax"]),
                                     _ptr(o.get("candidate")), _ptr(o["order"]), _ptr(o["mask"]),
                                     _ptr(o["n_accepted"]), _ptr(o["E"]), _ld(o["E"]),
-                                    *[_ptr(state[k]) for k in LOOP_STATE_KEYS], _ptr(ws), ws.numel(),
-                                    _stream(stream)), "dg_sampler_loop_step")
+                                    *[_ptr(state[k]) for k in LOOP_STATE_KEYS], _flags(two_pass), _ptr(ws),
+                                    ws.numel(), _stream(stream)), "dg_sampler_loop_step")
     return o
 
 
@@ -421,7 +432,7 @@ def dg_sampler_loop_step_e4m3(logits: torch.Tensor, n_req: int, L_c: int, Q: tor
                               entropy_threshold: float, step_limit: int, min_accept: int = 0, vocab_start: int = 0,
                               vocab_end: int | None = None, V: int | None = None, out: dict | None = None,
                               ws: torch.Tensor | None = None, temperature: float = 0.0, seed: int = 0, offset: int = 0,
-                              stream=None) -> dict:
+                              stream=None, two_pass: bool = False) -> dict:
     """dg_sampler_loop_step with the 8-bit table (Q uint8 [rows_pad, d], scale fp32 [rows_pad])."""
     R = n_req * L_c
     V = logits.shape[1] if V is None else V
@@ -443,8 +454,8 @@ def dg_sampler_loop_step_e4m3(logits: torch.Tensor, n_req: int, L_c: int, Q: tor
                                          _ptr(o["m"]), _ptr(o["lse"]), _ptr(o["H"]), _ptr(o["kappa"]),
                                          _ptr(o["argmax"]), _ptr(o.get("candidate")), _ptr(o["order"]),
                                          _ptr(o["mask"]), _ptr(o["n_accepted"]), _ptr(o["E"]), _ld(o["E"]),
-                                         *[_ptr(state[k]) for k in LOOP_STATE_KEYS], _ptr(ws), ws.numel(),
-                                         _stream(stream)), "dg_sampler_loop_step_e4m3")
+                                         *[_ptr(state[k]) for k in LOOP_STATE_KEYS], _flags(two_pass), _ptr(ws),
+                                         ws.numel(), _stream(stream)), "dg_sampler_loop_step_e4m3")
     return o
 
 

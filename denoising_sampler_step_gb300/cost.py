@@ -76,6 +76,12 @@ class StepCost:
         return self.rows * self.vocab * F32_BYTES + self.w_bytes + self.out_bytes
 
     @property
+    def step_bytes(self) -> int:
+        """One fused step: the logits once, W once, E, and per row the statistics (m, lse, H,
+        kappa, argmax), the order entry and the mask byte."""
+        return self.gemm_bytes + self.rows * (5 * 4 + 4 + 1)
+
+    @property
     def e4m3_table_bytes(self) -> int:
         """The 8-bit table of the slice: one E4M3 code per entry and one fp32 scale per row."""
         return self.vocab * self.d + self.vocab * F32_BYTES

@@ -344,13 +344,11 @@ dg_status dg_sum_partials(const float *const *partials, int32_t T, int64_t R, in
 namespace {
 
 // The step reads the logits once (the product folds the row statistics) when the slice is
-// the whole vocabulary and the workspace has room; DGSAMP_TWO_PASS=1 forces the statistics
-// pass before the product (for comparisons).
+// the whole vocabulary and the workspace has room, unless the caller asks for two passes.
 bool use_single_pass(int64_t R, int64_t V, int64_t vocab_start, int64_t vocab_end, int64_t d, size_t ws_bytes,
-                     int fmt) {
+                     int fmt, uint32_t flags) {
     if (vocab_start != 0 || vocab_end != V) return false;
-    if (const char *env = getenv("DGSAMP_TWO_PASS"))
-        if (env[0] == '1') return false;
+    if (flags & DG_STEP_TWO_PASS) return false;
     const int sms = device_sm_count();
     SoftEmbedPlan plan;
     if (sms <= 0 || !plan_soft_embed(R, vocab_start, vocab_end, d, sms, &plan, fmt)) return false;
@@ -363,8 +361,9 @@ dg_status run_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, i
                    int64_t vocab_start, int64_t vocab_end, int64_t rows_pad, int64_t d, float gamma,
                    const float *budgets, int32_t min_accept, float *m, float *lse, float *H, float *kappa,
                    int32_t *argmax, int32_t *order, uint8_t *mask, int32_t *n_accepted, float *E, int64_t ldo,
-                   void *workspace, size_t workspace_bytes, cudaStream_t s, const LoopArgs *loop) {
+                   void *workspace, size_t workspace_bytes, cudaStream_t s, const LoopArgs *loop, uint32_t flags) {
     if (n_req < 0 || L_c < 1) return fail(DG_ERR_INVALID_ARG, "step: need n_req >= 0 and L_c >= 1");
+    if (flags & ~(uint32_t)DG_STEP_TWO_PASS) return fail(DG_ERR_INVALID_ARG, "step: unknown flags 0x%x", flags);
     const int64_t R = (int64_t)n_req * L_c;
     dg_status st = check_stats_args(logits, R, V, ldl);
     if (st != DG_OK) return st;
@@ -387,7 +386,7 @@ dg_status run_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, i
     if (R == 0) return DG_OK;
     const uint8_t *eligible = loop ? loop->eligible : nullptr;
     const bool draw_t1 = sampled && loop->temperature == 1.0f;  // the single pass folds this draw
-    if ((!sampled || draw_t1) && use_single_pass(R, V, vocab_start, vocab_end, d, workspace_bytes, W.fmt)) {
+    if ((!sampled || draw_t1) && use_single_pass(R, V, vocab_start, vocab_end, d, workspace_bytes, W.fmt, flags)) {
         // one read of the logits: the product folds the statistics (and at temperature 1 the
         // draw); the acceptance runs on them after the reduce starts
         AcceptArgs acc{H, kappa, budgets, n_req, L_c, min_accept, order, mask, n_accepted, eligible};
@@ -432,11 +431,11 @@ dg_status dg_sampler_step(const float *logits, int32_t n_req, int32_t L_c, int64
                           int64_t vocab_start, int64_t vocab_end, int64_t rows_pad, int64_t ldw, int64_t d,
                           float gamma, const float *budgets, int32_t min_accept, float *m, float *lse, float *H,
                           float *kappa, int32_t *argmax, int32_t *order, uint8_t *mask, int32_t *n_accepted, float *E,
-                          int64_t ldo, void *workspace, size_t workspace_bytes, dg_stream_t stream) {
+                          int64_t ldo, uint32_t flags, void *workspace, size_t workspace_bytes, dg_stream_t stream) {
     t_last_error[0] = 0;
     return run_step(logits, n_req, L_c, V, ldl, EmbedTable{kTableBf16, W, ldw, nullptr}, vocab_start, vocab_end,
                     rows_pad, d, gamma, budgets, min_accept, m, lse, H, kappa, argmax, order, mask, n_accepted, E,
-                    ldo, workspace, workspace_bytes, (cudaStream_t)stream, nullptr);
+                    ldo, workspace, workspace_bytes, (cudaStream_t)stream, nullptr, flags);
 }
 
 dg_status dg_sampler_step_e4m3(const float *logits, int32_t n_req, int32_t L_c, int64_t V, int64_t ldl,
@@ -444,11 +443,11 @@ dg_status dg_sampler_step_e4m3(const float *logits, int32_t n_req, int32_t L_c, 
                                int64_t rows_pad, int64_t ldq, int64_t d, float gamma, const float *budgets,
                                int32_t min_accept, float *m, float *lse, float *H, float *kappa, int32_t *argmax,
                                int32_t *order, uint8_t *mask, int32_t *n_accepted, float *E, int64_t ldo,
-                               void *workspace, size_t workspace_bytes, dg_stream_t stream) {
+                               uint32_t flags, void *workspace, size_t workspace_bytes, dg_stream_t stream) {
     t_last_error[0] = 0;
     return run_step(logits, n_req, L_c, V, ldl, EmbedTable{kTableE4m3, Q, ldq, scale}, vocab_start, vocab_end,
                     rows_pad, d, gamma, budgets, min_accept, m, lse, H, kappa, argmax, order, mask, n_accepted, E,
-                    ldo, workspace, workspace_bytes, (cudaStream_t)stream, nullptr);
+                    ldo, workspace, workspace_bytes, (cudaStream_t)stream, nullptr, flags);
 }
 
 dg_status dg_sampler_loop_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, int64_t ldl,
@@ -459,13 +458,13 @@ dg_status dg_sampler_loop_step(const float *logits, int32_t n_req, int32_t L_c, 
                                float *kappa, int32_t *argmax, int32_t *candidate, int32_t *order, uint8_t *mask,
                                int32_t *n_accepted, float *E, int64_t ldo, int32_t *canvas, uint8_t *eligible,
                                int32_t *prev_argmax, int32_t *stable, int32_t *steps, uint8_t *converged,
-                               void *workspace, size_t workspace_bytes, dg_stream_t stream) {
+                               uint32_t flags, void *workspace, size_t workspace_bytes, dg_stream_t stream) {
     t_last_error[0] = 0;
     LoopArgs loop{stable_steps, entropy_threshold, step_limit, temperature, seed, offset, candidate, canvas,
                   eligible, prev_argmax, stable, steps, converged};
     return run_step(logits, n_req, L_c, V, ldl, EmbedTable{kTableBf16, W, ldw, nullptr}, vocab_start, vocab_end,
                     rows_pad, d, gamma, budgets, min_accept, m, lse, H, kappa, argmax, order, mask, n_accepted, E,
-                    ldo, workspace, workspace_bytes, (cudaStream_t)stream, &loop);
+                    ldo, workspace, workspace_bytes, (cudaStream_t)stream, &loop, flags);
 }
 
 dg_status dg_sampler_loop_step_e4m3(const float *logits, int32_t n_req, int32_t L_c, int64_t V, int64_t ldl,
@@ -476,14 +475,14 @@ dg_status dg_sampler_loop_step_e4m3(const float *logits, int32_t n_req, int32_t 
                                     float *lse, float *H, float *kappa, int32_t *argmax, int32_t *candidate,
                                     int32_t *order, uint8_t *mask, int32_t *n_accepted, float *E, int64_t ldo,
                                     int32_t *canvas, uint8_t *eligible, int32_t *prev_argmax, int32_t *stable,
-                                    int32_t *steps, uint8_t *converged, void *workspace, size_t workspace_bytes,
-                                    dg_stream_t stream) {
+                                    int32_t *steps, uint8_t *converged, uint32_t flags, void *workspace,
+                                    size_t workspace_bytes, dg_stream_t stream) {
     t_last_error[0] = 0;
     LoopArgs loop{stable_steps, entropy_threshold, step_limit, temperature, seed, offset, candidate, canvas,
                   eligible, prev_argmax, stable, steps, converged};
     return run_step(logits, n_req, L_c, V, ldl, EmbedTable{kTableE4m3, Q, ldq, scale}, vocab_start, vocab_end,
                     rows_pad, d, gamma, budgets, min_accept, m, lse, H, kappa, argmax, order, mask, n_accepted, E,
-                    ldo, workspace, workspace_bytes, (cudaStream_t)stream, &loop);
+                    ldo, workspace, workspace_bytes, (cudaStream_t)stream, &loop, flags);
 }
 
 dg_status dg_entropy_accept_eligible(const float *H, const float *kappa, const uint8_t *eligible, int32_t n_req,

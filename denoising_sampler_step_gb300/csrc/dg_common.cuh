@@ -161,9 +161,9 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
-// Loads of a tcgen05 CTA pair: the tile lands in the executing CTA's shared memory and the
-// byte count completes on `bar`, which may be the barrier of the pair's other CTA (a
-// shared::cluster address).
+// Loads of a tcgen05 CTA pair (cta_group::2): the tile lands in the executing CTA's shared
+// memory and the byte count completes on `bar`, which may be the barrier of the pair's other
+// CTA (a shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void *tmap, uint32_t bar, int x, int y,
                                                       uint64_t policy) {
     asm volatile(
@@ -181,17 +181,6 @@ __device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const void *
         : "memory");
 }
 
-// The same load delivered to the same shared-memory offset of every CTA in cta_mask
-// (this GPU's own memory only); each destination's barrier at `bar` gets the bytes.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void *tmap, uint32_t bar, int x, int y,
-                                                      uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(tmap), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
-        : "memory");
-}
-
 // As tma_load_2d, with an L2 cache-eviction policy for the fetched lines.
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *tmap, uint32_t bar, int x, int y,
                                                  uint64_t policy) {
@@ -202,23 +191,13 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *tmap,
         : "memory");
 }
 
-// As tma_load_2d_multicast, with an L2 cache-eviction policy for the fetched lines.
-__device__ __forceinline__ void tma_load_2d_multicast_hint(uint32_t dst, const void *tmap, uint32_t bar, int x,
-                                                           int y, uint16_t cta_mask, uint64_t policy) {
+// As tma_load_2d_hint for a 3-D tensor map (x innermost).
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap, uint32_t bar, int x, int y, int z,
+                                                 uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(dst),
-        "l"(tmap), "r"(bar), "r"(x), "r"(y), "h"(cta_mask), "l"(policy)
-        : "memory");
-}
-
-// As tma_load_2d_multicast_hint for a 3-D tensor map (x innermost).
-__device__ __forceinline__ void tma_load_3d_multicast_hint(uint32_t dst, const void *tmap, uint32_t bar, int x,
-                                                           int y, int z, uint16_t cta_mask, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6, %7;" ::"r"(dst),
-        "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(cta_mask), "l"(policy)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
         : "memory");
 }
 
@@ -299,7 +278,9 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc,
         : "memory");
 }
 
-__device__ __forceinline__ void umma_commit_pair_multicast(uint32_t bar, uint16_t cta_mask) {
+// The barrier at the same offset in every CTA of cta_mask receives one arrival once every
+// tcgen05.mma of the pair issued so far by this thread has finished (a signal, not a load).
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t cta_mask) {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
             bar),

@@ -232,13 +232,7 @@ int stats_cluster_size(int64_t R, int64_t V) {
 
 cudaError_t launch_row_stats(const float *logits, int64_t R, int64_t V, int64_t ldl, float *m, float *lse,
                              float *H, float *kappa, int32_t *argmax, cudaStream_t stream) {
-    int c = stats_cluster_size(R, V);
-    // tuning override: DGSAMP_STATS_CLUSTER=1|2|4|8 forces the CTAs per row
-    if (const char *env = getenv("DGSAMP_STATS_CLUSTER")) {
-        const int v = atoi(env);
-        if (v == 1 || v == 2 || v == 4 || v == 8) c = v;
-    }
-    switch (c) {
+    switch (stats_cluster_size(R, V)) {
         case 1: return launch_stats<1>(logits, R, V, ldl, m, lse, H, kappa, argmax, stream);
         case 2: return launch_stats<2>(logits, R, V, ldl, m, lse, H, kappa, argmax, stream);
         case 4: return launch_stats<4>(logits, R, V, ldl, m, lse, H, kappa, argmax, stream);

@@ -7,23 +7,24 @@
 // padded shard rows are never part of the product).
 //
 // Kernel design (the one dense contraction of the step, on the tcgen05 tensor cores):
-//   - a cluster of two CTAs owns 256 output rows (128 each) x up to 512 output
-//     columns and one contiguous range of 32-entry vocabulary blocks (split-K over
+//   - a cluster of two CTAs, a tcgen05 CTA pair, owns 256 output rows (128 each) x up to
+//     512 output columns and one contiguous range of 32-entry vocabulary blocks (split-K over
 //     the vocabulary); each CTA's fp32 accumulator fills its 512 TMEM columns;
-//   - per block, each CTA loads its logits tile [128 x 32] fp32 by TMA into a logits ring
-//     (warp 2) and half of the W tile [32 x 512] bf16 by TMA multicast into both CTAs'
-//     W ring (warp 0), so every W byte leaves L2 once per cluster; a W slot is
-//     released when both CTAs' MMAs have read it, an A slot when this CTA's have;
+//   - per block, each CTA loads its logits tile [128 x 32] fp32 by TMA and 128 of every 256
+//     columns of the W tile [32 x 512] bf16 (the pair form of the TMA load, counted on the
+//     even CTA's barrier): every W byte leaves L2 once, and W and A share a six-deep ring;
 //   - eight producer warps (two groups of four taking alternate blocks, 32 rows each) turn
 //     the logits tile into the bf16 A operand, exp2(l*log2e - lse*log2e) rounded to
 //     nearest even, in the K-major 64-byte-swizzled layout, and hand the logits slot
 //     back at once; the probabilities never go to global memory;
-//   - warp 1 issues tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32) for the two
-//     256-column halves; tcgen05.commit, multicast to both CTAs, frees the stage once
-//     both have consumed it;
-//   - the same eight warps then read the accumulator with tcgen05.ld and store the
-//     partial tile; splitk_reduce_kernel adds the split partials in split order,
-//     multiplies by gamma and writes E (bitwise reproducible).
+//   - one thread of the even CTA issues tcgen05.mma.cta_group::2 (M=256 over both CTAs' rows,
+//     N=256, K=16, bf16 x bf16 -> fp32) for the two 256-column halves once its producers
+//     have arrived, both CTAs' W bytes have landed and the odd CTA's producers have signalled
+//     (a 16-byte bulk copy per warp onto the same barrier); tcgen05.commit to both CTAs frees
+//     the W and A slots once the MMAs have read them;
+//   - every warp then reads the accumulator with tcgen05.ld and stores the partial tile;
+//     splitk_reduce_kernel adds the split partials in split order, multiplies by gamma
+//     and writes E (bitwise reproducible).
 //   A column tail of 256 or fewer (d = 2816 = 5 x 512 + 256) is a half-width tile; it gets
 //   as many splits as the full tiles, since a block's time is set by the stage round trip.
 //   W loads mark their lines evict-first, which keeps the logits (read by every column
@@ -42,6 +43,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdlib>
 #include <mutex>
 
@@ -59,14 +61,7 @@ constexpr int BK = 32;           // vocabulary entries per block
 #ifndef DG_SE_LSTAGES
 #define DG_SE_LSTAGES 4
 #endif
-#ifndef DG_SE_PAIR
-#define DG_SE_PAIR 0
-#endif
-#ifndef DG_SE_STAGES
-#define DG_SE_STAGES (DG_SE_PAIR ? 6 : 4)
-#endif
 constexpr int LSTAGES = DG_SE_LSTAGES;  // logits ring, released by the producers once read
-constexpr int STAGES = DG_SE_STAGES;    // W and A rings (one index), released once both CTAs' MMAs are done
 constexpr int PRODUCER_WARPS = 8;
 #ifndef DG_SE_PGROUPS
 #define DG_SE_PGROUPS 2
@@ -85,14 +80,18 @@ constexpr int ROWS_PER_LANE = 128 / (32 * GROUP_WARPS);
 constexpr int THREADS = 384;
 constexpr int TMEM_COLS = 512;
 constexpr uint16_t kPairMask = 0x3;
-// A cluster of two CTAs holds the two 128-row halves of a 256-row tile.
-// Default: each CTA issues M = 128 MMAs and the two share whole W tiles by TMA multicast.
-// DG_SE_PAIR=1: the two CTAs form a tcgen05 CTA pair; the even CTA issues M = 256 MMAs over
-//   both CTAs' rows and each CTA holds 128 of every 256 W columns (half-size W slots, a
-//   deeper ring).  Correct, but slower here: the odd CTA's producers must signal the even
-//   CTA's barrier with a cluster-scope release, which costs about a microsecond per block.
-constexpr bool kPair = DG_SE_PAIR != 0;
+// A cluster of two CTAs.
+// bf16 table: a tcgen05 CTA pair holding the two 128-row halves of a 256-row tile and one
+//   column tile.  The even CTA issues M = 256 MMAs over both CTAs' rows (cta_group::2); each
+//   CTA loads 128 of every 256 W columns, so each W byte leaves L2 once and a W slot is half
+//   a block's tile.  The odd CTA's W bytes complete on the even CTA's barrier (the pair form
+//   of the TMA load), and its producers signal a finished A tile with a 16-byte bulk copy that
+//   completes on that barrier too.
+// 8-bit table: one row block and two column tiles; each CTA issues M = 128 MMAs and loads its
+//   own W tile; the A operand is shared (each CTA computes every other block's and copies it).
 constexpr int kCtasPerUnit = 2;
+// ring depth of the bf16 pair (W and A slots, one index): half-size W slots leave room for six
+constexpr int kPairStages = 6;
 
 constexpr int L_BYTES = BM * BK * 4;      // logits tile, rows of 128 B (128-byte swizzle)
 constexpr int W_BOX_BYTES = BK * 128;     // one TMA box: 32 rows x 128 bytes (64 bf16 or 128 e4m3 columns)
@@ -111,10 +110,10 @@ struct Fmt;
 template <>
 struct Fmt<kBf16> {
     static constexpr int BN = 512;                // output columns per cluster tile: halves of 256 + 256
-    static constexpr int WST = STAGES;            // W ring depth (the A ring's: one index for both)
-    static constexpr int AST = STAGES;            // A ring depth
+    static constexpr int WST = kPairStages;       // W ring depth (the A ring's: one index for both)
+    static constexpr int AST = kPairStages;       // A ring depth
     static constexpr int BPS = 1;                 // vocabulary blocks per ring slot
-    static constexpr int W_SLOT = (kPair ? BK * BN : BK * BN * 2);  // the part of a block's W tile one CTA holds
+    static constexpr int W_SLOT = BK * BN;        // this CTA's 128 of every 256 columns of a block's W tile
     static constexpr int SF_BYTES = 0;
 };
 template <>
@@ -155,7 +154,10 @@ static_assert(kSfaCol + 4 * Fmt<kE4m3>::AST * Fmt<kE4m3>::BPS <= kSfbCol && kSfb
 // each producer group keeps to every other slot of the logits and A rings
 // a group waits only for phases its own blocks need, and no slot can run two phases ahead
 // of its waiter, so the depths need not be multiples of the group count
-static_assert(LSTAGES >= PGROUPS && STAGES >= PGROUPS, "a slot per producer group at least");
+static_assert(LSTAGES >= PGROUPS && kPairStages >= PGROUPS, "a slot per producer group at least");
+// the bf16 pair's A-ready signals: 16 bytes per producer warp in the even CTA, after the barriers
+constexpr int kSigOffset = 256;
+static_assert(kSigOffset + 16 * (PRODUCER_WARPS + 1) <= 512, "signal area inside the barrier region");
 
 struct Params {
     const float *lse;
@@ -236,7 +238,6 @@ template <int F>
 __global__ void __launch_bounds__(THREADS, 1)
     soft_embed_kernel(const __grid_constant__ CUtensorMap tm_logits, const __grid_constant__ CUtensorMap tm_w,
                       const Params p) {
-    static_assert(F == kBf16 || !kPair, "the 8-bit table runs in multicast mode");
     constexpr int BN = Fmt<F>::BN;
     constexpr int W_SLOT = Fmt<F>::W_SLOT;
     constexpr int WST = Fmt<F>::WST;
@@ -249,9 +250,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                   "8-bit table: a slot holds one block of each CTA; a warp copies 32 whole rows");
     static_assert(AST >= PGROUPS, "an A slot per producer group at least");
     // a block's W bytes complete on its A slot's barrier (one index for both rings), so the
-    // MMA thread waits on one barrier per block (not in the CTA-pair diagnostic build)
+    // MMA thread waits on one barrier per block
     static_assert(WST == AST, "one ring index");
-    constexpr bool kWOnA = !kPair;
+    // bf16 table: the tcgen05 CTA pair (M = 256 over both CTAs' rows)
+    constexpr bool kPairMma = F == kBf16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *l_ring = smem;
@@ -263,13 +265,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L_RING + W_RING + A_RING + Fmt<F>::SF_BYTES);
     uint64_t *full_l = bars;                   // logits tile landed
     uint64_t *empty_l = full_l + LSTAGES;      // the producer warps have read it
-    uint64_t *full_w = empty_l + LSTAGES;      // W tile landed (both halves)
-    uint64_t *full_a = full_w + WST;           // A operand written by a producer group
+    uint64_t *full_a = empty_l + LSTAGES;      // A operand written and the W tile landed
     uint64_t *empty = full_a + AST;            // MMAs done with the A slot (and, one ring, the W slot: both CTAs')
     uint64_t *acc_full = empty + AST;          // accumulator complete
     uint64_t *full_s = acc_full + 1;           // 8-bit table: a block's row scales staged
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(full_s + LSTAGES);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    // bf16 pair: 16-byte landing places of the odd CTA's A-ready signals (one per producer
+    // warp, in the even CTA; never read) and the source of those copies
+    uint8_t *sig_area = reinterpret_cast<uint8_t *>(bars) + kSigOffset;
 
     // Overlap with the neighbours on the stream (programmatic dependent launch): this grid
     // may start while the row-statistics grid before it runs, so every thread calls
@@ -331,21 +335,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(smem_u32(&full_s[s]), 1);
         }
         for (int s = 0; s < AST; ++s) {
-            // pair: the even CTA's full_w counts both CTAs' W bytes, its full_a both CTAs'
-            // producer groups; one commit reaches each CTA's empty.  Multicast: each CTA's
-            // full_w counts the whole tile, and both CTAs' commits reach each empty.  8-bit
-            // table: an A slot this CTA fills counts its producer group's warps, one its
-            // partner fills counts the MMA thread's arrival (with the copied bytes); both
-            // CTAs' commits reach each empty (the slot is read in both)
-            int fa = kPair ? 2 * GROUP_WARPS : GROUP_WARPS;
-            // 8-bit table: this CTA's block (its producer group), the partner's (the MMA thread's
-            // arrival with the copied bytes) and the W TMA's arrival
-            if (F == kE4m3) fa = GROUP_WARPS + 1;
-            if (kWOnA) fa += 1;  // the W TMA's arrival
+            // full_a: the producer group's warps and the W TMA's arrival (with the W bytes);
+            // 8-bit table: also the MMA thread's arrival for the partner's block (with the
+            // copied bytes).  empty: this CTA's commit; 8-bit table: both CTAs' commits (the
+            // slot's A operand is read in both)
+            const int fa = GROUP_WARPS + 1 + (F == kE4m3 ? 1 : 0);
             mbar_init(smem_u32(&full_a[s]), fa);
-            mbar_init(smem_u32(&empty[s]), kPair ? 1 : kCtasPerUnit);
+            mbar_init(smem_u32(&empty[s]), F == kE4m3 ? kCtasPerUnit : 1);
         }
-        for (int s = 0; s < WST; ++s) mbar_init(smem_u32(&full_w[s]), 1);
         mbar_init(smem_u32(acc_full), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -359,7 +356,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
     if (warp == 0) {
-        if (kPair)
+        if constexpr (kPairMma)
             tmem_alloc_pair<TMEM_COLS>(smem_u32(tmem_slot));  // a joint allocation in both CTAs
         else
             tmem_alloc<TMEM_COLS>(smem_u32(tmem_slot));
@@ -367,7 +364,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // the peer's barriers exist before any multicast or commit reaches them
+    // the peer's barriers exist before any copy or commit reaches them
     cluster_sync_all();
     const uint32_t tmem_base = *tmem_slot;
     bool ok = true;  // false once this thread gave up on a wait
@@ -399,21 +396,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool producer = F == kE4m3 ? warp >= 4 : ((warp & 3) != 0 && warp < 11);
     if (warp == kWarpW) {
         // ------------------------------------------------------------ W TMA
-        // pair: this CTA's 128 columns of each 256-column half (atoms 4h + 2 rank, +1), the
-        //   bytes counted on the even CTA's full_w, which that CTA arms for both;
-        // multicast: this CTA's half of the boxes, delivered to both CTAs.
+        // bf16 pair: each CTA loads its 128 columns of each 256-column half (atoms 4h + 2 rank
+        // and + 1), the bytes counted on the even CTA's A slot barrier, which that CTA arms
+        // for both CTAs' bytes and the odd CTA's A-ready signals; 8-bit table: each CTA loads
+        // its own tile's 128-column atoms of the slot's two blocks, counted on its own A slot
+        // barrier.  W lines are marked evict-first
         if (lane == 0) {
             int issued[WST];
             for (int s = 0; s < WST; ++s) issued[s] = 0;
-            const int nbox = 4 * halves / kCtasPerUnit;  // multicast: this CTA's share of the 4 * halves boxes
             const uint64_t w_policy = l2_policy_evict_first();
-            // 3-D map: one load per CTA (pair: per 256-column half) fetches W_ATOMS or 2
-            // atoms; multicast tail tiles: the second CTA's atoms lie past d, arrive
-            // zero-filled and are not used
+            // bf16: a 3-D map fetches a CTA's 2 atoms of a half in one load
             const bool w3d = p.w3d;
-            const uint32_t w_bytes = kPair ? (uint32_t)halves * 2 * 2 * W_BOX_BYTES
-                                           : (w3d ? (uint32_t)W_SLOT : (uint32_t)halves * W_SLOT / 2);
-            const uint32_t lead = map_to_cta(smem_u32(&full_w[0]), 0);  // the even CTA's full_w[0]
+            const uint32_t lead_a = map_to_cta(smem_u32(&full_a[0]), 0);  // the even CTA's full_a[0]
             for (int i = 0; i < nkb / BPS; ++i) {  // ring slots (BPS blocks each)
                 const int s = i % WST;
                 const uint32_t u = (uint32_t)(i / WST);
@@ -426,7 +420,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 const int64_t k = p.k_begin + (kb0 + (int64_t)BPS * i) * BK;
-                const uint32_t bw = smem_u32(kWOnA ? &full_a[s] : &full_w[s]);
+                const uint32_t bw = smem_u32(&full_a[s]);
                 const int wy = (int)(k - p.vocab_start);
                 if constexpr (F == kE4m3) {
                     // this CTA's own tile for the slot's two blocks: four 128-column atoms of 64
@@ -435,12 +429,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int a = 0; a < 2 * halves; ++a)
                         tma_load_2d_hint(smem_u32(w_ring + s * W_SLOT + a * BPS * W_BOX_BYTES), &tm_w, bw,
                                          col0 + 128 * a, wy, w_policy);
-                    issued[s] = (int)u + 1;
-                    continue;
-                }
-                if (kPair) {
-                    if (rank == 0) mbar_arrive_expect_tx(bw, w_bytes);
-                    const uint32_t bl = lead + 8u * (uint32_t)s;
+                } else {
+                    // both CTAs' W bytes of the slot, and the odd CTA's four A-ready signals
+                    if (rank == 0)
+                        mbar_arrive_expect_tx(bw, (uint32_t)halves * W_SLOT + 16u * GROUP_WARPS);
+                    const uint32_t bl = lead_a + 8u * (uint32_t)s;
                     for (int h = 0; h < halves; ++h) {
                         const uint32_t dst = smem_u32(w_ring + s * W_SLOT + h * 2 * W_BOX_BYTES);
                         const int atom = col0 / 64 + 4 * h + 2 * (int)rank;
@@ -451,17 +444,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                             tma_load_2d_pair_hint(dst + W_BOX_BYTES, &tm_w, bl, 64 * (atom + 1), wy, w_policy);
                         }
                     }
-                    issued[s] = (int)u + 1;
-                    continue;
-                }
-                mbar_arrive_expect_tx(bw, w_bytes);
-                if (w3d)
-                    tma_load_3d_multicast_hint(smem_u32(w_ring + s * W_SLOT + (int)rank * 4 * W_BOX_BYTES), &tm_w, bw,
-                                               0, wy, col0 / 64 + 4 * (int)rank, kPairMask, w_policy);
-                for (int b = 0; b < (w3d ? 0 : nbox); ++b) {
-                    const int box = (int)rank * nbox + b;
-                    tma_load_2d_multicast_hint(smem_u32(w_ring + s * W_SLOT + box * W_BOX_BYTES), &tm_w, bw,
-                                               col0 + 64 * box, wy, kPairMask, w_policy);
                 }
                 issued[s] = (int)u + 1;
             }
@@ -469,12 +451,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 grid_dependency_wait();
                 grid_launch_dependents();
             }
-            // loads in flight finish before the CTA may leave (pair: the even CTA's full_w
-            // counts both CTAs' loads, and the odd CTA leaves only after the final cluster
+            // loads in flight finish before the CTA may leave (bf16 pair: the even CTA's barriers
+            // count both CTAs' loads, and the odd CTA leaves only after the final cluster
             // barrier, which the even CTA reaches after this drain)
-            if (!ok && (!kPair || rank == 0))
+            if (!ok && (!kPairMma || rank == 0))
                 for (int s = 0; s < WST; ++s)
-                    if (issued[s] > 0) drain_wait(smem_u32(kWOnA ? &full_a[s] : &full_w[s]), (issued[s] - 1) & 1);
+                    if (issued[s] > 0) drain_wait(smem_u32(&full_a[s]), (issued[s] - 1) & 1);
         }
     } else if (warp == kWarpL) {
         // ------------------------------------------------------------ logits TMA
@@ -509,11 +491,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
-        // (pair: the even CTA's thread issues for both CTAs; the odd CTA's has no role)
-        if (lane == 0 && (!kPair || rank == 0)) {
+        // (bf16 pair: the even CTA's thread issues for both CTAs; the odd CTA's has no role)
+        if (lane == 0 && (!kPairMma || rank == 0)) {
             grid_dependency_wait();  // nothing to issue before the producers' first tile anyway
             grid_launch_dependents();
-            constexpr uint32_t idesc = idesc_bf16_f32(kPair ? 2 * BM : BM, 256, /*A K-major*/ 0, /*B N-major*/ 1);
+            constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, 256, /*A K-major*/ 0, /*B N-major*/ 1);
             // operand descriptors of slot 0; a slot, a K = 16 step or a 256-column half is a
             // constant added to the start-address field (addresses stay below 2^18 bytes)
             // A: K-major, 64-byte rows, 8-row groups 512 B apart; +32 B per K = 16 step
@@ -521,7 +503,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // B: N-major, 64-column atoms 4 KiB apart (LBO), 8-row groups 1 KiB apart (SBO);
             // +2 KiB per K = 16 step
             const uint64_t b_desc0 = smem_desc(smem_u32(w_ring), BPS * W_BOX_BYTES, 1024, 2);
-            // a CTA's part of one 256-column half: 4 atoms (multicast) or 2 (pair)
+            // a CTA's part of one 256-column half: 2 atoms
             constexpr uint64_t kA_K16 = 32 >> 4, kB_K16 = 2048 >> 4, kB_HALF = (W_SLOT / 2) >> 4;
             // 8-bit table: the B scale factors (all 1) go into their columns once; per block the
             // stage's A scale chunk goes into its four columns ahead of the block's MMAs (the copy
@@ -534,13 +516,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             // a block's two tiles are tested together (their latencies overlap), and right
             // after the previous block's MMAs are issued, ahead of its commit; the bounded
             // waits run only when a tile is not there yet
-            // pair: the odd CTA's producers and loads arrive from the other CTA, so the tests
-            // acquire at cluster scope
+            // bf16 pair: the odd CTA's loads and signals complete from the other CTA, so the
+            // tests acquire at cluster scope
             auto test = [&](uint32_t bar, uint32_t ph) {
-                return kPair ? mbar_try_wait_cluster(bar, ph) : mbar_try_wait(bar, ph);
+                return kPairMma ? mbar_try_wait_cluster(bar, ph) : mbar_try_wait(bar, ph);
             };
             auto wait = [&](uint32_t bar, uint32_t ph) {
-                return kPair ? mbar_wait_cluster(bar, ph, abort_flag) : mbar_wait(bar, ph, abort_flag);
+                return kPairMma ? mbar_wait_cluster(bar, ph, abort_flag) : mbar_wait(bar, ph, abort_flag);
             };
             // 8-bit table: a slot the partner fills completes on its copies' bytes and one
             // arrival of this thread (the bytes may land first), made before the slot is tested
@@ -550,12 +532,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             };
             arm(0);
             bool a_in = nkb > 0 && test(smem_u32(&full_a[0]), 0);
-            bool w_in = kWOnA || (nkb > 0 && test(smem_u32(&full_w[0]), 0));
             for (int i = 0; i < nkb / BPS; ++i) {  // ring slots (BPS blocks each)
                 const int s = i % AST;
                 const uint32_t ph = (uint32_t)(i / AST) & 1;
-                if (!(a_in && w_in) &&
-                    (!wait(smem_u32(&full_a[s]), ph) || (!kWOnA && !wait(smem_u32(&full_w[s]), ph)))) {
+                if (!a_in && !wait(smem_u32(&full_a[s]), ph)) {
                     ok = false;
                     break;
                 }
@@ -587,33 +567,27 @@ __global__ void __launch_bounds__(THREADS, 1)
                         umma_mxf8(tmem_base, adb + kA_K16, bdb, id_l0, sfa, sfb, 1u);
                         if (halves == 2) umma_mxf8(tmem_base + 256, adb + kA_K16, bdb + kB_HALF8, id_l1, sfa, sfb, 1u);
                     }
-                } else if (kPair) {
+                } else {
                     umma_bf16_pair(tmem_base, ad, bd, idesc, acc);
                     if (halves == 2) umma_bf16_pair(tmem_base + 256, ad, bd + kB_HALF, idesc, acc);
                     umma_bf16_pair(tmem_base, ad + kA_K16, bd + kB_K16, idesc, 1u);
                     if (halves == 2) umma_bf16_pair(tmem_base + 256, ad + kA_K16, bd + kB_HALF + kB_K16, idesc, 1u);
-                } else {
-                    umma_bf16(tmem_base, ad, bd, idesc, acc);
-                    if (halves == 2) umma_bf16(tmem_base + 256, ad, bd + kB_HALF, idesc, acc);
-                    umma_bf16(tmem_base, ad + kA_K16, bd + kB_K16, idesc, 1u);
-                    if (halves == 2) umma_bf16(tmem_base + 256, ad + kA_K16, bd + kB_HALF + kB_K16, idesc, 1u);
                 }
                 if (i + 1 < nkb / BPS) {
                     arm(i + 1);
                     a_in = test(smem_u32(&full_a[(i + 1) % AST]), (uint32_t)((i + 1) / AST) & 1);
-                    w_in = kWOnA || test(smem_u32(&full_w[(i + 1) % AST]), (uint32_t)((i + 1) / AST) & 1);
                 }
-                // one commit releases the W and A slots once both CTAs' MMAs have read them
-                // (8-bit table: the A slot is read in both, the W slot is this CTA's own)
-                if (kPair) {
-                    umma_commit_pair_multicast(smem_u32(&empty[s]), kPairMask);
-                } else {
+                // one commit releases the W and A slots of both CTAs once the MMAs have read
+                // them (bf16 pair: the pair's MMAs read both CTAs' slots; 8-bit table: the A
+                // slot is read in both CTAs)
+                if constexpr (F == kE4m3)
                     umma_commit_multicast(smem_u32(&empty[s]), kPairMask);
-                }
+                else
+                    umma_commit_pair(smem_u32(&empty[s]), kPairMask);
                 issued_any = true;
             }
-            if (kPair)
-                umma_commit_pair_multicast(smem_u32(acc_full), kPairMask);
+            if constexpr (kPairMma)
+                umma_commit_pair(smem_u32(acc_full), kPairMask);
             else
                 umma_commit(smem_u32(acc_full));
             if (*abort_flag && issued_any) drain_wait(smem_u32(acc_full), 0);
@@ -905,10 +879,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             fence_proxy_async_smem();
             __syncwarp();  // every lane's A stores (and proxy fence) before the arrival
             if (lane == 0) {
-                if (kPair && rank != 0)  // the even CTA's MMA thread reads this CTA's rows too
-                    mbar_arrive_remote(map_to_cta(smem_u32(&full_a[s]), 0));
-                else
+                if (kPairMma && rank != 0) {
+                    // the even CTA's MMA thread reads this CTA's rows too: a 16-byte copy that
+                    // completes on its barrier tells it this warp's rows are in place (issued
+                    // after the rows' stores and proxy fence; the bytes are never read)
+                    bulk_copy_to_cluster(map_to_cta(smem_u32(sig_area + 16 * (1 + pw)), 0), smem_u32(sig_area), 16u,
+                                         map_to_cta(smem_u32(&full_a[s]), 0));
+                } else {
                     mbar_arrive(smem_u32(&full_a[s]));
+                }
                 if constexpr (F == kE4m3) {
                     // the warp's 32 A rows (2 KiB) and 32 scale rows (512 B) to the same slot of
                     // the partner CTA, completing on its full_a
@@ -1144,12 +1123,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
     }
-    // neither CTA leaves while the other may still multicast into it or commit to it
+    // neither CTA leaves while the other may still copy into it or commit to it
     cluster_sync_all();
     if (warp == 0) {
         __syncwarp();
         tc_fence_after();
-        if (kPair)
+        if constexpr (kPairMma)
             tmem_dealloc_pair<TMEM_COLS>(tmem_base);
         else
             tmem_dealloc<TMEM_COLS>(tmem_base);
@@ -1381,16 +1360,6 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// The 8-bit kernel; the CTA-pair diagnostic build has none (its launches are refused), and
-// names the bf16 kernel in its place so that nothing instantiates the 8-bit one.
-template <bool Pair>
-constexpr auto e4m3_kernel() {
-    if constexpr (Pair)
-        return soft_embed_kernel<kBf16>;
-    else
-        return soft_embed_kernel<kE4m3>;
-}
-
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -1404,6 +1373,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     });
     return fn;
 }
+
+constexpr int kMaxAttrDevices = 64;
 
 int tile_width(int fmt) { return fmt == kE4m3 ? Fmt<kE4m3>::BN : Fmt<kBf16>::BN; }
 
@@ -1478,11 +1449,6 @@ bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t 
             best = (int)S;
         }
     }
-    // tuning override: DGSAMP_SOFT_EMBED_SPLITS=<n> forces the split count (clamped)
-    if (const char *env = getenv("DGSAMP_SOFT_EMBED_SPLITS")) {
-        const long v = strtol(env, nullptr, 10);
-        if (v >= 1) best = (int)(v < pl.nkb ? v : pl.nkb);
-    }
     pl.splits = best;
     pl.workspace_bytes = soft_embed_workspace_bytes(pl, pl.splits);
     pl.single_pass_bytes = pl.workspace_bytes + single_pass_extra_bytes(pl, R);
@@ -1501,10 +1467,6 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     }
     const bool e4 = tab.fmt == kE4m3;
     const int64_t ldw = tab.ldw;
-    if (e4 && kPair) {
-        *msg = "soft embed: the CTA-pair diagnostic build serves the bf16 table only";
-        return cudaErrorNotSupported;
-    }
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
     if (!encode) {
         *msg = "cuTensorMapEncodeTiled is not available from the driver";
@@ -1543,7 +1505,7 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     } else if (atoms * 64 <= ldw) {
         const cuuint64_t dims[3] = {64, (cuuint64_t)(vocab_end - vocab_start), (cuuint64_t)atoms};
         const cuuint64_t strides[2] = {(cuuint64_t)ldw * 2, 128};
-        const cuuint32_t box[3] = {64, BK, kPair ? 2u : 4u};
+        const cuuint32_t box[3] = {64, BK, 2u};  // one CTA's 2 atoms of a 256-column half
         const cuuint32_t estr[3] = {1, 1, 1};
         w3d = encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(W), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1561,15 +1523,19 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
             return cudaErrorInvalidValue;
         }
     }
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
+    // the shared-memory limit is raised once per device (a function attribute belongs to the
+    // device's context); setting it twice from racing threads is harmless
+    static std::atomic<int> attr_set[kMaxAttrDevices];
+    int dev = 0;
+    cudaError_t attr_err = cudaGetDevice(&dev);
+    if (attr_err == cudaSuccess && (dev >= kMaxAttrDevices || !attr_set[dev].load(std::memory_order_acquire))) {
         attr_err = cudaFuncSetAttribute(soft_embed_kernel<kBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         smem_bytes<kBf16>());
         if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(e4m3_kernel<kPair>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+            attr_err = cudaFuncSetAttribute(soft_embed_kernel<kE4m3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             smem_bytes<kE4m3>());
-    });
+        if (attr_err == cudaSuccess && dev < kMaxAttrDevices) attr_set[dev].store(1, std::memory_order_release);
+    }
     if (attr_err != cudaSuccess) {
         *msg = "could not raise the shared-memory limit of the soft-embed kernel";
         return attr_err;
@@ -1644,7 +1610,7 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     attr[1].val.programmaticStreamSerializationAllowed = overlap_previous ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = e4 ? cudaLaunchKernelEx(&cfg, e4m3_kernel<kPair>(), tm_l, tm_w, p)
+    cudaError_t e = e4 ? cudaLaunchKernelEx(&cfg, soft_embed_kernel<kE4m3>, tm_l, tm_w, p)
                        : cudaLaunchKernelEx(&cfg, soft_embed_kernel<kBf16>, tm_l, tm_w, p);
     if (e != cudaSuccess) {
         *msg = "soft-embed kernel launch failed";

@@ -19,7 +19,8 @@ class SamplerStep:
 
     def __init__(self, W: torch.Tensor, n_req: int, L_c: int, V: int, gamma: float,
                  vocab_start: int = 0, vocab_end: int | None = None, min_accept: int = 0,
-                 device: str | torch.device = "cuda", scale: torch.Tensor | None = None):
+                 device: str | torch.device = "cuda", scale: torch.Tensor | None = None,
+                 two_pass: bool = False):
         self.device = torch.device(device)
         self.W = W
         self.scale = scale
@@ -30,6 +31,7 @@ class SamplerStep:
         self.vocab_start = vocab_start
         self.vocab_end = V if vocab_end is None else vocab_end
         self.min_accept = min_accept
+        self.two_pass = bool(two_pass)  # statistics before the product (DG_STEP_TWO_PASS)
         R, d, dev = self.R, self.d, self.device
         self.out = {k: torch.empty(R, dtype=torch.float32, device=dev) for k in ("m", "lse", "H", "kappa")}
         self.out.update(argmax=torch.empty(R, dtype=torch.int32, device=dev),
@@ -48,11 +50,11 @@ class SamplerStep:
             return B.dg_sampler_step_e4m3(logits, self.n_req, self.L_c, self.W, self.scale, self.gamma, budgets,
                                           min_accept=self.min_accept, vocab_start=self.vocab_start,
                                           vocab_end=self.vocab_end, V=self.V, out=self.out, ws=self.ws,
-                                          stream=stream)
+                                          stream=stream, two_pass=self.two_pass)
         return B.dg_sampler_step(logits, self.n_req, self.L_c, self.W, self.gamma, budgets,
                                  min_accept=self.min_accept, vocab_start=self.vocab_start,
                                  vocab_end=self.vocab_end, V=self.V, out=self.out, ws=self.ws,
-                                 stream=stream)
+                                 stream=stream, two_pass=self.two_pass)
 
     # -- host inputs and results
     def host_buffers(self, ldl: int | None = None) -> dict:
@@ -155,7 +157,8 @@ class SamplerLoop(SamplerStep):
                                             self.step_limit, min_accept=self.min_accept,
                                             vocab_start=self.vocab_start, vocab_end=self.vocab_end, V=self.V,
                                             out=self.out, ws=self.ws, temperature=self.temperature,
-                                            seed=self.seed, offset=self.offset, stream=stream)
+                                            seed=self.seed, offset=self.offset, stream=stream,
+                                            two_pass=self.two_pass)
             self.offset += 1
             return o
         o = B.dg_sampler_loop_step(logits, self.n_req, self.L_c, self.W, self.gamma, budgets, self.state,
@@ -163,6 +166,6 @@ class SamplerLoop(SamplerStep):
                                    min_accept=self.min_accept, vocab_start=self.vocab_start,
                                    vocab_end=self.vocab_end, V=self.V, out=self.out, ws=self.ws,
                                    temperature=self.temperature, seed=self.seed, offset=self.offset,
-                                   stream=stream)
+                                   stream=stream, two_pass=self.two_pass)
         self.offset += 1
         return o

@@ -56,6 +56,20 @@ typedef enum dg_status {
     DG_ERR_TIMEOUT = 4       /* a device-side wait gave up (reported by dg_get_device_status) */
 } dg_status;
 
+/*
+ * Options of the sampler-step calls (dg_sampler_step, dg_sampler_loop_step and their 8-bit
+ * table forms), OR-ed into their `flags` argument.  Any other bit is DG_ERR_INVALID_ARG.
+ *   DG_STEP_TWO_PASS  run the row-statistics pass before the product even when the slice is
+ *                     the whole vocabulary (the logits are then read twice; the single pass
+ *                     is the default there).  Results agree with the single pass within the
+ *                     stated tolerances; the flag exists to compare the two and to keep the
+ *                     two-pass workspace size.
+ */
+typedef enum dg_step_flags {
+    DG_STEP_DEFAULT = 0,
+    DG_STEP_TWO_PASS = 1
+} dg_step_flags;
+
 /* Library version, major*10000 + minor*100 + patch. */
 int dg_version(void);
 
@@ -200,8 +214,9 @@ dg_status dg_sum_partials(const float *const *partials, int32_t T, int64_t R, in
  * (split, row) whose probabilities against c could overflow (their sum above e^82, or the
  * split's maximum 64 nats below c) is recomputed against lse on the CUDA cores (exact,
  * slow, rare: one-hot rows).  E then equals the two-pass result up
- * to the bf16 rounding of different probabilities.  The environment variable
- * DGSAMP_TWO_PASS=1 forces the statistics pass before the product.
+ * to the bf16 rounding of different probabilities.  flags = DG_STEP_TWO_PASS runs the
+ * statistics pass before the product instead (a workspace of the two-pass size is enough
+ * then).
  */
 dg_status dg_sampler_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, int64_t ldl,
                           const uint16_t *W, int64_t vocab_start, int64_t vocab_end,
@@ -209,7 +224,7 @@ dg_status dg_sampler_step(const float *logits, int32_t n_req, int32_t L_c, int64
                           const float *budgets, int32_t min_accept,
                           float *m, float *lse, float *H, float *kappa, int32_t *argmax,
                           int32_t *order, uint8_t *mask, int32_t *n_accepted,
-                          float *E, int64_t ldo,
+                          float *E, int64_t ldo, uint32_t flags,
                           void *workspace, size_t workspace_bytes, dg_stream_t stream);
 
 /*
@@ -364,7 +379,7 @@ dg_status dg_loop_update(const int32_t *candidate, const int32_t *argmax, const 
  * the loop state (canvas, eligible, prev_argmax, stable, steps, converged) is read and
  * written in place, so successive calls on one stream (or one captured graph,
  * replayed) run successive steps.  A negative, infinite or NaN temperature is
- * DG_ERR_INVALID_ARG.
+ * DG_ERR_INVALID_ARG.  flags as dg_sampler_step.
  */
 dg_status dg_sampler_loop_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V,
                                int64_t ldl, const uint16_t *W, int64_t vocab_start,
@@ -376,7 +391,7 @@ dg_status dg_sampler_loop_step(const float *logits, int32_t n_req, int32_t L_c, 
                                int32_t *candidate, int32_t *order, uint8_t *mask,
                                int32_t *n_accepted, float *E, int64_t ldo,
                                int32_t *canvas, uint8_t *eligible, int32_t *prev_argmax,
-                               int32_t *stable, int32_t *steps, uint8_t *converged,
+                               int32_t *stable, int32_t *steps, uint8_t *converged, uint32_t flags,
                                void *workspace, size_t workspace_bytes, dg_stream_t stream);
 
 /*
@@ -428,7 +443,8 @@ dg_status dg_soft_embed_e4m3(const float *logits, int64_t ldl, const float *lse,
 /*
  * dg_sampler_step with the 8-bit table (Q, scale, ldq as dg_soft_embed_e4m3).  With the
  * whole vocabulary and a workspace of dg_soft_embed_workspace_size_e4m3 bytes it is the
- * single-pass step (the same references, redo rule and statistics as dg_sampler_step).
+ * single-pass step (the same references, redo rule and statistics as dg_sampler_step);
+ * flags as dg_sampler_step.
  */
 dg_status dg_sampler_step_e4m3(const float *logits, int32_t n_req, int32_t L_c, int64_t V,
                                int64_t ldl, const uint8_t *Q, const float *scale,
@@ -436,8 +452,8 @@ dg_status dg_sampler_step_e4m3(const float *logits, int32_t n_req, int32_t L_c, 
                                int64_t ldq, int64_t d, float gamma, const float *budgets,
                                int32_t min_accept, float *m, float *lse, float *H, float *kappa,
                                int32_t *argmax, int32_t *order, uint8_t *mask,
-                               int32_t *n_accepted, float *E, int64_t ldo, void *workspace,
-                               size_t workspace_bytes, dg_stream_t stream);
+                               int32_t *n_accepted, float *E, int64_t ldo, uint32_t flags,
+                               void *workspace, size_t workspace_bytes, dg_stream_t stream);
 
 /*
  * dg_sampler_loop_step with the 8-bit table (Q, scale, ldq as dg_soft_embed_e4m3; the loop
@@ -456,8 +472,8 @@ dg_status dg_sampler_loop_step_e4m3(const float *logits, int32_t n_req, int32_t 
                                     int32_t *order, uint8_t *mask, int32_t *n_accepted, float *E,
                                     int64_t ldo, int32_t *canvas, uint8_t *eligible,
                                     int32_t *prev_argmax, int32_t *stable, int32_t *steps,
-                                    uint8_t *converged, void *workspace, size_t workspace_bytes,
-                                    dg_stream_t stream);
+                                    uint8_t *converged, uint32_t flags, void *workspace,
+                                    size_t workspace_bytes, dg_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -119,8 +119,21 @@ def test_step_checks_slice_against_vocabulary(lib):
     L = lib.lib
     p = ctypes.c_void_p(256)
     st = L.dg_sampler_step(p, 1, 16, 4096, 4096, p, 0, 8192, 8192, 256, 256, 16.0, p, 0,
-                           p, p, p, p, p, p, p, p, p, 256, p, 1 << 20, None)
+                           p, p, p, p, p, p, p, p, p, 256, 0, p, 1 << 20, None)
     assert st == 1
+
+
+def test_step_rejects_unknown_flags(lib):
+    L = lib.lib
+    p = ctypes.c_void_p(256)
+    for flags in (2, 1 << 31, 3):
+        st = L.dg_sampler_step(p, 1, 16, 4096, 4096, p, 0, 4096, 4096, 256, 256, 16.0, p, 0,
+                               p, p, p, p, p, p, p, p, p, 256, flags, p, 1 << 20, None)
+        assert st == 1 and b"flags" in L.dg_last_error(), flags
+        st = L.dg_sampler_step_e4m3(p, 1, 16, 4096, 4096, p, p, 0, 4096, 4096, 256, 256, 1.0, p, 0, p, p, p, p, p,
+                                    p, p, p, p, 256, flags, p, 1 << 20, None)
+        assert st == 1 and b"flags" in L.dg_last_error(), flags
+    assert lib.DG_STEP_TWO_PASS == 1
 
 
 def test_accept_eligible_rejects_bad_arguments(lib):
@@ -154,7 +167,7 @@ def test_loop_step_checks_its_loop_arguments(lib):
     p = ctypes.c_void_p(256)
     step = [p, 1, 16, 4096, 4096, p, 0, 4096, 4096, 256, 256, 16.0, p, 0]
     outs = [p] * 10 + [256]
-    ws = [p, 1 << 20, None]
+    ws = [0, p, 1 << 20, None]   # flags, workspace, its size, stream
     argmax_mode = [0.0, 0, 0]
     assert L.dg_sampler_loop_step(*step, 2, 0.5, 0, *argmax_mode, *outs, *([p] * 6), *ws) == 1   # step_limit 0
     assert L.dg_sampler_loop_step(*step, 2, 0.5, 10, *argmax_mode, *outs, p, None, p, p, p, p, *ws) == 1
@@ -214,5 +227,5 @@ def test_e4m3_calls_reject_bad_arguments(lib):
                                 1 << 20, None) == 2
     # the step checks its slice against V like the bf16 step
     st = L.dg_sampler_step_e4m3(p, 1, 16, 4096, 4096, p, p, 0, 5000, 8192, 256, 256, 1.0, p, 0, p, p, p, p, p, p, p,
-                                p, p, 256, p, 1 << 20, None)
+                                p, p, 256, 0, p, 1 << 20, None)
     assert st == 1
