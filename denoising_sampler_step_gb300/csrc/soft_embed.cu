@@ -182,7 +182,7 @@ struct Params {
     int64_t ldl;
     float *ref;          // [splits][R] c, then (after the statistics) exp(c - lse)
     float4 *state;       // [splits][n_tiles][R] row summaries (m, argmax bits, rest, t) of the blocks
-                         // i of the split with (i / PGROUPS) % n_tiles == the column tile
+                         // of the split the column tile folds (`fold` in the producers)
     int *counts;         // [0] (split, row) pairs to redo: the reference was too far from the maximum
     int2 *redo;          // [splits * R] the pairs
     // single pass with the temperature-1 draw: the folded blocks also take the draw's first
@@ -226,6 +226,42 @@ __device__ __forceinline__ float max32(const float (&v)[32]) {
     const float b0 = max3f(a[0], a[1], a[2]), b1 = max3f(a[3], a[4], a[5]), b2 = max3f(a[6], a[7], a[8]);
     const float b3 = fmaxf(a[9], a[10]);
     return fmaxf(max3f(b0, b1, b2), b3);
+}
+
+// Sum of 16 values as a tree (15 additions, depth 4).
+__device__ __forceinline__ float sum16(const float *v) {
+    float a[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) a[t] = v[2 * t] + v[2 * t + 1];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) a[t] = a[2 * t] + a[2 * t + 1];
+    return (a[0] + a[1]) + (a[2] + a[3]);
+}
+
+// The single pass's statistics fold of the bf16 product, kept relative to the split's
+// reference c (the exponentials e = exp(l - c) the producers already formed): the running
+// maximum M of the lane's row over the folded blocks, A the index of its first occurrence,
+// E = exp(M - c), R = the sum of e over the other entries, T = the sum of e (l - c) over all
+// entries; R and T in two levels (R16, T16 over up to 16 blocks) so that no fp32 sum runs
+// over more than a few dozen terms.  No exponential per block: a block whose maximum does
+// not pass M adds all its e to R, and only a block that raises M takes the exact sum of its
+// other entries (keeping the argmax's own term out of R keeps kappa = log1p(rest) exact for
+// rows near one-hot).  Blocks more than 60 nats above c (e could overflow) take the
+// statistics kernel's fold instead.
+struct RefState {
+    float M;
+    int A;
+    float E;
+    float R, T, R16, T16;
+};
+
+// The RowState (m, a, rest, t relative to m) of a RefState: rest = R exp(c - M),
+// t = exp(c - M) (T - (M - c)(R + E)).
+__device__ __forceinline__ rowstate::RowState ref_to_row_state(const RefState &r, float c) {
+    if (r.M == -INFINITY) return rowstate::empty_row_state();
+    const float R = r.R + r.R16, T = r.T + r.T16;
+    const float inv = ex2_approx((c - r.M) * kLog2e);
+    return rowstate::RowState{r.M, r.A, R * inv, inv * fmaf(-(r.M - c), R + r.E, T)};
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -368,16 +404,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     cluster_sync_all();
     const uint32_t tmem_base = *tmem_slot;
     bool ok = true;  // false once this thread gave up on a wait
-    // single pass: the producers' reference per row and their row statistics; column tile
-    // nt folds the split's blocks i with (i / PGROUPS) % n_tiles == nt (every block is folded
-    // by one column tile, and evenly by the producer groups), after handing the block's A
-    // tile over, so that the fold stays off the product's critical path; in three levels (a
-    // block, 16 blocks, all) so that no fp32 sum runs over more than a few dozen terms: rest
-    // keeps kappa = log1p(rest) accurate near one-hot
+    // single pass: the producers' reference per row and their row statistics; each block of
+    // the split is folded by one column tile (`fold` below), evenly by the producer groups,
+    // after handing the block's A tile over, so that the fold stays off the product's
+    // critical path; in levels (a block, 16 blocks, all) so that no fp32 sum runs over more
+    // than a few dozen terms: rest keeps kappa = log1p(rest) accurate near one-hot
     int my_grp = -1;
     int my_rows[ROWS_PER_LANE];
     float my_ref[ROWS_PER_LANE];
     rowstate::RowState my_st[ROWS_PER_LANE], my_st16[ROWS_PER_LANE];
+    RefState my_rs[ROWS_PER_LANE];  // bf16 table: the fold relative to the reference c
     int my_folded = 0;
     float my_gbest[ROWS_PER_LANE];  // the draw's first level: best group score and group
     int my_gidx[ROWS_PER_LANE];
@@ -387,6 +423,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         my_ref[q] = 0.0f;
         my_st[q] = rowstate::empty_row_state();
         my_st16[q] = rowstate::empty_row_state();
+        my_rs[q] = RefState{-INFINITY, 0x7fffffff, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
         my_gbest[q] = -INFINITY;
         my_gidx[q] = 0x7fffffff;
     }
@@ -712,9 +749,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             const bool edge = (k < p.vocab_start) || (k + BK > p.vocab_end);
             uint32_t packed[ROWS_PER_LANE][16];
             uint32_t sf_word[ROWS_PER_LANE];  // 8-bit table: the (row, block) scale bytes
-            // every block is folded once per row block: (bf16) by column tile (i / PGROUPS) %
-            // n_tiles, (8-bit table) by the CTA producing it in cluster (i / 4) % (n_tiles / 2)
-            const bool fold = p.fused && (F == kE4m3 ? (i >> 2) % ntp_count == ntp : (i / PGROUPS) % p.n_tiles == nt);
+            // every block is folded once per row block: (bf16) by column tile (i / PGROUPS +
+            // (i % PGROUPS) (n_tiles / 2)) % n_tiles, so that the two producer groups' folds fall
+            // half a cycle apart and one group keeps producing while the other folds; (8-bit
+            // table) by the CTA producing it in cluster (i / 4) % (n_tiles / 2)
+            const bool fold =
+                p.fused && (F == kE4m3 ? (i >> 2) % ntp_count == ntp
+                                       : (i / PGROUPS + (i % PGROUPS) * (p.n_tiles / 2)) % p.n_tiles == nt);
             // 8-bit table: the block's normalised row scales u (0 outside the slice) and their
             // exponent E (row scale = u 2^E), staged by warp 0
             float us[F == kE4m3 ? 32 : 1];
@@ -902,12 +943,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (fold) {
 #pragma unroll
                 for (int q = 0; q < ROWS_PER_LANE; ++q) {
-                    // the block's summary from the probabilities' own exponentials e = exp(l - c):
-                    // relative to the block max bm, exp(l - bm) = e exp(c - bm); a block whose max
-                    // lies more than 60 nats from c (e or exp(c - bm) may overflow) takes the
-                    // statistics kernel's fold instead.  Entries that underflow in e lie more than
-                    // 87 nats below c, so below every row maximum by as much: they add nothing
-                    // the fp32 statistics could hold.
+                    // the block's statistics from the probabilities' own exponentials e = exp(l - c)
+                    // (bf16 table: sums against c, RefState; 8-bit table: a block summary relative
+                    // to the block max bm, exp(l - bm) = e exp(c - bm)).  A block whose max lies
+                    // more than 60 nats above c (e may overflow) takes the statistics kernel's fold
+                    // instead.  Entries that underflow in e lie more than 87 nats below c, so below
+                    // every row maximum by as much: they add nothing the fp32 statistics could hold.
                     float xb[32];
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
@@ -922,11 +963,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             if (k + t < p.vocab_start || k + t >= p.vocab_end) xb[t] = -INFINITY;
                     }
                     float bm = bmq[q];  // the 8-bit path's block maximum
-                    if constexpr (F == kBf16) {
-                        bm = xb[0];
-#pragma unroll
-                        for (int t = 1; t < 32; ++t) bm = fmaxf(bm, xb[t]);
-                    }
+                    if constexpr (F == kBf16) bm = max32(xb);
                     rowstate::RowState blk = rowstate::empty_row_state();
                     float glm[2] = {-INFINITY, -INFINITY};  // the two groups' log-masses
                     if (F == kE4m3 && bm > -INFINITY) {
@@ -954,30 +991,47 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 glm[h] = my_ref[q] + philox::kLn2 * (__log2f(gsum) + kfq[q] - 7.0f);
                             }
                         }
-                    } else if (F == kBf16 && bm > -INFINITY && fabsf(bm - my_ref[q]) <= 60.0f) {
-                        int ja = 31;
+                    } else if (F == kBf16 && bm > -INFINITY && bm - my_ref[q] <= 60.0f) {
+                        // the block's sums against c (see RefState); a block with a masked (-inf)
+                        // entry gets NaN from 0 * -inf in the first sum of e (l - c) and takes the
+                        // guarded one
+                        const float *ev = ek[q];
+                        const float s_lo = sum16(ev), s_hi = sum16(ev + 16);
+                        const float S = s_lo + s_hi;
+                        float tx[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                        for (int t = 31; t >= 0; --t)
-                            if (xb[t] == bm) ja = t;
-                        float se = 0.0f, sd = 0.0f;
+                        for (int t = 0; t < 32; ++t) tx[t & 3] = fmaf(ev[t], xb[t], tx[t & 3]);
+                        float Tx = (tx[0] + tx[1]) + (tx[2] + tx[3]);
+                        if (Tx != Tx) {
+                            Tx = 0.0f;
 #pragma unroll
-                        for (int t = 0; t < 32; ++t) {
-                            se += t == ja ? 0.0f : ek[q][t];
-                            sd = fmaf(ek[q][t], fmaxf(xb[t] - bm, -FLT_MAX), sd);
+                            for (int t = 0; t < 32; ++t) Tx = fmaf(ev[t], fmaxf(xb[t], -FLT_MAX), Tx);
                         }
-                        const float inv = ex2_approx((my_ref[q] - bm) * kLog2e);
-                        blk = rowstate::RowState{bm, (int)(k + ja), se * inv, sd * inv};
+                        RefState &rs = my_rs[q];
+                        if (bm > rs.M) {
+                            // a new maximum: its first occurrence leaves the sum, the old one enters it
+                            int ja = 31;
+#pragma unroll
+                            for (int t = 31; t >= 0; --t)
+                                if (xb[t] == bm) ja = t;
+                            float se = 0.0f;
+#pragma unroll
+                            for (int t = 0; t < 32; ++t) se += t == ja ? 0.0f : ev[t];
+                            rs.R16 += rs.E + se;
+                            // e of the new maximum, formed exactly as the producers formed ev[ja]
+                            rs.E = ex2_approx(fmaf(bm, kLog2e, neg_lse2[q]));
+                            rs.M = bm;
+                            rs.A = (int)(k + ja);
+                        } else {
+                            rs.R16 += S;  // equal maxima keep the earlier index
+                        }
+                        rs.T16 += fmaf(-my_ref[q], S, Tx);
                         if (p.draw) {  // the two groups' log-masses, c + ln(sum of e)
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                float gsum = 0.0f;
-#pragma unroll
-                                for (int t = 0; t < 16; ++t) gsum += ek[q][16 * h + t];
-                                glm[h] = my_ref[q] + philox::kLn2 * __log2f(gsum);
-                            }
+                            glm[0] = my_ref[q] + philox::kLn2 * __log2f(s_lo);
+                            glm[1] = my_ref[q] + philox::kLn2 * __log2f(s_hi);
                         }
                     } else if (F == kBf16 && bm > -INFINITY) {
-                    // the statistics kernel's fold over this row's 32 entries, in two halves
+                    // far above c: the statistics kernel's fold over this row's 32 entries, in two halves
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         float xs[16];
@@ -1031,13 +1085,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int q = 0; q < ROWS_PER_LANE; ++q) {
                         rowstate::merge(my_st[q], my_st16[q]);
                         my_st16[q] = rowstate::empty_row_state();
+                        my_rs[q].R += my_rs[q].R16;
+                        my_rs[q].T += my_rs[q].T16;
+                        my_rs[q].R16 = 0.0f;
+                        my_rs[q].T16 = 0.0f;
                     }
                 }
             }
         }
         if (p.fused)
 #pragma unroll
-            for (int q = 0; q < ROWS_PER_LANE; ++q) rowstate::merge(my_st[q], my_st16[q]);
+            for (int q = 0; q < ROWS_PER_LANE; ++q) {
+                rowstate::merge(my_st[q], my_st16[q]);
+                if constexpr (F == kBf16) rowstate::merge(my_st[q], ref_to_row_state(my_rs[q], my_ref[q]));
+            }
     }
 
     // threads without a role in the main loop (lanes 1-31 of the single-thread roles, and
