@@ -15,7 +15,10 @@
 // partial tile it later reads, so nothing has to be cleared, but two calls whose
 // kernels overlap on the GPU (different streams, no ordering between them) race on
 // it.  The first call on each device looks up the array's device address (with that
-// device current); make that first call before any stream capture.
+// device current), and so does the first call after the device's context was created
+// anew (a device reset reloads the library's device code at another address); make those
+// calls before any stream capture.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -34,19 +37,49 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 constexpr int kMaxScratchDevices = 64;
 std::mutex g_scratch_mutex;
 void *g_scratch_ptr[kMaxScratchDevices] = {};
+unsigned long long g_scratch_ctx[kMaxScratchDevices] = {};  // context the address belongs to
 
-// Device address of g_static_scratch on the current device (looked up once per device).
+// Unique id of the calling thread's current CUDA context (0 when there is none or the driver
+// cannot tell): a context created anew after a reset gets another id.
+unsigned long long current_context_id() {
+    typedef CUresult (*GetCurrent)(CUcontext *);
+    typedef CUresult (*GetId)(CUcontext, unsigned long long *);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *a = nullptr, *b = nullptr;
+        cudaDriverEntryPointQueryResult q1, q2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &q1) == cudaSuccess &&
+            q1 == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &q2) == cudaSuccess &&
+            q2 == cudaDriverEntryPointSuccess) {
+            get_current = reinterpret_cast<GetCurrent>(a);
+            get_id = reinterpret_cast<GetId>(b);
+        }
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of g_static_scratch on the current device: looked up once per device and
+// again whenever the device's context is not the one the address was taken in (without a
+// context id it is looked up on every call).
 dg_status scratch_address(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "soft embed (no alloc): no current device");
     if (dev < 0 || dev >= kMaxScratchDevices) return fail(DG_ERR_UNSUPPORTED, "soft embed (no alloc): device %d", dev);
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_ptr[dev]) {
+    const unsigned long long ctx = current_context_id();
+    if (!g_scratch_ptr[dev] || ctx == 0 || g_scratch_ctx[dev] != ctx) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_static_scratch);
         if (e != cudaSuccess) return cuda_fail(e, "soft embed (no alloc): scratch address lookup");
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = current_context_id();  // the lookup may have made the context current
     }
     *out = g_scratch_ptr[dev];
     return DG_OK;

@@ -145,15 +145,19 @@ dg_status dg_soft_embed(const float *logits, int64_t ldl, const float *lse, int6
  * Same arguments, results and errors as dg_soft_embed, without the workspace: the
  * split-K partial tiles go to a 16 MiB array compiled into the library, which every
  * GPU that loads the library holds until the process exits.  The call allocates
- * and frees nothing.  A shape whose output, padded to whole tiles and held in fp32,
- * needs more than 16 MiB even with one vocabulary split (about 4 Mi entries: R = 1024
- * at d = 2816 fits, R = 8192 does not) returns
- * DG_ERR_UNSUPPORTED.  Results match dg_soft_embed within the soft-embedding
- * tolerance; the number of splits (hence the order of the additions) may differ.
+ * and frees nothing.  One vocabulary split's partial tiles take
+ *     ceil(R / 256) * 256  x  ceil(d / 512) * 512  x  4 bytes
+ * (rows in whole 256-row tiles, columns in whole 512-column tiles); a shape for which
+ * that exceeds 16 MiB (16,777,216 bytes) returns DG_ERR_UNSUPPORTED: R = 1024 at d = 2816
+ * (12 MiB) fits, R = 1100 (padded to 1280 rows, 15 MiB) fits, R = 1400 does not.  When
+ * several splits do not fit, the call uses as many as fit.  Results match dg_soft_embed
+ * within the soft-embedding tolerance; the number of splits (hence the order of the
+ * additions) may differ.
  * The array is shared by every call on a device and keeps the last call's data;
  * calls whose kernels may overlap on the GPU race on it, so order them on one
- * stream.  The first call on each device looks up the array's device address with
- * that device current: make it before any stream capture.
+ * stream.  The first call on each device, and the first after the device's context
+ * was created anew (a device reset), looks up the array's device address with that
+ * device current: make those calls before any stream capture.
  */
 dg_status dg_soft_embed_no_alloc(const float *logits, int64_t ldl, const float *lse, int64_t R,
                                  int64_t vocab_start, int64_t vocab_end,
