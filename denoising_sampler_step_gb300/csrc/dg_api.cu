@@ -8,9 +8,11 @@
 #include <cstdlib>
 #include <cstring>
 
+#include <cstdint>
+
+#include "accept.cuh"
 #include "dg_common.cuh"
 #include "dg_internal.h"
-#include <cstdint>
 
 namespace dg {
 
@@ -130,17 +132,8 @@ dg_status run_soft_embed(const float *logits, int64_t ldl, const float *lse, int
 
 // The acceptance launch of a step, queued between the soft-embed product and its reduce
 // so that it runs on a spare SM while the product streams (it reads only row statistics).
-struct AcceptArgs {
-    const float *H, *kappa, *budgets;
-    int32_t n_req, L_c, min_accept;
-    int32_t *order;
-    uint8_t *mask;
-    int32_t *n_accepted;
-    const uint8_t *eligible;  // NULL: every position
-};
-
 cudaError_t accept_hook(void *ctx, cudaStream_t stream) {
-    const AcceptArgs *a = static_cast<const AcceptArgs *>(ctx);
+    const AcceptSpec *a = static_cast<const AcceptSpec *>(ctx);
     return launch_entropy_accept(a->H, a->kappa, a->n_req, a->L_c, a->budgets, a->min_accept, a->order, a->mask,
                                  a->n_accepted, stream, /*overlap_previous=*/true, a->eligible);
 }
@@ -389,11 +382,12 @@ dg_status run_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, i
     if ((!sampled || draw_t1) && use_single_pass(R, V, vocab_start, vocab_end, d, workspace_bytes, W.fmt, flags)) {
         // one read of the logits: the product folds the statistics (and at temperature 1 the
         // draw); the acceptance runs on them after the reduce starts
-        AcceptArgs acc{H, kappa, budgets, n_req, L_c, min_accept, order, mask, n_accepted, eligible};
+        // the acceptance runs inside the reduce kernel, on the statistics the product's fold gave
+        AcceptSpec acc{H, kappa, budgets, n_req, L_c, min_accept, order, mask, n_accepted, eligible};
         SinglePassOut so{m, lse, H, kappa, argmax, draw_t1 ? loop->candidate : nullptr,
-                         draw_t1 ? loop->seed : 0, draw_t1 ? loop->offset : 0};
+                         draw_t1 ? loop->seed : 0, draw_t1 ? loop->offset : 0, &acc};
         st = run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, d, gamma, E, ldo, workspace,
-                            workspace_bytes, s, accept_hook, &acc, false, &so);
+                            workspace_bytes, s, nullptr, nullptr, false, &so);
         if (st != DG_OK || !loop) return st;
         cudaError_t e = launch_loop_update(draw_t1 ? loop->candidate : argmax, argmax, H, mask, n_req, L_c,
                                            loop->stable_steps,
@@ -412,7 +406,7 @@ dg_status run_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, i
         st = run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, d, gamma, E, ldo, workspace,
                             workspace_bytes, s);
     } else {
-        AcceptArgs acc{H, kappa, budgets, n_req, L_c, min_accept, order, mask, n_accepted, eligible};
+        AcceptSpec acc{H, kappa, budgets, n_req, L_c, min_accept, order, mask, n_accepted, eligible};
         // the product overlaps the tail of the statistics kernel (its W and logits loads do
         // not depend on it), the acceptance overlaps the product
         st = run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, d, gamma, E, ldo, workspace,

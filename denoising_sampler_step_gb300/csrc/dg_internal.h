@@ -13,6 +13,8 @@ int stats_cluster_size(int64_t R, int64_t V);
 cudaError_t launch_row_stats(const float *logits, int64_t R, int64_t V, int64_t ldl, float *m, float *lse,
                              float *H, float *kappa, int32_t *argmax, cudaStream_t stream);
 
+// Threads of an acceptance CTA for L_c positions: a power of two >= L_c (at least 32).
+int accept_threads(int32_t L_c);
 cudaError_t launch_entropy_accept(const float *H, const float *kappa, int32_t n_req, int32_t L_c,
                                   const float *budgets, int32_t min_accept, int32_t *order,
                                   uint8_t *mask, int32_t *n_accepted, cudaStream_t stream,
@@ -50,13 +52,16 @@ struct SoftEmbedPlan {
     size_t workspace_bytes;    // the product and its reduce
     size_t single_pass_bytes;  // the same with the single pass's statistics (launch_soft_embed `single`)
 };
+struct AcceptSpec;
 // Single pass: the product also folds the row statistics (no lse needed before it); they are
-// written here after it, before `between` runs.
+// written here after it.  With `accept`, the reduce kernel also runs that acceptance (in extra
+// CTAs, on the statistics) and `between` is not called.
 struct SinglePassOut {
     float *m, *lse, *H, *kappa;
     int32_t *argmax;
     int32_t *candidate;     // non-NULL: also draw at temperature 1 (two-level Gumbel-max); kappa is
     uint64_t seed, offset;  // then -ln p of the drawn token
+    const AcceptSpec *accept;
 };
 bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t d, int num_sms,
                      SoftEmbedPlan *plan, int fmt = kTableBf16);

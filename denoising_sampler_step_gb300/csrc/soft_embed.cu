@@ -47,6 +47,7 @@
 #include <cstdlib>
 #include <mutex>
 
+#include "accept.cuh"
 #include "dg_common.cuh"
 #include "dg_internal.h"
 #include "philox.cuh"
@@ -180,11 +181,10 @@ struct Params {
     int fused;
     const float *logits; // the reference's source (the split's first kRefEntries entries)
     int64_t ldl;
-    float *ref;          // [splits][R] c, then (after the statistics) exp(c - lse)
+    float *ref;          // [splits][R] c, then (after the statistics) exp(c - lse), or -1 where the
+                         // (split, row) must be recomputed (kRedo)
     float4 *state;       // [splits][n_tiles][R] row summaries (m, argmax bits, rest, t) of the blocks
                          // of the split the column tile folds (`fold` in the producers)
-    int *counts;         // [0] (split, row) pairs to redo: the reference was too far from the maximum
-    int2 *redo;          // [splits * R] the pairs
     // single pass with the temperature-1 draw: the folded blocks also take the draw's first
     // level (a group of 16 entries by log-mass + Gumbel), the statistics kernel the second
     int draw;
@@ -213,6 +213,8 @@ __host__ __device__ inline void split_range(const Params &p, int j, int S, int64
 
 constexpr float kRefSumLog = 82.0f;
 constexpr float kRefBelow = 64.0f;
+// The scale the statistics kernel leaves for a (split, row) the reduce recomputes.
+constexpr float kRedo = -1.0f;
 // The reference is the largest of a split's first kRefEntries logits.
 constexpr int kRefEntries = 32;
 
@@ -319,8 +321,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     // lets it start once its own wait has returned.
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
-    // single pass: the redo count starts at zero (the statistics kernel after this one counts)
-    if (p.fused && blockIdx.x == 0 && threadIdx.x == 0) p.counts[0] = 0;
 
     // work of this cluster (or CTA): (n-tile, row block, split)
     const int pair = blockIdx.x / kCtasPerUnit;
@@ -1196,22 +1196,63 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
+// Single pass, the rare (split, row) pairs whose reference was too far from their maximum
+// (scale kRedo): the split's partial for row i and columns c .. c + 3, recomputed on the CUDA
+// cores against lse (fp32, vocabulary in order).
+template <int F>
+__device__ float4 redo_partial(const Params &p, const void *__restrict__ Wv, int64_t ldw, int d, float lse_i,
+                               int j, int i, int c) {
+    int64_t kb0, kb1;
+    split_range(p, j, p.splits, &kb0, &kb1);
+    int64_t v0 = p.k_begin + kb0 * BK, v1 = p.k_begin + kb1 * BK;
+    if (v0 < p.vocab_start) v0 = p.vocab_start;
+    if (v1 > p.vocab_end) v1 = p.vocab_end;
+    const float l2 = lse_i * kLog2e;
+    const float *lrow = p.logits + (int64_t)i * p.ldl;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int64_t v = v0; v < v1; ++v) {
+        const float pv = ex2_approx(fmaf(lrow[v], kLog2e, -l2));
+        if constexpr (F == kE4m3) {
+            const uint8_t *wr = static_cast<const uint8_t *>(Wv) + (v - p.vocab_start) * ldw + c;
+            const float ps = pv * p.w_scale[v - p.vocab_start];
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                if (c + t < d) acc[t] = fmaf(ps, e4m3_to_f32(wr[t]), acc[t]);
+        } else {
+            const uint16_t *wr = static_cast<const uint16_t *>(Wv) + (v - p.vocab_start) * ldw + c;
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                if (c + t < d) acc[t] = fmaf(pv, __uint_as_float((uint32_t)wr[t] << 16), acc[t]);
+        }
+    }
+    return make_float4(acc[0], acc[1], acc[2], acc[3]);
+}
+
 // E[i, c] = gamma * sum over the splits of column c's tile, in split order.
-// Single pass: each split's partial is scaled by f[split][row] = exp(c - lse) first.
-template <int BN>
+// Single pass (scale given): each split's partial is scaled by f[split][row] = exp(c - lse)
+// first, and a pair marked kRedo is recomputed (redo_partial) and taken with scale 1; the
+// first n_acc CTAs run the acceptance of request blockIdx.x on the statistics instead (they
+// need blockDim.x >= the acceptance's threads and its keys in dynamic shared memory).
+template <int F>
 __global__ void splitk_reduce_kernel(const float4 *__restrict__ ws, const Params p, int d, float gamma,
                                      float *__restrict__ out, int64_t ldo, int vec_out,
-                                     const float *__restrict__ scale) {
-    // the kernel queued next (the single pass's acceptance) reads nothing this one writes;
-    // when this one overlaps the kernel before it (the single pass's redo), it reads the
-    // partials only after that one has completed
+                                     const float *__restrict__ scale, const void *__restrict__ Wv, int64_t ldw,
+                                     const float *__restrict__ lse, const AcceptSpec acc, int n_acc) {
+    constexpr int BN = Fmt<F>::BN;
+    // the kernel queued next reads nothing this one writes; this one reads the partials and
+    // the statistics only after the kernel before it (the single pass's statistics) completed
     grid_launch_dependents();
     grid_dependency_wait();
+    if ((int)blockIdx.x < n_acc) {
+        extern __shared__ unsigned long long keys[];
+        accept_request(acc, (int)blockIdx.x, keys);
+        return;
+    }
     const int64_t groups = ((int64_t)d + 3) / 4;  // column groups of 4
     const int64_t total = (int64_t)p.R * groups;
     const int64_t tile_elems = (int64_t)(BN / 4) * BM;  // float4 per partial tile
-    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
-         t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t nthreads = (int64_t)(gridDim.x - n_acc) * blockDim.x;
+    for (int64_t t = (blockIdx.x - n_acc) * (int64_t)blockDim.x + threadIdx.x; t < total; t += nthreads) {
         // consecutive threads take consecutive rows of one column group: coalesced reads
         const int64_t g = t / p.R;
         const int i = (int)(t - g * p.R);
@@ -1222,10 +1263,14 @@ __global__ void splitk_reduce_kernel(const float4 *__restrict__ ws, const Params
         const int64_t split_stride = (int64_t)p.m_tiles * p.n_tiles * tile_elems;
         const float4 *src = ws + ((int64_t)mt * p.n_tiles + nt) * tile_elems + (int64_t)cg * BM + r;
         // loads issued four at a time, added strictly in split order
-        float4 acc = src[0];
+        float4 acc4 = src[0];
         if (scale) {
-            const float f = scale[i];
-            acc = make_float4(f * acc.x, f * acc.y, f * acc.z, f * acc.w);
+            float f = scale[i];
+            if (f < 0.0f) {
+                acc4 = redo_partial<F>(p, Wv, ldw, d, lse[i], 0, i, c);
+                f = 1.0f;
+            }
+            acc4 = make_float4(f * acc4.x, f * acc4.y, f * acc4.z, f * acc4.w);
         }
         int s = 1;
         for (; s + 4 <= S; s += 4) {
@@ -1238,25 +1283,34 @@ __global__ void splitk_reduce_kernel(const float4 *__restrict__ ws, const Params
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                acc.x = fmaf(f[q], v[q].x, acc.x);
-                acc.y = fmaf(f[q], v[q].y, acc.y);
-                acc.z = fmaf(f[q], v[q].z, acc.z);
-                acc.w = fmaf(f[q], v[q].w, acc.w);
+                if (f[q] < 0.0f) {
+                    v[q] = redo_partial<F>(p, Wv, ldw, d, lse[i], s + q, i, c);
+                    f[q] = 1.0f;
+                }
+                acc4.x = fmaf(f[q], v[q].x, acc4.x);
+                acc4.y = fmaf(f[q], v[q].y, acc4.y);
+                acc4.z = fmaf(f[q], v[q].z, acc4.z);
+                acc4.w = fmaf(f[q], v[q].w, acc4.w);
             }
         }
         for (; s < S; ++s) {
-            const float4 v = src[s * split_stride];
-            const float f = scale ? scale[(int64_t)s * p.R + i] : 1.0f;
-            acc.x = fmaf(f, v.x, acc.x);
-            acc.y = fmaf(f, v.y, acc.y);
-            acc.z = fmaf(f, v.z, acc.z);
-            acc.w = fmaf(f, v.w, acc.w);
+            float4 v = src[s * split_stride];
+            float f = scale ? scale[(int64_t)s * p.R + i] : 1.0f;
+            if (f < 0.0f) {
+                v = redo_partial<F>(p, Wv, ldw, d, lse[i], s, i, c);
+                f = 1.0f;
+            }
+            acc4.x = fmaf(f, v.x, acc4.x);
+            acc4.y = fmaf(f, v.y, acc4.y);
+            acc4.z = fmaf(f, v.z, acc4.z);
+            acc4.w = fmaf(f, v.w, acc4.w);
         }
         float *o = out + (int64_t)i * ldo + c;
         if (vec_out && c + 4 <= d) {
-            *reinterpret_cast<float4 *>(o) = make_float4(gamma * acc.x, gamma * acc.y, gamma * acc.z, gamma * acc.w);
+            *reinterpret_cast<float4 *>(o) =
+                make_float4(gamma * acc4.x, gamma * acc4.y, gamma * acc4.z, gamma * acc4.w);
         } else {
-            const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+            const float a4[4] = {acc4.x, acc4.y, acc4.z, acc4.w};
             for (int e = 0; e < 4 && c + e < d; ++e) o[e] = gamma * a4[e];
         }
     }
@@ -1264,9 +1318,9 @@ __global__ void splitk_reduce_kernel(const float4 *__restrict__ ws, const Params
 
 // Single pass, after the product: per row (one warp), lane l merges the tile summaries of
 // splits l, l + 32, ... (tile order), checks each split's maximum against its reference
-// (pairs whose probabilities could overflow are listed for the redo pass), the lanes' states merge in a
-// fixed shuffle tree, lane 0 writes the statistics, and each split's reference becomes its
-// scale exp(c - lse).
+// (a pair whose probabilities could overflow gets the scale kRedo, and the reduce recomputes
+// it), the lanes' states merge in a fixed shuffle tree, lane 0 writes the statistics, and
+// each split's reference becomes its scale exp(c - lse).
 __global__ void __launch_bounds__(256)
     single_pass_stats_kernel(const Params p, float *__restrict__ out_m, float *__restrict__ out_lse,
                              float *__restrict__ out_H, float *__restrict__ out_kappa,
@@ -1280,7 +1334,8 @@ __global__ void __launch_bounds__(256)
     rowstate::RowState st = rowstate::empty_row_state();
     float dbest = -INFINITY;  // the draw's first level: best group score and group
     int dgrp = 0x7fffffff;
-    for (int s = lane; s < p.splits; s += 32) {
+    uint32_t redo_bits = 0;  // bit k: split lane + 32 k is recomputed by the reduce
+    for (int s = lane, kk = 0; s < p.splits; s += 32, ++kk) {
         rowstate::RowState sp = rowstate::empty_row_state();
         for (int t = 0; t < p.n_tiles; ++t) {
             const float4 v = p.state[((int64_t)s * p.n_tiles + t) * p.R + row];
@@ -1297,10 +1352,8 @@ __global__ void __launch_bounds__(256)
         // the split's probabilities against its reference: ln of their sum is
         // (m - c) + ln Z_split; list the pair for the redo pass if they could overflow
         const float gap = sp.m - p.ref[(int64_t)s * p.R + row];
-        if (sp.m > -INFINITY && !(gap + log1pf(sp.rest) <= kRefSumLog && gap >= -kRefBelow)) {
-            const int slot = atomicAdd(&p.counts[0], 1);
-            p.redo[slot] = make_int2(s, (int)row);
-        }
+        if (sp.m > -INFINITY && !(gap + log1pf(sp.rest) <= kRefSumLog && gap >= -kRefBelow))
+            redo_bits |= 1u << kk;
         rowstate::merge(st, sp);
     }
 #pragma unroll
@@ -1324,10 +1377,12 @@ __global__ void __launch_bounds__(256)
     }
     lse = __shfl_sync(0xffffffffu, lse, 0);
     const float m = __shfl_sync(0xffffffffu, st.m, 0);
-    for (int s = lane; s < p.splits; s += 32) {
+    for (int s = lane, kk = 0; s < p.splits; s += 32, ++kk) {
         float *r = p.ref + (int64_t)s * p.R + row;
         // c <= m <= lse: at most 1; a row without a distribution gets NaN, as in the two-pass step
-        *r = m == -INFINITY ? __int_as_float(0x7fc00000) : ex2_approx((*r - lse) * kLog2e);
+        *r = m == -INFINITY          ? __int_as_float(0x7fc00000)
+             : (redo_bits >> kk) & 1u ? kRedo
+                                      : ex2_approx((*r - lse) * kLog2e);
     }
     if (p.draw) {
         // the second level: lanes 0-15 draw inside the chosen group (temperature 1); kappa
@@ -1370,57 +1425,6 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// Single pass, the rare (split, row) pairs whose reference was too far from the maximum:
-// their partial, sum over the split of exp(l - lse) W[v, :], is recomputed on the CUDA
-// cores (fp32, vocabulary in order) for every column tile, and the scale set to 1.  One CTA
-// per listed pair, in turn; nothing to do when the list is empty.
-template <int F>
-__global__ void __launch_bounds__(256)
-    single_pass_redo_kernel(const Params p, const void *__restrict__ Wv, int64_t ldw, int d,
-                            const float *__restrict__ lse) {
-    constexpr int BN = Fmt<F>::BN;
-    grid_dependency_wait();  // the list is complete once the statistics kernel is
-    grid_launch_dependents();
-    const int n = p.counts[0];
-    for (int e = blockIdx.x; e < n; e += gridDim.x) {
-        const int2 sr = p.redo[e];
-        const int j = sr.x, row = sr.y;
-        int64_t kb0, kb1;
-        split_range(p, j, p.splits, &kb0, &kb1);
-        int64_t v0 = p.k_begin + kb0 * BK, v1 = p.k_begin + kb1 * BK;
-        if (v0 < p.vocab_start) v0 = p.vocab_start;
-        if (v1 > p.vocab_end) v1 = p.vocab_end;
-        const float l2 = lse[row] * kLog2e;
-        const float *lrow = p.logits + (int64_t)row * p.ldl;
-        const int mt = row / BM, r = row % BM;
-        const int64_t tile_elems = (int64_t)(BN / 4) * BM;
-        float4 *ws = reinterpret_cast<float4 *>(p.ws);
-        for (int c4 = threadIdx.x; c4 * 4 < d; c4 += blockDim.x) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int64_t v = v0; v < v1; ++v) {
-                const float pv = ex2_approx(fmaf(lrow[v], kLog2e, -l2));
-                if constexpr (F == kE4m3) {
-                    const uint8_t *wr = static_cast<const uint8_t *>(Wv) + (v - p.vocab_start) * ldw + 4 * c4;
-                    const float ps = pv * p.w_scale[v - p.vocab_start];
-#pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        if (4 * c4 + t < d) acc[t] = fmaf(ps, e4m3_to_f32(wr[t]), acc[t]);
-                } else {
-                    const uint16_t *wr = static_cast<const uint16_t *>(Wv) + (v - p.vocab_start) * ldw + 4 * c4;
-#pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        if (4 * c4 + t < d) acc[t] = fmaf(pv, __uint_as_float((uint32_t)wr[t] << 16), acc[t]);
-                }
-            }
-            const int c = 4 * c4;
-            const int nt = c / BN, cg = (c % BN) / 4;
-            ws[((int64_t)j * p.m_tiles * p.n_tiles + (int64_t)mt * p.n_tiles + nt) * tile_elems + (int64_t)cg * BM + r] =
-                make_float4(acc[0], acc[1], acc[2], acc[3]);
-        }
-        if (threadIdx.x == 0) p.ref[(int64_t)j * p.R + row] = 1.0f;
-    }
-}
-
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -1460,11 +1464,12 @@ size_t soft_embed_workspace_bytes(const SoftEmbedPlan &plan, int splits) {
 }
 
 // The single pass's extra workspace, after the partial tiles: references / scales
-// [splits][R] fp32, summaries [splits][R] x 16 B, two counters, the redo list [splits][R] x 8 B.
+// [splits][R] fp32, summaries [splits][n_tiles][R] x 16 B, the draw's first level
+// [splits][n_tiles][R] x 8 B.
 static size_t align16(size_t b) { return (b + 15) & ~size_t(15); }
 size_t single_pass_extra_bytes(const SoftEmbedPlan &plan, int64_t R) {
     const size_t n = (size_t)plan.splits * (size_t)R;
-    return align16(n * 4) + n * (size_t)plan.n_tiles * 16 + 16 + align16(n * 8) + n * (size_t)plan.n_tiles * 8;
+    return align16(n * 4) + n * (size_t)plan.n_tiles * 16 + n * (size_t)plan.n_tiles * 8;
 }
 
 bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t d, int num_sms,
@@ -1626,8 +1631,6 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     p.ldl = ldl;
     p.ref = nullptr;
     p.state = nullptr;
-    p.counts = nullptr;
-    p.redo = nullptr;
     p.draw = 0;
     p.k0 = p.k1 = p.o0 = p.o1 = 0;
     p.draws = nullptr;
@@ -1639,10 +1642,6 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
         x += align16(n * 4);
         p.state = reinterpret_cast<float4 *>(x);
         x += n * (size_t)plan.n_tiles * 16;
-        p.counts = reinterpret_cast<int *>(x);
-        x += 16;
-        p.redo = reinterpret_cast<int2 *>(x);
-        x += align16(n * 8);
         if (single->candidate) {
             p.draw = 1;
             p.draws = reinterpret_cast<float2 *>(x);
@@ -1695,21 +1694,13 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
         cudaLaunchConfig_t c1 = small_cfg((unsigned)((R * 32 + 255) / 256));
         e = cudaLaunchKernelEx(&c1, single_pass_stats_kernel, p, single->m, single->lse, single->H, single->kappa,
                                single->argmax);
-        if (e == cudaSuccess) {
-            cudaLaunchConfig_t c2 = small_cfg(64);
-            e = e4 ? cudaLaunchKernelEx(&c2, single_pass_redo_kernel<kE4m3>, p, tab.W, ldw, (int)d,
-                                        (const float *)single->lse)
-                   : cudaLaunchKernelEx(&c2, single_pass_redo_kernel<kBf16>, p, tab.W, ldw, (int)d,
-                                        (const float *)single->lse);
-        }
         if (e != cudaSuccess) {
-            *msg = "single pass: statistics or redo launch failed";
+            *msg = "single pass: statistics launch failed";
             return e;
         }
     }
-    // two passes: the acceptance overlaps the product, then the reduce; single pass: the
-    // acceptance needs the statistics that follow the product, so the reduce goes first
-    // and lets the acceptance start at once
+    // two passes: the acceptance (between) overlaps the product, then the reduce; single pass:
+    // the reduce kernel also runs the acceptance, in its first CTAs, on the statistics
     if (between && !single) {
         e = between(ctx, stream);
         if (e != cudaSuccess) {
@@ -1717,32 +1708,32 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
             return e;
         }
     }
+    const AcceptSpec no_accept{nullptr, nullptr, nullptr, 0, 1, 0, nullptr, nullptr, nullptr, nullptr};
+    const AcceptSpec &acc = (single && single->accept) ? *single->accept : no_accept;
+    const int n_acc = (single && single->accept) ? acc.n_req : 0;
+    const int threads = n_acc > 0 ? (accept_threads(acc.L_c) > 256 ? accept_threads(acc.L_c) : 256) : 256;
     const int vec_out = (ldo % 4 == 0) && (((uintptr_t)out & 15) == 0);
     const int64_t total = R * ((d + 3) / 4);
-    int64_t blocks = (total + 255) / 256;
-    const int64_t cap = (int64_t)device_sm_count() * 8;
+    int64_t blocks = (total + threads - 1) / threads;
+    const int64_t cap = (int64_t)device_sm_count() * 8 * 256 / threads;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    if (single) {
-        cudaLaunchConfig_t c3 = small_cfg((unsigned)blocks);
-        e = e4 ? cudaLaunchKernelEx(&c3, splitk_reduce_kernel<Fmt<kE4m3>::BN>, static_cast<const float4 *>(workspace),
-                                    p, (int)d, gamma, out, ldo, vec_out, (const float *)p.ref)
-               : cudaLaunchKernelEx(&c3, splitk_reduce_kernel<Fmt<kBf16>::BN>, static_cast<const float4 *>(workspace),
-                                    p, (int)d, gamma, out, ldo, vec_out, (const float *)p.ref);
-    } else {
-        if (e4)
-            splitk_reduce_kernel<Fmt<kE4m3>::BN><<<(unsigned)blocks, 256, 0, stream>>>(
-                static_cast<const float4 *>(workspace), p, (int)d, gamma, out, ldo, vec_out, nullptr);
-        else
-            splitk_reduce_kernel<Fmt<kBf16>::BN><<<(unsigned)blocks, 256, 0, stream>>>(
-                static_cast<const float4 *>(workspace), p, (int)d, gamma, out, ldo, vec_out, nullptr);
-        e = cudaGetLastError();
-    }
+    cudaLaunchConfig_t c3 = small_cfg((unsigned)(blocks + n_acc));
+    c3.blockDim = dim3((unsigned)threads, 1, 1);
+    c3.dynamicSmemBytes = n_acc > 0 ? threads * sizeof(unsigned long long) : 0;
+    c3.numAttrs = single ? 1 : 0;  // the plain reduce follows the product without overlap
+    const float4 *ws4 = static_cast<const float4 *>(workspace);
+    const float *scale = single ? (const float *)p.ref : nullptr;
+    const float *lse_s = single ? (const float *)single->lse : nullptr;
+    e = e4 ? cudaLaunchKernelEx(&c3, splitk_reduce_kernel<kE4m3>, ws4, p, (int)d, gamma, out, ldo, vec_out, scale,
+                                tab.W, ldw, lse_s, acc, n_acc)
+           : cudaLaunchKernelEx(&c3, splitk_reduce_kernel<kBf16>, ws4, p, (int)d, gamma, out, ldo, vec_out, scale,
+                                tab.W, ldw, lse_s, acc, n_acc);
     if (e != cudaSuccess) {
         *msg = "split-K reduce launch failed";
         return e;
     }
-    if (between && single) {
+    if (between && single && !single->accept) {
         e = between(ctx, stream);
         if (e != cudaSuccess) *msg = "launch after the reduce failed";
     }
