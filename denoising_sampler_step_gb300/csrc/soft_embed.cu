@@ -81,16 +81,24 @@ constexpr int ROWS_PER_LANE = 128 / (32 * GROUP_WARPS);
 constexpr int THREADS = 384;
 constexpr int TMEM_COLS = 512;
 constexpr uint16_t kPairMask = 0x3;
-// A cluster of two CTAs.
-// bf16 table: a tcgen05 CTA pair holding the two 128-row halves of a 256-row tile and one
-//   column tile.  The even CTA issues M = 256 MMAs over both CTAs' rows (cta_group::2); each
-//   CTA loads 128 of every 256 W columns, so each W byte leaves L2 once and a W slot is half
-//   a block's tile.  The odd CTA's W bytes complete on the even CTA's barrier (the pair form
-//   of the TMA load), and its producers signal a finished A tile with a 16-byte bulk copy that
-//   completes on that barrier too.
-// 8-bit table: one row block and two column tiles; each CTA issues M = 128 MMAs and loads its
-//   own W tile; the A operand is shared (each CTA computes every other block's and copies it).
-constexpr int kCtasPerUnit = 2;
+// A cluster of CTAs.
+// bf16 table: four CTAs, two tcgen05 CTA pairs (ranks 0-1 and 2-3) over the same 256 rows and
+//   two adjacent column tiles: rank r holds rows 128 (r & 1) ... of the 256 and column tile
+//   2 cp + (r >> 1).  In each pair the even CTA issues M = 256 MMAs over both CTAs' rows
+//   (cta_group::2); each CTA loads 128 of every 256 W columns, so each W byte leaves L2 once
+//   and a W slot is half a block's tile.  The odd CTA's W bytes complete on the even CTA's
+//   barrier (the pair form of the TMA load).  The A operand is shared between the pairs: for
+//   block i the CTAs with (r >> 1) == i % 2 load its logits and form its A tile, keep it and
+//   copy it to the CTA with the same rows in the other pair (r ^ 2); a pair's odd CTA tells
+//   its even CTA that its rows are in place with a 16-byte bulk copy onto the even CTA's
+//   barrier (directly when it formed them, relayed when they were copied in).
+// 8-bit table: two CTAs, one row block and two column tiles; each CTA issues M = 128 MMAs and
+//   loads its own W tile; the A operand is shared the same way (each CTA computes every other
+//   block's and copies it).
+constexpr int kCtasPerUnit = 2;  // the 8-bit table's cluster
+constexpr int kQuadCtas = 4;     // the bf16 table's cluster
+template <int F>
+__host__ __device__ constexpr int cluster_ctas() { return F == kTableBf16 ? kQuadCtas : kCtasPerUnit; }
 // ring depth of the bf16 pair (W and A slots, one index): half-size W slots leave room for six
 constexpr int kPairStages = 6;
 
@@ -158,7 +166,7 @@ static_assert(kSfaCol + 4 * Fmt<kE4m3>::AST * Fmt<kE4m3>::BPS <= kSfbCol && kSfb
 static_assert(LSTAGES >= PGROUPS && kPairStages >= PGROUPS, "a slot per producer group at least");
 // the bf16 pair's A-ready signals: 16 bytes per producer warp in the even CTA, after the barriers
 constexpr int kSigOffset = 256;
-static_assert(kSigOffset + 16 * (PRODUCER_WARPS + 1) <= 512, "signal area inside the barrier region");
+static_assert(kSigOffset + 16 * (PRODUCER_WARPS + 2) <= 512, "signal area inside the barrier region");
 
 struct Params {
     const float *lse;
@@ -322,10 +330,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
 
-    // work of this cluster (or CTA): (n-tile, row block, split)
-    const int pair = blockIdx.x / kCtasPerUnit;
-    const int m_pairs = p.m_tiles / kCtasPerUnit;
-    const int full_pairs = p.splits * m_pairs * p.n_full;
+    // work of this cluster: (column tile(s), row block(s), split)
+    const int pair = blockIdx.x / cluster_ctas<F>();
+    const int m_pairs = p.m_tiles / 2;
     int nt, mp, j, S, halves, mt;
     // 8-bit table: a cluster is one row block and two adjacent column tiles (CTA c takes
     // tile 2 ntp + c; n_tiles is even, a last odd tile's partner lies past d and reads zeros)
@@ -340,24 +347,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         nt = 2 * ntp + (int)rank;
         halves = nt < p.n_full ? 2 : 1;
         mp = 0;
-    } else if (pair < full_pairs) {
-        nt = pair % p.n_full;
-        mp = (pair / p.n_full) % m_pairs;
-        j = pair / (p.n_full * m_pairs);
-        S = p.splits;
-        halves = 2;
     } else {
-        const int q = pair - full_pairs;
-        nt = p.n_full;
-        mp = q % m_pairs;
-        j = q / m_pairs;
-        S = p.tail_splits;
-        halves = 1;
+        // bf16: cluster (column pair cp, row pair mp, split j); n_tiles is even (a last odd
+        // tile's partner lies past d and reads zeros); tiles from n_full on are half width
+        ntp = pair % ntp_count;
+        mp = (pair / ntp_count) % m_pairs;
+        j = pair / (ntp_count * m_pairs);
+        S = p.splits;
+        nt = 2 * ntp + (int)(rank >> 1);
+        halves = nt < p.n_full ? 2 : 1;
+        mt = 2 * mp + (int)(rank & 1);
     }
-    if (F != kE4m3) mt = kCtasPerUnit * mp + (int)rank;
-    // 8-bit table: CTA c produces (loads the logits of, stages the scales of, computes the A
-    // operand of) the blocks i with i % 2 == c and copies each A operand to its partner
-    const int i0 = F == kE4m3 ? (int)rank : 0, di = F == kE4m3 ? 2 : 1;
+    // the column parity of this CTA in its cluster: it produces (loads the logits of, stages
+    // the scales of, computes the A operand of) the blocks i with i % 2 == cpar and copies each
+    // A operand to the CTA with the same rows in the other column tile
+    const int cpar = F == kE4m3 ? (int)rank : (int)(rank >> 1);
+    const int i0 = cpar, di = 2;
     int64_t kb0, kb1;
     split_range(p, j, S, &kb0, &kb1);
     const int nkb = (int)(kb1 - kb0);
@@ -371,13 +376,19 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(smem_u32(&full_s[s]), 1);
         }
         for (int s = 0; s < AST; ++s) {
-            // full_a: the producer group's warps and the W TMA's arrival (with the W bytes);
-            // 8-bit table: also the MMA thread's arrival for the partner's block (with the
-            // copied bytes).  empty: this CTA's commit; 8-bit table: both CTAs' commits (the
-            // slot's A operand is read in both)
-            const int fa = GROUP_WARPS + 1 + (F == kE4m3 ? 1 : 0);
+            // full_a, 8-bit table: this CTA's producer group, the partner's block (the MMA
+            // thread's arrival, with the copied bytes) and the W TMA's arrival (with the W bytes).
+            // bf16, a pair's even CTA: a slot of its own parity, the producer group's warps and
+            // the W TMA's arrival (with both CTAs' W bytes and the odd CTA's four signals); a slot
+            // of the other parity, the W TMA's arrival alone (with the W bytes, the copied A tile
+            // and the odd CTA's relayed signal).  bf16, odd CTA: the relay's arrival (with the
+            // copied A tile; slots of the other parity only).
+            // empty: the commits of every CTA pair (8-bit table: both CTAs) that reads the slot or
+            // copies into it
+            int fa = GROUP_WARPS + 2;
+            if (F == kBf16) fa = (rank & 1) == 0 && (s & 1) == cpar ? GROUP_WARPS + 1 : 1;
             mbar_init(smem_u32(&full_a[s]), fa);
-            mbar_init(smem_u32(&empty[s]), F == kE4m3 ? kCtasPerUnit : 1);
+            mbar_init(smem_u32(&empty[s]), 2);
         }
         mbar_init(smem_u32(acc_full), 1);
         *abort_flag = 0;
@@ -433,9 +444,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool producer = F == kE4m3 ? warp >= 4 : ((warp & 3) != 0 && warp < 11);
     if (warp == kWarpW) {
         // ------------------------------------------------------------ W TMA
-        // bf16 pair: each CTA loads its 128 columns of each 256-column half (atoms 4h + 2 rank
-        // and + 1), the bytes counted on the even CTA's A slot barrier, which that CTA arms
-        // for both CTAs' bytes and the odd CTA's A-ready signals; 8-bit table: each CTA loads
+        // bf16: each CTA loads its 128 columns of each 256-column half (atoms 4h + 2 (rank & 1)
+        // and + 1), the bytes counted on its pair's even CTA's A slot barrier, which that CTA
+        // arms for both CTAs' bytes and the odd CTA's A-ready signals (or, for a block the other
+        // pair forms, the copied A tile and the relayed signal); 8-bit table: each CTA loads
         // its own tile's 128-column atoms of the slot's two blocks, counted on its own A slot
         // barrier.  W lines are marked evict-first
         if (lane == 0) {
@@ -444,7 +456,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t w_policy = l2_policy_evict_first();
             // bf16: a 3-D map fetches a CTA's 2 atoms of a half in one load
             const bool w3d = p.w3d;
-            const uint32_t lead_a = map_to_cta(smem_u32(&full_a[0]), 0);  // the even CTA's full_a[0]
+            const uint32_t lead_a = map_to_cta(smem_u32(&full_a[0]), rank & ~1u);  // the pair's even CTA's full_a[0]
             for (int i = 0; i < nkb / BPS; ++i) {  // ring slots (BPS blocks each)
                 const int s = i % WST;
                 const uint32_t u = (uint32_t)(i / WST);
@@ -467,13 +479,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                         tma_load_2d_hint(smem_u32(w_ring + s * W_SLOT + a * BPS * W_BOX_BYTES), &tm_w, bw,
                                          col0 + 128 * a, wy, w_policy);
                 } else {
-                    // both CTAs' W bytes of the slot, and the odd CTA's four A-ready signals
-                    if (rank == 0)
-                        mbar_arrive_expect_tx(bw, (uint32_t)halves * W_SLOT + 16u * GROUP_WARPS);
+                    // both CTAs' W bytes of the slot, and the odd CTA's four A-ready signals (a block
+                    // this pair forms) or the A tile copied in and the odd CTA's relayed signal
+                    if ((rank & 1) == 0)
+                        mbar_arrive_expect_tx(bw, (uint32_t)halves * W_SLOT +
+                                                      ((i & 1) == cpar ? 16u * GROUP_WARPS : (uint32_t)A_BYTES + 16u));
                     const uint32_t bl = lead_a + 8u * (uint32_t)s;
                     for (int h = 0; h < halves; ++h) {
                         const uint32_t dst = smem_u32(w_ring + s * W_SLOT + h * 2 * W_BOX_BYTES);
-                        const int atom = col0 / 64 + 4 * h + 2 * (int)rank;
+                        const int atom = col0 / 64 + 4 * h + 2 * (int)(rank & 1);  // this CTA's half of the pair
                         if (w3d) {
                             tma_load_3d_pair_hint(dst, &tm_w, bl, 0, wy, atom, w_policy);
                         } else {
@@ -491,7 +505,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // loads in flight finish before the CTA may leave (bf16 pair: the even CTA's barriers
             // count both CTAs' loads, and the odd CTA leaves only after the final cluster
             // barrier, which the even CTA reaches after this drain)
-            if (!ok && (!kPairMma || rank == 0))
+            if (!ok && (!kPairMma || (rank & 1) == 0))
                 for (int s = 0; s < WST; ++s)
                     if (issued[s] > 0) drain_wait(smem_u32(&full_a[s]), (issued[s] - 1) & 1);
         }
@@ -528,8 +542,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
-        // (bf16 pair: the even CTA's thread issues for both CTAs; the odd CTA's has no role)
-        if (lane == 0 && (!kPairMma || rank == 0)) {
+        // (bf16: a pair's even CTA's thread issues for both CTAs; the odd CTA's relays)
+        if (lane == 0 && kPairMma && (rank & 1) != 0) {
+            // relay: the A tiles of the blocks the other pair forms arrive here by copy; once one
+            // has landed, a 16-byte copy onto the even CTA's barrier tells its MMA thread
+            const uint32_t lead = rank & ~1u;
+            for (int i = 1 - cpar; i < nkb; i += 2) {
+                const int s = i % AST;
+                const uint32_t u = (uint32_t)(i / AST);
+                mbar_arrive_expect_tx(smem_u32(&full_a[s]), (uint32_t)A_BYTES);
+                if (!mbar_wait(smem_u32(&full_a[s]), u & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                bulk_copy_to_cluster(map_to_cta(smem_u32(sig_area + 16 * (PRODUCER_WARPS + 1)), lead),
+                                     smem_u32(sig_area), 16u, map_to_cta(smem_u32(&full_a[s]), lead));
+            }
+        } else if (lane == 0 && (!kPairMma || (rank & 1) == 0)) {
             grid_dependency_wait();  // nothing to issue before the producers' first tile anyway
             grid_launch_dependents();
             constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, 256, /*A K-major*/ 0, /*B N-major*/ 1);
@@ -614,17 +643,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                     arm(i + 1);
                     a_in = test(smem_u32(&full_a[(i + 1) % AST]), (uint32_t)((i + 1) / AST) & 1);
                 }
-                // one commit releases the W and A slots of both CTAs once the MMAs have read
-                // them (bf16 pair: the pair's MMAs read both CTAs' slots; 8-bit table: the A
-                // slot is read in both CTAs)
+                // one commit releases the W and A slots once the MMAs have read them: 8-bit table,
+                // in both CTAs (the A slot is read in both); bf16, in all four CTAs (the pair's MMAs
+                // read both its CTAs' slots, and the other pair's CTAs copy A tiles into them)
                 if constexpr (F == kE4m3)
                     umma_commit_multicast(smem_u32(&empty[s]), kPairMask);
                 else
-                    umma_commit_pair(smem_u32(&empty[s]), kPairMask);
+                    umma_commit_pair(smem_u32(&empty[s]), 0xF);
                 issued_any = true;
             }
             if constexpr (kPairMma)
-                umma_commit_pair(smem_u32(acc_full), kPairMask);
+                umma_commit_pair(smem_u32(acc_full), (uint16_t)(kPairMask << (rank & 2u)));  // this pair
             else
                 umma_commit(smem_u32(acc_full));
             if (*abort_flag && issued_any) drain_wait(smem_u32(acc_full), 0);
@@ -749,13 +778,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             const bool edge = (k < p.vocab_start) || (k + BK > p.vocab_end);
             uint32_t packed[ROWS_PER_LANE][16];
             uint32_t sf_word[ROWS_PER_LANE];  // 8-bit table: the (row, block) scale bytes
-            // every block is folded once per row block: (bf16) by column tile (i / PGROUPS +
-            // (i % PGROUPS) (n_tiles / 2)) % n_tiles, so that the two producer groups' folds fall
-            // half a cycle apart and one group keeps producing while the other folds; (8-bit
-            // table) by the CTA producing it in cluster (i / 4) % (n_tiles / 2)
-            const bool fold =
-                p.fused && (F == kE4m3 ? (i >> 2) % ntp_count == ntp
-                                       : (i / PGROUPS + (i % PGROUPS) * (p.n_tiles / 2)) % p.n_tiles == nt);
+            // every block is folded once per row block, by the producers of a CTA that forms it:
+            // (bf16) the one in column pair (i / 2) % (n_tiles / 2), (8-bit table) the one in
+            // cluster (i / 4) % (n_tiles / 2); a CTA's folds alternate between its producer groups
+            const bool fold = p.fused && (F == kE4m3 ? (i >> 2) : (i >> 1)) % ntp_count == ntp;
             // 8-bit table: the block's normalised row scales u (0 outside the slice) and their
             // exponent E (row scale = u 2^E), staged by warp 0
             float us[F == kE4m3 ? 32 : 1];
@@ -920,12 +946,23 @@ __global__ void __launch_bounds__(THREADS, 1)
             fence_proxy_async_smem();
             __syncwarp();  // every lane's A stores (and proxy fence) before the arrival
             if (lane == 0) {
-                if (kPairMma && rank != 0) {
-                    // the even CTA's MMA thread reads this CTA's rows too: a 16-byte copy that
-                    // completes on its barrier tells it this warp's rows are in place (issued
-                    // after the rows' stores and proxy fence; the bytes are never read)
-                    bulk_copy_to_cluster(map_to_cta(smem_u32(sig_area + 16 * (1 + pw)), 0), smem_u32(sig_area), 16u,
-                                         map_to_cta(smem_u32(&full_a[s]), 0));
+                if constexpr (kPairMma) {
+                    if (rank & 1) {
+                        // the pair's even CTA's MMA thread reads this CTA's rows too: a 16-byte
+                        // copy that completes on its barrier tells it this warp's rows are in
+                        // place (issued after the rows' stores and proxy fence; never read)
+                        const uint32_t lead = rank & ~1u;
+                        bulk_copy_to_cluster(map_to_cta(smem_u32(sig_area + 16 * (1 + pw)), lead), smem_u32(sig_area),
+                                             16u, map_to_cta(smem_u32(&full_a[s]), lead));
+                    } else {
+                        mbar_arrive(smem_u32(&full_a[s]));
+                    }
+                    // the warp's 32 A rows (2 KiB) to the same slot of the CTA with the same rows
+                    // in the other column tile, completing on its full_a
+                    const uint32_t twin = rank ^ 2u;
+                    const uint32_t a_src = smem_u32(at + wig * 2048);
+                    bulk_copy_to_cluster(map_to_cta(a_src, twin), a_src, 2048u,
+                                         map_to_cta(smem_u32(&full_a[s]), twin));
                 } else {
                     mbar_arrive(smem_u32(&full_a[s]));
                 }
@@ -1472,6 +1509,52 @@ size_t single_pass_extra_bytes(const SoftEmbedPlan &plan, int64_t R) {
     return align16(n * 4) + n * (size_t)plan.n_tiles * 16 + n * (size_t)plan.n_tiles * 8;
 }
 
+// The product kernels' shared-memory limit, raised once per device (a function attribute
+// belongs to the device's context; setting it twice from racing threads is harmless).
+static cudaError_t ensure_kernel_attributes() {
+    static std::atomic<int> attr_set[kMaxAttrDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < kMaxAttrDevices && attr_set[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    e = cudaFuncSetAttribute(soft_embed_kernel<kBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<kBf16>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(soft_embed_kernel<kE4m3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_bytes<kE4m3>());
+    if (e == cudaSuccess && dev < kMaxAttrDevices) attr_set[dev].store(1, std::memory_order_release);
+    return e;
+}
+
+// Clusters of the bf16 product (four CTAs) that fit on the current device at once (36 on a
+// 152-SM GB300: whole clusters must sit in one GPC), looked up once per device.
+static int quad_clusters_per_wave(int num_sms) {
+    static std::atomic<int> cached[kMaxAttrDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return num_sms / kQuadCtas;
+    if (dev < kMaxAttrDevices) {
+        const int c = cached[dev].load(std::memory_order_acquire);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (ensure_kernel_attributes() == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kQuadCtas * 64, 1, 1);
+        cfg.blockDim = dim3(THREADS, 1, 1);
+        cfg.dynamicSmemBytes = smem_bytes<kBf16>();
+        cudaLaunchAttribute a[1];
+        a[0].id = cudaLaunchAttributeClusterDimension;
+        a[0].val.clusterDim.x = kQuadCtas;
+        a[0].val.clusterDim.y = 1;
+        a[0].val.clusterDim.z = 1;
+        cfg.attrs = a;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, (void *)soft_embed_kernel<kBf16>, &cfg) != cudaSuccess) n = 0;
+    }
+    if (n <= 0) n = num_sms / kQuadCtas;
+    if (dev < kMaxAttrDevices) cached[dev].store(n, std::memory_order_release);
+    return n;
+}
+
 bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t d, int num_sms,
                      SoftEmbedPlan *plan, int fmt) {
     if (R <= 0 || d <= 0 || vocab_end <= vocab_start || vocab_start < 0 || num_sms < 2) return false;
@@ -1481,21 +1564,25 @@ bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t 
     pl.bn = tile_width(fmt);
     pl.k_begin = vocab_start & ~int64_t(3);
     pl.nkb = (vocab_end - pl.k_begin + BK - 1) / BK;
-    int64_t m_pairs = (R + kCtasPerUnit * BM - 1) / (kCtasPerUnit * BM);  // row blocks per unit
-    pl.m_tiles = (int)(kCtasPerUnit * m_pairs);
+    int64_t m_pairs = (R + 2 * BM - 1) / (2 * BM);  // 256-row blocks
+    pl.m_tiles = (int)(2 * m_pairs);
     int n_full, tail;
     column_tiles(d, pl.bn, &pl.n_tiles, &n_full, &tail);
+    // clusters of two column tiles (bf16: and both 128-row halves of a 256-row block; 8-bit
+    // table: one 128-row block): an even tile count, a last odd tile's partner past d
+    pl.n_tiles += pl.n_tiles & 1;
+    int64_t clusters;
     if (fmt == kE4m3) {
-        // clusters of one row block and two column tiles: every row block, an even tile count
         pl.m_tiles = (int)((R + BM - 1) / BM);
-        pl.n_tiles += pl.n_tiles & 1;
         m_pairs = pl.m_tiles;
-        n_full = pl.n_tiles / 2;
-        tail = 0;
+        clusters = num_sms / kCtasPerUnit;
+    } else {
+        clusters = quad_clusters_per_wave(num_sms);
     }
+    n_full = pl.n_tiles / 2;  // units per split and row block: column pairs
+    tail = 0;
     // choose the vocabulary splits that finish soonest: whole waves of clusters times
-    // the largest per-cluster work (vocabulary blocks x 256-column halves)
-    const int64_t clusters = num_sms / kCtasPerUnit;
+    // the largest per-cluster work (vocabulary blocks)
     int best = 1;
     double best_t = 1e300;
     // at least 16 blocks (four rounds of the stage ring) per split, at most 64 splits
@@ -1589,26 +1676,14 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
             return cudaErrorInvalidValue;
         }
     }
-    // the shared-memory limit is raised once per device (a function attribute belongs to the
-    // device's context); setting it twice from racing threads is harmless
-    static std::atomic<int> attr_set[kMaxAttrDevices];
-    int dev = 0;
-    cudaError_t attr_err = cudaGetDevice(&dev);
-    if (attr_err == cudaSuccess && (dev >= kMaxAttrDevices || !attr_set[dev].load(std::memory_order_acquire))) {
-        attr_err = cudaFuncSetAttribute(soft_embed_kernel<kBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        smem_bytes<kBf16>());
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(soft_embed_kernel<kE4m3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            smem_bytes<kE4m3>());
-        if (attr_err == cudaSuccess && dev < kMaxAttrDevices) attr_set[dev].store(1, std::memory_order_release);
-    }
+    const cudaError_t attr_err = ensure_kernel_attributes();
     if (attr_err != cudaSuccess) {
         *msg = "could not raise the shared-memory limit of the soft-embed kernel";
         return attr_err;
     }
     int n_tiles, n_full, tail;
     column_tiles(d, plan.bn, &n_tiles, &n_full, &tail);
-    if (e4) n_tiles = plan.n_tiles;  // rounded up to pairs of column tiles
+    n_tiles = plan.n_tiles;  // rounded up to pairs of column tiles
     Params p;
     p.lse = lse;
     p.ws = static_cast<float *>(workspace);
@@ -1653,17 +1728,18 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
         }
         overlap_previous = false;  // nothing before it to wait for
     }
-    const int64_t pairs = e4 ? (int64_t)plan.m_tiles * (n_tiles / 2) * p.splits
-                             : (int64_t)(plan.m_tiles / kCtasPerUnit) * (n_full * (int64_t)p.splits + p.tail_splits);
+    // clusters: (column pair, row block, split); bf16 row blocks are 256 rows (a CTA pair)
+    const int64_t units = (int64_t)(e4 ? plan.m_tiles : plan.m_tiles / 2) * (n_tiles / 2) * p.splits;
+    const int cluster = e4 ? cluster_ctas<kE4m3>() : cluster_ctas<kBf16>();
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(kCtasPerUnit * pairs), 1, 1);
+    cfg.gridDim = dim3((unsigned)(cluster * units), 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = e4 ? smem_bytes<kE4m3>() : smem_bytes<kBf16>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCtasPerUnit;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
