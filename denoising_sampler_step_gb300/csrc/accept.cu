@@ -8,7 +8,10 @@ namespace {
 
 __global__ void __launch_bounds__(1024) accept_kernel(const AcceptSpec a) {
     extern __shared__ unsigned long long keys[];  // blockDim.x entries
-    accept_request(a, blockIdx.x, keys);
+    __shared__ float H_s[1024];
+    __shared__ double warp_tot[32];
+    __shared__ int first_fail;
+    accept_request(a, blockIdx.x, blockDim.x, AcceptSmem{keys, H_s, warp_tot, &first_fail});
 }
 
 }  // namespace

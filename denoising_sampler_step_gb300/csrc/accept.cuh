@@ -39,14 +39,22 @@ __device__ __forceinline__ uint32_t order_bits(float x) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Request q by the whole CTA; blockDim.x is a power of two >= L_c (at most 1024) and `keys`
-// holds blockDim.x entries of shared memory.
-__device__ __forceinline__ void accept_request(const AcceptSpec &a, int q, unsigned long long *keys) {
-    __shared__ float H_s[1024];
-    __shared__ double warp_tot[32];
-    __shared__ int first_fail;
+// Shared memory of one acceptance: NT sort keys, L_c entropies, 32 warp totals, a count.
+struct AcceptSmem {
+    unsigned long long *keys;
+    float *H;
+    double *warp_tot;
+    int *first_fail;
+};
+
+// Request q by the whole CTA.  NT is a power of two >= L_c (at most 1024) and at most
+// blockDim.x; threads from NT on hold padding keys and only keep the CTA's barriers.
+__device__ __forceinline__ void accept_request(const AcceptSpec &a, int q, int NT, const AcceptSmem &sm) {
+    unsigned long long *keys = sm.keys;
+    float *H_s = sm.H;
+    double *warp_tot = sm.warp_tot;
+    int &first_fail = *sm.first_fail;
     const int tid = threadIdx.x;
-    const int NT = blockDim.x;
     const int64_t base = (int64_t)q * a.L_c;
 
     const bool el = tid < a.L_c && (!a.eligible || a.eligible[base + tid]);
@@ -63,9 +71,9 @@ __device__ __forceinline__ void accept_request(const AcceptSpec &a, int q, unsig
         for (int j = k >> 1; j > 0; j >>= 1) {
             unsigned long long other;
             if (j >= 32) {
-                keys[tid] = key;
+                if (tid < NT) keys[tid] = key;
                 __syncthreads();
-                other = keys[tid ^ j];
+                other = tid < NT ? keys[tid ^ j] : key;
                 __syncthreads();
             } else {
                 other = __shfl_xor_sync(0xffffffffu, key, j);

@@ -1271,7 +1271,7 @@ __device__ float4 redo_partial(const Params &p, const void *__restrict__ Wv, int
 // first n_acc CTAs run the acceptance of request blockIdx.x on the statistics instead (they
 // need blockDim.x >= the acceptance's threads and its keys in dynamic shared memory).
 template <int F>
-__global__ void splitk_reduce_kernel(const float4 *__restrict__ ws, const Params p, int d, float gamma,
+__global__ void __launch_bounds__(1024) splitk_reduce_kernel(const float4 *__restrict__ ws, const Params p, int d, float gamma,
                                      float *__restrict__ out, int64_t ldo, int vec_out,
                                      const float *__restrict__ scale, const void *__restrict__ Wv, int64_t ldw,
                                      const float *__restrict__ lse, const AcceptSpec acc, int n_acc) {
@@ -1282,7 +1282,10 @@ __global__ void splitk_reduce_kernel(const float4 *__restrict__ ws, const Params
     grid_dependency_wait();
     if ((int)blockIdx.x < n_acc) {
         extern __shared__ unsigned long long keys[];
-        accept_request(acc, (int)blockIdx.x, keys);
+        __shared__ float H_s[1024];
+        __shared__ double warp_tot[32];
+        __shared__ int first_fail;
+        accept_request(acc, (int)blockIdx.x, blockDim.x, AcceptSmem{keys, H_s, warp_tot, &first_fail});
         return;
     }
     const int64_t groups = ((int64_t)d + 3) / 4;  // column groups of 4
@@ -1374,21 +1377,34 @@ __global__ void __launch_bounds__(256)
     uint32_t redo_bits = 0;  // bit k: split lane + 32 k is recomputed by the reduce
     for (int s = lane, kk = 0; s < p.splits; s += 32, ++kk) {
         rowstate::RowState sp = rowstate::empty_row_state();
-        for (int t = 0; t < p.n_tiles; ++t) {
-            const float4 v = p.state[((int64_t)s * p.n_tiles + t) * p.R + row];
-            rowstate::merge(sp, rowstate::RowState{v.x, __float_as_int(v.y), v.z, v.w});
-            if (p.draw) {
-                const float2 dv = p.draws[((int64_t)s * p.n_tiles + t) * p.R + row];
-                const int gi = __float_as_int(dv.y);
-                if (dv.x > dbest || (dv.x == dbest && gi < dgrp)) {
-                    dbest = dv.x;
-                    dgrp = gi;
-                }
+        const float c = p.ref[(int64_t)s * p.R + row];
+        // eight tiles' summaries in flight at once (unconditional loads: past the last tile
+        // they repeat it), then merged in tile order
+        for (int t0 = 0; t0 < p.n_tiles; t0 += 8) {
+            float4 v[8];
+            float2 dv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int64_t at = ((int64_t)s * p.n_tiles + min(t0 + u, p.n_tiles - 1)) * p.R + row;
+                v[u] = p.state[at];
+                dv[u] = p.draw ? p.draws[at] : make_float2(0.f, 0.f);
             }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (t0 + u < p.n_tiles) {
+                    rowstate::merge(sp, rowstate::RowState{v[u].x, __float_as_int(v[u].y), v[u].z, v[u].w});
+                    if (p.draw) {
+                        const int gi = __float_as_int(dv[u].y);
+                        if (dv[u].x > dbest || (dv[u].x == dbest && gi < dgrp)) {
+                            dbest = dv[u].x;
+                            dgrp = gi;
+                        }
+                    }
+                }
         }
         // the split's probabilities against its reference: ln of their sum is
         // (m - c) + ln Z_split; list the pair for the redo pass if they could overflow
-        const float gap = sp.m - p.ref[(int64_t)s * p.R + row];
+        const float gap = sp.m - c;
         if (sp.m > -INFINITY && !(gap + log1pf(sp.rest) <= kRefSumLog && gap >= -kRefBelow))
             redo_bits |= 1u << kk;
         rowstate::merge(st, sp);

@@ -166,3 +166,37 @@ def test_two_pass_canvas256_full_size(B):
     rows = np.arange(wl.R)   # every row
     ref = soft_embed(x, ost["lse"], 0, wl.V, Wb, wl.gamma, rows=rows)
     assert rel_l2(out["E"].cpu().numpy()[rows], ref).max() <= E_TOL
+
+
+def test_single_pass_many_small_requests(B):
+    """600 rows as 300 requests of 2 positions: the reduce kernel's acceptance CTAs (one per
+    request) far outnumber its reduce CTAs' rows per request."""
+    wl = inputs.WORKLOADS["tiny"].with_(n_req=300, L_c=2, seed=11, budget=("uniform", 0.5, 8.0))
+    x, budgets, ost, _ = guarded(wl)
+    Wb = inputs.embedding_bf16(wl)
+    out = run_step(B, x, wl, w_dev(Wb), budgets)
+    check_stats(out, ost)
+    acc = entropy_accept(ost["H"], ost["kappa"], wl.n_req, wl.L_c, budgets)
+    for k in ("order", "mask", "n_accepted"):
+        assert np.array_equal(out[k].cpu().numpy(), acc[k]), k
+    ref = soft_embed(x, ost["lse"], 0, wl.V, Wb, wl.gamma, rows=np.arange(wl.R))
+    assert rel_l2(out["E"].cpu().numpy(), ref).max() <= E_TOL
+
+
+def test_single_pass_repeats_bit_for_bit_on_a_dirty_workspace(B):
+    """Steps on one workspace that starts filled with 0xff bytes, with a plain product on the
+    same workspace between them, give the same bits: nothing depends on its prior contents."""
+    wl = inputs.WORKLOADS["tiny"].with_(n_req=4, seed=5, budget=("uniform", 0.5, 6.0))
+    x, budgets, _, _ = guarded(wl)
+    Wb = inputs.embedding_bf16(wl)
+    xd, Wd, bd = dev(x), w_dev(Wb), dev(budgets)
+    ws = B.workspace(wl.R, wl.V, wl.d, xd.device)
+    ws.fill_(255)
+    first = B.dg_sampler_step(xd, wl.n_req, wl.L_c, Wd, wl.gamma, bd, ws=ws)
+    for _ in range(3):
+        B.dg_soft_embed(xd, first["lse"], 0, wl.V, Wd, 1.0, ws=ws)
+        again = B.dg_sampler_step(xd, wl.n_req, wl.L_c, Wd, wl.gamma, bd, ws=ws)
+        torch.cuda.synchronize()
+        for k in ("E", "lse", "H", "kappa", "argmax", "order", "mask", "n_accepted"):
+            assert torch.equal(first[k], again[k]), k
+    B.dg_get_device_status()
