@@ -27,7 +27,7 @@
 //     and writes E (bitwise reproducible).
 //   A column tail of 256 or fewer (d = 2816 = 5 x 512 + 256) is a half-width tile; it gets
 //   as many splits as the full tiles, since a block's time is set by the stage round trip.
-//   W loads mark their lines evict-first, which keeps the logits (read by every column
+//   bf16 W loads mark their lines evict-first, which keeps the logits (read by every column
 //   tile of a row block) in L2.
 //   Every barrier wait is bounded (about a second); a wait that gives up records
 //   DG_ERR_TIMEOUT, drains what is in flight and leaves the kernel.
@@ -453,7 +453,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             int issued[WST];
             for (int s = 0; s < WST; ++s) issued[s] = 0;
-            const uint64_t w_policy = l2_policy_evict_first();
+            // bf16: every W byte leaves L2 once (evict first); 8-bit table: both row-block
+            // clusters of a column pair read each W tile, close together (ordinary priority)
+            const uint64_t w_policy = F == kE4m3 ? l2_policy_evict_normal() : l2_policy_evict_first();
             // bf16: a 3-D map fetches a CTA's 2 atoms of a half in one load
             const bool w3d = p.w3d;
             const uint32_t lead_a = map_to_cta(smem_u32(&full_a[0]), rank & ~1u);  // the pair's even CTA's full_a[0]
