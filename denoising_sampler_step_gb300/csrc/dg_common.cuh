@@ -381,28 +381,31 @@ __host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N, int a_mn_ma
            | ((uint32_t)sfa_id << 29);     // A scale-factor byte
 }
 
-// D[tmem] (+)= (A * 2^sfa) (B * 2^sfb), block-scaled E4M3 x E4M3, one CTA.  The scale factors
-// live in TMEM (M = 128: row m's word at lane m, column sfa + m / 32).
-__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+// D (+)= (A * 2^sfa) (B * 2^sfb) over the CTA pair, block-scaled E4M3 x E4M3: M = 256 rows (128
+// in each CTA's shared memory and TMEM), B split by N between the two CTAs (N/2 columns each,
+// at the same address); each CTA's TMEM holds the scale factors of its own rows (row m's word
+// at lane m, column sfa + m / 32) and of B at the same columns.  Issued by the even CTA.
+__device__ __forceinline__ void umma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
 }
 
 // Copies 32 rows x 16 bytes of shared memory (the matrix described by sdesc) into four TMEM
-// columns of every 32-lane quarter (the same data in each quarter).  Ordered before the
-// tcgen05.mma the same thread issues after it.
-__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+// columns of every 32-lane quarter (the same data in each quarter), in both CTAs of the pair,
+// each from its own shared memory at the same address.  Issued by the even CTA; ordered
+// before the tcgen05.mma the same thread issues after it.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4_pair(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
-// As tmem_cp_32x128b_warpx4 for 128 rows x 16 bytes: row m's four words go to lane m.
-__device__ __forceinline__ void tmem_cp_128x128b(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+// As tmem_cp_32x128b_warpx4_pair for 128 rows x 16 bytes: row m's four words go to lane m.
+__device__ __forceinline__ void tmem_cp_128x128b_pair(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from this CTA's

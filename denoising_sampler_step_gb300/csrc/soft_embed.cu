@@ -33,13 +33,13 @@
 //   DG_ERR_TIMEOUT, drains what is in flight and leaves the kernel.
 //
 // The same kernel, instantiated for an 8-bit table (E4M3 codes with one fp32 scale per
-// vocabulary row), runs block-scaled E4M3 MMAs (kind::mxf8f6f4): the producers take each
-// block's exponentials against its own maximum, fold in the (normalised, staged) row scales
-// and split each value into two E4M3 parts under a power-of-two scale per (row, block) that
-// the MMA applies from TMEM; a cluster holds one row block and two 480-column tiles, and each
-// CTA computes every other block's A operand and copies it to its partner.  Each ring slot
-// holds two blocks, one from each CTA, so the MMA thread's wait, scale copy and commit serve
-// eight MMAs.
+// vocabulary row), runs block-scaled E4M3 MMAs (kind::mxf8f6f4) on the same four-CTA layout:
+// the producers take each block's exponentials against its own maximum, fold in the
+// (normalised, staged) row scales and split each value into two E4M3 parts under a
+// power-of-two scale per (row, block); each CTA keeps the scales of its rows with its A tile
+// (and copies them with it), and per block the pair's MMA thread copies them into both CTAs'
+// TMEM ahead of four M = 256 MMAs (two column halves, high and low parts).  Column tiles are
+// 480 wide (256 + 224), so that the scale factors fit beside the accumulator in TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -74,10 +74,7 @@ constexpr int ROWS_PER_LANE = 128 / (32 * GROUP_WARPS);
 // shared-memory work of the other warps on its scheduler (warp % 4), so: warp 4 issues the
 // MMAs and warp 8 the logits TMA (scheduler 0, no producers); warp 11 issues the W TMA
 // (scheduler 3, two producers); warps 1-3, 5-7, 9 and 10 produce A.  Every warp takes part
-// in the epilogue.  The 8-bit table's producers have about three times the work per entry
-// and set the pace, so there each producer group spans all four schedulers: warps 4-7 and
-// 8-11 produce A, warp 0 issues the MMAs, warp 1 the logits TMA, warp 2 the W TMA and warp 3
-// stages the row scales.
+// in the epilogue.  The 8-bit table has the same roles; its warp 0 stages the row scales.
 constexpr int THREADS = 384;
 constexpr int TMEM_COLS = 512;
 constexpr uint16_t kPairMask = 0x3;
@@ -92,14 +89,11 @@ constexpr uint16_t kPairMask = 0x3;
 //   copy it to the CTA with the same rows in the other pair (r ^ 2); a pair's odd CTA tells
 //   its even CTA that its rows are in place with a 16-byte bulk copy onto the even CTA's
 //   barrier (directly when it formed them, relayed when they were copied in).
-// 8-bit table: two CTAs, one row block and two column tiles; each CTA issues M = 128 MMAs and
-//   loads its own W tile; the A operand is shared the same way (each CTA computes every other
-//   block's and copies it).
-constexpr int kCtasPerUnit = 2;  // the 8-bit table's cluster
-constexpr int kQuadCtas = 4;     // the bf16 table's cluster
-template <int F>
-__host__ __device__ constexpr int cluster_ctas() { return F == kTableBf16 ? kQuadCtas : kCtasPerUnit; }
-// ring depth of the bf16 pair (W and A slots, one index): half-size W slots leave room for six
+// 8-bit table: the same four CTAs, with 480-column tiles; a CTA's A tile carries the (row,
+//   block) scale factors, which travel with it.
+constexpr int kQuadCtas = 4;  // the product's cluster
+// ring depth of the pair (W and A slots, one index): half-size W slots leave room for six
+// (and the 8-bit table's TMEM holds the scale factors of six slots)
 constexpr int kPairStages = 6;
 
 constexpr int L_BYTES = BM * BK * 4;      // logits tile, rows of 128 B (128-byte swizzle)
@@ -121,7 +115,6 @@ struct Fmt<kBf16> {
     static constexpr int BN = 512;                // output columns per cluster tile: halves of 256 + 256
     static constexpr int WST = kPairStages;       // W ring depth (the A ring's: one index for both)
     static constexpr int AST = kPairStages;       // A ring depth
-    static constexpr int BPS = 1;                 // vocabulary blocks per ring slot
     static constexpr int W_SLOT = BK * BN;        // this CTA's 128 of every 256 columns of a block's W tile
     static constexpr int SF_BYTES = 0;
 };
@@ -131,26 +124,23 @@ struct Fmt<kE4m3> {
     // 480: halves of 256 + 224
     static constexpr int BN = 480;
     static constexpr int N1 = 224;                // N of the second half
-    // three slots of two blocks: each producer group (two per CTA, one block per slot each)
-    // stores its next block while both CTAs' MMAs of its previous one are still in flight
-    static constexpr int WST = 3;
-    static constexpr int AST = 3;
-    // a ring slot holds two vocabulary blocks, one from each CTA of the cluster: the MMA
-    // thread's barrier wait, scale copy and commit then serve eight MMAs instead of four
-    static constexpr int BPS = 2;
-    static constexpr int W_SLOT = 4 * BPS * W_BOX_BYTES;  // four 128-column atoms of 64 rows (the last atom's final 32 columns unused)
-    // per-stage A scale matrices (128 rows x 16 bytes), the B scale chunk, then the staged
+    static constexpr int WST = kPairStages;
+    static constexpr int AST = kPairStages;
+    // this CTA's N/2 columns of each half: one 128-column atom of 32 rows per half (of the
+    // second half's atom 112 columns are used)
+    static constexpr int W_SLOT = 2 * W_BOX_BYTES;
+    // per-slot A scale matrices (128 rows x 16 bytes), the B scale chunk, then the staged
     // row scales (one slot per logits stage: 32 normalised scales and their exponent)
-    static constexpr int SF_STAGE = 2048 * BPS;  // a slot's blocks' A scale matrices, one after the other
+    static constexpr int SF_STAGE = 2048;
     static constexpr int SF_BYTES = AST * SF_STAGE + 512 + LSTAGES * 160;
 };
 constexpr int S_SLOT = 160;
 // TMEM columns of the scale factors (8-bit table): four per A slot (lane m's word in column
-// m / 32), then eight for the B scales (two 128-column groups of N)
+// m / 32), then eight for the B scales
 constexpr uint32_t kSfaCol = 480, kSfbCol = 504;
 template <int F>
 constexpr int smem_bytes() {
-    return L_RING + Fmt<F>::WST * Fmt<F>::W_SLOT + Fmt<F>::AST * Fmt<F>::BPS * A_BYTES + Fmt<F>::SF_BYTES + 1024 /*align*/ +
+    return L_RING + Fmt<F>::WST * Fmt<F>::W_SLOT + Fmt<F>::AST * A_BYTES + Fmt<F>::SF_BYTES + 1024 /*align*/ +
            512 /*barriers*/;
 }
 
@@ -158,7 +148,7 @@ static_assert(L_BYTES % 1024 == 0 && Fmt<kBf16>::W_SLOT % 1024 == 0 && Fmt<kE4m3
                   A_BYTES % 1024 == 0,
               "1 KiB alignment");
 static_assert(smem_bytes<kBf16>() <= 232448 && smem_bytes<kE4m3>() <= 232448, "shared memory per CTA");
-static_assert(kSfaCol + 4 * Fmt<kE4m3>::AST * Fmt<kE4m3>::BPS <= kSfbCol && kSfbCol + 8 <= TMEM_COLS,
+static_assert(kSfaCol + 4 * Fmt<kE4m3>::AST <= kSfbCol && kSfbCol + 8 <= TMEM_COLS,
               "scale-factor columns");
 // each producer group keeps to every other slot of the logits and A rings
 // a group waits only for phases its own blocks need, and no slot can run two phases ahead
@@ -183,7 +173,6 @@ struct Params {
     int w3d;             // 1: the W map is 3-D (atom columns x rows x atoms), one load per CTA and block
     // 8-bit table: the fp32 scale of vocabulary entry v is w_scale[v - vocab_start]
     const float *w_scale;
-    int pair_blocks;     // 8-bit table: splits hold whole pairs of blocks (two per ring slot)
     // single pass (no lse yet): each split's probabilities are taken against a reference
     // c per row, exp(l - c), and the column-tile-0 clusters also fold the row statistics
     int fused;
@@ -205,18 +194,10 @@ struct Params {
 // of exp(l - c) over the split passes e^kRefSumLog (about 4e35, so that with |W| <= 100 the
 // fp32 partial stays below 4e37), or when the split's maximum lies more than kRefBelow nats
 // below c (everything would underflow).
-// Vocabulary blocks [kb0, kb1) of split j of S.  Pair mode (the 8-bit table's two blocks per
-// ring slot): the bounds are even, and the last split may end one block past the slice (that
-// block reads zeros).
+// Vocabulary blocks [kb0, kb1) of split j of S.
 __host__ __device__ inline void split_range(const Params &p, int j, int S, int64_t *kb0, int64_t *kb1) {
-    if (p.pair_blocks) {
-        const int64_t np = (p.nkb + 1) / 2;
-        *kb0 = 2 * ((int64_t)j * np / S);
-        *kb1 = 2 * ((int64_t)(j + 1) * np / S);
-    } else {
-        *kb0 = (int64_t)j * p.nkb / S;
-        *kb1 = (int64_t)(j + 1) * p.nkb / S;
-    }
+    *kb0 = (int64_t)j * p.nkb / S;
+    *kb1 = (int64_t)(j + 1) * p.nkb / S;
 }
 
 constexpr float kRefSumLog = 82.0f;
@@ -289,17 +270,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int WST = Fmt<F>::WST;
     constexpr int AST = Fmt<F>::AST;
     constexpr int W_RING = WST * W_SLOT;
-    constexpr int BPS = Fmt<F>::BPS;
-    constexpr int A_SLOT = BPS * A_BYTES;
+    constexpr int A_SLOT = A_BYTES;
     constexpr int A_RING = AST * A_SLOT;
-    static_assert(F == kBf16 || (BPS == 2 && ROWS_PER_LANE == 1),
-                  "8-bit table: a slot holds one block of each CTA; a warp copies 32 whole rows");
+    static_assert(ROWS_PER_LANE == 1, "a warp copies 32 whole rows");
     static_assert(AST >= PGROUPS, "an A slot per producer group at least");
     // a block's W bytes complete on its A slot's barrier (one index for both rings), so the
     // MMA thread waits on one barrier per block
     static_assert(WST == AST, "one ring index");
-    // bf16 table: the tcgen05 CTA pair (M = 256 over both CTAs' rows)
-    constexpr bool kPairMma = F == kBf16;
+    // the scale rows that travel with an 8-bit A tile
+    constexpr uint32_t kSfRows = F == kE4m3 ? (uint32_t)Fmt<kE4m3>::SF_STAGE : 0u;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *l_ring = smem;
@@ -330,38 +309,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
 
-    // work of this cluster: (column tile(s), row block(s), split)
-    const int pair = blockIdx.x / cluster_ctas<F>();
+    // work of this cluster: (column pair cp, row pair mp, split j); n_tiles is even (a last
+    // odd tile's partner lies past d and reads zeros); tiles from n_full on are half width
+    const int pair = blockIdx.x / kQuadCtas;
     const int m_pairs = p.m_tiles / 2;
-    int nt, mp, j, S, halves, mt;
-    // 8-bit table: a cluster is one row block and two adjacent column tiles (CTA c takes
-    // tile 2 ntp + c; n_tiles is even, a last odd tile's partner lies past d and reads zeros)
     const int ntp_count = p.n_tiles / 2;
-    int ntp = 0;
-    if (F == kE4m3) {
-        // the row blocks that read the same W tiles take adjacent clusters
-        mt = pair % p.m_tiles;
-        ntp = (pair / p.m_tiles) % ntp_count;
-        j = pair / (ntp_count * p.m_tiles);
-        S = p.splits;
-        nt = 2 * ntp + (int)rank;
-        halves = nt < p.n_full ? 2 : 1;
-        mp = 0;
-    } else {
-        // bf16: cluster (column pair cp, row pair mp, split j); n_tiles is even (a last odd
-        // tile's partner lies past d and reads zeros); tiles from n_full on are half width
-        ntp = pair % ntp_count;
-        mp = (pair / ntp_count) % m_pairs;
-        j = pair / (ntp_count * m_pairs);
-        S = p.splits;
-        nt = 2 * ntp + (int)(rank >> 1);
-        halves = nt < p.n_full ? 2 : 1;
-        mt = 2 * mp + (int)(rank & 1);
-    }
+    const int ntp = pair % ntp_count;
+    const int mp = (pair / ntp_count) % m_pairs;
+    const int j = pair / (ntp_count * m_pairs);
+    const int S = p.splits;
+    const int nt = 2 * ntp + (int)(rank >> 1);
+    const int halves = nt < p.n_full ? 2 : 1;
+    const int mt = 2 * mp + (int)(rank & 1);
     // the column parity of this CTA in its cluster: it produces (loads the logits of, stages
     // the scales of, computes the A operand of) the blocks i with i % 2 == cpar and copies each
     // A operand to the CTA with the same rows in the other column tile
-    const int cpar = F == kE4m3 ? (int)rank : (int)(rank >> 1);
+    const int cpar = (int)(rank >> 1);
     const int i0 = cpar, di = 2;
     int64_t kb0, kb1;
     split_range(p, j, S, &kb0, &kb1);
@@ -376,17 +339,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(smem_u32(&full_s[s]), 1);
         }
         for (int s = 0; s < AST; ++s) {
-            // full_a, 8-bit table: this CTA's producer group, the partner's block (the MMA
-            // thread's arrival, with the copied bytes) and the W TMA's arrival (with the W bytes).
-            // bf16, a pair's even CTA: a slot of its own parity, the producer group's warps and
+            // full_a, a pair's even CTA: a slot of its own parity, the producer group's warps and
             // the W TMA's arrival (with both CTAs' W bytes and the odd CTA's four signals); a slot
             // of the other parity, the W TMA's arrival alone (with the W bytes, the copied A tile
-            // and the odd CTA's relayed signal).  bf16, odd CTA: the relay's arrival (with the
-            // copied A tile; slots of the other parity only).
-            // empty: the commits of every CTA pair (8-bit table: both CTAs) that reads the slot or
-            // copies into it
-            int fa = GROUP_WARPS + 2;
-            if (F == kBf16) fa = (rank & 1) == 0 && (s & 1) == cpar ? GROUP_WARPS + 1 : 1;
+            // (8-bit table: and its scale rows) and the odd CTA's relayed signal).  Odd CTA: the
+            // relay's arrival (with the copied A tile; slots of the other parity only).
+            // empty: the commits of both CTA pairs (the pair that reads the slot and the one that
+            // copies into it)
+            const int fa = (rank & 1) == 0 && (s & 1) == cpar ? GROUP_WARPS + 1 : 1;
             mbar_init(smem_u32(&full_a[s]), fa);
             mbar_init(smem_u32(&empty[s]), 2);
         }
@@ -402,12 +362,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_proxy_async_smem();
     }
     __syncwarp();
-    if (warp == 0) {
-        if constexpr (kPairMma)
-            tmem_alloc_pair<TMEM_COLS>(smem_u32(tmem_slot));  // a joint allocation in both CTAs
-        else
-            tmem_alloc<TMEM_COLS>(smem_u32(tmem_slot));
-    }
+    if (warp == 0) tmem_alloc_pair<TMEM_COLS>(smem_u32(tmem_slot));  // a joint allocation in both CTAs
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -439,17 +394,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         my_gidx[q] = 0x7fffffff;
     }
 
-    constexpr int kWarpW = F == kE4m3 ? 2 : 11, kWarpL = F == kE4m3 ? 1 : 8, kWarpMma = F == kE4m3 ? 0 : 4;
-    constexpr int kWarpStage = 3;
-    const bool producer = F == kE4m3 ? warp >= 4 : ((warp & 3) != 0 && warp < 11);
+    constexpr int kWarpW = 11, kWarpL = 8, kWarpMma = 4, kWarpStage = 0;
+    const bool producer = (warp & 3) != 0 && warp < 11;
     if (warp == kWarpW) {
         // ------------------------------------------------------------ W TMA
-        // bf16: each CTA loads its 128 columns of each 256-column half (atoms 4h + 2 (rank & 1)
-        // and + 1), the bytes counted on its pair's even CTA's A slot barrier, which that CTA
-        // arms for both CTAs' bytes and the odd CTA's A-ready signals (or, for a block the other
-        // pair forms, the copied A tile and the relayed signal); 8-bit table: each CTA loads
-        // its own tile's 128-column atoms of the slot's two blocks, counted on its own A slot
-        // barrier.  W lines are marked evict-first
+        // each CTA loads its N/2 columns of each half (bf16: atoms 4h + 2 (rank & 1) and + 1 of
+        // 64 columns; 8-bit table: one 128-column atom at 256 h + (rank & 1) N_h / 2), the bytes
+        // counted on its pair's even CTA's A slot barrier, which that CTA arms for both CTAs'
+        // bytes and the odd CTA's A-ready signals (or, for a block the other pair forms, the
+        // copied A tile, its scale rows and the relayed signal)
         if (lane == 0) {
             int issued[WST];
             for (int s = 0; s < WST; ++s) issued[s] = 0;
@@ -459,7 +412,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // bf16: a 3-D map fetches a CTA's 2 atoms of a half in one load
             const bool w3d = p.w3d;
             const uint32_t lead_a = map_to_cta(smem_u32(&full_a[0]), rank & ~1u);  // the pair's even CTA's full_a[0]
-            for (int i = 0; i < nkb / BPS; ++i) {  // ring slots (BPS blocks each)
+            for (int i = 0; i < nkb; ++i) {  // one block per ring slot
                 const int s = i % WST;
                 const uint32_t u = (uint32_t)(i / WST);
                 if (i == WST) {  // the first round of W loads is out
@@ -470,23 +423,24 @@ __global__ void __launch_bounds__(THREADS, 1)
                     ok = false;
                     break;
                 }
-                const int64_t k = p.k_begin + (kb0 + (int64_t)BPS * i) * BK;
+                const int64_t k = p.k_begin + (kb0 + (int64_t)i) * BK;
                 const uint32_t bw = smem_u32(&full_a[s]);
                 const int wy = (int)(k - p.vocab_start);
+                // both CTAs' W bytes of the slot, and the odd CTA's four A-ready signals (a block
+                // this pair forms) or the A tile (and scale rows) copied in and the odd CTA's
+                // relayed signal
+                if ((rank & 1) == 0)
+                    mbar_arrive_expect_tx(bw, (uint32_t)halves * W_SLOT +
+                                                  ((i & 1) == cpar ? 16u * GROUP_WARPS
+                                                                   : (uint32_t)A_BYTES + kSfRows + 16u));
+                const uint32_t bl = lead_a + 8u * (uint32_t)s;
                 if constexpr (F == kE4m3) {
-                    // this CTA's own tile for the slot's two blocks: four 128-column atoms of 64
-                    // rows (two for a half-width tile)
-                    mbar_arrive_expect_tx(bw, (uint32_t)halves * 2 * BPS * W_BOX_BYTES);
-                    for (int a = 0; a < 2 * halves; ++a)
-                        tma_load_2d_hint(smem_u32(w_ring + s * W_SLOT + a * BPS * W_BOX_BYTES), &tm_w, bw,
-                                         col0 + 128 * a, wy, w_policy);
+                    for (int h = 0; h < halves; ++h) {
+                        const int xh = col0 + 256 * h + (int)(rank & 1) * (h == 0 ? 128 : Fmt<kE4m3>::N1 / 2);
+                        tma_load_2d_pair_hint(smem_u32(w_ring + s * W_SLOT + h * W_BOX_BYTES), &tm_w, bl, xh, wy,
+                                              w_policy);
+                    }
                 } else {
-                    // both CTAs' W bytes of the slot, and the odd CTA's four A-ready signals (a block
-                    // this pair forms) or the A tile copied in and the odd CTA's relayed signal
-                    if ((rank & 1) == 0)
-                        mbar_arrive_expect_tx(bw, (uint32_t)halves * W_SLOT +
-                                                      ((i & 1) == cpar ? 16u * GROUP_WARPS : (uint32_t)A_BYTES + 16u));
-                    const uint32_t bl = lead_a + 8u * (uint32_t)s;
                     for (int h = 0; h < halves; ++h) {
                         const uint32_t dst = smem_u32(w_ring + s * W_SLOT + h * 2 * W_BOX_BYTES);
                         const int atom = col0 / 64 + 4 * h + 2 * (int)(rank & 1);  // this CTA's half of the pair
@@ -500,14 +454,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 issued[s] = (int)u + 1;
             }
-            if (nkb / BPS <= WST) {
+            if (nkb <= WST) {
                 grid_dependency_wait();
                 grid_launch_dependents();
             }
             // loads in flight finish before the CTA may leave (bf16 pair: the even CTA's barriers
             // count both CTAs' loads, and the odd CTA leaves only after the final cluster
             // barrier, which the even CTA reaches after this drain)
-            if (!ok && (!kPairMma || (rank & 1) == 0))
+            if (!ok && (rank & 1) == 0)
                 for (int s = 0; s < WST; ++s)
                     if (issued[s] > 0) drain_wait(smem_u32(&full_a[s]), (issued[s] - 1) & 1);
         }
@@ -544,15 +498,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
-        // (bf16: a pair's even CTA's thread issues for both CTAs; the odd CTA's relays)
-        if (lane == 0 && kPairMma && (rank & 1) != 0) {
-            // relay: the A tiles of the blocks the other pair forms arrive here by copy; once one
-            // has landed, a 16-byte copy onto the even CTA's barrier tells its MMA thread
+        // (a pair's even CTA's thread issues for both CTAs; the odd CTA's relays)
+        if (lane == 0 && (rank & 1) != 0) {
+            // relay: the A tiles (8-bit table: with their scale rows) of the blocks the other pair
+            // forms arrive here by copy; once one has landed, a 16-byte copy onto the even CTA's
+            // barrier tells its MMA thread
             const uint32_t lead = rank & ~1u;
             for (int i = 1 - cpar; i < nkb; i += 2) {
                 const int s = i % AST;
                 const uint32_t u = (uint32_t)(i / AST);
-                mbar_arrive_expect_tx(smem_u32(&full_a[s]), (uint32_t)A_BYTES);
+                mbar_arrive_expect_tx(smem_u32(&full_a[s]), (uint32_t)A_BYTES + kSfRows);
                 if (!mbar_wait(smem_u32(&full_a[s]), u & 1, abort_flag)) {
                     ok = false;
                     break;
@@ -560,50 +515,38 @@ __global__ void __launch_bounds__(THREADS, 1)
                 bulk_copy_to_cluster(map_to_cta(smem_u32(sig_area + 16 * (PRODUCER_WARPS + 1)), lead),
                                      smem_u32(sig_area), 16u, map_to_cta(smem_u32(&full_a[s]), lead));
             }
-        } else if (lane == 0 && (!kPairMma || (rank & 1) == 0)) {
+        } else if (lane == 0) {
             grid_dependency_wait();  // nothing to issue before the producers' first tile anyway
             grid_launch_dependents();
             constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, 256, /*A K-major*/ 0, /*B N-major*/ 1);
-            // operand descriptors of slot 0; a slot, a K = 16 step or a 256-column half is a
-            // constant added to the start-address field (addresses stay below 2^18 bytes)
-            // A: K-major, 64-byte rows, 8-row groups 512 B apart; +32 B per K = 16 step
+            // operand descriptors of slot 0; a slot, a K = 16 step or a half is a constant added
+            // to the start-address field (addresses stay below 2^18 bytes)
+            // A: K-major, 64-byte rows, 8-row groups 512 B apart; +32 B per K = 16 step (bf16) or
+            // from the high to the low E4M3 parts (8-bit table)
             const uint64_t a_desc0 = smem_desc(smem_u32(a_ring), 16, 512, 4);
-            // B: N-major, 64-column atoms 4 KiB apart (LBO), 8-row groups 1 KiB apart (SBO);
-            // +2 KiB per K = 16 step
-            const uint64_t b_desc0 = smem_desc(smem_u32(w_ring), BPS * W_BOX_BYTES, 1024, 2);
-            // a CTA's part of one 256-column half: 2 atoms
+            // B: N-major, atoms of 128-byte rows 4 KiB apart (LBO), 8-row groups 1 KiB apart
+            // (SBO); bf16: +2 KiB per K = 16 step, a half is 2 atoms; 8-bit table: one K = 32 step
+            // per block, a half is 1 atom
+            const uint64_t b_desc0 = smem_desc(smem_u32(w_ring), W_BOX_BYTES, 1024, 2);
             constexpr uint64_t kA_K16 = 32 >> 4, kB_K16 = 2048 >> 4, kB_HALF = (W_SLOT / 2) >> 4;
             // 8-bit table: the B scale factors (all 1) go into their columns once; per block the
-            // stage's A scale chunk goes into its four columns ahead of the block's MMAs (the copy
-            // and the MMAs run in issue order; the commit covers both)
+            // slot's A scale chunk goes into its four columns ahead of the block's MMAs (the copy
+            // and the MMAs run in issue order; the commit covers both); each copy fills both CTAs
+            // of the pair, each from its own shared memory
             if constexpr (F == kE4m3) {
                 const uint64_t sfb_desc = smem_desc(smem_u32(sfb_chunk), 16, 128, 0);
-                for (int q = 0; q < 8; q += 4) tmem_cp_32x128b_warpx4(tmem_base + kSfbCol + q, sfb_desc);
+                for (int q = 0; q < 8; q += 4) tmem_cp_32x128b_warpx4_pair(tmem_base + kSfbCol + q, sfb_desc);
             }
             bool issued_any = false;
-            // a block's two tiles are tested together (their latencies overlap), and right
-            // after the previous block's MMAs are issued, ahead of its commit; the bounded
-            // waits run only when a tile is not there yet
-            // bf16 pair: the odd CTA's loads and signals complete from the other CTA, so the
-            // tests acquire at cluster scope
-            auto test = [&](uint32_t bar, uint32_t ph) {
-                return kPairMma ? mbar_try_wait_cluster(bar, ph) : mbar_try_wait(bar, ph);
-            };
-            auto wait = [&](uint32_t bar, uint32_t ph) {
-                return kPairMma ? mbar_wait_cluster(bar, ph, abort_flag) : mbar_wait(bar, ph, abort_flag);
-            };
-            // 8-bit table: a slot the partner fills completes on its copies' bytes and one
-            // arrival of this thread (the bytes may land first), made before the slot is tested
-            auto arm = [&](int i) {  // every slot holds one block of the partner's
-                if (F == kE4m3 && i < nkb / BPS)
-                    mbar_arrive_expect_tx(smem_u32(&full_a[i % AST]), GROUP_WARPS * (2048u + 512u));
-            };
-            arm(0);
-            bool a_in = nkb > 0 && test(smem_u32(&full_a[0]), 0);
-            for (int i = 0; i < nkb / BPS; ++i) {  // ring slots (BPS blocks each)
+            // a block's tiles are tested right after the previous block's MMAs are issued, ahead
+            // of its commit; the bounded waits run only when a tile is not there yet.  The odd
+            // CTA's loads and signals complete from the other CTA, so the tests acquire at
+            // cluster scope
+            bool a_in = nkb > 0 && mbar_try_wait_cluster(smem_u32(&full_a[0]), 0);
+            for (int i = 0; i < nkb; ++i) {
                 const int s = i % AST;
                 const uint32_t ph = (uint32_t)(i / AST) & 1;
-                if (!a_in && !wait(smem_u32(&full_a[s]), ph)) {
+                if (!a_in && !mbar_wait_cluster(smem_u32(&full_a[s]), ph, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -613,51 +556,34 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t acc = i > 0 ? 1u : 0u;
                 if constexpr (F == kE4m3) {
                     // high parts, then low parts (the word's four bytes are the same scale)
-                    constexpr uint32_t id_h0 = idesc_mxf8_e4m3(BM, 256, 0, 1, 0, 0);
-                    constexpr uint32_t id_h1 = idesc_mxf8_e4m3(BM, Fmt<F>::N1, 0, 1, 0, 0);
-                    constexpr uint32_t id_l0 = idesc_mxf8_e4m3(BM, 256, 0, 1, 1, 0);
-                    constexpr uint32_t id_l1 = idesc_mxf8_e4m3(BM, Fmt<F>::N1, 0, 1, 1, 0);
-                    constexpr uint64_t kB_HALF8 = (2 * BPS * W_BOX_BYTES) >> 4;
+                    constexpr uint32_t id_h0 = idesc_mxf8_e4m3(2 * BM, 256, 0, 1, 0, 0);
+                    constexpr uint32_t id_h1 = idesc_mxf8_e4m3(2 * BM, Fmt<F>::N1, 0, 1, 0, 0);
+                    constexpr uint32_t id_l0 = idesc_mxf8_e4m3(2 * BM, 256, 0, 1, 1, 0);
+                    constexpr uint32_t id_l1 = idesc_mxf8_e4m3(2 * BM, Fmt<F>::N1, 0, 1, 1, 0);
+                    constexpr uint64_t kB_ATOM = W_BOX_BYTES >> 4;
                     const uint32_t sfb = tmem_base + kSfbCol;
-                    // the slot's TMEM scale slots: free, as the A slot is, once both CTAs' MMAs of
-                    // the blocks before in this slot are done (its producers waited for that)
-#pragma unroll
-                    for (int b = 0; b < BPS; ++b) {
-                        const uint32_t sfa = tmem_base + kSfaCol + 4 * (uint32_t)(BPS * s + b);
-                        tmem_cp_128x128b(sfa, smem_desc(smem_u32(sf_ring + s * Fmt<kE4m3>::SF_STAGE + b * 2048), 16,
-                                                        128, 0));
-                        // block b: its A tile, and its 32 rows of each W atom
-                        const uint64_t adb = ad + (uint64_t)((b * A_BYTES) >> 4);
-                        const uint64_t bdb = bd + (uint64_t)((b * BK * 128) >> 4);
-                        const uint32_t accb = (i > 0 || b > 0) ? 1u : 0u;
-                        umma_mxf8(tmem_base, adb, bdb, id_h0, sfa, sfb, accb);
-                        if (halves == 2) umma_mxf8(tmem_base + 256, adb, bdb + kB_HALF8, id_h1, sfa, sfb, accb);
-                        umma_mxf8(tmem_base, adb + kA_K16, bdb, id_l0, sfa, sfb, 1u);
-                        if (halves == 2) umma_mxf8(tmem_base + 256, adb + kA_K16, bdb + kB_HALF8, id_l1, sfa, sfb, 1u);
-                    }
+                    // the slot's TMEM scale columns: free, as the A slot is, once the MMAs of the
+                    // slot's previous block are done (its producers waited for that)
+                    const uint32_t sfa = tmem_base + kSfaCol + 4 * (uint32_t)s;
+                    tmem_cp_128x128b_pair(sfa, smem_desc(smem_u32(sf_ring + s * Fmt<kE4m3>::SF_STAGE), 16, 128, 0));
+                    umma_mxf8_pair(tmem_base, ad, bd, id_h0, sfa, sfb, acc);
+                    if (halves == 2) umma_mxf8_pair(tmem_base + 256, ad, bd + kB_ATOM, id_h1, sfa, sfb, acc);
+                    umma_mxf8_pair(tmem_base, ad + kA_K16, bd, id_l0, sfa, sfb, 1u);
+                    if (halves == 2) umma_mxf8_pair(tmem_base + 256, ad + kA_K16, bd + kB_ATOM, id_l1, sfa, sfb, 1u);
                 } else {
                     umma_bf16_pair(tmem_base, ad, bd, idesc, acc);
                     if (halves == 2) umma_bf16_pair(tmem_base + 256, ad, bd + kB_HALF, idesc, acc);
                     umma_bf16_pair(tmem_base, ad + kA_K16, bd + kB_K16, idesc, 1u);
                     if (halves == 2) umma_bf16_pair(tmem_base + 256, ad + kA_K16, bd + kB_HALF + kB_K16, idesc, 1u);
                 }
-                if (i + 1 < nkb / BPS) {
-                    arm(i + 1);
-                    a_in = test(smem_u32(&full_a[(i + 1) % AST]), (uint32_t)((i + 1) / AST) & 1);
-                }
-                // one commit releases the W and A slots once the MMAs have read them: 8-bit table,
-                // in both CTAs (the A slot is read in both); bf16, in all four CTAs (the pair's MMAs
-                // read both its CTAs' slots, and the other pair's CTAs copy A tiles into them)
-                if constexpr (F == kE4m3)
-                    umma_commit_multicast(smem_u32(&empty[s]), kPairMask);
-                else
-                    umma_commit_pair(smem_u32(&empty[s]), 0xF);
+                if (i + 1 < nkb) a_in = mbar_try_wait_cluster(smem_u32(&full_a[(i + 1) % AST]), (uint32_t)((i + 1) / AST) & 1);
+                // one commit releases the W and A slots, in all four CTAs, once the MMAs have read
+                // them (the pair's MMAs read both its CTAs' slots, and the other pair's CTAs copy
+                // A tiles into them)
+                umma_commit_pair(smem_u32(&empty[s]), 0xF);
                 issued_any = true;
             }
-            if constexpr (kPairMma)
-                umma_commit_pair(smem_u32(acc_full), (uint16_t)(kPairMask << (rank & 2u)));  // this pair
-            else
-                umma_commit(smem_u32(acc_full));
+            umma_commit_pair(smem_u32(acc_full), (uint16_t)(kPairMask << (rank & 2u)));  // this pair
             if (*abort_flag && issued_any) drain_wait(smem_u32(acc_full), 0);
         }
     } else if (F == kE4m3 && warp == kWarpStage) {
@@ -712,8 +638,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // PGROUPS groups take the blocks in turn, so a warp has PGROUPS block times for the
         // dependent chain of one block (barrier waits, stores, proxy fence, arrival); a
         // warp converts ROWS_PER_LANE * 32 rows x all 32 entries of its group's block
-        // producer 0..7 (warps 1-3, 5-7, 9, 10; 8-bit table: warps 4-11)
-        const int pw = F == kE4m3 ? warp - 4 : 3 * (warp >> 2) + (warp & 3) - 1;
+        // producer 0..7 (warps 1-3, 5-7, 9, 10)
+        const int pw = 3 * (warp >> 2) + (warp & 3) - 1;
         const int grp = pw / GROUP_WARPS;
         const int wig = pw % GROUP_WARPS;
         my_grp = grp;
@@ -763,11 +689,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         // table: by li)
         for (int li = grp, i = i0 + di * grp; i < nkb; li += PGROUPS, i += di * PGROUPS) {
             const int sl = li % LSTAGES;
-            // the A ring: slot of block i (8-bit table: slot li holds blocks 2 li and 2 li + 1,
-            // this CTA's at position rank)
-            const int s = (F == kE4m3 ? li : i) % AST;
+            // the A ring: slot of block i
+            const int s = i % AST;
             const uint32_t ul = (uint32_t)(li / LSTAGES);
-            const uint32_t u = (uint32_t)((F == kE4m3 ? li : i) / AST);
+            const uint32_t u = (uint32_t)(i / AST);
             // every lane waits (acquire), the warp decides together; the 8-bit table's staged
             // row scales share the logits slot's index and phase
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_l[sl]), ul & 1, abort_flag) &&
@@ -781,9 +706,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t packed[ROWS_PER_LANE][16];
             uint32_t sf_word[ROWS_PER_LANE];  // 8-bit table: the (row, block) scale bytes
             // every block is folded once per row block, by the producers of a CTA that forms it:
-            // (bf16) the one in column pair (i / 2) % (n_tiles / 2), (8-bit table) the one in
-            // cluster (i / 4) % (n_tiles / 2); a CTA's folds alternate between its producer groups
-            const bool fold = p.fused && (F == kE4m3 ? (i >> 2) : (i >> 1)) % ntp_count == ntp;
+            // the one in column pair (i / 2) % (n_tiles / 2); a CTA's folds alternate between its
+            // producer groups
+            const bool fold = p.fused && (i >> 1) % ntp_count == ntp;
             // 8-bit table: the block's normalised row scales u (0 outside the slice) and their
             // exponent E (row scale = u 2^E), staged by warp 0
             float us[F == kE4m3 ? 32 : 1];
@@ -930,8 +855,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 ok = false;
                 break;
             }
-            uint8_t *at = a_ring + s * A_SLOT + (F == kE4m3 ? (int)rank * A_BYTES : 0);
-            uint8_t *sft = sf_ring + s * Fmt<kE4m3>::SF_STAGE + (int)rank * 2048;  // 8-bit table
+            uint8_t *at = a_ring + s * A_SLOT;
+            uint8_t *sft = sf_ring + s * Fmt<kE4m3>::SF_STAGE;  // 8-bit table
 #pragma unroll
             for (int q = 0; q < ROWS_PER_LANE; ++q) {
                 const int r = rr[q];
@@ -948,35 +873,26 @@ __global__ void __launch_bounds__(THREADS, 1)
             fence_proxy_async_smem();
             __syncwarp();  // every lane's A stores (and proxy fence) before the arrival
             if (lane == 0) {
-                if constexpr (kPairMma) {
-                    if (rank & 1) {
-                        // the pair's even CTA's MMA thread reads this CTA's rows too: a 16-byte
-                        // copy that completes on its barrier tells it this warp's rows are in
-                        // place (issued after the rows' stores and proxy fence; never read)
-                        const uint32_t lead = rank & ~1u;
-                        bulk_copy_to_cluster(map_to_cta(smem_u32(sig_area + 16 * (1 + pw)), lead), smem_u32(sig_area),
-                                             16u, map_to_cta(smem_u32(&full_a[s]), lead));
-                    } else {
-                        mbar_arrive(smem_u32(&full_a[s]));
-                    }
-                    // the warp's 32 A rows (2 KiB) to the same slot of the CTA with the same rows
-                    // in the other column tile, completing on its full_a
-                    const uint32_t twin = rank ^ 2u;
-                    const uint32_t a_src = smem_u32(at + wig * 2048);
-                    bulk_copy_to_cluster(map_to_cta(a_src, twin), a_src, 2048u,
-                                         map_to_cta(smem_u32(&full_a[s]), twin));
+                if (rank & 1) {
+                    // the pair's even CTA's MMA thread reads this CTA's rows (and scale rows) too:
+                    // a 16-byte copy that completes on its barrier tells it this warp's rows are
+                    // in place (issued after the rows' stores and proxy fence; never read)
+                    const uint32_t lead = rank & ~1u;
+                    bulk_copy_to_cluster(map_to_cta(smem_u32(sig_area + 16 * (1 + pw)), lead), smem_u32(sig_area),
+                                         16u, map_to_cta(smem_u32(&full_a[s]), lead));
                 } else {
                     mbar_arrive(smem_u32(&full_a[s]));
                 }
+                // the warp's 32 A rows (2 KiB; 8-bit table: and its 32 scale rows, 512 B) to the
+                // same slot of the CTA with the same rows in the other column tile, completing on
+                // its full_a
+                const uint32_t twin = rank ^ 2u;
+                const uint32_t tbar = map_to_cta(smem_u32(&full_a[s]), twin);
+                const uint32_t a_src = smem_u32(at + wig * 2048);
+                bulk_copy_to_cluster(map_to_cta(a_src, twin), a_src, 2048u, tbar);
                 if constexpr (F == kE4m3) {
-                    // the warp's 32 A rows (2 KiB) and 32 scale rows (512 B) to the same slot of
-                    // the partner CTA, completing on its full_a
-                    const uint32_t peer = rank ^ 1u;
-                    const uint32_t pbar = map_to_cta(smem_u32(&full_a[s]), peer);
-                    const uint32_t a_src = smem_u32(at + wig * 2048);
                     const uint32_t f_src = smem_u32(sft + wig * 512);
-                    bulk_copy_to_cluster(map_to_cta(a_src, peer), a_src, 2048u, pbar);
-                    bulk_copy_to_cluster(map_to_cta(f_src, peer), f_src, 512u, pbar);
+                    bulk_copy_to_cluster(map_to_cta(f_src, twin), f_src, 512u, tbar);
                 }
             }
             if (fold) {
@@ -1228,10 +1144,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0) {
         __syncwarp();
         tc_fence_after();
-        if constexpr (kPairMma)
-            tmem_dealloc_pair<TMEM_COLS>(tmem_base);
-        else
-            tmem_dealloc<TMEM_COLS>(tmem_base);
+        tmem_dealloc_pair<TMEM_COLS>(tmem_base);
     }
 }
 
@@ -1543,14 +1456,15 @@ static cudaError_t ensure_kernel_attributes() {
     return e;
 }
 
-// Clusters of the bf16 product (four CTAs) that fit on the current device at once (36 on a
-// 152-SM GB300: whole clusters must sit in one GPC), looked up once per device.
-static int quad_clusters_per_wave(int num_sms) {
-    static std::atomic<int> cached[kMaxAttrDevices];
+// Clusters of the product (four CTAs) for a table format that fit on the current device at
+// once (36 on a 152-SM GB300: whole clusters must sit in one GPC), looked up once per device.
+static int quad_clusters_per_wave(int fmt, int num_sms) {
+    static std::atomic<int> cached[2][kMaxAttrDevices];
+    const int f = fmt == kE4m3 ? 1 : 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return num_sms / kQuadCtas;
     if (dev < kMaxAttrDevices) {
-        const int c = cached[dev].load(std::memory_order_acquire);
+        const int c = cached[f][dev].load(std::memory_order_acquire);
         if (c > 0) return c;
     }
     int n = 0;
@@ -1558,7 +1472,7 @@ static int quad_clusters_per_wave(int num_sms) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(kQuadCtas * 64, 1, 1);
         cfg.blockDim = dim3(THREADS, 1, 1);
-        cfg.dynamicSmemBytes = smem_bytes<kBf16>();
+        cfg.dynamicSmemBytes = f ? smem_bytes<kE4m3>() : smem_bytes<kBf16>();
         cudaLaunchAttribute a[1];
         a[0].id = cudaLaunchAttributeClusterDimension;
         a[0].val.clusterDim.x = kQuadCtas;
@@ -1566,10 +1480,11 @@ static int quad_clusters_per_wave(int num_sms) {
         a[0].val.clusterDim.z = 1;
         cfg.attrs = a;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, (void *)soft_embed_kernel<kBf16>, &cfg) != cudaSuccess) n = 0;
+        const void *fn = f ? (const void *)soft_embed_kernel<kE4m3> : (const void *)soft_embed_kernel<kBf16>;
+        if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) n = 0;
     }
     if (n <= 0) n = num_sms / kQuadCtas;
-    if (dev < kMaxAttrDevices) cached[dev].store(n, std::memory_order_release);
+    if (dev < kMaxAttrDevices) cached[f][dev].store(n, std::memory_order_release);
     return n;
 }
 
@@ -1586,17 +1501,10 @@ bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t 
     pl.m_tiles = (int)(2 * m_pairs);
     int n_full, tail;
     column_tiles(d, pl.bn, &pl.n_tiles, &n_full, &tail);
-    // clusters of two column tiles (bf16: and both 128-row halves of a 256-row block; 8-bit
-    // table: one 128-row block): an even tile count, a last odd tile's partner past d
+    // clusters of two column tiles and both 128-row halves of a 256-row block: an even tile
+    // count, a last odd tile's partner past d
     pl.n_tiles += pl.n_tiles & 1;
-    int64_t clusters;
-    if (fmt == kE4m3) {
-        pl.m_tiles = (int)((R + BM - 1) / BM);
-        m_pairs = pl.m_tiles;
-        clusters = num_sms / kCtasPerUnit;
-    } else {
-        clusters = quad_clusters_per_wave(num_sms);
-    }
+    const int64_t clusters = quad_clusters_per_wave(fmt, num_sms);
     n_full = pl.n_tiles / 2;  // units per split and row block: column pairs
     tail = 0;
     // choose the vocabulary splits that finish soonest: whole waves of clusters times
@@ -1665,7 +1573,7 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     if (e4) {
         const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)(vocab_end - vocab_start)};
         const cuuint64_t strides[1] = {(cuuint64_t)ldw};
-        const cuuint32_t box[2] = {128, (cuuint32_t)(Fmt<kE4m3>::BPS * BK)};  // a ring slot's two blocks
+        const cuuint32_t box[2] = {128, (cuuint32_t)BK};  // one 128-column atom of a block
         const cuuint32_t estr[2] = {1, 1};
         if (encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(tab.W), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1718,7 +1626,6 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     p.tail_splits = tail_splits_of(plan.splits, tail);
     p.w3d = w3d;
     p.w_scale = e4 ? tab.scale : nullptr;
-    p.pair_blocks = e4 ? 1 : 0;
     p.fused = single ? 1 : 0;
     p.logits = logits;
     p.ldl = ldl;
@@ -1746,9 +1653,9 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
         }
         overlap_previous = false;  // nothing before it to wait for
     }
-    // clusters: (column pair, row block, split); bf16 row blocks are 256 rows (a CTA pair)
-    const int64_t units = (int64_t)(e4 ? plan.m_tiles : plan.m_tiles / 2) * (n_tiles / 2) * p.splits;
-    const int cluster = e4 ? cluster_ctas<kE4m3>() : cluster_ctas<kBf16>();
+    // clusters: (column pair, 256-row block, split)
+    const int64_t units = (int64_t)(plan.m_tiles / 2) * (n_tiles / 2) * p.splits;
+    const int cluster = kQuadCtas;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(cluster * units), 1, 1);
