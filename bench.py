@@ -240,6 +240,80 @@ def other_configs(args, dev, B, inputs, SamplerStep, cost) -> dict:
     return res
 
 
+def run_sharded(args) -> None:
+    """The vocabulary-parallel step (calvarado04.com, "The fix" and "Why not just all-gather the
+    weights"): rank r of N holds the logit columns and W rows of vocabulary shard r; per step
+    it summarises its rows, all-gathers the 16-byte summaries, combines them in shard order,
+    accepts, forms its partial embedding against the global lse and all-gathers the partials,
+    which every rank adds in shard order.  One canvas per step over all ranks (strong scaling);
+    N = 1 runs the same code over a one-rank NCCL group."""
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{args.master_port}", rank=0, world_size=1,
+                                device_id=torch.device("cuda", local))
+    import __graft_entry__
+    __graft_entry__.build()
+    from denoising_sampler_step_gb300 import binding as B
+    from denoising_sampler_step_gb300 import inputs
+    from denoising_sampler_step_gb300.vocab_parallel import ShardedStep, TorchComm, shard_bounds
+
+    wl = inputs.WORKLOADS[WORKLOAD]
+    dev = torch.device("cuda", local)
+    s, e = shard_bounds(wl.V, world)[rank]
+    x = inputs.logits(wl)  # every rank draws the same canvas and keeps its columns
+    Wb = inputs.embedding_bf16(wl)
+    shard = torch.from_numpy(np.ascontiguousarray(x[:, s:e])).to(dev)
+    Wsh = torch.from_numpy(np.ascontiguousarray(Wb[s:e]).view(np.int16)).to(dev).view(torch.bfloat16)
+    bd = torch.from_numpy(inputs.budgets(wl)).to(dev)
+    del x, Wb
+    comm = TorchComm()
+    st = ShardedStep(wl.n_req, wl.L_c, wl.gamma)
+    stream = torch.cuda.current_stream(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        st.rank_step(shard, s, Wsh, bd, comm)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        st.rank_step(shard, s, Wsh, bd, comm)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    clk = clocks.stop()
+    mx = torch.tensor([t0.elapsed_time(t1)], device=dev)
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    ms = mx.item()
+    B.dg_get_device_status()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": wl.R * args.steps / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "mode": "sharded",
+            "dtype": "f32 statistics, bf16 x bf16 -> f32 tensor-core product", "data": "synthetic",
+            "config": config_of(wl),
+            "parallelism": f"vocabulary-parallel over {world} rank(s): shard [{s}, {e}) on rank 0; NCCL "
+                           "all-gathers of the row summaries and of the partial embeddings",
+            "all_gather_bytes_per_rank_per_step": {"row_summaries": world * wl.R * 16,
+                                                    "partial_embeddings": world * wl.R * wl.d * 4},
+            "gpu_launches": 6 * args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line))
+    dist.destroy_process_group()
+
+
 def spawn_ranks(args) -> int:
     """--gpus N > 1 without torchrun: start torchrun on 127.0.0.1 with N ranks running this
     script (same arguments) and return its exit status."""
@@ -264,6 +338,9 @@ def main() -> None:
     ap.add_argument("--only", choices=["soft_embed", "step", "soft_embed_e4m3", "step_e4m3"], default=None,
                     help="profiling target: run only this call (warm-up, then --steps calls) and print "
                          "its mean duration; no JSON line")
+    ap.add_argument("--mode", default="replicas", choices=["replicas", "sharded"],
+                    help="replicas: each rank steps its own canvas (the driver's line); sharded: the "
+                         "vocabulary-parallel step over all ranks, one canvas per step (NCCL all-gathers)")
     ap.add_argument("--sustained", type=float, default=0.0,
                     help="also run the step and the soft-embed call back to back for this many seconds "
                          "each, sampling clocks and power every 20 ms")
@@ -276,6 +353,9 @@ def main() -> None:
         sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world_env}: start one rank per GPU")
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.mode == "sharded":
+        run_sharded(args)
         return
 
     import numpy as np

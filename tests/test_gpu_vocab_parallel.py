@@ -126,3 +126,33 @@ def test_sharded_step_over_an_8bit_table(B):
         assert np.array_equal(out[k].cpu().numpy(), acc[k]), k
     ref = soft_embed_e4m3(x[:, :wl.V], ost["lse"], 0, wl.V, Q, scale, wl.gamma)
     assert rel_l2(out["E"].cpu().numpy(), ref).max() <= E_TOL
+
+
+def test_rank_step_over_a_one_rank_nccl_group(B):
+    """rank_step with its gathers over a real NCCL process group of one rank (the whole
+    vocabulary is the rank's shard): statistics, acceptance and E against the oracle.  The
+    same code runs one rank per GPU when there are several."""
+    import socket
+    import torch.distributed as dist
+    from denoising_sampler_step_gb300.vocab_parallel import TorchComm
+    if dist.is_initialized():
+        pytest.skip("a process group is already set up in this process")
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1)
+    try:
+        wl = inputs.WORKLOADS["tiny"].with_(n_req=2, L_c=32, V=40000, d=512, seed=79, budget=("uniform", 2.0, 20.0))
+        x, budgets, ost, _ = guarded(wl)
+        Wb = inputs.embedding_bf16(wl)
+        out = ShardedStep(wl.n_req, wl.L_c, wl.gamma).rank_step(dev(x), 0, w_dev(Wb), dev(budgets), TorchComm())
+        torch.cuda.synchronize()
+        B.dg_get_device_status()
+        check_stats(out, ost)
+        acc = entropy_accept(ost["H"], ost["kappa"], wl.n_req, wl.L_c, budgets)
+        for k in ("order", "mask", "n_accepted"):
+            assert np.array_equal(out[k].cpu().numpy(), acc[k]), k
+        ref = soft_embed(x, ost["lse"], 0, wl.V, Wb, wl.gamma)
+        assert rel_l2(out["E"].cpu().numpy(), ref).max() <= E_TOL
+    finally:
+        dist.destroy_process_group()
