@@ -83,6 +83,15 @@ lib.dg_sampler_loop_step_e4m3.argtypes = [_p, _i32, _i32, _i64, _i64, _p, _p, _i
                                           _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i64,
                                           _p, _p, _p, _p, _p, _p, _u32, _p, _sz, _p]
 lib.dg_sampler_loop_step_e4m3.restype = ctypes.c_int
+lib.dg_soft_embed_shard_begin.argtypes = [_p, _i64, _i64, _i64, _i64, _p, _i64, _i64, _i64, _p, _p, _sz, _p]
+lib.dg_soft_embed_shard_begin.restype = ctypes.c_int
+lib.dg_soft_embed_shard_end.argtypes = [_p, _i64, _p, _i64, _i64, _p, _i64, _i64, _i64, _f32, _p, _i64, _p, _sz, _p]
+lib.dg_soft_embed_shard_end.restype = ctypes.c_int
+lib.dg_soft_embed_shard_begin_e4m3.argtypes = [_p, _i64, _i64, _i64, _i64, _p, _p, _i64, _i64, _i64, _p, _p, _sz, _p]
+lib.dg_soft_embed_shard_begin_e4m3.restype = ctypes.c_int
+lib.dg_soft_embed_shard_end_e4m3.argtypes = [_p, _i64, _p, _i64, _i64, _p, _p, _i64, _i64, _i64, _f32, _p, _i64, _p,
+                                             _sz, _p]
+lib.dg_soft_embed_shard_end_e4m3.restype = ctypes.c_int
 
 STATUS = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED", 3: "DG_ERR_CUDA", 4: "DG_ERR_TIMEOUT"}
 
@@ -161,6 +170,59 @@ def dg_row_stats_partial(shard: torch.Tensor, vocab_offset: int, n: int | None =
     _check(lib.dg_row_stats_partial(_ptr(shard), R, n, _ld(shard), vocab_offset, _ptr(o), _stream(stream)),
            "dg_row_stats_partial")
     return o
+
+
+def dg_soft_embed_shard_begin(shard: torch.Tensor, vocab_offset: int, W_shard, ws: torch.Tensor,
+                              stream=None, out: torch.Tensor | None = None) -> torch.Tensor:
+    """First call of a shard's one-read soft embedding: the shard's [R, 4] row summaries (the
+    format of dg_row_stats_partial); the split partials stay in `ws` for dg_soft_embed_shard_end.
+    W_shard: bf16 [rows_pad, >= d], or an 8-bit table (codes, row scales)."""
+    R, n = shard.shape
+    o = out if out is not None else _new((R, 4), torch.float32, shard.device)
+    if isinstance(W_shard, tuple):
+        Q, scale = W_shard
+        _check(lib.dg_soft_embed_shard_begin_e4m3(_ptr(shard), _ld(shard), R, n, vocab_offset, _ptr(Q), _ptr(scale),
+                                                  Q.shape[0], _ld(Q), Q.shape[1], _ptr(o), _ptr(ws), ws.numel(),
+                                                  _stream(stream)), "dg_soft_embed_shard_begin_e4m3")
+    else:
+        _check(lib.dg_soft_embed_shard_begin(_ptr(shard), _ld(shard), R, n, vocab_offset, _ptr(W_shard),
+                                             W_shard.shape[0], _ld(W_shard), W_shard.shape[1], _ptr(o), _ptr(ws),
+                                             ws.numel(), _stream(stream)), "dg_soft_embed_shard_begin")
+    return o
+
+
+def dg_soft_embed_shard_end(shard: torch.Tensor, lse: torch.Tensor, W_shard, gamma: float, ws: torch.Tensor,
+                            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Second call: gamma * E_shard [R, d] from the partials the first call left in `ws`, scaled
+    against the full-row lse."""
+    R, n = shard.shape
+    d = W_shard[0].shape[1] if isinstance(W_shard, tuple) else W_shard.shape[1]
+    if out is None:
+        out = _new((R, d), torch.float32, shard.device)
+    if isinstance(W_shard, tuple):
+        Q, scale = W_shard
+        _check(lib.dg_soft_embed_shard_end_e4m3(_ptr(shard), _ld(shard), _ptr(lse), R, n, _ptr(Q), _ptr(scale),
+                                                Q.shape[0], _ld(Q), d, gamma, _ptr(out), _ld(out), _ptr(ws),
+                                                ws.numel(), _stream(stream)), "dg_soft_embed_shard_end_e4m3")
+    else:
+        _check(lib.dg_soft_embed_shard_end(_ptr(shard), _ld(shard), _ptr(lse), R, n, _ptr(W_shard),
+                                           W_shard.shape[0], _ld(W_shard), d, gamma, _ptr(out), _ld(out), _ptr(ws),
+                                           ws.numel(), _stream(stream)), "dg_soft_embed_shard_end")
+    return out
+
+
+def dg_soft_embed_shard_begin_e4m3(shard: torch.Tensor, vocab_offset: int, Q_shard: torch.Tensor,
+                                   scale_shard: torch.Tensor, ws: torch.Tensor, stream=None,
+                                   out: torch.Tensor | None = None) -> torch.Tensor:
+    """dg_soft_embed_shard_begin over an 8-bit table shard (codes, row scales)."""
+    return dg_soft_embed_shard_begin(shard, vocab_offset, (Q_shard, scale_shard), ws, stream=stream, out=out)
+
+
+def dg_soft_embed_shard_end_e4m3(shard: torch.Tensor, lse: torch.Tensor, Q_shard: torch.Tensor,
+                                 scale_shard: torch.Tensor, gamma: float, ws: torch.Tensor,
+                                 out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """dg_soft_embed_shard_end over an 8-bit table shard (codes, row scales)."""
+    return dg_soft_embed_shard_end(shard, lse, (Q_shard, scale_shard), gamma, ws, out=out, stream=stream)
 
 
 def dg_row_stats_combine(states: torch.Tensor, stream=None, out: dict | None = None) -> dict:

@@ -195,6 +195,49 @@ int device_sm_count() {
 
 }  // namespace dg
 
+namespace dg {
+namespace {
+
+// The two calls of a vocabulary shard's single pass (phase 1: product and row summaries; phase
+// 2: the reduce against the full-row lse), over the shard's own logit columns [0, n).
+dg_status run_shard_phase(int phase, const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t n,
+                          int64_t vocab_offset, const EmbedTable &tab, int64_t rows_pad, int64_t d, float gamma,
+                          float *state, float *out, int64_t ldo, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    const char *what = phase == 1 ? "shard begin" : "shard end";
+    if (n < 1) return fail(DG_ERR_INVALID_ARG, "%s: the shard needs at least one vocabulary entry", what);
+    // the first call writes no lse and no E: its row summaries stand in for both pointers here
+    dg_status st = phase == 1 ? check_table_args(logits, ldl, state, R, 0, n, tab, rows_pad, d, state, d)
+                              : check_table_args(logits, ldl, lse, R, 0, n, tab, rows_pad, d, out, ldo);
+    if (st != DG_OK) return st;
+    if (phase == 1) {
+        if (vocab_offset < 0 || vocab_offset + n > INT32_MAX - 1)
+            return fail(DG_ERR_INVALID_ARG, "shard begin: the shard must lie in [0, 2^31 - 1)");
+        if (reinterpret_cast<uintptr_t>(state) % 16 != 0)
+            return fail(DG_ERR_UNSUPPORTED, "shard begin: state must be 16-byte aligned");
+    }
+    if (R == 0) return DG_OK;
+    const int sms = device_sm_count();
+    if (sms <= 0) return fail(DG_ERR_CUDA, "%s: no CUDA device", what);
+    SoftEmbedPlan plan;
+    if (!plan_soft_embed(R, 0, n, d, sms, &plan, tab.fmt)) return fail(DG_ERR_INVALID_ARG, "%s: no plan for shape", what);
+    if (!ws || ws_bytes < plan.single_pass_bytes)
+        return fail(DG_ERR_INVALID_ARG, "%s: workspace of %zu bytes is below the %zu needed", what, ws_bytes,
+                    plan.single_pass_bytes);
+    if (!aligned16(ws)) return fail(DG_ERR_UNSUPPORTED, "%s: workspace must be 16-byte aligned", what);
+    SinglePassOut so{};
+    so.phase = phase;
+    so.shard_state = state;
+    so.vocab_offset = vocab_offset;
+    so.lse = const_cast<float *>(lse);
+    const char *msg = what;
+    cudaError_t e = launch_soft_embed(logits, ldl, lse, R, 0, n, tab, d, gamma, out, ldo, ws, plan, stream, &msg,
+                                      nullptr, nullptr, false, &so);
+    return e == cudaSuccess ? DG_OK : cuda_fail(e, msg);
+}
+
+}  // namespace
+}  // namespace dg
+
 using namespace dg;
 
 extern "C" {
@@ -295,6 +338,42 @@ dg_status dg_soft_embed_e4m3(const float *logits, int64_t ldl, const float *lse,
     if (st != DG_OK) return st;
     return run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, tab, d, gamma, out, ldo, workspace,
                           workspace_bytes, (cudaStream_t)stream);
+}
+
+dg_status dg_soft_embed_shard_begin(const float *logits, int64_t ldl, int64_t R, int64_t n, int64_t vocab_offset,
+                                    const uint16_t *W_shard, int64_t rows_pad, int64_t ldw, int64_t d, float *state,
+                                    void *workspace, size_t workspace_bytes, dg_stream_t stream) {
+    t_last_error[0] = 0;
+    return run_shard_phase(1, logits, ldl, nullptr, R, n, vocab_offset, EmbedTable{kTableBf16, W_shard, ldw, nullptr},
+                           rows_pad, d, 1.0f, state, nullptr, d, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+dg_status dg_soft_embed_shard_end(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t n,
+                                  const uint16_t *W_shard, int64_t rows_pad, int64_t ldw, int64_t d, float gamma,
+                                  float *out, int64_t ldo, void *workspace, size_t workspace_bytes,
+                                  dg_stream_t stream) {
+    t_last_error[0] = 0;
+    return run_shard_phase(2, logits, ldl, lse, R, n, 0, EmbedTable{kTableBf16, W_shard, ldw, nullptr}, rows_pad, d,
+                           gamma, nullptr, out, ldo, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+dg_status dg_soft_embed_shard_begin_e4m3(const float *logits, int64_t ldl, int64_t R, int64_t n, int64_t vocab_offset,
+                                         const uint8_t *Q_shard, const float *scale_shard, int64_t rows_pad,
+                                         int64_t ldq, int64_t d, float *state, void *workspace,
+                                         size_t workspace_bytes, dg_stream_t stream) {
+    t_last_error[0] = 0;
+    return run_shard_phase(1, logits, ldl, nullptr, R, n, vocab_offset,
+                           EmbedTable{kTableE4m3, Q_shard, ldq, scale_shard}, rows_pad, d, 1.0f, state, nullptr, d,
+                           workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+dg_status dg_soft_embed_shard_end_e4m3(const float *logits, int64_t ldl, const float *lse, int64_t R, int64_t n,
+                                       const uint8_t *Q_shard, const float *scale_shard, int64_t rows_pad,
+                                       int64_t ldq, int64_t d, float gamma, float *out, int64_t ldo, void *workspace,
+                                       size_t workspace_bytes, dg_stream_t stream) {
+    t_last_error[0] = 0;
+    return run_shard_phase(2, logits, ldl, lse, R, n, 0, EmbedTable{kTableE4m3, Q_shard, ldq, scale_shard}, rows_pad,
+                           d, gamma, nullptr, out, ldo, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
 dg_status dg_quantize_e4m3(const uint16_t *W, int64_t V, int64_t d, int64_t ldw, uint8_t *Q, int64_t ldq,

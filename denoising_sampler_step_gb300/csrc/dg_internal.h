@@ -62,6 +62,13 @@ struct SinglePassOut {
     int32_t *candidate;     // non-NULL: also draw at temperature 1 (two-level Gumbel-max); kappa is
     uint64_t seed, offset;  // then -ln p of the drawn token
     const AcceptSpec *accept;
+    // a vocabulary shard in two calls around the ranks' exchange of row summaries:
+    // 0 the whole step; 1 the product and the shard's row summaries (shard_state, argmax as
+    // vocab_offset + column; the split partials stay in the workspace); 2 the reduce, its scales
+    // taken against the full-row lse (`lse`: read, not written)
+    int phase;
+    float *shard_state;
+    int64_t vocab_offset;
 };
 bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t d, int num_sms,
                      SoftEmbedPlan *plan, int fmt = kTableBf16);

@@ -1393,6 +1393,57 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// A vocabulary shard's first call, after the single pass's product: per row (one warp) the
+// splits' tile summaries merged as single_pass_stats_kernel merges them, written as the
+// shard's 16-byte row summary (m, argmax as vocab_offset + column, rest, t: the format of
+// dg_row_stats_partial), and each split whose probabilities against its reference could
+// overflow marked for the second call (its reference becomes +inf).
+__global__ void __launch_bounds__(256)
+    shard_summary_kernel(const Params p, float4 *__restrict__ out_state, int64_t vocab_offset) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (row >= p.R) return;  // warp-uniform
+    rowstate::RowState st = rowstate::empty_row_state();
+    for (int s = lane; s < p.splits; s += 32) {
+        rowstate::RowState sp = rowstate::empty_row_state();
+        float *ref = p.ref + (int64_t)s * p.R + row;
+        const float c = *ref;
+        for (int t0 = 0; t0 < p.n_tiles; t0 += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                v[u] = p.state[((int64_t)s * p.n_tiles + min(t0 + u, p.n_tiles - 1)) * p.R + row];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (t0 + u < p.n_tiles)
+                    rowstate::merge(sp, rowstate::RowState{v[u].x, __float_as_int(v[u].y), v[u].z, v[u].w});
+        }
+        const float gap = sp.m - c;
+        if (sp.m > -INFINITY && !(gap + log1pf(sp.rest) <= kRefSumLog && gap >= -kRefBelow)) *ref = INFINITY;
+        rowstate::merge(st, sp);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) rowstate::merge(st, rowstate::shfl_down(st, off));
+    if (lane == 0) {
+        const int a = st.m == -INFINITY ? 0x7fffffff : (int)(st.a + vocab_offset);
+        out_state[row] = make_float4(st.m, __int_as_float(a), st.rest, st.t);
+    }
+}
+
+// A vocabulary shard's second call: each split's reference becomes its scale exp(c - lse) against
+// the full-row lse (NaN for a row without a distribution), or kRedo where the first call marked it.
+__global__ void __launch_bounds__(256) shard_scale_kernel(const Params p, const float *__restrict__ lse) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)p.splits * p.R) return;
+    const int64_t row = idx % p.R;
+    const float c = p.ref[idx];
+    p.ref[idx] = c == INFINITY ? kRedo : ex2_approx((c - lse[row]) * kLog2e);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -1671,11 +1722,15 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     attr[1].val.programmaticStreamSerializationAllowed = overlap_previous ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = e4 ? cudaLaunchKernelEx(&cfg, soft_embed_kernel<kE4m3>, tm_l, tm_w, p)
-                       : cudaLaunchKernelEx(&cfg, soft_embed_kernel<kBf16>, tm_l, tm_w, p);
-    if (e != cudaSuccess) {
-        *msg = "soft-embed kernel launch failed";
-        return e;
+    const int phase = single ? single->phase : 0;
+    cudaError_t e = cudaSuccess;
+    if (phase != 2) {  // the second call of a shard reduces what the first one left
+        e = e4 ? cudaLaunchKernelEx(&cfg, soft_embed_kernel<kE4m3>, tm_l, tm_w, p)
+               : cudaLaunchKernelEx(&cfg, soft_embed_kernel<kBf16>, tm_l, tm_w, p);
+        if (e != cudaSuccess) {
+            *msg = "soft-embed kernel launch failed";
+            return e;
+        }
     }
     // the single pass's small kernels each start while the one before finishes (programmatic
     // dependent launch); each waits for its predecessor before it reads what that one wrote
@@ -1691,7 +1746,22 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
         c.numAttrs = 1;
         return c;
     };
-    if (single) {
+    if (phase == 1) {
+        cudaLaunchConfig_t c1 = small_cfg((unsigned)((R * 32 + 255) / 256));
+        e = cudaLaunchKernelEx(&c1, shard_summary_kernel, p, reinterpret_cast<float4 *>(single->shard_state),
+                               single->vocab_offset);
+        if (e != cudaSuccess) *msg = "shard: row summary launch failed";
+        return e;
+    }
+    if (phase == 2) {
+        cudaLaunchConfig_t c1 = small_cfg((unsigned)(((int64_t)p.splits * R + 255) / 256));
+        c1.numAttrs = 0;  // the first call's kernels (and the exchange between) come before it
+        e = cudaLaunchKernelEx(&c1, shard_scale_kernel, p, (const float *)single->lse);
+        if (e != cudaSuccess) {
+            *msg = "shard: scale launch failed";
+            return e;
+        }
+    } else if (single) {
         cudaLaunchConfig_t c1 = small_cfg((unsigned)((R * 32 + 255) / 256));
         e = cudaLaunchKernelEx(&c1, single_pass_stats_kernel, p, single->m, single->lse, single->H, single->kappa,
                                single->argmax);

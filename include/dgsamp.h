@@ -267,6 +267,56 @@ dg_status dg_row_stats_combine(const float *states, int32_t T, int64_t R, float 
                                float *H, float *kappa, int32_t *argmax, dg_stream_t stream);
 
 /*
+ * A vocabulary shard's soft embedding in one read of its logits ([P1] "The fix": each rank
+ * holds the logit columns and the W rows of one contiguous vocabulary range; the softmax is
+ * over all V entries).  Two calls around the ranks' exchange of row summaries:
+ *
+ *   1. dg_soft_embed_shard_begin: the product over the shard's columns [0, n) with
+ *      exp(l - c) against a per-row, per-split reference c, folding the row statistics on
+ *      the way; writes the shard's 16-byte row summaries `state` in dg_row_stats_partial's
+ *      format (argmax = vocab_offset + column) and keeps the split partials and references
+ *      in `workspace`.
+ *   2. (the caller gathers every shard's `state` in shard order and runs
+ *      dg_row_stats_combine: the full-row m, lse, H, kappa, argmax)
+ *   3. dg_soft_embed_shard_end: with that full-row `lse`, scales each split's partial by
+ *      exp(c - lse), recomputes on the CUDA cores the rare (split, row) pairs whose
+ *      probabilities against c could overflow (as dg_sampler_step's single pass does), adds
+ *      the splits in a fixed order and writes out = gamma * E_shard.
+ *
+ * The shard's E then equals dg_soft_embed over the same columns with the full-row lse, up
+ * to the bf16 rounding of different probabilities (exp(l - c) scaled afterwards instead of
+ * exp(l - lse)).  Both calls take the same logits, W_shard, R, n and d, and the same
+ * workspace of at least dg_soft_embed_workspace_size(R, n, d) bytes (the _e4m3 forms:
+ * dg_soft_embed_workspace_size_e4m3), which must not be used for anything else in between.
+ *   logits   [R, ldl] fp32, the shard's n columns (the layout rules of dg_soft_embed)
+ *   W_shard  [rows_pad >= n, ldw] bf16 bits; the _e4m3 forms: Q_shard [rows_pad, ldq] E4M3
+ *            codes and scale_shard [rows_pad] fp32 row scales (as dg_soft_embed_e4m3)
+ *   state    [R] x 16 bytes, 16-byte aligned (begin)
+ *   lse      [R] fp32, the full-row log-sum-exp (end; NaN for a row without a distribution,
+ *            whose E is then NaN)
+ * Errors: n < 1, or the argument rules of dg_soft_embed and dg_row_stats_partial.
+ * Asynchronous; R == 0 queues nothing.
+ */
+dg_status dg_soft_embed_shard_begin(const float *logits, int64_t ldl, int64_t R, int64_t n,
+                                    int64_t vocab_offset, const uint16_t *W_shard, int64_t rows_pad,
+                                    int64_t ldw, int64_t d, float *state, void *workspace,
+                                    size_t workspace_bytes, dg_stream_t stream);
+dg_status dg_soft_embed_shard_end(const float *logits, int64_t ldl, const float *lse, int64_t R,
+                                  int64_t n, const uint16_t *W_shard, int64_t rows_pad, int64_t ldw,
+                                  int64_t d, float gamma, float *out, int64_t ldo, void *workspace,
+                                  size_t workspace_bytes, dg_stream_t stream);
+dg_status dg_soft_embed_shard_begin_e4m3(const float *logits, int64_t ldl, int64_t R, int64_t n,
+                                         int64_t vocab_offset, const uint8_t *Q_shard,
+                                         const float *scale_shard, int64_t rows_pad, int64_t ldq,
+                                         int64_t d, float *state, void *workspace,
+                                         size_t workspace_bytes, dg_stream_t stream);
+dg_status dg_soft_embed_shard_end_e4m3(const float *logits, int64_t ldl, const float *lse, int64_t R,
+                                       int64_t n, const uint8_t *Q_shard, const float *scale_shard,
+                                       int64_t rows_pad, int64_t ldq, int64_t d, float gamma,
+                                       float *out, int64_t ldo, void *workspace,
+                                       size_t workspace_bytes, dg_stream_t stream);
+
+/*
  * Stochastic candidates ([P2] sampling loop: candidate tokens are sampled at every
  * position).  For each row i, a categorical draw from softmax(l_i / temperature), taken
  * as a two-level Gumbel-max (an exact categorical sampler): with z = l_i / temperature,

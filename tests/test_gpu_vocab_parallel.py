@@ -65,15 +65,17 @@ def test_shard_summaries_and_their_combination(B, V, T):
     assert c["argmax"][4].item() == 5 and c["argmax"][2].item() == V - 1
 
 
-def test_sharded_step_on_one_device(B):
-    """Four uneven shards in one process: statistics, acceptance and E against the oracle;
-    E against the unsharded product (the partition identity)."""
+@pytest.mark.parametrize("two_pass", [False, True])
+def test_sharded_step_on_one_device(B, two_pass):
+    """Four uneven shards in one process, each read once (the shard calls) or twice:
+    statistics, acceptance and E against the oracle; E against the unsharded product (the
+    partition identity)."""
     wl = inputs.WORKLOADS["tiny"].with_(n_req=3, L_c=32, V=40001, d=256, seed=77, budget=("uniform", 2.0, 20.0))
     x, budgets, ost, _ = guarded(wl, ld=40004)       # the unsharded calls need ldl % 4 == 0
     Wb = inputs.embedding_bf16(wl)
     Wd = w_dev(Wb)
     bounds = shard_bounds(wl.V, 4)
-    step = ShardedStep(wl.n_req, wl.L_c, wl.gamma)
+    step = ShardedStep(wl.n_req, wl.L_c, wl.gamma, two_pass=two_pass)
     out = step.local_step([shard_tensor(x, s, e) for s, e in bounds], [s for s, _ in bounds],
                           [Wd[s:e] for s, e in bounds], dev(budgets))
     torch.cuda.synchronize()
@@ -86,7 +88,10 @@ def test_sharded_step_on_one_device(B):
     assert rel_l2(E, soft_embed(x[:, :wl.V], ost["lse"], 0, wl.V, Wb, wl.gamma)).max() <= E_TOL
     xd = dev(x)
     full = B.dg_soft_embed(xd, B.dg_row_stats(xd, V=wl.V)["lse"], 0, wl.V, Wd, wl.gamma).cpu().numpy()
-    assert rel_l2(E, full.astype(np.float64)).max() <= 1e-3
+    # two passes: the same bf16 probabilities as the unsharded product, only the fp32 additions
+    # reassociated; one read: probabilities exp(l - c) rounded before their scale, so the two
+    # agree to the bf16 rounding (the tolerance), as the single-pass step and the two-pass one do
+    assert rel_l2(E, full.astype(np.float64)).max() <= (1e-3 if two_pass else E_TOL)
 
 
 @pytest.mark.slow
@@ -156,3 +161,55 @@ def test_rank_step_over_a_one_rank_nccl_group(B):
         assert rel_l2(out["E"].cpu().numpy(), ref).max() <= E_TOL
     finally:
         dist.destroy_process_group()
+
+
+def test_shard_calls_summaries_and_redo_rows(B):
+    """The one-read shard calls on three uneven shards: each shard's summaries against the
+    oracle's (m and the argmax exact, rest and t to 1e-5), the combined statistics against the
+    whole-row oracle, and E against the oracle, with rows whose probabilities against a split's
+    reference could overflow (the second call recomputes them), rows whose mass lies in one
+    shard only and a row without a distribution."""
+    wl = inputs.WORKLOADS["tiny"].with_(n_req=1, L_c=24, V=40000, d=256, seed=81, budget=5.0)
+    x = inputs.logits(wl)
+    x[0, 12345] = 1.0e4                     # one-hot: overflow against any reference
+    x[1, 30000] = 90.0                      # 90 nats above the rest, in the last shard
+    x[2, :20000] = -np.inf                  # no mass in the first shard
+    x[3, :] = -np.inf                       # no distribution
+    x[4, :] -= 300.0                        # far below the default reference
+    Wb = inputs.embedding_bf16(wl)
+    bounds = shard_bounds(wl.V, 3)
+    states, parts = [], []
+    shards = [shard_tensor(x, s, e) for s, e in bounds]
+    wss = [B.workspace(wl.R, e - s, wl.d, shards[0].device) for s, e in bounds]
+    for (s, e), sh, ws in zip(bounds, shards, wss):
+        st = B.dg_soft_embed_shard_begin(sh, s, w_dev(Wb[s:e]), ws)
+        o = row_stats_partial(x[:, s:e], s)
+        g = st.cpu().numpy()
+        assert np.array_equal(g[:, 1].view(np.int32), o["a"].astype(np.int32))
+        assert np.array_equal(g[:, 0], o["m"].astype(np.float32))
+        fin = np.isfinite(o["m"])
+        for col, k in ((2, "rest"), (3, "t")):
+            err = np.abs(g[fin, col] - o[k][fin]) / np.maximum(1.0, np.abs(o[k][fin]))
+            assert err.max() <= 1e-5, k
+        states.append(st)
+    c = B.dg_row_stats_combine(torch.stack(states))
+    ost = row_stats(x)
+    check_stats(c, ost)
+    for (s, e), sh, ws in zip(bounds, shards, wss):
+        parts.append(B.dg_soft_embed_shard_end(sh, c["lse"], w_dev(Wb[s:e]), 1.0, ws))
+    E = B.dg_sum_partials(parts, wl.gamma).cpu().numpy()
+    torch.cuda.synchronize()
+    B.dg_get_device_status()
+    rows = np.array([0, 1, 2, 4, 5, 23])
+    assert rel_l2(E[rows], soft_embed(x, ost["lse"], 0, wl.V, Wb, wl.gamma, rows=rows)).max() <= E_TOL
+    assert np.all(np.isnan(E[3]))
+
+
+def test_shard_calls_reject_an_empty_shard(B):
+    from denoising_sampler_step_gb300.binding import DgError
+    x = dev(np.zeros((4, 8), np.float32))
+    W = w_dev(np.zeros((8, 64), np.uint16))
+    ws = B.workspace(4, 8, 64, x.device)
+    with pytest.raises(DgError) as ei:
+        B.dg_soft_embed_shard_begin(x[:, :0], 0, W, ws)
+    assert ei.value.status == 1

@@ -17,7 +17,18 @@ from oracle.partition_oracle import row_stats_combine, row_stats_partial
 
 
 class OracleOps:
-    """The five per-rank calls, on CPU tensors, by the oracle (float64)."""
+    """The per-rank calls, on CPU tensors, by the oracle (float64).  The one-read shard calls
+    are the same two results: the shard's summaries first, its product against the full-row
+    lse second."""
+
+    def workspace(self, shard, W_shard):
+        return None
+
+    def shard_begin(self, shard, vocab_offset, W_shard, ws):
+        return self.row_stats_partial(shard, vocab_offset)
+
+    def shard_end(self, shard, lse, W_shard, ws):
+        return self.soft_embed_shard(shard, lse, W_shard)
 
     def row_stats_partial(self, shard, vocab_offset):
         p = row_stats_partial(shard.numpy(), vocab_offset)
@@ -75,14 +86,14 @@ def _free_port():
     return port
 
 
-def _worker(rank, world, port, q):
+def _worker(rank, world, port, q, two_pass=False):
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         x, W, budgets = problem()
         s, e = shard_bounds(WL.V, world)[rank]
-        step = ShardedStep(WL.n_req, WL.L_c, WL.gamma, min_accept=1)
+        step = ShardedStep(WL.n_req, WL.L_c, WL.gamma, min_accept=1, two_pass=two_pass)
         out = step.rank_step(torch.from_numpy(np.ascontiguousarray(x[:, s:e])), s,
                              torch.from_numpy(W[s:e].view(np.int16)), torch.from_numpy(budgets), TorchComm(),
                              ops=OracleOps())
@@ -91,12 +102,13 @@ def _worker(rank, world, port, q):
         dist.destroy_process_group()
 
 
-def test_two_gloo_ranks_give_the_unsharded_step():
+@pytest.mark.parametrize("two_pass", [False, True])
+def test_two_gloo_ranks_give_the_unsharded_step(two_pass):
     world = 2
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q, two_pass)) for r in range(world)]
     for p in procs:
         p.start()
     res = dict(q.get(timeout=180) for _ in range(world))
@@ -110,11 +122,11 @@ def test_two_gloo_ranks_give_the_unsharded_step():
         assert np.array_equal(res[0][k], res[1][k], equal_nan=True), k
 
 
-@pytest.mark.parametrize("T", [1, 3, 5])
-def test_local_shards_give_the_unsharded_step(T):
+@pytest.mark.parametrize("T,two_pass", [(1, False), (3, False), (5, False), (3, True)])
+def test_local_shards_give_the_unsharded_step(T, two_pass):
     x, W, budgets = problem()
     bounds = shard_bounds(WL.V, T)
-    step = ShardedStep(WL.n_req, WL.L_c, WL.gamma, min_accept=1)
+    step = ShardedStep(WL.n_req, WL.L_c, WL.gamma, min_accept=1, two_pass=two_pass)
     out = step.local_step([torch.from_numpy(np.ascontiguousarray(x[:, s:e])) for s, e in bounds],
                           [s for s, _ in bounds], [torch.from_numpy(W[s:e].view(np.int16)) for s, e in bounds],
                           torch.from_numpy(budgets), ops=OracleOps())
