@@ -176,6 +176,15 @@ __device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const void *
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d_pair_hint(uint32_t dst, const void *tmap, uint32_t bar, int x, int y,
+                                                      int z, int w, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "l"(policy)
+        : "memory");
+}
+
 // L2 policy that marks the lines it touches as first to evict (data read once).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t pol;

@@ -45,6 +45,7 @@
 
 #include <atomic>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "accept.cuh"
@@ -170,7 +171,8 @@ struct Params {
     int n_full;          // n-tiles of full width (two halves)
     int tail_halves;     // 1 if the last n-tile is 256 wide or less, else 0
     int splits, tail_splits;
-    int w3d;             // 1: the W map is 3-D (atom columns x rows x atoms), one load per CTA and block
+    int w3d;             // 1: the W map is 3-D (atom columns x rows x atoms), one load per CTA and half
+    int w4d_atoms;       // > 0: the 4-D W map (both halves in one load) holds this many atoms per row
     // 8-bit table: the fp32 scale of vocabulary entry v is w_scale[v - vocab_start]
     const float *w_scale;
     // single pass (no lse yet): each split's probabilities are taken against a reference
@@ -264,6 +266,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <int F>
 __global__ void __launch_bounds__(THREADS, 1)
     soft_embed_kernel(const __grid_constant__ CUtensorMap tm_logits, const __grid_constant__ CUtensorMap tm_w,
+                      const __grid_constant__ CUtensorMap tm_w4,
                       const Params p) {
     constexpr int BN = Fmt<F>::BN;
     constexpr int W_SLOT = Fmt<F>::W_SLOT;
@@ -355,6 +358,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_mbar_init();
         prefetch_tmap(&tm_logits);
         prefetch_tmap(&tm_w);
+        if (p.w4d_atoms > 0) prefetch_tmap(&tm_w4);
     }
     if constexpr (F == kE4m3) {
         // the B scale chunk: every byte 127, a factor of 1 (the table's row scales go into A)
@@ -409,7 +413,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             // bf16: every W byte leaves L2 once (evict first); 8-bit table: both row-block
             // clusters of a column pair read each W tile, close together (ordinary priority)
             const uint64_t w_policy = F == kE4m3 ? l2_policy_evict_normal() : l2_policy_evict_first();
-            // bf16: a 3-D map fetches a CTA's 2 atoms of a half in one load
+            // bf16: a 4-D map fetches a CTA's four atoms of a full-width tile in one load, a 3-D
+            // map its two atoms of a half (the TMA unit's cost is per load, not per byte: two
+            // 64-column boxes per half in place of one 3-D load made the product 8 % slower,
+            // and one load per block in place of two made it 4 % faster)
             const bool w3d = p.w3d;
             const uint32_t lead_a = map_to_cta(smem_u32(&full_a[0]), rank & ~1u);  // the pair's even CTA's full_a[0]
             for (int i = 0; i < nkb; ++i) {  // one block per ring slot
@@ -440,6 +447,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                         tma_load_2d_pair_hint(smem_u32(w_ring + s * W_SLOT + h * W_BOX_BYTES), &tm_w, bl, xh, wy,
                                               w_policy);
                     }
+                } else if (halves == 2 && col0 / 64 + 2 * (int)(rank & 1) + 6 <= p.w4d_atoms) {
+                    // both halves' atoms (4h + 2 (rank & 1) and + 1) in one load
+                    tma_load_4d_pair_hint(smem_u32(w_ring + s * W_SLOT), &tm_w4, bl, 0, wy,
+                                          col0 / 64 + 2 * (int)(rank & 1), 0, w_policy);
                 } else {
                     for (int h = 0; h < halves; ++h) {
                         const uint32_t dst = smem_u32(w_ring + s * W_SLOT + h * 2 * W_BOX_BYTES);
@@ -1602,7 +1613,9 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
         *msg = "cuTensorMapEncodeTiled is not available from the driver";
         return cudaErrorNotSupported;
     }
-    CUtensorMap tm_l, tm_w;
+    CUtensorMap tm_l, tm_w, tm_w4;
+    memset(&tm_w4, 0, sizeof(tm_w4));
+    int w4d_atoms = 0;
     {
         const cuuint64_t dims[2] = {(cuuint64_t)vocab_end, (cuuint64_t)R};
         const cuuint64_t strides[1] = {(cuuint64_t)ldl * 4};
@@ -1640,6 +1653,19 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
         w3d = encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(W), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        // a 4-D view (64 columns, rows, atoms 128 bytes apart, halves 512 bytes apart) over the
+        // atoms that lie wholly inside the row pitch: a CTA's four atoms of a full-width tile
+        // in one load, used where the last of them lies inside the pitch too (the kernel checks)
+        const int64_t pitch_atoms = ldw / 64;
+        const cuuint64_t dims4[4] = {64, (cuuint64_t)(vocab_end - vocab_start), (cuuint64_t)pitch_atoms, 2};
+        const cuuint64_t strides4[3] = {(cuuint64_t)ldw * 2, 128, 512};
+        const cuuint32_t box4[4] = {64, BK, 2u, 2u};
+        const cuuint32_t estr4[4] = {1, 1, 1, 1};
+        if (w3d && pitch_atoms >= 6 &&
+            encode(&tm_w4, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(W), dims4, strides4, box4,
+                   estr4, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+            w4d_atoms = (int)pitch_atoms;
     }
     if (!e4 && !w3d) {
         const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)(vocab_end - vocab_start)};
@@ -1676,6 +1702,7 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     p.splits = plan.splits;
     p.tail_splits = tail_splits_of(plan.splits, tail);
     p.w3d = w3d;
+    p.w4d_atoms = w4d_atoms;
     p.w_scale = e4 ? tab.scale : nullptr;
     p.fused = single ? 1 : 0;
     p.logits = logits;
@@ -1725,8 +1752,8 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     const int phase = single ? single->phase : 0;
     cudaError_t e = cudaSuccess;
     if (phase != 2) {  // the second call of a shard reduces what the first one left
-        e = e4 ? cudaLaunchKernelEx(&cfg, soft_embed_kernel<kE4m3>, tm_l, tm_w, p)
-               : cudaLaunchKernelEx(&cfg, soft_embed_kernel<kBf16>, tm_l, tm_w, p);
+        e = e4 ? cudaLaunchKernelEx(&cfg, soft_embed_kernel<kE4m3>, tm_l, tm_w, tm_w4, p)
+               : cudaLaunchKernelEx(&cfg, soft_embed_kernel<kBf16>, tm_l, tm_w, tm_w4, p);
         if (e != cudaSuccess) {
             *msg = "soft-embed kernel launch failed";
             return e;
