@@ -1228,48 +1228,47 @@ __global__ void __launch_bounds__(1024) splitk_reduce_kernel(const float4 *__res
         const int S = nt < p.n_full ? p.splits : p.tail_splits;
         const int64_t split_stride = (int64_t)p.m_tiles * p.n_tiles * tile_elems;
         const float4 *src = ws + ((int64_t)mt * p.n_tiles + nt) * tile_elems + (int64_t)cg * BM + r;
-        // loads issued four at a time, added strictly in split order
-        float4 acc4 = src[0];
-        if (scale) {
-            float f = scale[i];
-            if (f < 0.0f) {
-                acc4 = redo_partial<F>(p, Wv, ldw, d, lse[i], 0, i, c);
-                f = 1.0f;
-            }
-            acc4 = make_float4(f * acc4.x, f * acc4.y, f * acc4.z, f * acc4.w);
-        }
-        int s = 1;
-        for (; s + 4 <= S; s += 4) {
-            float4 v[4];
-            float f[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+        // the partials (and scales) of kRedBatch splits loaded together, clamped to the last
+        // split so that every load is unconditional, then added strictly in split order
+        constexpr int kRedBatch = 6;
+        float4 acc4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int s0 = 0; s0 < S; s0 += kRedBatch) {
+            float4 v[kRedBatch];
+            float f[kRedBatch];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                v[q] = src[(s + q) * split_stride];
-                if (scale) f[q] = scale[(int64_t)(s + q) * p.R + i];
+            for (int q = 0; q < kRedBatch; ++q) {
+                const int sq = min(s0 + q, S - 1);
+                v[q] = src[sq * split_stride];
+                f[q] = scale ? scale[(int64_t)sq * p.R + i] : 1.0f;
             }
+            bool redo = false;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if (f[q] < 0.0f) {
-                    v[q] = redo_partial<F>(p, Wv, ldw, d, lse[i], s + q, i, c);
-                    f[q] = 1.0f;
+            for (int q = 0; q < kRedBatch; ++q) redo |= f[q] < 0.0f;
+            if (!redo) {
+#pragma unroll
+                for (int q = 0; q < kRedBatch; ++q) {
+                    if (s0 + q >= S) break;
+                    acc4.x = fmaf(f[q], v[q].x, acc4.x);
+                    acc4.y = fmaf(f[q], v[q].y, acc4.y);
+                    acc4.z = fmaf(f[q], v[q].z, acc4.z);
+                    acc4.w = fmaf(f[q], v[q].w, acc4.w);
                 }
-                acc4.x = fmaf(f[q], v[q].x, acc4.x);
-                acc4.y = fmaf(f[q], v[q].y, acc4.y);
-                acc4.z = fmaf(f[q], v[q].z, acc4.z);
-                acc4.w = fmaf(f[q], v[q].w, acc4.w);
+            } else {
+                // a (split, row) to recompute (rare): the batch again, one split at a time
+#pragma unroll 1
+                for (int sq = s0; sq < S && sq < s0 + kRedBatch; ++sq) {
+                    float4 vq = src[sq * split_stride];
+                    float fq = scale[(int64_t)sq * p.R + i];
+                    if (fq < 0.0f) {
+                        vq = redo_partial<F>(p, Wv, ldw, d, lse[i], sq, i, c);
+                        fq = 1.0f;
+                    }
+                    acc4.x = fmaf(fq, vq.x, acc4.x);
+                    acc4.y = fmaf(fq, vq.y, acc4.y);
+                    acc4.z = fmaf(fq, vq.z, acc4.z);
+                    acc4.w = fmaf(fq, vq.w, acc4.w);
+                }
             }
-        }
-        for (; s < S; ++s) {
-            float4 v = src[s * split_stride];
-            float f = scale ? scale[(int64_t)s * p.R + i] : 1.0f;
-            if (f < 0.0f) {
-                v = redo_partial<F>(p, Wv, ldw, d, lse[i], s, i, c);
-                f = 1.0f;
-            }
-            acc4.x = fmaf(f, v.x, acc4.x);
-            acc4.y = fmaf(f, v.y, acc4.y);
-            acc4.z = fmaf(f, v.z, acc4.z);
-            acc4.w = fmaf(f, v.w, acc4.w);
         }
         float *o = out + (int64_t)i * ldo + c;
         if (vec_out && c + 4 <= d) {
