@@ -1652,19 +1652,6 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
         w3d = encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(W), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-        // a 4-D view (64 columns, rows, atoms 128 bytes apart, halves 512 bytes apart) over the
-        // atoms that lie wholly inside the row pitch: a CTA's four atoms of a full-width tile
-        // in one load, used where the last of them lies inside the pitch too (the kernel checks)
-        const int64_t pitch_atoms = ldw / 64;
-        const cuuint64_t dims4[4] = {64, (cuuint64_t)(vocab_end - vocab_start), (cuuint64_t)pitch_atoms, 2};
-        const cuuint64_t strides4[3] = {(cuuint64_t)ldw * 2, 128, 512};
-        const cuuint32_t box4[4] = {64, BK, 2u, 2u};
-        const cuuint32_t estr4[4] = {1, 1, 1, 1};
-        if (w3d && pitch_atoms >= 6 &&
-            encode(&tm_w4, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(W), dims4, strides4, box4,
-                   estr4, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
-            w4d_atoms = (int)pitch_atoms;
     }
     if (!e4 && !w3d) {
         const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)(vocab_end - vocab_start)};
@@ -1677,6 +1664,21 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
             *msg = "tensor map of the embedding shard could not be encoded";
             return cudaErrorInvalidValue;
         }
+    }
+    if (!e4) {
+        // a 4-D view (64 columns, rows, atoms 128 bytes apart, halves 512 bytes apart) over the
+        // atoms that lie wholly inside the row pitch: a CTA's four atoms of a full-width tile
+        // in one load, used where the last of them lies inside the pitch too (the kernel checks)
+        const int64_t pitch_atoms = ldw / 64;
+        const cuuint64_t dims4[4] = {64, (cuuint64_t)(vocab_end - vocab_start), (cuuint64_t)pitch_atoms, 2};
+        const cuuint64_t strides4[3] = {(cuuint64_t)ldw * 2, 128, 512};
+        const cuuint32_t box4[4] = {64, BK, 2u, 2u};
+        const cuuint32_t estr4[4] = {1, 1, 1, 1};
+        if (pitch_atoms >= 6 &&
+            encode(&tm_w4, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(W), dims4, strides4, box4,
+                   estr4, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+            w4d_atoms = (int)pitch_atoms;
     }
     const cudaError_t attr_err = ensure_kernel_attributes();
     if (attr_err != cudaSuccess) {

@@ -176,6 +176,33 @@ def test_soft_embed_shapes(B, R, V, d):
     assert rel_l2(E, ref).max() <= E_TOL
 
 
+@pytest.mark.parametrize("d,ldw", [(960, 960), (1000, 1000), (1000, 1024), (600, 608), (2816, 2880)])
+def test_soft_embed_w_load_paths_with_nan_pitch_padding(B, d, ldw):
+    """Every way the product loads W: one 4-D load of a CTA's four atoms per block, a 3-D
+    load per half where the fourth atom would pass the row pitch (d = 960: the second tile),
+    64-column 2-D boxes where the pitch does not hold whole atoms (d = 1000, 600), and 4-D
+    loads that read the pitch's padding columns (ldw > d), which hold NaN here and must not
+    reach E.  The plain product and the single-pass step, 256 rows (one row block)."""
+    R, V = 256, 8192
+    wl = inputs.Workload("case", 1, R, V, d, (0.5, 4.0), (0.0, 8.0), 2.0, seed=d + ldw)
+    x = inputs.logits(wl)
+    Wb = inputs.embedding_bf16(wl)
+    pitch = np.full((V, ldw), 0x7FC0, np.uint16)
+    pitch[:, :d] = Wb
+    Wd = w_dev(pitch)[:, :d]
+    assert Wd.stride(0) == ldw
+    xd = dev(x)
+    st = B.dg_row_stats(xd, V=V)
+    E = B.dg_soft_embed(xd, st["lse"], 0, V, Wd, wl.gamma).cpu().numpy()
+    ref = soft_embed(x, row_stats(x)["lse"], 0, V, Wb, wl.gamma)
+    assert np.all(np.isfinite(E))
+    assert rel_l2(E, ref).max() <= E_TOL
+    g = B.dg_sampler_step(xd, 1, R, Wd, wl.gamma, dev(np.full(1, 1e9, np.float32)))
+    Es = g["E"].cpu().numpy()
+    assert np.all(np.isfinite(Es))
+    assert rel_l2(Es, ref).max() <= E_TOL
+
+
 def test_soft_embed_ragged_slices_with_nan_padding(B):
     R, V, d = 40, 4096, 256
     full, ref_full, (x, Wb, st, xd, _, gamma) = embed_case(B, R, V, d, seed=11, ldl=4100)
