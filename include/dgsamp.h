@@ -146,8 +146,8 @@ dg_status dg_soft_embed(const float *logits, int64_t ldl, const float *lse, int6
  * split-K partial tiles go to a 16 MiB array compiled into the library, which every
  * GPU that loads the library holds until the process exits.  The call allocates
  * and frees nothing.  One vocabulary split's partial tiles take
- *     ceil(R / 256) * 256  x  ceil(d / 512) * 512  x  4 bytes
- * (rows in whole 256-row tiles, columns in whole 512-column tiles); a shape for which
+ *     ceil(R / 256) * 256  x  ceil(d / 1024) * 1024  x  4 bytes
+ * (rows in whole 256-row tiles, columns in whole pairs of 512-column tiles); a shape for which
  * that exceeds 16 MiB (16,777,216 bytes) returns DG_ERR_UNSUPPORTED: R = 1024 at d = 2816
  * (12 MiB) fits, R = 1100 (padded to 1280 rows, 15 MiB) fits, R = 1400 does not.  When
  * several splits do not fit, the call uses as many as fit.  Results match dg_soft_embed

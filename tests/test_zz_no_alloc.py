@@ -81,8 +81,8 @@ def test_no_alloc_small_case_matches_the_oracle(B):
 
 def one_split_bytes(R, d):
     """Partial tiles of one vocabulary split: rows in whole 256-row tiles, columns in whole
-    512-column tiles, fp32 (the size rule the header states)."""
-    return -(-R // 256) * 256 * (-(-d // 512) * 512) * 4
+    pairs of 512-column tiles, fp32 (the size rule the header states)."""
+    return -(-R // 256) * 256 * (-(-d // 1024) * 1024) * 4
 
 
 SCRATCH_BYTES = 16 << 20
@@ -106,10 +106,12 @@ def test_no_alloc_lowers_the_split_count_to_fit(B):
         assert rel_l2(got, ref).max() <= E_TOL
 
 
-@pytest.mark.parametrize("R,fits", [(8192, False), (1400, False), (1100, True)])
-def test_no_alloc_size_rule(B, R, fits):
+@pytest.mark.parametrize("R,d,fits", [(8192, 2816, False), (1400, 2816, False), (1100, 2816, True),
+                                      (2048, 1200, True), (2304, 1200, False)])
+def test_no_alloc_size_rule(B, R, d, fits):
+    """d = 1,200 takes three 512-column tiles, padded to a pair of pairs (2,048 columns):
+    2,048 rows fill the 16 MiB exactly, 2,304 do not fit."""
     from denoising_sampler_step_gb300.binding import DgError
-    d = 2816
     assert (one_split_bytes(R, d) <= SCRATCH_BYTES) == fits
     x = torch.zeros((R, 64), dtype=torch.float32, device="cuda")
     lse = torch.zeros(R, dtype=torch.float32, device="cuda")
