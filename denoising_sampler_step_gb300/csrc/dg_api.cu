@@ -462,17 +462,18 @@ dg_status run_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, i
         // one read of the logits: the product folds the statistics (and at temperature 1 the
         // draw); the acceptance runs on them after the reduce starts
         // the acceptance runs inside the reduce kernel, on the statistics the product's fold gave
+        // (and, in a loop step, each request's loop-state update right after its acceptance)
         AcceptSpec acc{H, kappa, budgets, n_req, L_c, min_accept, order, mask, n_accepted, eligible};
+        LoopSpec ls{};
+        if (loop)
+            ls = LoopSpec{draw_t1 ? loop->candidate : argmax, argmax, H, mask, L_c, loop->stable_steps,
+                          loop->step_limit, loop->entropy_threshold, loop->canvas, loop->eligible,
+                          loop->prev_argmax, loop->stable, loop->steps, loop->converged};
         SinglePassOut so{m, lse, H, kappa, argmax, draw_t1 ? loop->candidate : nullptr,
                          draw_t1 ? loop->seed : 0, draw_t1 ? loop->offset : 0, &acc};
-        st = run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, d, gamma, E, ldo, workspace,
-                            workspace_bytes, s, nullptr, nullptr, false, &so);
-        if (st != DG_OK || !loop) return st;
-        cudaError_t e = launch_loop_update(draw_t1 ? loop->candidate : argmax, argmax, H, mask, n_req, L_c,
-                                           loop->stable_steps,
-                                           loop->entropy_threshold, loop->step_limit, loop->canvas, loop->eligible,
-                                           loop->prev_argmax, loop->stable, loop->steps, loop->converged, s);
-        return e == cudaSuccess ? DG_OK : cuda_fail(e, "step: loop update launch");
+        so.loop = loop ? &ls : nullptr;
+        return run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, d, gamma, E, ldo, workspace,
+                              workspace_bytes, s, nullptr, nullptr, false, &so);
     }
     cudaError_t e = sampled ? launch_row_stats_sample(logits, R, V, ldl, loop->temperature, loop->seed, loop->offset,
                                                       m, lse, H, kappa, argmax, loop->candidate, nullptr, s)

@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "../../include/dgsamp.h"
+#include "loop.cuh"
 
 namespace dg {
 
@@ -69,6 +70,8 @@ struct SinglePassOut {
     int phase;
     float *shard_state;
     int64_t vocab_offset;
+    // non-NULL: the denoising-loop update, run by each request's acceptance CTA right after it
+    const LoopSpec *loop;
 };
 bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t d, int num_sms,
                      SoftEmbedPlan *plan, int fmt = kTableBf16);

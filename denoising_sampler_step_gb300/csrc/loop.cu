@@ -1,16 +1,8 @@
-// Denoising-loop state after a step (agentlenshq.com, "サンプリングループとエントロピー境界
-// デノイジング": kept tokens; a canvas has converged when the argmax predictions have been
-// stable for several steps and the mean entropy per token is below a threshold, or when
-// the step limit is reached).
-//
-// One CTA per request, one thread per position:
-//   canvas[p] = candidate[p] and eligible[p] = 0 where the step kept p (mask[p]);
-//   stable    = stable + 1 if every argmax equals the previous step's, else 0;
-//   prev[p]   = argmax[p];  steps += 1;
-//   converged = (stable >= stable_steps && mean H < threshold) || steps >= step_limit,
-//   mean H summed in fp64 in a fixed order (warp shuffles, then the warp totals in order).
+// The denoising-loop update as its own kernel (the steps that do not run it inside the
+// reduce kernel): one CTA per request, as loop_update_request describes.
 #include "dg_common.cuh"
 #include "dg_internal.h"
+#include "loop.cuh"
 
 namespace dg {
 
@@ -23,39 +15,9 @@ __global__ void __launch_bounds__(1024)
                        int32_t *__restrict__ canvas, uint8_t *__restrict__ eligible, int32_t *__restrict__ prev,
                        int32_t *__restrict__ stable, int32_t *__restrict__ steps, uint8_t *__restrict__ converged) {
     __shared__ double warp_sum[32];
-    const int q = blockIdx.x, tid = threadIdx.x;
-    const int64_t base = (int64_t)q * L_c;
-    const bool in = tid < L_c;
-    int32_t am = 0;
-    double h = 0.0;
-    bool same = true;
-    if (in) {
-        am = argmax[base + tid];
-        h = (double)H[base + tid];
-        same = am == prev[base + tid];
-    }
-    const bool all_same = __syncthreads_and(same);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) h += __shfl_down_sync(0xffffffffu, h, off);
-    if ((tid & 31) == 0) warp_sum[tid >> 5] = h;
-    __syncthreads();
-    if (in) {
-        if (mask[base + tid]) {
-            canvas[base + tid] = candidate[base + tid];
-            eligible[base + tid] = 0;
-        }
-        prev[base + tid] = am;
-    }
-    if (tid == 0) {
-        double total = 0.0;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) total += warp_sum[w];
-        const double mean_H = total / (double)L_c;
-        const int32_t s = all_same ? stable[q] + 1 : 0;
-        const int32_t n = steps[q] + 1;
-        stable[q] = s;
-        steps[q] = n;
-        converged[q] = ((s >= stable_steps && mean_H < (double)threshold) || n >= step_limit) ? 1 : 0;
-    }
+    const LoopSpec l{candidate, argmax, H, mask, L_c, stable_steps, step_limit, threshold,
+                     canvas, eligible, prev, stable, steps, converged};
+    loop_update_request(l, (int)blockIdx.x, warp_sum);
 }
 
 }  // namespace

@@ -1200,7 +1200,8 @@ template <int F>
 __global__ void __launch_bounds__(1024) splitk_reduce_kernel(const float4 *__restrict__ ws, const Params p, int d, float gamma,
                                      float *__restrict__ out, int64_t ldo, int vec_out,
                                      const float *__restrict__ scale, const void *__restrict__ Wv, int64_t ldw,
-                                     const float *__restrict__ lse, const AcceptSpec acc, int n_acc) {
+                                     const float *__restrict__ lse, const AcceptSpec acc, int n_acc,
+                                     const LoopSpec loop) {
     constexpr int BN = Fmt<F>::BN;
     // the kernel queued next reads nothing this one writes; this one reads the partials and
     // the statistics only after the kernel before it (the single pass's statistics) completed
@@ -1212,6 +1213,10 @@ __global__ void __launch_bounds__(1024) splitk_reduce_kernel(const float4 *__res
         __shared__ double warp_tot[32];
         __shared__ int first_fail;
         accept_request(acc, (int)blockIdx.x, blockDim.x, AcceptSmem{keys, H_s, warp_tot, &first_fail});
+        if (loop.canvas) {
+            __syncthreads();  // the request's mask written, warp_tot free again
+            loop_update_request(loop, (int)blockIdx.x, warp_tot);
+        }
         return;
     }
     const int64_t groups = ((int64_t)d + 3) / 4;  // column groups of 4
@@ -1824,10 +1829,12 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     const float4 *ws4 = static_cast<const float4 *>(workspace);
     const float *scale = single ? (const float *)p.ref : nullptr;
     const float *lse_s = single ? (const float *)single->lse : nullptr;
+    const LoopSpec no_loop{};
+    const LoopSpec &lp = (n_acc > 0 && single->loop) ? *single->loop : no_loop;
     e = e4 ? cudaLaunchKernelEx(&c3, splitk_reduce_kernel<kE4m3>, ws4, p, (int)d, gamma, out, ldo, vec_out, scale,
-                                tab.W, ldw, lse_s, acc, n_acc)
+                                tab.W, ldw, lse_s, acc, n_acc, lp)
            : cudaLaunchKernelEx(&c3, splitk_reduce_kernel<kBf16>, ws4, p, (int)d, gamma, out, ldo, vec_out, scale,
-                                tab.W, ldw, lse_s, acc, n_acc);
+                                tab.W, ldw, lse_s, acc, n_acc, lp);
     if (e != cudaSuccess) {
         *msg = "split-K reduce launch failed";
         return e;
