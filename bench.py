@@ -291,6 +291,39 @@ def run_sharded(args) -> None:
     t1.record(stream)
     torch.cuda.synchronize(dev)
     dist.barrier()
+    # the same rank step, 16 of them captured in one CUDA graph (NCCL collectives included) and
+    # replayed: the eager loop above issues each step's launches and collectives from Python,
+    # which at one rank takes about as long as the GPU work itself
+    gms = None
+    graph_error = None
+    try:
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            st.rank_step(shard, s, Wsh, bd, comm)
+        stream.wait_stream(cap)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for _ in range(LOOP_STEPS):
+                st.rank_step(shard, s, Wsh, bd, comm)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        dist.barrier()
+        reps = max(1, -(-args.steps // LOOP_STEPS))
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        dist.barrier()
+        gm = torch.tensor([g0.elapsed_time(g1) / (reps * LOOP_STEPS)], device=dev)
+        dist.all_reduce(gm, op=dist.ReduceOp.MAX)
+        gms = gm.item()
+        del g
+    except Exception as ex:  # report, do not hide the eager number
+        graph_error = str(ex)[:200]
     clk = clocks.stop()
     mx = torch.tensor([t0.elapsed_time(t1)], device=dev)
     dist.all_reduce(mx, op=dist.ReduceOp.MAX)
@@ -309,6 +342,10 @@ def run_sharded(args) -> None:
                                                     "partial_embeddings": world * wl.R * wl.d * 4},
             "gpu_launches": 6 * args.steps,
             "clocks": clk,
+            "graph": ({"ms_per_step": gms, "value": wl.R / (gms * 1e-3),
+                       "how": f"{LOOP_STEPS} rank steps (their NCCL all-gathers included) captured in one "
+                              "CUDA graph and replayed; max over ranks"}
+                      if gms is not None else {"ms_per_step": None, "error": graph_error}),
         }
         print(json.dumps(line))
     dist.destroy_process_group()
