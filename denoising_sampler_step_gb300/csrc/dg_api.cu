@@ -457,21 +457,21 @@ dg_status run_step(const float *logits, int32_t n_req, int32_t L_c, int64_t V, i
     }
     if (R == 0) return DG_OK;
     const uint8_t *eligible = loop ? loop->eligible : nullptr;
-    const bool draw_t1 = sampled && loop->temperature == 1.0f;  // the single pass folds this draw
-    if ((!sampled || draw_t1) && use_single_pass(R, V, vocab_start, vocab_end, d, workspace_bytes, W.fmt, flags)) {
-        // one read of the logits: the product folds the statistics (and at temperature 1 the
-        // draw); the acceptance runs on them after the reduce starts
-        // the acceptance runs inside the reduce kernel, on the statistics the product's fold gave
+    if (use_single_pass(R, V, vocab_start, vocab_end, d, workspace_bytes, W.fmt, flags)) {
+        // one read of the logits: the product folds the statistics (and, in a sampling loop
+        // step, the draw's first level); the acceptance runs inside the reduce kernel, on the
+        // statistics the product's fold gave
         // (and, in a loop step, each request's loop-state update right after its acceptance)
         AcceptSpec acc{H, kappa, budgets, n_req, L_c, min_accept, order, mask, n_accepted, eligible};
         LoopSpec ls{};
         if (loop)
-            ls = LoopSpec{draw_t1 ? loop->candidate : argmax, argmax, H, mask, L_c, loop->stable_steps,
+            ls = LoopSpec{sampled ? loop->candidate : argmax, argmax, H, mask, L_c, loop->stable_steps,
                           loop->step_limit, loop->entropy_threshold, loop->canvas, loop->eligible,
                           loop->prev_argmax, loop->stable, loop->steps, loop->converged};
-        SinglePassOut so{m, lse, H, kappa, argmax, draw_t1 ? loop->candidate : nullptr,
-                         draw_t1 ? loop->seed : 0, draw_t1 ? loop->offset : 0, &acc};
+        SinglePassOut so{m, lse, H, kappa, argmax, sampled ? loop->candidate : nullptr,
+                         sampled ? loop->seed : 0, sampled ? loop->offset : 0, &acc};
         so.loop = loop ? &ls : nullptr;
+        so.temperature = sampled ? loop->temperature : 1.0f;
         return run_soft_embed(logits, ldl, lse, R, vocab_start, vocab_end, W, d, gamma, E, ldo, workspace,
                               workspace_bytes, s, nullptr, nullptr, false, &so);
     }

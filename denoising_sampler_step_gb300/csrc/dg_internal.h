@@ -60,8 +60,8 @@ struct AcceptSpec;
 struct SinglePassOut {
     float *m, *lse, *H, *kappa;
     int32_t *argmax;
-    int32_t *candidate;     // non-NULL: also draw at temperature 1 (two-level Gumbel-max); kappa is
-    uint64_t seed, offset;  // then -ln p of the drawn token
+    int32_t *candidate;     // non-NULL: also draw (two-level Gumbel-max from softmax(l / T)); kappa
+    uint64_t seed, offset;  // is then -ln p of the drawn token under softmax(l)
     const AcceptSpec *accept;
     // a vocabulary shard in two calls around the ranks' exchange of row summaries:
     // 0 the whole step; 1 the product and the shard's row summaries (shard_state, argmax as
@@ -72,6 +72,7 @@ struct SinglePassOut {
     int64_t vocab_offset;
     // non-NULL: the denoising-loop update, run by each request's acceptance CTA right after it
     const LoopSpec *loop;
+    float temperature;  // T of the draw (0 is taken as 1)
 };
 bool plan_soft_embed(int64_t R, int64_t vocab_start, int64_t vocab_end, int64_t d, int num_sms,
                      SoftEmbedPlan *plan, int fmt = kTableBf16);

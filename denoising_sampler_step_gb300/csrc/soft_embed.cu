@@ -184,9 +184,11 @@ struct Params {
                          // (split, row) must be recomputed (kRedo)
     float4 *state;       // [splits][n_tiles][R] row summaries (m, argmax bits, rest, t) of the blocks
                          // of the split the column tile folds (`fold` in the producers)
-    // single pass with the temperature-1 draw: the folded blocks also take the draw's first
-    // level (a group of 16 entries by log-mass + Gumbel), the statistics kernel the second
+    // single pass with the draw at temperature 1 / inv_tau: the folded blocks also take the
+    // draw's first level (a group of 16 entries by the log-mass of l / T + Gumbel), the
+    // statistics kernel the second
     int draw;
+    float inv_tau;
     uint32_t k0, k1, o0, o1;  // Philox key (seed) and counter offset words
     float2 *draws;            // [splits][n_tiles][R] best group score, group (int bits)
     int32_t *candidate;       // [R] the drawn tokens
@@ -948,7 +950,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const float f = fmaf(bm, kLog2e, neg_lse2[q]) - kfq[q];
                         const float inv = ex2_approx(-7.0f - f);
                         blk = rowstate::RowState{bm, (int)(k + ja), se * inv, sd * inv};
-                        if (p.draw) {  // c + ln(sum of exp(l - c)) = c + ln 2 (log2(sum e'') + k - 7)
+                        if (p.draw && p.inv_tau == 1.0f) {  // c + ln(sum of exp(l - c)) = c + ln 2 (log2(sum e'') + k - 7)
 #pragma unroll
                             for (int h = 0; h < 2; ++h) {
                                 float gsum = 0.0f;
@@ -992,7 +994,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             rs.R16 += S;  // equal maxima keep the earlier index
                         }
                         rs.T16 += fmaf(-my_ref[q], S, Tx);
-                        if (p.draw) {  // the two groups' log-masses, c + ln(sum of e)
+                        if (p.draw && p.inv_tau == 1.0f) {  // the two groups' log-masses, c + ln(sum of e)
                             glm[0] = my_ref[q] + philox::kLn2 * __log2f(s_lo);
                             glm[1] = my_ref[q] + philox::kLn2 * __log2f(s_hi);
                         }
@@ -1018,7 +1020,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                         rowstate::absorb<16>(blk, xs, bs);
                     }
-                    if (p.draw) {  // far from c: the log-masses against the block max
+                    if (p.draw && p.inv_tau == 1.0f) {  // far from c: the log-masses against the block max
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             float gsum = 0.0f;
@@ -1027,6 +1029,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                             glm[h] = bm + philox::kLn2 * __log2f(gsum);
                         }
                     }
+                    }
+                    if (p.draw && p.inv_tau != 1.0f && bm > -INFINITY) {
+                        // another temperature: the two groups' log-masses of l / T, against the
+                        // block maximum (entries at -inf add nothing)
+                        const float sl = kLog2e * p.inv_tau;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            float gsum = 0.0f;
+#pragma unroll
+                            for (int t = 0; t < 16; ++t) gsum += ex2_approx((xb[16 * h + t] - bm) * sl);
+                            glm[h] = bm * p.inv_tau + philox::kLn2 * __log2f(gsum);
+                        }
                     }
                     rowstate::merge(my_st16[q], blk);
                     if (p.draw && bm > -INFINITY) {
@@ -1377,7 +1391,7 @@ __global__ void __launch_bounds__(256)
         float sc = -INFINITY;
         if (valid && l != -INFINITY) {
             const philox::Philox w = philox::philox4x32_10((uint32_t)(v >> 2), (uint32_t)row, p.o0, p.o1, p.k0, p.k1);
-            sc = l - philox::kLn2 * __log2f(philox::neg_log_uniform(philox::philox_word(w, (int)(v & 3))));
+            sc = l * p.inv_tau - philox::kLn2 * __log2f(philox::neg_log_uniform(philox::philox_word(w, (int)(v & 3))));
         }
         int bi = valid ? (int)v : 0x7fffffff;
         float bl = l;
@@ -1716,6 +1730,7 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
     p.ref = nullptr;
     p.state = nullptr;
     p.draw = 0;
+    p.inv_tau = 1.0f;
     p.k0 = p.k1 = p.o0 = p.o1 = 0;
     p.draws = nullptr;
     p.candidate = nullptr;
@@ -1728,6 +1743,7 @@ cudaError_t launch_soft_embed(const float *logits, int64_t ldl, const float *lse
         x += n * (size_t)plan.n_tiles * 16;
         if (single->candidate) {
             p.draw = 1;
+            p.inv_tau = single->temperature > 0.0f ? 1.0f / single->temperature : 1.0f;
             p.draws = reinterpret_cast<float2 *>(x);
             p.candidate = single->candidate;
             p.k0 = (uint32_t)single->seed;

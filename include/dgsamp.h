@@ -425,10 +425,13 @@ dg_status dg_loop_update(const int32_t *candidate, const int32_t *argmax, const 
  * dg_loop_update.
  *   temperature == 0: the candidate is the argmax and kappa is dg_row_stats' (ln Z);
  *                     `candidate` may be NULL.
- *   temperature > 0:  dg_row_stats_sample draws the candidates (seed, offset; advance
- *                     the offset every step) into `candidate`, kappa is -ln p of the
- *                     drawn token, and the canvas takes the drawn tokens; stability is
- *                     still judged on the argmax.
+ *   temperature > 0:  the candidates are drawn as dg_row_stats_sample draws them (seed,
+ *                     offset; advance the offset every step) into `candidate`, kappa is
+ *                     -ln p of the drawn token, and the canvas takes the drawn tokens;
+ *                     stability is still judged on the argmax.  Over the whole vocabulary
+ *                     (one read of the logits) the draw is folded into the product, with
+ *                     the same distribution and Philox stream; over a slice, or with
+ *                     DG_STEP_TWO_PASS, dg_row_stats_sample itself runs first.
  * Other arguments as dg_sampler_step, dg_entropy_accept_eligible and dg_loop_update;
  * the loop state (canvas, eligible, prev_argmax, stable, steps, converged) is read and
  * written in place, so successive calls on one stream (or one captured graph,

@@ -182,7 +182,7 @@ def test_step_canvas256_full_size(B):
     assert rel_l2(out["E"].cpu().numpy()[rows], ref).max() <= E_TOL
 
 
-@pytest.mark.parametrize("temperature", [0.0, 1.0])
+@pytest.mark.parametrize("temperature", [0.0, 1.0, 0.7])
 def test_loop_over_the_8bit_table_matches_the_oracle_chain(B, temperature):
     """Denoising-loop steps over the 8-bit table (argmax, and drawn candidates with the draw
     folded into the single pass): statistics, candidates, acceptance and the whole loop

@@ -293,19 +293,19 @@ def sampled_chain_inputs(wl, steps, temperature, seed):
     return budgets, thr, chain
 
 
-@pytest.mark.parametrize("temperature", [1.0, 0.7])
-def test_sampled_loop_chain_matches_oracle(B, temperature):
+@pytest.mark.parametrize("temperature,two_pass", [(1.0, False), (0.7, False), (0.7, True)])
+def test_sampled_loop_chain_matches_oracle(B, temperature, two_pass):
     """A sampling loop (Philox offset = step): at every step the statistics and the draw
-    (folded into the single pass at temperature 1, the fused statistics + draw pass before
-    the product otherwise), the acceptance by -ln p of the drawn token over the eligible
-    positions, the canvas of drawn tokens and the argmax-judged state, bit-exact against
-    the oracle chain."""
+    (folded into the single pass, or with two passes the fused statistics + draw pass before
+    the product), the acceptance by -ln p of the drawn token over the eligible positions,
+    the canvas of drawn tokens and the argmax-judged state, bit-exact against the oracle
+    chain."""
     from denoising_sampler_step_gb300.step import SamplerLoop
     wl, seed = SAMPLED_WL, 2024
     budgets, thr, chain = sampled_chain_inputs(wl, N_STEPS, temperature, seed)
     Wb = inputs.embedding_bf16(wl)
     lp = SamplerLoop(w_dev(Wb), wl.n_req, wl.L_c, wl.V, wl.gamma, STABLE_STEPS, thr, STEP_LIMIT,
-                     temperature=temperature, seed=seed, min_accept=1)
+                     temperature=temperature, seed=seed, min_accept=1, two_pass=two_pass)
     bud = dev(budgets)
     for t, (x, st, sm, kc, acc, o) in enumerate(chain):
         out = lp(dev(x), bud)

@@ -117,11 +117,13 @@ def test_single_pass_largest_canvas(B):
     assert rel_l2(out["E"].cpu().numpy()[rows], ref).max() <= E_TOL
 
 
-def test_single_pass_draw_at_temperature_one(B):
-    """The loop step at temperature 1 folds the draw into the product: the candidates
-    against the two-level oracle draw (unique where both decisions lead by 1e-3), kappa =
-    -ln p of the drawn token; rows far from their reference (one-hot, 90 nats up, masked
-    starts, shifted) take the fallback folds."""
+@pytest.mark.parametrize("temperature", [1.0, 0.7, 1.6])
+def test_single_pass_draw(B, temperature):
+    """A sampling loop step folds the draw into the product: the candidates against the
+    two-level oracle draw from softmax(l / T) (unique where both decisions lead by 1e-3),
+    kappa = -ln p of the drawn token under softmax(l); rows far from their reference
+    (one-hot, 90 nats up, masked starts, shifted) take the fallback folds.  At T = 1 the
+    groups' log-masses come from the product's own exponentials, at other T from their own."""
     from oracle import candidate_kappa, row_sample
     from tests.test_gpu_parity import check_sample
     wl = inputs.WORKLOADS["tiny"].with_(V=40000, d=256, L_c=24, n_req=2, seed=17, budget=5.0)
@@ -136,10 +138,10 @@ def test_single_pass_draw_at_temperature_one(B):
     Wd = w_dev(Wb)
     state = B.new_loop_state(wl.n_req, wl.L_c, "cuda")
     out = B.dg_sampler_loop_step(dev(x), wl.n_req, wl.L_c, Wd, wl.gamma, dev(inputs.budgets(wl)), state, 2, 1.0, 10,
-                                 temperature=1.0, seed=31, offset=4)
+                                 temperature=temperature, seed=31, offset=4)
     torch.cuda.synchronize()
     B.dg_get_device_status()
-    o = row_sample(x, 1.0, 31, 4)
+    o = row_sample(x, temperature, 31, 4)
     g = {"candidate": out["candidate"], "log_p": torch.from_numpy(o["log_p"].astype(np.float32))}
     check_sample(g, o)
     cand = out["candidate"].cpu().numpy()
