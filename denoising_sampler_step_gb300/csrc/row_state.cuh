@@ -1,6 +1,7 @@
-// Online softmax statistics of one row (shared by the statistics kernel and the fused
-// statistics + sampling kernel; both fold entries in the same order with the same
-// arithmetic, so their statistics agree bit for bit).
+// Online softmax statistics of one row (shared by the statistics kernel, the fused
+// statistics + sampling kernel and the product's fallback fold: the same arithmetic, so
+// their maxima and argmax agree exactly and their sums up to the order in which each
+// kernel visits the entries).
 //
 // Each thread keeps an online state (m, a, rest, t) over the entries it saw:
 //   m    = running max, a = index of its first occurrence,
