@@ -7,30 +7,38 @@
 // padded shard rows are never part of the product).
 //
 // Kernel design (the one dense contraction of the step, on the tcgen05 tensor cores):
-//   - a cluster of two CTAs, a tcgen05 CTA pair, owns 256 output rows (128 each) x up to
-//     512 output columns and one contiguous range of 32-entry vocabulary blocks (split-K over
-//     the vocabulary); each CTA's fp32 accumulator fills its 512 TMEM columns;
-//   - per block, each CTA loads its logits tile [128 x 32] fp32 by TMA and 128 of every 256
-//     columns of the W tile [32 x 512] bf16 (the pair form of the TMA load, counted on the
-//     even CTA's barrier): every W byte leaves L2 once, and W and A share a six-deep ring;
-//   - eight producer warps (two groups of four taking alternate blocks, 32 rows each) turn
-//     the logits tile into the bf16 A operand, exp2(l*log2e - lse*log2e) rounded to
-//     nearest even, in the K-major 64-byte-swizzled layout, and hand the logits slot
-//     back at once; the probabilities never go to global memory;
-//   - one thread of the even CTA issues tcgen05.mma.cta_group::2 (M=256 over both CTAs' rows,
-//     N=256, K=16, bf16 x bf16 -> fp32) for the two 256-column halves once its producers
-//     have arrived, both CTAs' W bytes have landed and the odd CTA's producers have signalled
-//     (a 16-byte bulk copy per warp onto the same barrier); tcgen05.commit to both CTAs frees
-//     the W and A slots once the MMAs have read them;
+//   - a cluster of four CTAs, two tcgen05 CTA pairs, owns 256 output rows x two adjacent
+//     512-column tiles and one contiguous range of 32-entry vocabulary blocks (split-K over
+//     the vocabulary): each pair (M = 256, 128 rows per CTA) computes one column tile into
+//     its CTAs' 512 TMEM columns;
+//   - per block, each CTA loads its 128 of every 256 W columns of its pair's tile — four
+//     64-column atoms of 32 rows in one 4-D TMA load (the pair form, counted on the even
+//     CTA's barrier): every W byte leaves L2 once, and W and A share a six-deep ring;
+//   - the CTAs of one column parity form a block's A operand: they load its logits tile
+//     [128 x 32] fp32 by TMA, and eight producer warps (two groups of four taking alternate
+//     blocks, 32 rows each) turn it into bf16 exp2(l*log2e - lse*log2e) (rounded to nearest
+//     even) in the K-major 64-byte-swizzled layout, hand the logits slot back at once and
+//     copy their rows to the CTA with the same rows in the other pair; the probabilities
+//     never go to global memory;
+//   - one thread of each pair's even CTA issues tcgen05.mma.cta_group::2 (M = 256, N = 256,
+//     K = 16, bf16 x bf16 -> fp32) for the two 256-column halves once the A tile is in place
+//     in both CTAs (its producers' arrivals, the odd CTA's 16-byte signal copies, or the
+//     copied tile and the odd CTA's relayed signal) and both CTAs' W bytes have landed; one
+//     tcgen05.commit frees the W and A slots in all four CTAs once the MMAs have read them;
 //   - every warp then reads the accumulator with tcgen05.ld and stores the partial tile;
 //     splitk_reduce_kernel adds the split partials in split order, multiplies by gamma
 //     and writes E (bitwise reproducible).
-//   A column tail of 256 or fewer (d = 2816 = 5 x 512 + 256) is a half-width tile; it gets
-//   as many splits as the full tiles, since a block's time is set by the stage round trip.
-//   bf16 W loads mark their lines evict-first, which keeps the logits (read by every column
-//   tile of a row block) in L2.
-//   Every barrier wait is bounded (about a second); a wait that gives up records
-//   DG_ERR_TIMEOUT, drains what is in flight and leaves the kernel.
+//   A column tail of 256 or fewer (d = 2816 = 5 x 512 + 256) is a half-width tile.  bf16 W
+//   loads mark their lines evict-first, which keeps the logits in L2.  Every barrier wait is
+//   bounded (about a second); a wait that gives up records DG_ERR_TIMEOUT, drains what is in
+//   flight and leaves the kernel.
+//
+// Single pass (no lse yet): the producers form exp(l - c) against a per-(split, row)
+// reference c, and the CTAs of one column pair fold each block's row statistics (and, in a
+// sampling loop step, the draw's first level) from the same values; single_pass_stats_kernel
+// merges the split summaries into the row statistics and the scales exp(c - lse), and the
+// reduce applies them (recomputing the rare (split, row) whose probabilities against c
+// could overflow), with each request's acceptance (and loop update) in its first CTAs.
 //
 // The same kernel, instantiated for an 8-bit table (E4M3 codes with one fp32 scale per
 // vocabulary row), runs block-scaled E4M3 MMAs (kind::mxf8f6f4) on the same four-CTA layout:
