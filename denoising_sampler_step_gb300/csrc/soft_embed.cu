@@ -420,9 +420,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             int issued[WST];
             for (int s = 0; s < WST; ++s) issued[s] = 0;
-            // bf16: every W byte leaves L2 once (evict first); 8-bit table: both row-block
-            // clusters of a column pair read each W tile, close together (ordinary priority)
-            const uint64_t w_policy = F == kE4m3 ? l2_policy_evict_normal() : l2_policy_evict_first();
+            // bf16 over one 256-row block: every W byte leaves L2 once (evict first).  Over
+            // several row blocks (or the 8-bit table's two row-block clusters) the clusters of a
+            // column pair read each W tile close together: ordinary priority keeps it in L2 for
+            // them (at 2,048 rows evict-first made the product read W about five times from DRAM)
+            const uint64_t w_policy =
+                (F == kE4m3 || p.m_tiles > 2) ? l2_policy_evict_normal() : l2_policy_evict_first();
             // bf16: a 4-D map fetches a CTA's four atoms of a full-width tile in one load, a 3-D
             // map its two atoms of a half (the TMA unit's cost is per load, not per byte: two
             // 64-column boxes per half in place of one 3-D load made the product 8 % slower,
