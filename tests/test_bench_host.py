@@ -59,3 +59,32 @@ def test_default_bench_times_the_tensor_bound_workloads():
     names = bench.DEFAULT_ALSO.split(",")
     assert names == ["batch8", "late_batch32"]
     assert [inputs.WORKLOADS[n].R for n in names] == [2048, 8192]
+
+
+def test_stored_traffic_is_taken_on_the_current_kernel_source():
+    """The DRAM traffic the bench line reports comes from profiles/soft_embed_traffic.json only
+    while its kernel-source hash is the current one: the committed file matches the committed
+    kernel, and the traffic per call is what the profile states (1.02x the algorithmic bytes)."""
+    tj = bench.stored_traffic()
+    assert tj, "profiles/soft_embed_traffic.json was taken on another kernel source"
+    assert tj["kernel_source_sha"] == bench.source_sha()
+    from denoising_sampler_step_gb300 import cost
+    sc = cost.StepCost(rows=256, V=262144, d=2816, vocab=262144)
+    assert 1.0 <= tj["traffic_bytes_per_launch"] / sc.gemm_bytes <= 1.03
+    assert 1.0 <= tj["e4m3_traffic_bytes_per_launch"] / sc.e4m3_gemm_bytes <= 1.05
+
+
+def test_kernel_source_hash_ignores_comments_only(tmp_path, monkeypatch):
+    """Comments and blank space do not change the hash; code does."""
+    src = os.path.join(ROOT, "denoising_sampler_step_gb300", "csrc")
+    dst = tmp_path / "denoising_sampler_step_gb300" / "csrc"
+    dst.mkdir(parents=True)
+    for f in ("soft_embed.cu", "dg_common.cuh"):
+        (dst / f).write_text(open(os.path.join(src, f)).read())
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.source_sha()
+    p = dst / "soft_embed.cu"
+    p.write_text(p.read_text() + "\n// a comment\n/* and another */\n\n")
+    assert bench.source_sha() == h0
+    p.write_text(p.read_text() + "\nstatic int an_extra_line = 0;\n")
+    assert bench.source_sha() != h0
